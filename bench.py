@@ -1,0 +1,365 @@
+#!/usr/bin/env python
+"""Throughput of the Llama ubatch forward on one GB300 (or N independent replicas).
+
+Workload (default): the 8B-shape Llama with Q4_0 linear layers and Q8_0 embedding / head
+(vocab 128256, d 4096, 32 layers, 32/8 heads, head_dim 128, FFN 14336, RoPE theta 5e5, n_ctx
+8192), seeded synthetic weights and a uniform-random 2048-token prompt. One step = clear the
+cache, prefill the prompt in ubatches of 512 tokens, then 256 greedy decode steps on the device.
+
+Reported: decode tokens/s (value), prefill tokens/s, the roofline of the dominant kernel (the
+weight-streaming GEMV, against measured HBM bandwidth) and of the prefill matmuls (against the
+measured bf16 tensor peak), the end-to-end rate through the C ABI with host buffers, and the
+CPU oracle timed on a bounded sample on this host.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl lcx|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant GEMV (gate/up,
+# Q4_0, 8B shape, T = 1) from the committed ncu summary; None until captured for the
+# current kernel.
+GEMV_NCU_TRAFFIC_BYTES = None
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        j = json.load(open(p))
+        return j["hbm_gbs"], j["bf16_tflops"], j.get("bf16_tflops_sustained", j["bf16_tflops"]), "measured"
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while active."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows = []
+        self.proc = None
+        self.th = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.th = threading.Thread(target=self._read, daemon=True)
+        self.th.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([x.strip() for x in line.split(",")])
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.th:
+            self.th.join(timeout=2)
+        sm, mx, reasons = [], 0.0, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in self.rows:
+            try:
+                sm.append(float(r[1]))
+                mx = max(mx, float(r[2]))
+                for n, v in zip(names, r[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+            except (ValueError, IndexError):
+                continue
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": mx or None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------------- workload
+def workload_args(a):
+    import synth
+    cfg = synth.CONFIGS[a.config]
+    return cfg, a.prompt, a.decode_steps, a.n_ubatch
+
+
+def decode_bytes_per_step(cfg, host, pos0, n_steps):
+    """Algorithmic HBM bytes of the decode steps: all weights as stored (the embedding row only)
+    plus the K/V of every attended cell."""
+    w = host.output.nbytes + host.output_norm.nbytes
+    for L in host.layers:
+        w += sum(v.nbytes for v in L.values())
+    emb_row = host.tok_embd.shape[1]
+    kv_cell = cfg.n_layer * cfg.n_head_kv * cfg.head_dim * 2 * 2
+    cells = sum(pos0 + i + 1 for i in range(n_steps))
+    return n_steps * (w + emb_row) + kv_cell * cells
+
+
+def prefill_flops(cfg, n_prompt):
+    d, hd, H, KV, F, L, V = cfg.n_embd, cfg.head_dim, cfg.n_head, cfg.n_head_kv, cfg.n_ff, cfg.n_layer, cfg.n_vocab
+    lin = (H * hd + 2 * KV * hd) * d + d * H * hd + 3 * F * d
+    att = 4 * H * hd * sum(t + 1 for t in range(n_prompt)) * L
+    return 2 * n_prompt * lin * L + att + 2 * V * d
+
+
+def cpu_baseline(host, cfg, n_prompt=4, n_decode=2):
+    """The oracle as it stands, on this host's cores, over a bounded sample."""
+    import oracle
+    n = oracle.set_threads()
+    om = oracle.Model(host)
+    octx = oracle.Context(om, cfg.n_ctx, 1, 512)
+    prompt = np.asarray(host_prompt_cache.get("p"), dtype=np.int32)[:n_prompt]
+    t0 = time.perf_counter()
+    rc, _, am = octx.decode(prompt)
+    t1 = time.perf_counter()
+    tok = int(am[-1])
+    for _ in range(n_decode):
+        rc, _, am = octx.decode([tok])
+        tok = int(am[0])
+    t2 = time.perf_counter()
+    return {"value": n_decode / (t2 - t1), "unit": "tokens/s", "cores": n, "kind": "oracle",
+            "sample": f"{cfg.name} model, fp64 oracle: {n_prompt}-token prompt then {n_decode} decode steps "
+                      f"(decode rate; prefill {n_prompt / (t1 - t0):.3f} tokens/s)",
+            "prefill_tokens_per_s": n_prompt / (t1 - t0)}
+
+
+host_prompt_cache = {}
+
+
+def run_lcx(a, rank, world):
+    import torch
+
+    import llama_ubatch_forward_gb300 as lcx
+    import synth
+    from llama_ubatch_forward_gb300.torch_io import upload
+
+    lcx.build()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    cfg, n_prompt, n_dec, n_ub = workload_args(a)
+    t0 = time.perf_counter()
+    host = synth.make_model(cfg)
+    prompt = synth.prompt_tokens(cfg, n_prompt)
+    host_prompt_cache["p"] = prompt
+    log(f"[bench] model {cfg.name}: {host.weight_bytes() / 1e9:.2f} GB stored, generated in {time.perf_counter() - t0:.1f}s")
+    gm = upload(host)
+    stream = torch.cuda.Stream()
+    ctx = lcx.Context(gm, cfg.n_ctx, 1, n_ub, stream=stream)
+    gen = torch.zeros(n_dec, dtype=torch.int32, device=dev)
+    am_host = np.zeros(1, dtype=np.int32)
+
+    def step(ev=None):
+        ctx.kv_clear()
+        if ev:
+            ev[0].record(stream)
+        rc = ctx.decode(prompt, argmax_out=am_host)        # syncs for the first generated token
+        assert rc == 0, rc
+        if ev:
+            ev[1].record(stream)
+        rc = ctx.decode_greedy(0, int(am_host[0]), n_dec, gen)
+        assert rc == 0, rc
+        if ev:
+            ev[2].record(stream)
+
+    for _ in range(a.warmup):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(a.steps)]
+    g0 = torch.cuda.Event(enable_timing=True)
+    g1 = torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for k in range(a.steps):
+        step(evs[k])
+    g1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    total_ms = g0.elapsed_time(g1)
+    pre_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    dec_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    times = torch.tensor([total_ms, sum(pre_ms), sum(dec_ms)], dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(times, op=torch.distributed.ReduceOp.MAX)
+    total_ms, pre_sum, dec_sum = times.tolist()
+    decode_tps = world * a.steps * n_dec / (dec_sum / 1e3)
+    prefill_tps = world * a.steps * n_prompt / (pre_sum / 1e3)
+
+    # per-kernel-class durations: one more step with event brackets around every launch
+    ctx.set_profiling(True)
+    step()
+    prof = ctx.profile()
+    ctx.set_profiling(False)
+    launches_per_step = None
+    s0 = ctx.stats().n_kernels
+    step()
+    torch.cuda.synchronize()
+    launches_per_step = ctx.stats().n_kernels - s0
+
+    # end to end through the C ABI with host buffers: host token in, host argmax out, per step
+    e2e_steps = max(1, min(a.steps, 2))
+    torch.cuda.synchronize()
+    t_e2e = 0.0
+    for _ in range(e2e_steps):
+        ctx.kv_clear()
+        am = np.zeros(1, dtype=np.int32)
+        assert ctx.decode(prompt, argmax_out=am) == 0
+        tok = int(am[0])
+        s = time.perf_counter()
+        for _ in range(n_dec):
+            assert ctx.decode(np.array([tok], np.int32), argmax_out=am) == 0
+            tok = int(am[0])
+        t_e2e += time.perf_counter() - s
+    e2e_tps = world * e2e_steps * n_dec / t_e2e
+
+    hbm, bf16, bf16_sus, src = peaks()
+    g = prof["gemv"]
+    gemv_gbs = g["bytes"] / (g["ms"] / 1e3) / 1e9 if g["ms"] else 0.0
+    gm_ = prof["gemm"]
+    gemm_tf = gm_["flops"] / (gm_["ms"] / 1e3) / 1e12 if gm_["ms"] else 0.0
+    dec_bytes = decode_bytes_per_step(cfg, host, n_prompt, n_dec)
+    dec_gbs = dec_bytes / (sum(dec_ms) / a.steps / 1e3) / 1e9
+    pf = prefill_flops(cfg, n_prompt)
+    pre_tf = pf / (sum(pre_ms) / a.steps / 1e3) / 1e12
+    res = {
+        "metric": f"decode tokens/s ({cfg.name}-shape Llama, Q4_0 linears, batch 1, {n_dec} greedy steps after a "
+                  f"{n_prompt}-token prefill)",
+        "value": round(decode_tps, 2),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": a.steps,
+        "warmup": a.warmup,
+        "ms_per_step": round(total_ms / a.steps, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "q4_0 weights x f32 (decode GEMV), f16 x f16 -> f32 (prefill matmul)",
+        "data": "synthetic (seeded N(0,0.02) weights, uniform token ids)",
+        "config": {"workload": f"{cfg.name}: {n_prompt}-token prompt in ubatches of {n_ub}, then {n_dec} greedy "
+                               f"decode steps", "n_ctx": cfg.n_ctx, "n_ubatch": n_ub,
+                   "l2": "inputs larger than L2 (4.5 GB of weights streamed per decode step)",
+                   "parallelism": f"replicas x{world}"},
+        "prefill": {"value": round(prefill_tps, 1), "unit": "tokens/s",
+                    "achieved_tflops": round(pre_tf, 2),
+                    "roofline_frac": round(pre_tf / bf16, 4)},
+        "decode_roofline": {"bytes_per_step": dec_bytes, "achieved_gbs": round(dec_gbs, 1), "peak": hbm,
+                            "frac": round(dec_gbs / hbm, 4), "peak_source": src},
+        "roofline": {"bound": "hbm", "kernel": "gemv (weight-streaming, all decode matmuls)",
+                     "achieved": round(gemv_gbs, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(gemv_gbs / hbm, 4), "traffic": GEMV_NCU_TRAFFIC_BYTES,
+                     "peak_source": src, "launches_profiled": g["launches"],
+                     "avg_launch_us": round(g["ms"] * 1e3 / max(1, g["launches"]), 2)},
+        "roofline_prefill": {"bound": "tensor", "kernel": "gemm (prefill matmuls)", "achieved": round(gemm_tf, 2),
+                             "peak": bf16, "unit": "TFLOP/s", "frac": round(gemm_tf / bf16, 4), "traffic": None,
+                             "peak_source": src},
+        "kernel_profile": {k: {"launches": v["launches"], "ms": round(v["ms"], 3),
+                               "GBps": round(v["bytes"] / v["ms"] / 1e6, 1) if v["ms"] else None,
+                               "TFLOPps": round(v["flops"] / v["ms"] / 1e9, 2) if v["ms"] else None}
+                           for k, v in prof.items()},
+        "e2e": {"value": round(e2e_tps, 2), "unit": "tokens/s",
+                "h2d_bytes_per_step": n_prompt * 20 + n_dec * 20,
+                "d2h_bytes_per_step": 4 * (1 + n_dec),
+                "how": "lcx_decode per token with host token ids and host argmax (one sync per token)"},
+        "gpu_launches": int(launches_per_step * a.steps),
+        "clocks": clk,
+    }
+    if rank == 0:
+        try:
+            res["cpu_baseline"] = cpu_baseline(host, cfg)
+        except Exception as ex:  # the baseline is reported, not required
+            res["cpu_baseline"] = {"error": str(ex)}
+        print(json.dumps(res), flush=True)
+
+
+def run_reference(a, rank, world):
+    """The oracle as the reference arm: same workload shape and metric, bounded sample per step."""
+    if rank != 0:
+        return
+    import oracle
+    import synth
+    cfg, n_prompt, n_dec, n_ub = workload_args(a)
+    host = synth.make_model(cfg)
+    prompt = synth.prompt_tokens(cfg, 4)
+    n = oracle.set_threads()
+    om = oracle.Model(host)
+    per = 2  # decode steps per sample
+    times = []
+    for k in range(a.warmup + a.steps):
+        octx = oracle.Context(om, cfg.n_ctx, 1, n_ub)
+        rc, _, am = octx.decode(prompt)
+        tok = int(am[-1])
+        t0 = time.perf_counter()
+        for _ in range(per):
+            rc, _, am = octx.decode([tok])
+            tok = int(am[0])
+        if k >= a.warmup:
+            times.append(time.perf_counter() - t0)
+    v = a.steps * per / sum(times)
+    sample = f"{cfg.name} model, fp64 oracle: 4-token prompt then {per} decode steps per step"
+    print(json.dumps({
+        "impl": "reference", "metric": f"decode tokens/s ({cfg.name}-shape Llama, Q4_0 linears, batch 1, {n_dec} "
+                                       f"greedy steps after a {n_prompt}-token prefill)",
+        "value": round(v, 4), "unit": "tokens/s", "n_gpus": world, "steps": a.steps, "warmup": a.warmup,
+        "ms_per_step": round(1e3 * sum(times) / a.steps, 1), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,0.02) weights, uniform token ids)",
+        "config": {"workload": f"{cfg.name}: bounded sample of the decode workload", "n_ctx": cfg.n_ctx},
+        "cpu_baseline": {"value": round(v, 4), "unit": "tokens/s", "cores": n, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(v, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="lcx", choices=["lcx", "reference"])
+    ap.add_argument("--config", default="8b")
+    ap.add_argument("--prompt", type=int, default=2048)
+    ap.add_argument("--decode-steps", type=int, default=256)
+    ap.add_argument("--n-ubatch", type=int, default=512)
+    a = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1 and a.impl == "lcx":
+        import torch
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        torch.distributed.init_process_group("nccl")
+    if a.impl == "reference":
+        run_reference(a, rank, world)
+    else:
+        run_lcx(a, rank, world)
+    if world > 1 and a.impl == "lcx":
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,201 @@
+/*
+ * lcx.h -- C ABI of the GB300 Llama ubatch forward.
+ *
+ * One forward pass of a Llama-architecture decoder over one ubatch (a slice of a batch of
+ * tokens), in prefill (many tokens of a sequence) and decode (one new token per sequence),
+ * as the article "How inference works in llama.cpp" (romankryvolapov.com, llama-cpp) walks
+ * through it: token-embedding gather, then per layer RMSNorm, Q/K/V projections with
+ * block-quantized weights, RoPE, KV-cache append, causal grouped-query attention over the
+ * cache, output projection, RMSNorm and a SwiGLU feed-forward; then the final norm, the
+ * vocabulary logits and a greedy argmax.
+ *
+ * Every step runs in this library's CUDA kernels on one GPU. Pointers are plain host or
+ * device pointers; no call takes a framework type. All device work of a context is ordered on
+ * the CUDA stream given to lcx_ctx_create.
+ *
+ * Threading: a model may be shared by several contexts; a context is used by one host thread
+ * at a time.
+ */
+#ifndef LCX_H
+#define LCX_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Stored element types of weight tensors (step 4, GGUF tensor types: quantized types keep
+ * elements in fixed-size blocks that share one scale).
+ *   LCX_F16:  IEEE binary16, 2 bytes per element.
+ *   LCX_Q8_0: 34-byte blocks over 32 consecutive elements of a row: fp16 scale d (little
+ *             endian), then int8 q[32]; element value d * q.
+ *   LCX_Q4_0: 18-byte blocks over 32 elements: fp16 d, then 16 bytes; byte j holds element j
+ *             in its low nibble and element j + 16 in its high nibble; value d * (q - 8).
+ * Rows of a block-typed matrix hold ceil(K / 32) blocks; elements past K in the last block
+ * are ignored (their input is zero). */
+typedef enum { LCX_F16 = 1, LCX_Q4_0 = 2, LCX_Q8_0 = 8 } lcx_type;
+
+/* Model shape (step 5, load_hparams: n_embd, n_layer, n_ff, n_head, n_head_kv (GQA),
+ * rope_freq_base). head_dim is the per-head width (n_embd / n_head for these shapes).
+ * rms_eps is the RMSNorm epsilon; rope_theta the RoPE frequency base (frequency scale 1,
+ * no context extension). t_linear is the type of every layer matrix, t_embd of tok_embd,
+ * t_out of the output head. */
+typedef struct {
+    int32_t n_vocab, n_embd, n_layer, n_head, n_head_kv, head_dim, n_ff;
+    float rms_eps, rope_theta;
+    int32_t t_linear, t_embd, t_out;
+} lcx_hparams;
+
+/* One layer's weights as DEVICE pointers (step 5, load_arch_tensors for llama).
+ * Matrices are row-major [N][K] in stored form: row n holds the K inputs of output n.
+ *   wq [n_head*head_dim][n_embd], wk, wv [n_head_kv*head_dim][n_embd],
+ *   wo [n_embd][n_head*head_dim], w_gate, w_up [n_ff][n_embd],
+ *   w_down [n_embd][n_ff] (rows of ceil(n_ff/32) blocks).
+ * attn_norm, ffn_norm: float32 [n_embd] gains. */
+typedef struct {
+    const void *attn_norm, *wq, *wk, *wv, *wo, *ffn_norm, *w_gate, *w_up, *w_down;
+} lcx_layer_w;
+
+/* Model weights. tok_embd [n_vocab][n_embd] (t_embd), output_norm float32 [n_embd],
+ * output [n_vocab][n_embd] (t_out) or NULL: tied to tok_embd, as llama.cpp does when the file
+ * has no output matrix (step 5). layers: HOST array [n_layer] of device-pointer sets. */
+typedef struct {
+    const void *tok_embd, *output_norm, *output;
+    const lcx_layer_w *layers;
+} lcx_weights;
+
+/* A batch (step 11, llama_batch): HOST arrays of n_tokens entries.
+ *   token:  ids in [0, n_vocab).
+ *   pos:    NULL -> each token gets its sequence's last position + 1, + 2, ... in batch order.
+ *           Otherwise the positions of each sequence must continue from its last position by
+ *           +1 in batch order (a new sequence starts at 0).
+ *   seq_id: NULL -> every token belongs to sequence 0. One sequence per token.
+ *   logits: NULL -> only the last token is an output row; otherwise nonzero flags mark the
+ *           tokens whose logits are computed (step 13c, output rows). */
+typedef struct {
+    int32_t n_tokens;
+    const int32_t *token;
+    const int32_t *pos;
+    const int32_t *seq_id;
+    const int8_t *logits;
+} lcx_batch;
+
+typedef struct lcx_model lcx_model;
+typedef struct lcx_ctx lcx_ctx;
+
+/* Return codes (step 12, the return value of llama_decode). */
+enum {
+    LCX_OK = 0,
+    LCX_NO_KV_SLOT = 1,      /* the cache cannot hold the whole batch; nothing was committed */
+    LCX_ABORTED = 2,         /* the abort callback stopped the batch between ubatches */
+    LCX_INVALID = -1,        /* invalid batch or argument */
+    LCX_ALLOC_FAILED = -2,   /* device or host allocation failed */
+    LCX_COMPUTE_FAILED = -3  /* a CUDA launch or copy failed; the failed ubatch's cells are rolled back */
+};
+
+/* Builds a model over the caller's weights. The weights are BORROWED: they must stay valid
+ * until lcx_model_free. The model keeps its own device copy of every matrix re-laid out for
+ * the kernels (scale planes split from the quantized planes, Q/K/V and gate/up fused), so the
+ * caller may not change the weights afterwards without rebuilding the model.
+ * Requirements: n_embd % 64 == 0, head_dim even and <= 256, (n_head * head_dim) % 64 == 0,
+ * n_head % n_head_kv == 0, t_linear in {Q4_0, Q8_0}, t_out in {Q4_0, Q8_0} (t_embd when
+ * output is NULL), t_embd in {F16, Q8_0, Q4_0}.
+ * Returns NULL on failure with *err (if err != NULL) set to LCX_INVALID or LCX_ALLOC_FAILED.
+ * The current CUDA device at this call is the model's device. */
+lcx_model *lcx_model_create(const lcx_hparams *hp, const lcx_weights *w, int32_t *err);
+void lcx_model_free(lcx_model *model);
+
+/* Creates a context (step 10, llama_context): n_ctx cells of f16 K/V per layer shared by up
+ * to n_seq_max sequences (n_ctx is rounded up to a multiple of 256, as the context constructor
+ * does), and a workspace sized for n_ubatch tokens, reserved here so that decoding allocates
+ * nothing (the worst-case graph reservation). cuda_stream is a cudaStream_t or NULL for the
+ * default stream. Returns NULL on failure (invalid sizes, or allocation failure). */
+lcx_ctx *lcx_ctx_create(lcx_model *model, uint32_t n_ctx, uint32_t n_seq_max, uint32_t n_ubatch,
+                        void *cuda_stream);
+void lcx_ctx_free(lcx_ctx *ctx);
+
+/* Decodes a batch (step 12, llama_context::decode): validates and fills it, reserves cells
+ * for all of it (or returns LCX_NO_KV_SLOT with nothing committed), cuts it into ubatches of
+ * at most n_ubatch consecutive tokens and runs the forward over each in order. Tokens of the
+ * same ubatch see each other causally: a token attends every cell of its sequence with
+ * position <= its own, its own K/V included.
+ *   logits_out: DEVICE float32 [n_out][n_vocab] or NULL; rows are the flagged tokens in
+ *               batch order (step 14, the logits buffer).
+ *   argmax_out: host or device int32 [n_out] or NULL: the index of each row's largest logit
+ *               (lowest index on ties).
+ * Outputs are stream-ordered; when argmax_out is host memory the call synchronizes the stream
+ * before returning. Returns an LCX_* code. */
+int32_t lcx_decode(lcx_ctx *ctx, lcx_batch batch, float *logits_out, int32_t *argmax_out);
+
+/* Greedy generation on the device (the article's generation loop, step 15, with the sampler
+ * replaced by argmax): decodes `token` for sequence `seq` at its next position, then n_steps-1
+ * further single-token steps, each fed the argmax of the previous one without a host round
+ * trip. tokens_out (host or device int32 [n_steps]) receives the argmax of every step.
+ * Reserves all n_steps cells first (LCX_NO_KV_SLOT if they do not fit). */
+int32_t lcx_decode_greedy(lcx_ctx *ctx, int32_t seq, int32_t token, int32_t n_steps, int32_t *tokens_out);
+
+/* Frees every cell (the memory clear of the KV-cache section): every sequence becomes empty. */
+void lcx_kv_clear(lcx_ctx *ctx);
+
+/* The last position stored for `seq`, or -1 if it has none or seq is out of range. */
+int32_t lcx_seq_pos_max(const lcx_ctx *ctx, int32_t seq);
+
+/* Output rows written by the last lcx_decode (0 after a failed one). */
+int32_t lcx_n_outputs(const lcx_ctx *ctx);
+
+/* Abort callback (step 12, abort -> 2): called on the host before every ubatch after the
+ * first; a nonzero return stops the batch with LCX_ABORTED. Earlier ubatches stay in the cache;
+ * the cells of the stopped and later ubatches are released. cb NULL removes it. */
+void lcx_set_abort(lcx_ctx *ctx, int (*cb)(void *), void *user_data);
+
+/* Counters of a context, for tests and measurement. */
+typedef struct {
+    int64_t n_decode;          /* lcx_decode / lcx_decode_greedy calls that ran */
+    int64_t n_ubatch;          /* ubatches run in total */
+    int32_t n_ubatch_last;     /* ubatches of the last call */
+    int32_t n_outputs_last;    /* output rows of the last call */
+    int64_t n_kernels;         /* kernel launches issued by this context */
+    int64_t n_cells_used;      /* cells currently holding K/V */
+    uint32_t n_ctx;            /* cells in the cache (after rounding) */
+    uint32_t n_pages;          /* KV pages allocated (page = 64 cells of one sequence) */
+} lcx_stats;
+void lcx_get_stats(const lcx_ctx *ctx, lcx_stats *out);
+
+/* Per-kernel-class timing, for measurement. With profiling on, every kernel the context
+ * launches is bracketed by CUDA events on its stream and credited to a class with the
+ * algorithmic bytes and flops of that launch (weight and activation bytes as stored, KV bytes
+ * of the attended cells, 2 flops per multiply-add). Classes: gemv = weight-streaming matmuls
+ * of small ubatches, gemm = matmuls of large ubatches, attention, other (gather, norms, argmax).
+ * lcx_set_profiling(ctx, 1) clears the counters; lcx_get_profile synchronizes the stream and
+ * returns the totals since then. Profiling adds event records between launches. */
+typedef struct {
+    int64_t launches;
+    double ms, bytes, flops;
+} lcx_kernel_profile;
+typedef struct {
+    lcx_kernel_profile gemv, gemm, attention, other;
+} lcx_profile;
+int32_t lcx_set_profiling(lcx_ctx *ctx, int32_t on);
+int32_t lcx_get_profile(lcx_ctx *ctx, lcx_profile *out);
+
+/* A context with no device: every host-side rule of lcx_decode (validation, position and
+ * flag filling, cell reservation, ubatch split, abort, return codes) runs, and no kernel is
+ * launched; logits_out must be NULL and argmax_out is left untouched. For testing the host
+ * runtime on machines without a GPU. */
+lcx_ctx *lcx_ctx_create_host_only(const lcx_hparams *hp, uint32_t n_ctx, uint32_t n_seq_max, uint32_t n_ubatch);
+
+/* Row gather with dequantisation to float32 (step 13b, ggml_get_rows on the token
+ * embeddings): out[i][:] = the n_cols values of row ids[i] of `table` (stored type `type`).
+ * ids and out are DEVICE pointers; runs on cuda_stream. Returns LCX_OK or LCX_INVALID /
+ * LCX_COMPUTE_FAILED. */
+int32_t lcx_get_rows(int32_t type, const void *table, int64_t n_rows, int64_t n_cols, const int32_t *ids, int32_t n,
+                     float *out, void *cuda_stream);
+
+/* Last CUDA error string seen by the library in this process ("" if none). */
+const char *lcx_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LCX_H */

@@ -1,0 +1,224 @@
+"""Python binding of liblcx (include/lcx.h): argument marshalling only.
+
+Every step of the forward runs in the library's CUDA kernels; this module loads the in-tree
+shared library, mirrors the C structs with ctypes and wraps the calls under the same names.
+PyTorch, when used by callers, only provides device memory and streams.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "liblcx.so")
+_lib = None
+
+LCX_F16, LCX_Q4_0, LCX_Q8_0 = 1, 2, 8
+LCX_OK, LCX_NO_KV_SLOT, LCX_ABORTED = 0, 1, 2
+LCX_INVALID, LCX_ALLOC_FAILED, LCX_COMPUTE_FAILED = -1, -2, -3
+
+SYMBOLS = ("lcx_model_create", "lcx_model_free", "lcx_ctx_create", "lcx_ctx_free", "lcx_decode",
+           "lcx_decode_greedy", "lcx_kv_clear", "lcx_seq_pos_max", "lcx_n_outputs", "lcx_set_abort",
+           "lcx_get_stats", "lcx_ctx_create_host_only", "lcx_get_rows", "lcx_last_error", "lcx_set_profiling",
+           "lcx_get_profile")
+
+
+def build(force: bool = False) -> str:
+    from . import buildlib as _b
+    return _b.build(force=force)
+
+
+class lcx_hparams(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("n_vocab", "n_embd", "n_layer", "n_head", "n_head_kv",
+                                               "head_dim", "n_ff")] + \
+               [("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float)] + \
+               [(n, ctypes.c_int32) for n in ("t_linear", "t_embd", "t_out")]
+
+
+class lcx_layer_w(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("attn_norm", "wq", "wk", "wv", "wo", "ffn_norm", "w_gate",
+                                                "w_up", "w_down")]
+
+
+class lcx_weights(ctypes.Structure):
+    _fields_ = [("tok_embd", ctypes.c_void_p), ("output_norm", ctypes.c_void_p), ("output", ctypes.c_void_p),
+                ("layers", ctypes.POINTER(lcx_layer_w))]
+
+
+class lcx_batch(ctypes.Structure):
+    _fields_ = [("n_tokens", ctypes.c_int32), ("token", ctypes.c_void_p), ("pos", ctypes.c_void_p),
+                ("seq_id", ctypes.c_void_p), ("logits", ctypes.c_void_p)]
+
+
+class lcx_stats(ctypes.Structure):
+    _fields_ = [("n_decode", ctypes.c_int64), ("n_ubatch", ctypes.c_int64), ("n_ubatch_last", ctypes.c_int32),
+                ("n_outputs_last", ctypes.c_int32), ("n_kernels", ctypes.c_int64), ("n_cells_used", ctypes.c_int64),
+                ("n_ctx", ctypes.c_uint32), ("n_pages", ctypes.c_uint32)]
+
+
+class lcx_kernel_profile(ctypes.Structure):
+    _fields_ = [("launches", ctypes.c_int64), ("ms", ctypes.c_double), ("bytes", ctypes.c_double),
+                ("flops", ctypes.c_double)]
+
+
+class lcx_profile(ctypes.Structure):
+    _fields_ = [(n, lcx_kernel_profile) for n in ("gemv", "gemm", "attention", "other")]
+
+
+ABORT_CB = ctypes.CFUNCTYPE(ctypes.c_int, ctypes.c_void_p)
+
+
+def lib():
+    """The loaded library; raises if the CUDA extension has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"liblcx is not built ({LIB_PATH} missing): call llama_ubatch_forward_gb300.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i32, u32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_uint32, ctypes.c_int64
+        L.lcx_model_create.restype = vp
+        L.lcx_model_create.argtypes = [ctypes.POINTER(lcx_hparams), ctypes.POINTER(lcx_weights), ctypes.POINTER(i32)]
+        L.lcx_model_free.argtypes = [vp]
+        L.lcx_ctx_create.restype = vp
+        L.lcx_ctx_create.argtypes = [vp, u32, u32, u32, vp]
+        L.lcx_ctx_create_host_only.restype = vp
+        L.lcx_ctx_create_host_only.argtypes = [ctypes.POINTER(lcx_hparams), u32, u32, u32]
+        L.lcx_ctx_free.argtypes = [vp]
+        L.lcx_decode.restype = i32
+        L.lcx_decode.argtypes = [vp, lcx_batch, vp, vp]
+        L.lcx_decode_greedy.restype = i32
+        L.lcx_decode_greedy.argtypes = [vp, i32, i32, i32, vp]
+        L.lcx_kv_clear.argtypes = [vp]
+        L.lcx_seq_pos_max.restype = i32
+        L.lcx_seq_pos_max.argtypes = [vp, i32]
+        L.lcx_n_outputs.restype = i32
+        L.lcx_n_outputs.argtypes = [vp]
+        L.lcx_set_abort.argtypes = [vp, ABORT_CB, vp]
+        L.lcx_get_stats.argtypes = [vp, ctypes.POINTER(lcx_stats)]
+        L.lcx_get_rows.restype = i32
+        L.lcx_get_rows.argtypes = [i32, vp, i64, i64, vp, i32, vp, vp]
+        L.lcx_last_error.restype = ctypes.c_char_p
+        L.lcx_set_profiling.restype = i32
+        L.lcx_set_profiling.argtypes = [vp, i32]
+        L.lcx_get_profile.restype = i32
+        L.lcx_get_profile.argtypes = [vp, ctypes.POINTER(lcx_profile)]
+        _lib = L
+    return _lib
+
+
+def _ptr(a):
+    """Data pointer of a numpy array / torch tensor / int / None."""
+    if a is None:
+        return None
+    if isinstance(a, int):
+        return a
+    if hasattr(a, "data_ptr"):
+        return a.data_ptr()
+    return a.ctypes.data
+
+
+def make_batch(tokens, pos=None, seq_id=None, logits=None):
+    """An lcx_batch over host numpy int32/int8 arrays (kept alive by the returned tuple)."""
+    import numpy as np
+    keep = [np.ascontiguousarray(tokens, dtype=np.int32)]
+    b = lcx_batch(keep[0].size, keep[0].ctypes.data, None, None, None)
+    if pos is not None:
+        keep.append(np.ascontiguousarray(pos, dtype=np.int32)); b.pos = keep[-1].ctypes.data
+    if seq_id is not None:
+        keep.append(np.ascontiguousarray(seq_id, dtype=np.int32)); b.seq_id = keep[-1].ctypes.data
+    if logits is not None:
+        keep.append(np.ascontiguousarray(logits, dtype=np.int8)); b.logits = keep[-1].ctypes.data
+    return b, keep
+
+
+class Model:
+    """lcx_model over device weights. `weights` maps names to objects with data_ptr() (device);
+    they must outlive the model (the library borrows them)."""
+
+    def __init__(self, hp: lcx_hparams, tok_embd, output_norm, output, layers: list[dict]):
+        self.hp = hp
+        self._keep = (tok_embd, output_norm, output, layers)
+        arr = (lcx_layer_w * len(layers))()
+        for i, L in enumerate(layers):
+            arr[i] = lcx_layer_w(*[_ptr(L[n]) for n in ("attn_norm", "wq", "wk", "wv", "wo", "ffn_norm",
+                                                         "w_gate", "w_up", "w_down")])
+        self._arr = arr
+        w = lcx_weights(_ptr(tok_embd), _ptr(output_norm), _ptr(output), arr)
+        err = ctypes.c_int32(0)
+        self.h = lib().lcx_model_create(ctypes.byref(hp), ctypes.byref(w), ctypes.byref(err))
+        if not self.h:
+            raise RuntimeError(f"lcx_model_create failed ({err.value}): {lib().lcx_last_error().decode()}")
+
+    def close(self):
+        if getattr(self, "h", None):
+            lib().lcx_model_free(self.h)
+            self.h = None
+
+    __del__ = close
+
+
+class Context:
+    def __init__(self, model: Model | None, n_ctx: int, n_seq_max: int = 1, n_ubatch: int = 512, stream=None,
+                 host_only_hp: lcx_hparams | None = None):
+        self.model = model
+        if model is None:
+            self.h = lib().lcx_ctx_create_host_only(ctypes.byref(host_only_hp), n_ctx, n_seq_max, n_ubatch)
+            self.n_vocab = host_only_hp.n_vocab
+        else:
+            s = None if stream is None else (stream if isinstance(stream, int) else stream.cuda_stream)
+            self.h = lib().lcx_ctx_create(model.h, n_ctx, n_seq_max, n_ubatch, s)
+            self.n_vocab = model.hp.n_vocab
+        if not self.h:
+            raise RuntimeError(f"lcx_ctx_create failed: {lib().lcx_last_error().decode()}")
+        self._abort = None
+
+    def close(self):
+        if getattr(self, "h", None):
+            lib().lcx_ctx_free(self.h)
+            self.h = None
+
+    __del__ = close
+
+    def decode(self, tokens, pos=None, seq_id=None, logits=None, logits_out=None, argmax_out=None) -> int:
+        b, keep = make_batch(tokens, pos, seq_id, logits)
+        return lib().lcx_decode(self.h, b, _ptr(logits_out), _ptr(argmax_out))
+
+    def decode_greedy(self, seq: int, token: int, n_steps: int, tokens_out) -> int:
+        return lib().lcx_decode_greedy(self.h, seq, token, n_steps, _ptr(tokens_out))
+
+    def kv_clear(self):
+        lib().lcx_kv_clear(self.h)
+
+    def seq_pos_max(self, seq: int) -> int:
+        return lib().lcx_seq_pos_max(self.h, seq)
+
+    def n_outputs(self) -> int:
+        return lib().lcx_n_outputs(self.h)
+
+    def set_abort(self, fn):
+        """fn() -> bool, called before every ubatch after the first; None removes it."""
+        if fn is None:
+            self._abort = None
+            lib().lcx_set_abort(self.h, ABORT_CB(0), None)
+            return
+        self._abort = ABORT_CB(lambda _ud: 1 if fn() else 0)
+        lib().lcx_set_abort(self.h, self._abort, None)
+
+    def set_profiling(self, on: bool) -> int:
+        return lib().lcx_set_profiling(self.h, 1 if on else 0)
+
+    def profile(self) -> dict:
+        p = lcx_profile()
+        lib().lcx_get_profile(self.h, ctypes.byref(p))
+        return {n: {"launches": getattr(p, n).launches, "ms": getattr(p, n).ms, "bytes": getattr(p, n).bytes,
+                    "flops": getattr(p, n).flops} for n in ("gemv", "gemm", "attention", "other")}
+
+    def stats(self) -> lcx_stats:
+        s = lcx_stats()
+        lib().lcx_get_stats(self.h, ctypes.byref(s))
+        return s
+
+
+def get_rows(qtype: int, table, n_rows: int, n_cols: int, ids, out, stream=None) -> int:
+    s = None if stream is None else (stream if isinstance(stream, int) else stream.cuda_stream)
+    return lib().lcx_get_rows(qtype, _ptr(table), n_rows, n_cols, _ptr(ids), int(ids.numel()), _ptr(out), s)

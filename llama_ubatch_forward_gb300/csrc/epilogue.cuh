@@ -1,0 +1,87 @@
+// Epilogues shared by the weight-streaming GEMV and the tensor-core GEMM.
+//
+// A "quad" is 4 consecutive internal rows (outputs) of one token. The QKV epilogue applies
+// RoPE to adjacent pairs (2i, 2i+1) of Q and K -- the rotation of the article's per-layer
+// graph, read as the "normal" (adjacent-pair) llama mode -- and appends K and V to the cache
+// as f16 (KV-cache section: the new token's K/V are stored before attention reads them).
+#pragma once
+#include "lcx_internal.h"
+
+namespace lcx {
+
+__device__ __forceinline__ unsigned long long argmax_key(float v, int idx) {
+    uint32_t b = __float_as_uint(v);
+    b = (b & 0x80000000u) ? ~b : (b | 0x80000000u);   // order-preserving map of float bits
+    return ((unsigned long long)b << 32) | (unsigned long long)(0xffffffffu - (uint32_t)idx);
+}
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
+
+// cache address of (layer, cell, kv head, dim) in [L][n_pages][KV][kPage][hd]
+__device__ __forceinline__ size_t kv_off(const FwdArgs &a, int layer, int cell, int kvh, int dim) {
+    int page = cell / kPage, slot = cell % kPage;
+    return ((((size_t)layer * a.n_pages + page) * a.KV + kvh) * kPage + slot) * a.hd + dim;
+}
+
+// Epilogue of 4 consecutive rows r0..r0+3 (r0 % 4 == 0) of token t.
+template <int EPI>
+__device__ __forceinline__ void epi_quad(const FwdArgs &a, int layer, int t, int r0, int N, const float v[4],
+                                         unsigned long long &best) {
+    if (EPI == EPI_RESID) {
+        float *xr = a.x + (size_t)t * a.d;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (r0 + j < N) xr[r0 + j] += v[j];
+    } else if (EPI == EPI_LOGITS) {
+        float *lr = a.logits + (size_t)t * a.V;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (r0 + j < N) {
+                lr[r0 + j] = v[j];
+                unsigned long long k = argmax_key(v[j], r0 + j);
+                best = k > best ? k : best;
+            }
+    } else if (EPI == EPI_QKV) {
+        const int qw = a.H * a.hd, kw = a.KV * a.hd;
+        const int pos = a.ub.pos[t];
+#pragma unroll
+        for (int p = 0; p < 2; ++p) {
+            const int r = r0 + 2 * p;
+            if (r >= qw + 2 * kw) break;
+            float y0 = v[2 * p], y1 = v[2 * p + 1];
+            if (r < qw + kw) {   // q or k: rotate the pair
+                const int dim = r < qw ? r % a.hd : (r - qw) % a.hd;
+                const float2 cs = a.rope[(size_t)pos * (a.hd / 2) + dim / 2];
+                const float z0 = y0 * cs.x - y1 * cs.y, z1 = y0 * cs.y + y1 * cs.x;
+                y0 = z0;
+                y1 = z1;
+            }
+            if (r < qw) {
+                float *qr = a.q + (size_t)t * qw + r;
+                qr[0] = y0;
+                qr[1] = y1;
+            } else {
+                const bool isk = r < qw + kw;
+                const int rr = isk ? r - qw : r - qw - kw;
+                const int kvh = rr / a.hd, dim = rr % a.hd;
+                __half *dst = (isk ? a.kc : a.vc) + kv_off(a, layer, a.ub.cell[t], kvh, dim);
+                *reinterpret_cast<__half2 *>(dst) = __floats2half2_rn(y0, y1);
+            }
+        }
+    }
+}
+
+// SwiGLU epilogue: features f0..f0+3 of token t from gate g[4] and up u[4].
+template <bool OUT16>
+__device__ __forceinline__ void epi_swiglu(const FwdArgs &a, int t, int f0, const float g[4], const float u[4]) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int f = f0 + j;
+        if (f >= a.F) break;
+        const float h = silu_f(g[j]) * u[j];
+        if (OUT16) a.h16[(size_t)t * a.F_pad + f] = __float2half_rn(h);
+        else a.h32[(size_t)t * a.F_pad + f] = h;
+    }
+}
+
+}  // namespace lcx

@@ -1,0 +1,172 @@
+// Small kernels of the forward: weight re-layout, RoPE table, token-embedding gather,
+// RMSNorm to f16 (tensor-core path), argmax finalisation, row gather.
+#include "lcx_internal.h"
+
+namespace lcx {
+
+// ------------------------------------------------------------------ stored-block reads
+__device__ __forceinline__ float half_bits_to_float(uint16_t b) { return __half2float(__ushort_as_half(b)); }
+
+// value of element i of a stored row (F16, Q8_0 or Q4_0); exact in f32 for every type
+__device__ __forceinline__ float stored_elem(int type, const uint8_t *row, int64_t i) {
+    if (type == QF16) {
+        const uint8_t *p = row + 2 * i;
+        return half_bits_to_float((uint16_t)(p[0] | (p[1] << 8)));
+    }
+    int64_t b = i >> 5;
+    int e = (int)(i & 31);
+    if (type == Q8) {
+        const uint8_t *blk = row + b * 34;
+        float d = half_bits_to_float((uint16_t)(blk[0] | (blk[1] << 8)));
+        return d * (float)(int8_t)blk[2 + e];
+    }
+    const uint8_t *blk = row + b * 18;
+    float d = half_bits_to_float((uint16_t)(blk[0] | (blk[1] << 8)));
+    int q = e < 16 ? (blk[2 + e] & 15) : (blk[2 + e - 16] >> 4);
+    return d * (float)(q - 8);
+}
+
+__host__ __device__ inline int64_t stored_row_bytes(int type, int64_t k) {
+    return type == QF16 ? 2 * k : ((k + 31) / 32) * (type == Q8 ? 34 : 18);
+}
+
+// ------------------------------------------------------------------ repack
+// One thread per (source row, block): copies the block's quant bytes into the qs plane and
+// its scale into the scale plane at the destination row. gateup_chunked maps source row r of
+// the gate (row_offset 0) or up (row_offset 128) matrix to (r / 128) * 256 + row_offset + r % 128.
+__global__ void k_repack(const uint8_t *__restrict__ src, int type, int N_src, int nb_src, uint8_t *__restrict__ qs,
+                         __half *__restrict__ sc, int nb_dst, int row_offset, int gateup_chunked) {
+    int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= (int64_t)N_src * nb_src) return;
+    int r = (int)(idx / nb_src), b = (int)(idx % nb_src);
+    int dr = gateup_chunked ? (r / kRowTile) * (2 * kRowTile) + row_offset + (r % kRowTile) : r + row_offset;
+    const int bb = type == Q8 ? 34 : 18, qb = type == Q8 ? 32 : 16;
+    const uint8_t *blk = src + ((int64_t)r * nb_src + b) * bb;
+    uint8_t *dq = qs + ((int64_t)dr * nb_dst + b) * qb;
+    for (int i = 0; i < qb; ++i) dq[i] = blk[2 + i];
+    uint16_t dbits = (uint16_t)(blk[0] | (blk[1] << 8));
+    sc[((int64_t)(dr >> 2) * nb_dst + b) * 4 + (dr & 3)] = __ushort_as_half(dbits);
+}
+
+cudaError_t launch_repack(const void *src, int type, int N_src, int nb_src, QMat &dst, int row_offset,
+                          int gateup_chunked, cudaStream_t s) {
+    int64_t n = (int64_t)N_src * nb_src;
+    int threads = 256;
+    int64_t blocks = (n + threads - 1) / threads;
+    k_repack<<<(unsigned)blocks, threads, 0, s>>>((const uint8_t *)src, type, N_src, nb_src, dst.qs, dst.sc, dst.nb,
+                                                 row_offset, gateup_chunked);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ RoPE table
+// tab[p][i] = (cos, sin)(p * theta^(-2i/hd)), evaluated in double and rounded to float.
+__global__ void k_rope_table(float2 *tab, int n_pos, int hd, double theta) {
+    int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    int half_hd = hd / 2;
+    if (idx >= (int64_t)n_pos * half_hd) return;
+    int p = (int)(idx / half_hd), i = (int)(idx % half_hd);
+    double freq = pow(theta, -2.0 * (double)i / (double)hd);
+    double sn, cs;
+    sincos((double)p * freq, &sn, &cs);
+    tab[idx] = make_float2((float)cs, (float)sn);
+}
+
+cudaError_t launch_rope_table(float2 *tab, int n_pos, int hd, double theta, cudaStream_t s) {
+    int64_t n = (int64_t)n_pos * (hd / 2);
+    k_rope_table<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(tab, n_pos, hd, theta);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ embedding gather
+// Block t: x[t][:] = dequant(tok_embd[token t]). Block 0 also applies the ubatch's page-table
+// updates and clears the argmax keys of its output rows (both are read only by later kernels).
+__global__ void k_embed(const uint8_t *__restrict__ table, int type, int d, const int32_t *__restrict__ tok, float *x,
+                        const int32_t *__restrict__ pt_upd, int n_upd, int32_t *pt, unsigned long long *keys,
+                        int n_out) {
+    const int t = blockIdx.x;
+    const int id = tok[t];
+    const uint8_t *row = table + (int64_t)id * stored_row_bytes(type, d);
+    for (int i = threadIdx.x; i < d; i += blockDim.x) x[(int64_t)t * d + i] = stored_elem(type, row, i);
+    if (t == 0) {
+        for (int u = threadIdx.x; u < n_upd; u += blockDim.x) pt[pt_upd[2 * u]] = pt_upd[2 * u + 1];
+        for (int r = threadIdx.x; r < n_out; r += blockDim.x) keys[r] = 0ull;
+    }
+}
+
+cudaError_t launch_embed(const FwdArgs &a, int t_embd, const void *tok_embd, cudaStream_t s, int64_t &launches) {
+    k_embed<<<a.T, 256, 0, s>>>((const uint8_t *)tok_embd, t_embd, a.d, a.tok_src, a.x, a.ub.pt_upd, a.ub.n_upd, a.pt,
+                                a.amax_key, a.n_out);
+    ++launches;
+    return cudaGetLastError();
+}
+
+__global__ void k_get_rows(const uint8_t *__restrict__ table, int type, int64_t n_cols, const int32_t *__restrict__ ids,
+                           float *__restrict__ out) {
+    const int i = blockIdx.x;
+    const uint8_t *row = table + (int64_t)ids[i] * stored_row_bytes(type, n_cols);
+    for (int64_t c = threadIdx.x; c < n_cols; c += blockDim.x) out[(int64_t)i * n_cols + c] = stored_elem(type, row, c);
+}
+
+cudaError_t launch_get_rows(int type, const void *table, int64_t n_cols, const int32_t *ids, int n, float *out,
+                            cudaStream_t s) {
+    if (n <= 0) return cudaSuccess;
+    k_get_rows<<<n, 256, 0, s>>>((const uint8_t *)table, type, n_cols, ids, out);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ RMSNorm -> f16
+// out[r][:] = f16(x[row r] / sqrt(mean(x^2) + eps) * g); row r of x is rows[r] (or r).
+__global__ void k_rmsnorm_h(const float *__restrict__ x, const int32_t *__restrict__ rows, int d,
+                            const float *__restrict__ g, float eps, __half *__restrict__ out) {
+    const int r = blockIdx.x;
+    const float *xr = x + (int64_t)(rows ? rows[r] : r) * d;
+    float ss = 0.f;
+    for (int i = threadIdx.x * 4; i < d; i += blockDim.x * 4) {
+        float4 v = *reinterpret_cast<const float4 *>(xr + i);
+        ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+    }
+    __shared__ float red[32];
+    for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
+        for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (threadIdx.x == 0) red[0] = v;
+    }
+    __syncthreads();
+    const float rs = 1.0f / sqrtf(red[0] / (float)d + eps);
+    __half *orow = out + (int64_t)r * d;
+    for (int i = threadIdx.x * 4; i < d; i += blockDim.x * 4) {
+        float4 v = *reinterpret_cast<const float4 *>(xr + i);
+        float4 gg = *reinterpret_cast<const float4 *>(g + i);
+        __half2 a = __floats2half2_rn(v.x * rs * gg.x, v.y * rs * gg.y);
+        __half2 b = __floats2half2_rn(v.z * rs * gg.z, v.w * rs * gg.w);
+        *reinterpret_cast<__half2 *>(orow + i) = a;
+        *reinterpret_cast<__half2 *>(orow + i + 2) = b;
+    }
+}
+
+cudaError_t launch_rmsnorm_h(const float *x, const int32_t *rows, int T, int d, const float *g, float eps,
+                             __half *out, cudaStream_t s, int64_t &launches) {
+    k_rmsnorm_h<<<T, 256, 0, s>>>(x, rows, d, g, eps, out);
+    ++launches;
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ argmax
+// keys hold (ordered float bits << 32) | (0xffffffff - index): the max key is the largest
+// logit, ties to the lowest index.
+__global__ void k_argmax_final(const unsigned long long *__restrict__ keys, int n, int32_t *__restrict__ dst) {
+    int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n) dst[i] = (int32_t)(0xffffffffu - (uint32_t)(keys[i] & 0xffffffffull));
+}
+
+cudaError_t launch_argmax_final(const FwdArgs &a, int32_t *dst, cudaStream_t s, int64_t &launches) {
+    if (a.n_out <= 0) return cudaSuccess;
+    k_argmax_final<<<(a.n_out + 127) / 128, 128, 0, s>>>(a.amax_key, a.n_out, dst);
+    ++launches;
+    return cudaGetLastError();
+}
+
+}  // namespace lcx

@@ -1,0 +1,119 @@
+// Internal declarations shared by the lcx library's translation units (host runtime and
+// kernels). Not part of the public ABI (include/lcx.h).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace lcx {
+
+constexpr int kPage = 64;            // KV cells per page (all of one sequence)
+constexpr int kRowTile = 128;        // internal row padding of every matrix (tensor-core M tile)
+constexpr int kGemvMaxT = 8;         // largest ubatch the weight-streaming GEMV serves
+constexpr int kGemvSmemX = 160 * 1024;  // bytes of staged activations a GEMV CTA may hold
+
+enum QType { QF16 = 1, Q4 = 2, Q8 = 8 };
+
+// A weight matrix re-laid out for the kernels: N_pad rows of nb 32-element blocks.
+//   qs:  [N_pad][nb][16 B] (Q4_0 nibbles, GGUF order kept) or [N_pad][nb][32 B] (Q8_0 int8)
+//   sc:  [N_pad/4][nb][4] fp16 scales: the scales of 4 consecutive rows for one block are
+//        adjacent, so one 8-byte load brings a row quad's scales.
+// Rows >= N and blocks past the stored ones are zero (scale 0).
+struct QMat {
+    int type = 0;
+    int N = 0, N_pad = 0;   // logical and padded rows
+    int K = 0, nb = 0;      // padded input width (nb * 32) and blocks per row
+    uint8_t *qs = nullptr;
+    __half *sc = nullptr;
+    size_t qs_row_bytes() const { return (size_t)nb * (type == Q4 ? 16 : 32); }
+    size_t bytes() const { return (size_t)N_pad * qs_row_bytes() + (size_t)N_pad * nb * 2; }
+};
+
+struct DevLayer {
+    const float *attn_norm, *ffn_norm;
+    QMat qkv;      // rows [Wq; Wk; Wv]
+    QMat wo;
+    QMat gateup;   // chunks of 128 rows: gate rows c*128.., then up rows c*128.. (F padded to 128)
+    QMat down;     // K = F padded to 128
+};
+
+// Epilogue kinds shared by the GEMV and the GEMM.
+enum Epi { EPI_QKV = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_LOGITS = 3 };
+
+// Per-ubatch device metadata (one contiguous block, uploaded with one copy).
+struct UbDev {
+    const int32_t *tok;      // [T] token ids (or NULL: take the previous step's argmax)
+    const int32_t *pos;      // [T]
+    const int32_t *seq;      // [T]
+    const int32_t *cell;     // [T] flat cell = page * kPage + slot
+    const int32_t *out_rows; // [n_out] indices of flagged tokens within the ubatch
+    const int32_t *pt_upd;   // [n_upd][2] (flat page-table index, page)
+    int32_t n_upd;
+};
+
+// Everything a forward launch needs (device pointers).
+struct FwdArgs {
+    // shape
+    int d, H, KV, hd, F, F_pad, V, L;
+    float eps;
+    // metadata
+    int T, n_out;
+    UbDev ub;
+    const int32_t *tok_src;      // where the embed kernel reads token ids
+    // activations
+    float *x;          // [T][d] residual stream
+    __half *xh;        // [T][d] normed activations (GEMM path)
+    float *q;          // [T][H*hd]
+    float *o32;        // [T][H*hd]
+    __half *o16;       // [T][H*hd]
+    float *h32;        // [T][F_pad]
+    __half *h16;       // [T][F_pad]
+    float *logits;     // [n_out][V]
+    unsigned long long *amax_key;  // [n_out]
+    int32_t *amax_out; // [n_out] device
+    // attention scratch
+    float *att_part;   // partial (m, l, acc[hd]) per (token, q head, split)
+    int32_t *att_cnt;  // [T][KV] arrival counters, zero between launches
+    int att_max_split;
+    // KV cache
+    __half *kc, *vc;   // [L][n_pages][KV][kPage][hd]
+    int n_pages;
+    int32_t *pt;       // [n_seq_max][max_pages_per_seq]
+    int max_pages_per_seq;
+    const float2 *rope; // [n_ctx][hd/2] (cos, sin)
+};
+
+// ---------------------------------------------------------------- launchers (kernels *.cu)
+// All return cudaGetLastError() after the launch(es); `launches` counts kernels issued.
+cudaError_t launch_repack(const void *src, int type, int N_src, int nb_src, QMat &dst, int row_offset,
+                          int gateup_chunked, cudaStream_t s);
+cudaError_t launch_rope_table(float2 *tab, int n_pos, int hd, double theta, cudaStream_t s);
+cudaError_t launch_embed(const FwdArgs &a, int t_embd, const void *tok_embd, cudaStream_t s, int64_t &launches);
+cudaError_t launch_get_rows(int type, const void *table, int64_t n_cols, const int32_t *ids, int n, float *out,
+                            cudaStream_t s);
+cudaError_t launch_rmsnorm_h(const float *x, const int32_t *rows, int T, int d, const float *g, float eps,
+                             __half *out, cudaStream_t s, int64_t &launches);
+cudaError_t launch_argmax_final(const FwdArgs &a, int32_t *dst, cudaStream_t s, int64_t &launches);
+
+// y = W x for T <= kGemvMaxT tokens with the given epilogue; x rows are read from `x`
+// (rows `x_rows` if not NULL), normalised with gains `g` when g != NULL.
+struct GemvIn {
+    const float *x;
+    const int32_t *x_rows;
+    const float *g;
+};
+cudaError_t launch_gemv(const QMat &W, Epi epi, int T, const GemvIn &in, const FwdArgs &a, int layer,
+                        cudaStream_t s, int64_t &launches);
+bool gemv_fits(const QMat &W, int T);
+
+// GEMM for larger T: A = f16 activations [T][K]
+cudaError_t launch_gemm(const QMat &W, Epi epi, int T, const __half *A, const FwdArgs &a, int layer,
+                        cudaStream_t s, int64_t &launches);
+
+// attention over the cache for every token of the ubatch; writes o32 (f32) or o16
+cudaError_t launch_attention(const FwdArgs &a, int layer, int max_natt, bool out_f16, cudaStream_t s,
+                             int64_t &launches);
+int attention_splits(const FwdArgs &a, int max_natt, int *chunk);
+
+}  // namespace lcx

