@@ -192,6 +192,29 @@ lcx_ctx *lcx_ctx_create_host_only(const lcx_hparams *hp, uint32_t n_ctx, uint32_
 int32_t lcx_get_rows(int32_t type, const void *table, int64_t n_rows, int64_t n_cols, const int32_t *ids, int32_t n,
                      float *out, void *cuda_stream);
 
+/* The attention step of the forward (step 13c: scores of Q against the cached keys, causal
+ * mask, softmax, weighted sum of the cached values; KV-cache section: a token attends the
+ * cells of its sequence up to and including its own position) over caller-owned buffers of
+ * ONE layer, with the split-K kernel lcx_decode uses.
+ *   q:          DEVICE float32 [T][n_head * head_dim], RoPE already applied.
+ *   k_cache,
+ *   v_cache:    DEVICE f16 [n_pages][n_head_kv][64][head_dim]: page p holds 64 consecutive
+ *               positions of one sequence.
+ *   page_table: DEVICE int32 [n_seq][max_pages]: page ids of each sequence in position order.
+ *   pos, seq:   DEVICE int32 [T]: token t attends positions 0..pos[t] of sequence seq[t].
+ *   max_pos:    host upper bound of pos[] (sizes the split of the cell range).
+ *   out:        DEVICE float32 [T][n_head * head_dim].
+ *   workspace:  DEVICE scratch of at least lcx_attention_workspace_size(T, n_head, n_head_kv,
+ *               head_dim, max_pos) bytes (may be NULL when that size is 0); it is cleared by
+ *               the call as needed, and two calls sharing one workspace must not overlap.
+ * head_dim 64 or 128; n_head / n_head_kv in {1, 2, 4, 8}. Stream-ordered on cuda_stream.
+ * Returns LCX_OK, LCX_INVALID (bad sizes or a small workspace) or LCX_COMPUTE_FAILED. */
+size_t lcx_attention_workspace_size(int32_t T, int32_t n_head, int32_t n_head_kv, int32_t head_dim, int32_t max_pos);
+int32_t lcx_attention(int32_t T, int32_t n_head, int32_t n_head_kv, int32_t head_dim, const float *q,
+                      const void *k_cache, const void *v_cache, int32_t n_pages, const int32_t *page_table,
+                      int32_t max_pages, const int32_t *pos, const int32_t *seq, int32_t max_pos, float *out,
+                      void *workspace, size_t workspace_bytes, void *cuda_stream);
+
 /* Last CUDA error string seen by the library in this process ("" if none). */
 const char *lcx_last_error(void);
 

@@ -20,7 +20,7 @@ LCX_INVALID, LCX_ALLOC_FAILED, LCX_COMPUTE_FAILED = -1, -2, -3
 SYMBOLS = ("lcx_model_create", "lcx_model_free", "lcx_ctx_create", "lcx_ctx_free", "lcx_decode",
            "lcx_decode_greedy", "lcx_kv_clear", "lcx_seq_pos_max", "lcx_n_outputs", "lcx_set_abort",
            "lcx_get_stats", "lcx_ctx_create_host_only", "lcx_get_rows", "lcx_last_error", "lcx_set_profiling",
-           "lcx_get_profile")
+           "lcx_get_profile", "lcx_attention_workspace_size", "lcx_attention")
 
 
 def build(force: bool = False) -> str:
@@ -98,6 +98,11 @@ def lib():
         L.lcx_get_rows.restype = i32
         L.lcx_get_rows.argtypes = [i32, vp, i64, i64, vp, i32, vp, vp]
         L.lcx_last_error.restype = ctypes.c_char_p
+        L.lcx_attention_workspace_size.restype = ctypes.c_size_t
+        L.lcx_attention_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+        L.lcx_attention.restype = i32
+        L.lcx_attention.argtypes = [i32, i32, i32, i32, vp, vp, vp, i32, vp, i32, vp, vp, i32, vp, vp,
+                                    ctypes.c_size_t, vp]
         L.lcx_set_profiling.restype = i32
         L.lcx_set_profiling.argtypes = [vp, i32]
         L.lcx_get_profile.restype = i32
@@ -222,3 +227,20 @@ class Context:
 def get_rows(qtype: int, table, n_rows: int, n_cols: int, ids, out, stream=None) -> int:
     s = None if stream is None else (stream if isinstance(stream, int) else stream.cuda_stream)
     return lib().lcx_get_rows(qtype, _ptr(table), n_rows, n_cols, _ptr(ids), int(ids.numel()), _ptr(out), s)
+
+
+def attention(q, k_cache, v_cache, page_table, pos, seq, max_pos: int, out, workspace=None, stream=None) -> int:
+    """lcx_attention over torch device tensors: q [T][H*hd] f32, caches [n_pages][KV][64][hd] f16,
+    page_table [n_seq][max_pages] i32, pos/seq [T] i32, out [T][H*hd] f32."""
+    T = int(pos.numel())
+    n_pages, n_kv, _, hd = (int(x) for x in k_cache.shape)
+    H = int(q.shape[1]) // hd
+    s = None if stream is None else (stream if isinstance(stream, int) else stream.cuda_stream)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    return lib().lcx_attention(T, H, n_kv, hd, _ptr(q), _ptr(k_cache), _ptr(v_cache), n_pages, _ptr(page_table),
+                               int(page_table.shape[1]), _ptr(pos), _ptr(seq), max_pos, _ptr(out), _ptr(workspace),
+                               ws_bytes, s)
+
+
+def attention_workspace_size(T: int, n_head: int, n_head_kv: int, head_dim: int, max_pos: int) -> int:
+    return int(lib().lcx_attention_workspace_size(T, n_head, n_head_kv, head_dim, max_pos))

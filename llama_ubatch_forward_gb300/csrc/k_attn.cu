@@ -251,6 +251,19 @@ int attention_splits(const FwdArgs &a, int max_natt, int *chunk) {
     return ns;
 }
 
+size_t attention_scratch_bytes(const FwdArgs &a, int max_natt, size_t *counter_offset) {
+    int chunk = 0;
+    const int ns = attention_splits(a, max_natt, &chunk);
+    if (ns <= 1) {
+        if (counter_offset) *counter_offset = 0;
+        return 0;
+    }
+    const size_t part = (size_t)a.T * a.KV * ns * (a.H / a.KV) * (a.hd + 2) * sizeof(float);
+    const size_t off = (part + 255) / 256 * 256;
+    if (counter_offset) *counter_offset = off;
+    return off + (size_t)a.T * a.KV * sizeof(int32_t);
+}
+
 cudaError_t launch_attention(const FwdArgs &a, int layer, int max_natt, bool out_f16, cudaStream_t s,
                              int64_t &launches) {
     int chunk = 0;

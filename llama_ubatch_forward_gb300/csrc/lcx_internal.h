@@ -115,5 +115,8 @@ cudaError_t launch_gemm(const QMat &W, Epi epi, int T, const __half *A, const Fw
 cudaError_t launch_attention(const FwdArgs &a, int layer, int max_natt, bool out_f16, cudaStream_t s,
                              int64_t &launches);
 int attention_splits(const FwdArgs &a, int max_natt, int *chunk);
+// Scratch bytes one attention launch needs (partials, then arrival counters at
+// *counter_offset); 0 when every token fits in a single split.
+size_t attention_scratch_bytes(const FwdArgs &a, int max_natt, size_t *counter_offset);
 
 }  // namespace lcx

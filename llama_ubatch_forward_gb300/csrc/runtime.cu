@@ -33,6 +33,17 @@ void set_err(const char *what, cudaError_t e) {
 
 int round_up(int x, int m) { return (x + m - 1) / m * m; }
 
+}  // namespace
+
+namespace lcx {
+void set_error_text(const char *msg) {
+    std::lock_guard<std::mutex> lk(g_err_mu);
+    g_err = msg;
+}
+}  // namespace lcx
+
+namespace {
+
 bool valid_block_type(int t) { return t == LCX_Q4_0 || t == LCX_Q8_0; }
 
 }  // namespace
