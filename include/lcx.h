@@ -215,6 +215,26 @@ int32_t lcx_attention(int32_t T, int32_t n_head, int32_t n_head_kv, int32_t head
                       int32_t max_pages, const int32_t *pos, const int32_t *seq, int32_t max_pos, float *out,
                       void *workspace, size_t workspace_bytes, void *cuda_stream);
 
+/* lcx_attention for callers that cannot allocate device memory (the article has no
+ * counterpart: this is an interface addition of this library). Examples of such callers: a
+ * plugin whose host application owns every device allocation, a process whose device memory
+ * is fully reserved by a framework's caching allocator, a latency-critical path that cannot
+ * take cudaMalloc's implicit synchronisation. Same arguments and result as lcx_attention,
+ * without the workspace: the scratch is a fixed device array of
+ * LCX_ATTENTION_NOALLOC_SCRATCH_BYTES inside the library, present on every GPU that loads the
+ * library until the process exits. The call allocates nothing.
+ *   - The first call on a device looks up that array's device address (once per device, with
+ *     the device current); make that first call before any stream capture.
+ *   - Calls whose scratch need (lcx_attention_workspace_size) exceeds the array are rejected
+ *     with LCX_INVALID and a message in lcx_last_error().
+ *   - Every call on a device shares the one array: calls that overlap on the GPU (on different
+ *     streams, or from several host threads) race and must not be issued. */
+#define LCX_ATTENTION_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)
+int32_t lcx_attention_noalloc(int32_t T, int32_t n_head, int32_t n_head_kv, int32_t head_dim, const float *q,
+                              const void *k_cache, const void *v_cache, int32_t n_pages, const int32_t *page_table,
+                              int32_t max_pages, const int32_t *pos, const int32_t *seq, int32_t max_pos, float *out,
+                              void *cuda_stream);
+
 /* Last CUDA error string seen by the library in this process ("" if none). */
 const char *lcx_last_error(void);
 

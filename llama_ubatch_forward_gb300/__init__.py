@@ -20,7 +20,7 @@ LCX_INVALID, LCX_ALLOC_FAILED, LCX_COMPUTE_FAILED = -1, -2, -3
 SYMBOLS = ("lcx_model_create", "lcx_model_free", "lcx_ctx_create", "lcx_ctx_free", "lcx_decode",
            "lcx_decode_greedy", "lcx_kv_clear", "lcx_seq_pos_max", "lcx_n_outputs", "lcx_set_abort",
            "lcx_get_stats", "lcx_ctx_create_host_only", "lcx_get_rows", "lcx_last_error", "lcx_set_profiling",
-           "lcx_get_profile", "lcx_attention_workspace_size", "lcx_attention")
+           "lcx_get_profile", "lcx_attention_workspace_size", "lcx_attention", "lcx_attention_noalloc")
 
 
 def build(force: bool = False) -> str:
@@ -103,6 +103,8 @@ def lib():
         L.lcx_attention.restype = i32
         L.lcx_attention.argtypes = [i32, i32, i32, i32, vp, vp, vp, i32, vp, i32, vp, vp, i32, vp, vp,
                                     ctypes.c_size_t, vp]
+        L.lcx_attention_noalloc.restype = i32
+        L.lcx_attention_noalloc.argtypes = [i32, i32, i32, i32, vp, vp, vp, i32, vp, i32, vp, vp, i32, vp, vp]
         L.lcx_set_profiling.restype = i32
         L.lcx_set_profiling.argtypes = [vp, i32]
         L.lcx_get_profile.restype = i32
@@ -244,3 +246,14 @@ def attention(q, k_cache, v_cache, page_table, pos, seq, max_pos: int, out, work
 
 def attention_workspace_size(T: int, n_head: int, n_head_kv: int, head_dim: int, max_pos: int) -> int:
     return int(lib().lcx_attention_workspace_size(T, n_head, n_head_kv, head_dim, max_pos))
+
+
+def attention_noalloc(q, k_cache, v_cache, page_table, pos, seq, max_pos: int, out, stream=None) -> int:
+    """lcx_attention_noalloc (no workspace: the library's fixed device scratch is used)."""
+    T = int(pos.numel())
+    n_pages, n_kv, _, hd = (int(x) for x in k_cache.shape)
+    H = int(q.shape[1]) // hd
+    s = None if stream is None else (stream if isinstance(stream, int) else stream.cuda_stream)
+    return lib().lcx_attention_noalloc(T, H, n_kv, hd, _ptr(q), _ptr(k_cache), _ptr(v_cache), n_pages,
+                                       _ptr(page_table), int(page_table.shape[1]), _ptr(pos), _ptr(seq), max_pos,
+                                       _ptr(out), s)

@@ -24,6 +24,7 @@ static bool attn_args_ok(int32_t T, int32_t n_head, int32_t n_head_kv, int32_t h
     return true;
 }
 
+namespace lcx {
 FwdArgs attn_fwd_args(int32_t T, int32_t n_head, int32_t n_head_kv, int32_t head_dim, const float *q,
                       const void *k_cache, const void *v_cache, int32_t n_pages, const int32_t *page_table,
                       int32_t max_pages, const int32_t *pos, const int32_t *seq, float *out) {
@@ -44,6 +45,7 @@ FwdArgs attn_fwd_args(int32_t T, int32_t n_head, int32_t n_head_kv, int32_t head
     a.att_max_split = 64;
     return a;
 }
+}  // namespace lcx
 
 extern "C" size_t lcx_attention_workspace_size(int32_t T, int32_t n_head, int32_t n_head_kv, int32_t head_dim,
                                               int32_t max_pos) {
