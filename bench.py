@@ -167,7 +167,8 @@ def run_lcx(a, rank, world):
     log(f"[bench] model {cfg.name}: {host.weight_bytes() / 1e9:.2f} GB stored, generated in {time.perf_counter() - t0:.1f}s")
     gm = upload(host)
     stream = torch.cuda.Stream()
-    ctx = lcx.Context(gm, cfg.n_ctx, 1, n_ub, stream=stream)
+    n_ctx = a.n_ctx or cfg.n_ctx
+    ctx = lcx.Context(gm, n_ctx, 1, n_ub, stream=stream)
     gen = torch.zeros(n_dec, dtype=torch.int32, device=dev)
     am_host = np.zeros(1, dtype=np.int32)
 
@@ -211,9 +212,14 @@ def run_lcx(a, rank, world):
     decode_tps = world * a.steps * n_dec / (dec_sum / 1e3)
     prefill_tps = world * a.steps * n_prompt / (pre_sum / 1e3)
 
-    # per-kernel-class durations: one more step with event brackets around every launch
+    # per-kernel-class durations: one more step with event brackets around every launch,
+    # profiled separately for the prefill and the decode phase
+    ctx.kv_clear()
     ctx.set_profiling(True)
-    step()
+    assert ctx.decode(prompt, argmax_out=am_host) == 0
+    prof_pre = ctx.profile()
+    ctx.set_profiling(True)
+    assert ctx.decode_greedy(0, int(am_host[0]), n_dec, gen) == 0
     prof = ctx.profile()
     ctx.set_profiling(False)
     launches_per_step = None
@@ -241,7 +247,7 @@ def run_lcx(a, rank, world):
     hbm, bf16, bf16_sus, src = peaks()
     g = prof["gemv"]
     gemv_gbs = g["bytes"] / (g["ms"] / 1e3) / 1e9 if g["ms"] else 0.0
-    gm_ = prof["gemm"]
+    gm_ = prof_pre["gemm"]
     gemm_tf = gm_["flops"] / (gm_["ms"] / 1e3) / 1e12 if gm_["ms"] else 0.0
     dec_bytes = decode_bytes_per_step(cfg, host, n_prompt, n_dec)
     dec_gbs = dec_bytes / (sum(dec_ms) / a.steps / 1e3) / 1e9
@@ -278,10 +284,11 @@ def run_lcx(a, rank, world):
         "roofline_prefill": {"bound": "tensor", "kernel": "gemm (prefill matmuls)", "achieved": round(gemm_tf, 2),
                              "peak": bf16, "unit": "TFLOP/s", "frac": round(gemm_tf / bf16, 4), "traffic": None,
                              "peak_source": src},
-        "kernel_profile": {k: {"launches": v["launches"], "ms": round(v["ms"], 3),
-                               "GBps": round(v["bytes"] / v["ms"] / 1e6, 1) if v["ms"] else None,
-                               "TFLOPps": round(v["flops"] / v["ms"] / 1e9, 2) if v["ms"] else None}
-                           for k, v in prof.items()},
+        "kernel_profile": {ph: {k: {"launches": v["launches"], "ms": round(v["ms"], 3),
+                                    "GBps": round(v["bytes"] / v["ms"] / 1e6, 1) if v["ms"] else None,
+                                    "TFLOPps": round(v["flops"] / v["ms"] / 1e9, 2) if v["ms"] else None}
+                                for k, v in pr.items() if v["launches"]}
+                           for ph, pr in (("prefill", prof_pre), ("decode", prof))},
         "e2e": {"value": round(e2e_tps, 2), "unit": "tokens/s",
                 "h2d_bytes_per_step": n_prompt * 20 + n_dec * 20,
                 "d2h_bytes_per_step": 4 * (1 + n_dec),
@@ -291,6 +298,8 @@ def run_lcx(a, rank, world):
     }
     if rank == 0:
         try:
+            if a.no_cpu_baseline:
+                raise RuntimeError("skipped (--no-cpu-baseline)")
             res["cpu_baseline"] = cpu_baseline(host, cfg)
         except Exception as ex:  # the baseline is reported, not required
             res["cpu_baseline"] = {"error": str(ex)}
@@ -344,6 +353,8 @@ def main():
     ap.add_argument("--prompt", type=int, default=2048)
     ap.add_argument("--decode-steps", type=int, default=256)
     ap.add_argument("--n-ubatch", type=int, default=512)
+    ap.add_argument("--n-ctx", type=int, default=0, help="override the context size (0: the config's)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
     a = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -94,10 +94,11 @@ enum {
     LCX_COMPUTE_FAILED = -3  /* a CUDA launch or copy failed; the failed ubatch's cells are rolled back */
 };
 
-/* Builds a model over the caller's weights. The weights are BORROWED: they must stay valid
- * until lcx_model_free. The model keeps its own device copy of every matrix re-laid out for
- * the kernels (scale planes split from the quantized planes, Q/K/V and gate/up fused), so the
- * caller may not change the weights afterwards without rebuilding the model.
+/* Builds a model over the caller's weights. The model keeps its own device copy of every layer
+ * matrix and of `output`, re-laid out for the kernels (scale planes split from the quantized
+ * planes, Q/K/V and gate/up fused): the caller may free or reuse those after this call
+ * returns. tok_embd, output_norm and the per-layer norm gains are BORROWED (read in place):
+ * they must stay valid and unchanged until lcx_model_free.
  * Requirements: n_embd % 64 == 0, head_dim even and <= 256, (n_head * head_dim) % 64 == 0,
  * n_head % n_head_kv == 0, t_linear in {Q4_0, Q8_0}, t_out in {Q4_0, Q8_0} (t_embd when
  * output is NULL), t_embd in {F16, Q8_0, Q4_0}.

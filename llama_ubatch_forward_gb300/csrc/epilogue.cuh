@@ -84,4 +84,17 @@ __device__ __forceinline__ void epi_swiglu(const FwdArgs &a, int t, int f0, cons
     }
 }
 
+// SwiGLU epilogue for two features f0, f0+1.
+template <bool OUT16>
+__device__ __forceinline__ void epi_swiglu2(const FwdArgs &a, int t, int f0, const float g[2], const float u[2]) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const int f = f0 + j;
+        if (f >= a.F) break;
+        const float h = silu_f(g[j]) * u[j];
+        if (OUT16) a.h16[(size_t)t * a.F_pad + f] = __float2half_rn(h);
+        else a.h32[(size_t)t * a.F_pad + f] = h;
+    }
+}
+
 }  // namespace lcx

@@ -26,11 +26,26 @@ __global__ void __launch_bounds__(128) k_attn(const FwdArgs a, const int layer, 
     constexpr int DPV = HD / 32;   // dims per lane in P.V
     const int t = blockIdx.z, kvh = blockIdx.y, sp = blockIdx.x;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    // The ubatch metadata and the page table were written before the preceding kernel ran, and
+    // the cells of earlier positions hold K/V stored by earlier ubatches: pull this CTA's rows
+    // into L2 while the preceding kernel (which writes q and the newest cells) finishes.
     const int pos = a.ub.pos[t], seq = a.ub.seq[t];
     const int n_att = pos + 1;
     const int ns_t = (n_att + chunk - 1) / chunk;
-    if (sp >= ns_t) return;
     const int c0 = sp * chunk, c1 = min(c0 + chunk, n_att);
+    if (sp < ns_t) {
+        const int32_t *ptr0 = a.pt + (size_t)seq * a.max_pages_per_seq;
+        constexpr int LPR = HD * 2 / 128;   // 128-byte lines per K or V row
+        for (int i = threadIdx.x; i < (c1 - c0) * LPR; i += blockDim.x) {
+            const int j = c0 + i / LPR;
+            const size_t row = (((size_t)layer * a.n_pages + ptr0[j / kPage]) * a.KV + kvh) * kPage + (j % kPage);
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(a.kc + row * HD + (i % LPR) * 64));
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(a.vc + row * HD + (i % LPR) * 64));
+        }
+    }
+    LCX_PDL_WAIT();
+    LCX_PDL_TRIGGER();
+    if (sp >= ns_t) return;
     const int qw = a.H * HD;
     const float scale = rsqrtf((float)HD);
 
@@ -57,85 +72,105 @@ __global__ void __launch_bounds__(128) k_attn(const FwdArgs a, const int layer, 
     const int32_t *ptrow = a.pt + (size_t)seq * a.max_pages_per_seq;
     const size_t layer_base = (size_t)layer * a.n_pages;
 
-    for (int j0 = c0 + warp * 4; j0 < c1; j0 += 16) {
-        const int j = j0 + cgrp;                 // this lane's cell in the group
-        const bool valid = j < c1;
-        float s[G];
-        int cellrow = 0;
-        if (valid) {
-            const int page = ptrow[j / kPage];
-            cellrow = (int)(((layer_base + page) * a.KV + kvh) * kPage + (j % kPage));
-            const __half *kp = a.kc + (size_t)cellrow * HD + sub * DPL;
-            float kf[DPL];
+    // Each warp takes super-groups of 16 consecutive cells (inside one 64-cell page): all K and
+    // V loads of a super-group are issued before any of them is used.
+    for (int j0 = c0 + warp * 16; j0 < c1; j0 += 64) {
+        const int page = ptrow[j0 / kPage];
+        const int row0 = (int)(((layer_base + page) * a.KV + kvh) * kPage + (j0 % kPage));
+        uint4 kraw[4][DPL / 8];
+        uint2 vraw[16];
 #pragma unroll
-            for (int i = 0; i < DPL; i += 8) {
-                const uint4 raw = *reinterpret_cast<const uint4 *>(kp + i);
-                const __half2 *h2 = reinterpret_cast<const __half2 *>(&raw);
+        for (int g4 = 0; g4 < 4; ++g4) {
+            const int j = j0 + 4 * g4 + cgrp;
+            if (j < c1) {
+                const __half *kp = a.kc + (size_t)(row0 + 4 * g4 + cgrp) * HD + sub * DPL;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 f = __half22float2(h2[e]);
-                    kf[i + 2 * e] = f.x;
-                    kf[i + 2 * e + 1] = f.y;
+                for (int i = 0; i < DPL / 8; ++i) kraw[g4][i] = *reinterpret_cast<const uint4 *>(kp + 8 * i);
+            } else {
+#pragma unroll
+                for (int i = 0; i < DPL / 8; ++i) kraw[g4][i] = make_uint4(0, 0, 0, 0);
+            }
+        }
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+            if (j0 + c < c1) {
+                const __half *vp = a.vc + (size_t)(row0 + c) * HD + lane * DPV;
+                if (DPV == 4) vraw[c] = *reinterpret_cast<const uint2 *>(vp);
+                else vraw[c] = make_uint2(*reinterpret_cast<const uint32_t *>(vp), 0u);
+            }
+        }
+#pragma unroll
+        for (int g4 = 0; g4 < 4; ++g4) {
+            if (j0 + 4 * g4 >= c1) break;
+            const int j = j0 + 4 * g4 + cgrp;   // this lane's cell in the group
+            const bool valid = j < c1;
+            float s[G];
+            {
+                float kf[DPL];
+#pragma unroll
+                for (int i = 0; i < DPL / 8; ++i) {
+                    const __half2 *h2 = reinterpret_cast<const __half2 *>(&kraw[g4][i]);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 f = __half22float2(h2[e]);
+                        kf[8 * i + 2 * e] = f.x;
+                        kf[8 * i + 2 * e + 1] = f.y;
+                    }
+                }
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    float d = 0.f;
+#pragma unroll
+                    for (int i = 0; i < DPL; ++i) d = fmaf(qr[g][i], kf[i], d);
+                    s[g] = d;
                 }
             }
 #pragma unroll
             for (int g = 0; g < G; ++g) {
-                float d = 0.f;
-#pragma unroll
-                for (int i = 0; i < DPL; ++i) d = fmaf(qr[g][i], kf[i], d);
-                s[g] = d;
+                float d = s[g];
+                d += __shfl_xor_sync(0xffffffffu, d, 1);
+                d += __shfl_xor_sync(0xffffffffu, d, 2);
+                d += __shfl_xor_sync(0xffffffffu, d, 4);
+                s[g] = valid ? d : -CUDART_INF_F;
             }
-        } else {
-#pragma unroll
-            for (int g = 0; g < G; ++g) s[g] = 0.f;
-        }
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-            float d = s[g];
-            d += __shfl_xor_sync(0xffffffffu, d, 1);
-            d += __shfl_xor_sync(0xffffffffu, d, 2);
-            d += __shfl_xor_sync(0xffffffffu, d, 4);
-            s[g] = valid ? d : -CUDART_INF_F;
-        }
-        // online softmax over the 4 cells of the group
-        float p[G], alpha[G];
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-            float mx = s[g];
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-            const float mn = fmaxf(m[g], mx);
-            alpha[g] = expf(m[g] - mn);
-            p[g] = expf(s[g] - mn);
-            float ps = p[g];
-            ps += __shfl_xor_sync(0xffffffffu, ps, 8);
-            ps += __shfl_xor_sync(0xffffffffu, ps, 16);
-            l[g] = l[g] * alpha[g] + ps;   // lanes l, l^8, l^16, l^24 hold the group's 4 cells
-            m[g] = mn;
-#pragma unroll
-            for (int i = 0; i < DPV; ++i) acc[g][i] *= alpha[g];
-        }
-        // P.V: lane owns dims lane * DPV .. + DPV
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const int cr = __shfl_sync(0xffffffffu, cellrow, 8 * c);
-            if (j0 + c >= c1) break;
-            float vf[DPV];
-            const __half *vp = a.vc + (size_t)cr * HD + lane * DPV;
-            if (DPV == 4) {
-                const uint2 raw = *reinterpret_cast<const uint2 *>(vp);
-                const float2 f0 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.x));
-                const float2 f1 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.y));
-                vf[0] = f0.x; vf[1 % DPV] = f0.y; vf[2 % DPV] = f1.x; vf[3 % DPV] = f1.y;
-            } else {
-                const float2 f0 = __half22float2(*reinterpret_cast<const __half2 *>(vp));
-                vf[0] = f0.x; vf[1 % DPV] = f0.y;
-            }
+            // online softmax over the 4 cells of the group
+            float p[G];
 #pragma unroll
             for (int g = 0; g < G; ++g) {
-                const float pc = __shfl_sync(0xffffffffu, p[g], 8 * c);
+                float mx = s[g];
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                const float mn = fmaxf(m[g], mx);
+                const float alpha = expf(m[g] - mn);
+                p[g] = expf(s[g] - mn);
+                float ps = p[g];
+                ps += __shfl_xor_sync(0xffffffffu, ps, 8);
+                ps += __shfl_xor_sync(0xffffffffu, ps, 16);
+                l[g] = l[g] * alpha + ps;   // lanes l, l^8, l^16, l^24 hold the group's 4 cells
+                m[g] = mn;
 #pragma unroll
-                for (int i = 0; i < DPV; ++i) acc[g][i] = fmaf(pc, vf[i], acc[g][i]);
+                for (int i = 0; i < DPV; ++i) acc[g][i] *= alpha;
+            }
+            // P.V: lane owns dims lane * DPV .. + DPV
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                if (j0 + 4 * g4 + c >= c1) break;
+                const uint2 raw = vraw[4 * g4 + c];
+                float vf[DPV];
+                const float2 f0 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.x));
+                vf[0] = f0.x;
+                vf[1 % DPV] = f0.y;
+                if (DPV == 4) {
+                    const float2 f1 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.y));
+                    vf[2 % DPV] = f1.x;
+                    vf[3 % DPV] = f1.y;
+                }
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    const float pc = __shfl_sync(0xffffffffu, p[g], 8 * c);
+#pragma unroll
+                    for (int i = 0; i < DPV; ++i) acc[g][i] = fmaf(pc, vf[i], acc[g][i]);
+                }
             }
         }
     }
@@ -190,18 +225,45 @@ __global__ void __launch_bounds__(128) k_attn(const FwdArgs a, const int layer, 
     __syncthreads();
     if (!last) return;
     __threadfence();
+    // merge weights of the splits: w_s = exp(M_s - M*) / L*, one warp per query head
+    __shared__ float sw[64][G];
+    for (int g = warp; g < G; g += 4) {
+        float ms[2], ls[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int s2 = lane + 32 * h;
+            const float *pr = part + ((prow + s2) * G + g) * (HD + 2);
+            ms[h] = s2 < ns_t ? __ldcg(pr) : -CUDART_INF_F;
+            ls[h] = s2 < ns_t ? __ldcg(pr + 1) : 0.f;
+        }
+        float M = fmaxf(ms[0], ms[1]);
+#pragma unroll
+        for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        float e[2], L = 0.f;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            e[h] = lane + 32 * h < ns_t ? expf(ms[h] - M) : 0.f;
+            L += e[h] * ls[h];
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+            if (lane + 32 * h < ns_t) sw[lane + 32 * h][g] = e[h] / L;
+    }
+    __syncthreads();
     for (int idx = threadIdx.x; idx < G * HD; idx += blockDim.x) {
         const int g = idx / HD, dd = idx % HD;
-        float M = -CUDART_INF_F;
-        for (int s2 = 0; s2 < ns_t; ++s2) M = fmaxf(M, __ldcg(part + ((prow + s2) * G + g) * (HD + 2)));
-        float L = 0.f, A = 0.f;
-        for (int s2 = 0; s2 < ns_t; ++s2) {
-            const float *pr = part + ((prow + s2) * G + g) * (HD + 2);
-            const float f = expf(__ldcg(pr) - M);
-            L += __ldcg(pr + 1) * f;
-            A += __ldcg(pr + 2 + dd) * f;
+        float o = 0.f;
+        int s2 = 0;
+        for (; s2 + 8 <= ns_t; s2 += 8) {   // 8 independent loads in flight
+            float v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = __ldcg(part + ((prow + s2 + u) * G + g) * (HD + 2) + 2 + dd);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) o = fmaf(sw[s2 + u][g], v[u], o);
         }
-        const float o = A / L;
+        for (; s2 < ns_t; ++s2) o = fmaf(sw[s2][g], __ldcg(part + ((prow + s2) * G + g) * (HD + 2) + 2 + dd), o);
         const size_t oi = (size_t)t * qw + (size_t)(kvh * G + g) * HD + dd;
         if (OUT16) a.o16[oi] = __float2half_rn(o);
         else a.o32[oi] = o;
@@ -212,9 +274,8 @@ __global__ void __launch_bounds__(128) k_attn(const FwdArgs a, const int layer, 
 template <int HD, int G>
 cudaError_t run(const FwdArgs &a, int layer, int chunk, int ns, bool out16, cudaStream_t s) {
     dim3 grid(ns, a.KV, a.T);
-    if (out16) k_attn<HD, G, true><<<grid, 128, 0, s>>>(a, layer, chunk, ns);
-    else k_attn<HD, G, false><<<grid, 128, 0, s>>>(a, layer, chunk, ns);
-    return cudaGetLastError();
+    if (out16) return launch_pdl(k_attn<HD, G, true>, grid, dim3(128), 0, s, a, layer, chunk, ns);
+    return launch_pdl(k_attn<HD, G, false>, grid, dim3(128), 0, s, a, layer, chunk, ns);
 }
 
 template <int HD>

@@ -28,6 +28,8 @@ __global__ void __launch_bounds__(256) k_gemm_simt(const uint8_t *__restrict__ q
                                                    const FwdArgs a, int layer) {
     __shared__ float Ws[32][TASKS * ROWS + 1];
     __shared__ float Xs[32][TT + 1];
+    LCX_PDL_WAIT();
+    LCX_PDL_TRIGGER();
     const int task0 = blockIdx.x * TASKS, tok0 = blockIdx.y * TT;
     const int K = nb * 32;
     const int tq = threadIdx.x % TASKS, tp = threadIdx.x / TASKS;   // task in tile, token pair
@@ -90,8 +92,8 @@ __global__ void __launch_bounds__(256) k_gemm_simt(const uint8_t *__restrict__ q
 template <int QT, int ROWS, int EPI, bool OUT16>
 cudaError_t run(const QMat &W, int n_tasks, int T, const __half *A, const FwdArgs &a, int layer, cudaStream_t s) {
     dim3 grid((n_tasks + TASKS - 1) / TASKS, (T + TT - 1) / TT);
-    k_gemm_simt<QT, ROWS, EPI, OUT16><<<grid, 256, 0, s>>>(W.qs, W.sc, W.N, W.nb, n_tasks, T, A, a, layer);
-    return cudaGetLastError();
+    return launch_pdl(k_gemm_simt<QT, ROWS, EPI, OUT16>, grid, dim3(256), 0, s, (const uint8_t *)W.qs,
+                      (const __half *)W.sc, W.N, W.nb, n_tasks, T, A, a, layer);
 }
 
 template <int QT>

@@ -10,7 +10,9 @@ cudaError_t dispatch_q8(const GemvParams &p, Epi epi, const FwdArgs &a, int laye
 
 bool gemv_fits(const QMat &W, int T) {
     int nt = T <= 1 ? 1 : T <= 2 ? 2 : T <= 4 ? 4 : 8;
-    return T <= kGemvMaxT && (size_t)nt * W.K * sizeof(float) <= (size_t)kGemvSmemX;
+    if (T > kGemvMaxT || (size_t)nt * gemv_detail::stage_bytes_per_token(W.nb) > (size_t)kGemvSmemX) return false;
+    const gemv_detail::StagePlan pl = gemv_detail::stage_plan(W.nb, W.type == Q8 ? 32 : 16, nt, false, kGemvSmemTotal);
+    return pl.slots >= 2;
 }
 
 cudaError_t launch_gemv(const QMat &W, Epi epi, int T, const GemvIn &in, const FwdArgs &a, int layer, cudaStream_t s,
@@ -23,7 +25,7 @@ cudaError_t launch_gemv(const QMat &W, Epi epi, int T, const GemvIn &in, const F
     p.K = W.K;
     p.T = T;
     p.in = in;
-    p.n_tasks = epi == EPI_SWIGLU ? (a.F + 3) / 4 : (W.N + 3) / 4;
+    p.n_tasks = epi == EPI_SWIGLU ? (a.F + 1) / 2 : (W.N + 3) / 4;
     ++launches;
     if (W.type == Q4) return gemv_detail::dispatch_q4(p, epi, a, layer, s);
     if (W.type == Q8) return gemv_detail::dispatch_q8(p, epi, a, layer, s);

@@ -1,98 +1,86 @@
 // Weight-streaming GEMV for decode ubatches (T <= 8 tokens): y = W x with W in Q4_0 / Q8_0.
 //
 // Decode is bound by reading the weights once (KV-cache section of the article: decode loads
-// memory, prefill loads the compute units), so this kernel is built around HBM streaming:
-//   * each warp owns a task of 4 rows (a quad) -- 8 rows for the gate/up pair of SwiGLU -- and
-//     its lanes stride over the row's 32-element blocks, so every load instruction of a warp
-//     reads 512 contiguous bytes (16 B of nibbles or 2 x 16 B of int8 per lane);
-//   * the activations are staged once per CTA in shared memory (RMSNorm fused into that
-//     prologue), in a 16-byte-chunk XOR swizzle so the lanes' 16-byte reads are conflict free;
-//   * nibbles are turned into exact floats in registers with one LOP3 each: OR-ing a nibble
-//     at bit s into the mantissa of 2^23 gives 2^23 + q*2^s, and subtracting 2^23 + 8*2^s
-//     leaves (q-8)*2^s exactly; the staged activation of that element is pre-multiplied by
-//     2^-s, so the packed f32x2 FMA sums exact products (no precision is lost to the trick);
-//   * a block's 32 products are summed, scaled once by the block's fp16 scale, accumulated
-//     in f32, and the row sums are reduced with warp shuffles.
+// memory, prefill loads the compute units), so the kernel is built to keep HBM busy with as
+// few instructions per weight as possible:
+//   * each warp owns a task of 4 rows and its lanes stride over the rows' 32-element blocks,
+//     so every load instruction of a warp reads 512 contiguous bytes (16 B of nibbles or
+//     2 x 16 B of int8 per lane); a row quad's 4 block scales arrive in one 8-byte load;
+//   * the activations are staged once per CTA in shared memory with the RMSNorm fused in, and
+//     each 32-element block of them is split into two int8 parts, x ~= s (hi + lo / 128) with
+//     s = max|x| / 127 (hi = round(x / s), lo = round(128 (x / s - hi))): about 14 bits of
+//     the block's range, finer than an f16 rounding of x;
+//   * a block's dot product with the stored integers q is then exact integer arithmetic,
+//     four elements per dp4a: P = 128 sum(q hi) + sum(q lo) (minus 8 (128 sum hi + sum lo) for
+//     Q4_0's offset), and the row accumulates d * s / 128 * P in f32 -- one I2F and one FMA
+//     per block instead of one float FMA per weight;
+//   * row sums are reduced with warp shuffles; epilogues (RoPE + KV append, residual add,
+//     SwiGLU, logits + argmax) are fused.
+// The weight rows stream through a shared-memory ring filled by TMA bulk copies (see k_gemv).
 #pragma once
 #include "epilogue.cuh"
 
 namespace lcx {
 namespace gemv_detail {
 
-__device__ __forceinline__ float2 f2add(float2 a, float2 b) { return __fadd2_rn(a, b); }
-__device__ __forceinline__ float2 f2fma(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
-__device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
+// ---------------------------------------------------------------- staged activations
+// Per token: hi plane [nb][32 B], lo plane [nb][32 B] (16-byte chunk c of block b stored at
+// chunk c ^ ((b >> 2) & 1): 8 lanes reading 8 consecutive blocks hit 8 distinct bank groups),
+// then meta [nb] (s / 128, C) with C = 8 (128 sum hi + sum lo) for Q4_0 and 0 for Q8_0.
+__host__ __device__ constexpr size_t stage_bytes_per_token(int nb) { return (size_t)nb * 72; }
 
-constexpr uint32_t kMagic = 0x4B000000u;   // 2^23
-constexpr float kTwo23 = 8388608.0f;
+__device__ __forceinline__ int plane_chunk_off(int b, int c) { return b * 32 + ((c ^ ((b >> 2) & 1)) << 4); }
 
-// shift (bit position) of the nibble holding element e of a Q4_0 block, after the split into
-// w (bytes 0..2 low half) and w >> 12 (the rest): lo/hi nibble of byte c
-__host__ __device__ constexpr int q4_shift(int c, int hi) {
-    return c == 0 ? (hi ? 4 : 0) : c == 1 ? (hi ? 12 : 8) : c == 2 ? (hi ? 8 : 16) : (hi ? 16 : 12);
+struct XQ {          // one block of one token, in registers
+    int4 h0, h1;     // hi words 0..3, 4..7
+    int4 l0, l1;     // lo words
+    float s;         // s / 128
+    int C;
+};
+
+__device__ __forceinline__ void load_xq(const uint8_t *stage_t, int nb, int b, XQ &x) {
+    const uint8_t *hp = stage_t, *lp = stage_t + (size_t)nb * 32;
+    const float2 *mp = reinterpret_cast<const float2 *>(stage_t + (size_t)nb * 64);
+    x.h0 = *reinterpret_cast<const int4 *>(hp + plane_chunk_off(b, 0));
+    x.h1 = *reinterpret_cast<const int4 *>(hp + plane_chunk_off(b, 1));
+    x.l0 = *reinterpret_cast<const int4 *>(lp + plane_chunk_off(b, 0));
+    x.l1 = *reinterpret_cast<const int4 *>(lp + plane_chunk_off(b, 1));
+    const float2 m = mp[b];
+    x.s = m.x;
+    x.C = __float_as_int(m.y);
 }
 
-// float offset of element chunk j (elements 4j..4j+3) of block b in the swizzled stage
-__device__ __forceinline__ int xs_chunk(int b, int j) { return (b * 8 + (j ^ (b & 7))) * 4; }
+__device__ __forceinline__ int xw(const int4 &a, const int4 &b, int i) {   // word i of the 8
+    return i == 0 ? a.x : i == 1 ? a.y : i == 2 ? a.z : i == 3 ? a.w : i == 4 ? b.x : i == 5 ? b.y : i == 6 ? b.z : b.w;
+}
 
-// Partial sums of one 32-element Q4_0 block against NT staged token vectors.
-template <int NT>
-__device__ __forceinline__ void q4_block(const uint4 w, const float *xs_b[NT], int b, float part[NT]) {
+// Integer dot of one Q4_0 block (16 bytes of nibbles) with a staged block: 128 sum(q hi) +
+// sum(q lo) - C, i.e. 128 / s times sum((q - 8) x) up to the staging rounding.
+__device__ __forceinline__ int q4_idot(const uint4 w, const XQ &x) {
     const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-    float2 acc[NT];
-#pragma unroll
-    for (int t = 0; t < NT; ++t) acc[t] = make_float2(0.f, 0.f);
+    int ph = 0, pl = 0;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const uint32_t lo = ws[i], hi = ws[i] >> 12;
-        // (q - 8) * 2^s for the low and high nibble of each byte c
-        const float2 d0 = f2add(make_float2(u2f((lo & 0xFu) | kMagic), u2f((lo & 0xF0u) | kMagic)),
-                                make_float2(-(kTwo23 + 8.f), -(kTwo23 + 128.f)));
-        const float2 d1 = f2add(make_float2(u2f((lo & 0xF00u) | kMagic), u2f((lo & 0xF000u) | kMagic)),
-                                make_float2(-(kTwo23 + 2048.f), -(kTwo23 + 32768.f)));
-        const float2 d2 = f2add(make_float2(u2f((lo & 0xF0000u) | kMagic), u2f((hi & 0xF00u) | kMagic)),
-                                make_float2(-(kTwo23 + 524288.f), -(kTwo23 + 2048.f)));
-        const float2 d3 = f2add(make_float2(u2f((hi & 0xF000u) | kMagic), u2f((hi & 0xF0000u) | kMagic)),
-                                make_float2(-(kTwo23 + 32768.f), -(kTwo23 + 524288.f)));
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-            const float4 xl = *reinterpret_cast<const float4 *>(xs_b[t] + xs_chunk(b, i));       // elements 4i..4i+3
-            const float4 xh = *reinterpret_cast<const float4 *>(xs_b[t] + xs_chunk(b, i + 4));   // elements 16+4i..
-            acc[t] = f2fma(d0, make_float2(xl.x, xh.x), acc[t]);
-            acc[t] = f2fma(d1, make_float2(xl.y, xh.y), acc[t]);
-            acc[t] = f2fma(d2, make_float2(xl.z, xh.z), acc[t]);
-            acc[t] = f2fma(d3, make_float2(xl.w, xh.w), acc[t]);
-        }
+        const int lo_n = (int)(ws[i] & 0x0F0F0F0Fu);          // elements 4i .. 4i+3
+        const int hi_n = (int)((ws[i] >> 4) & 0x0F0F0F0Fu);   // elements 16+4i .. 16+4i+3
+        ph = __dp4a(lo_n, xw(x.h0, x.h1, i), ph);
+        ph = __dp4a(hi_n, xw(x.h0, x.h1, 4 + i), ph);
+        pl = __dp4a(lo_n, xw(x.l0, x.l1, i), pl);
+        pl = __dp4a(hi_n, xw(x.l0, x.l1, 4 + i), pl);
     }
-#pragma unroll
-    for (int t = 0; t < NT; ++t) part[t] = acc[t].x + acc[t].y;
+    return ph * 128 + pl - x.C;
 }
 
-// Partial sums of one Q8_0 block (32 int8 in two uint4).
-template <int NT>
-__device__ __forceinline__ void q8_block(const uint4 w0, const uint4 w1, const float *xs_b[NT], int b,
-                                         float part[NT]) {
+// Integer dot of one Q8_0 block (32 int8 in two uint4): 128 sum(q hi) + sum(q lo).
+__device__ __forceinline__ int q8_idot(const uint4 w0, const uint4 w1, const XQ &x) {
     const uint32_t ws[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-    float2 acc[NT];
-#pragma unroll
-    for (int t = 0; t < NT; ++t) acc[t] = make_float2(0.f, 0.f);
-    const float2 off = make_float2(-(kTwo23 + 128.f), -(kTwo23 + 128.f));
+    int ph = 0, pl = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        const uint32_t u = ws[i] ^ 0x80808080u;   // int8 q -> q + 128 in each byte
-        const float2 da = f2add(make_float2(u2f(__byte_perm(u, kMagic, 0x7650u)),
-                                            u2f(__byte_perm(u, kMagic, 0x7651u))), off);
-        const float2 db = f2add(make_float2(u2f(__byte_perm(u, kMagic, 0x7652u)), u2f(__byte_perm(u, kMagic, 0x7653u))),
-                                off);
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-            const float4 x = *reinterpret_cast<const float4 *>(xs_b[t] + xs_chunk(b, i));
-            acc[t] = f2fma(da, make_float2(x.x, x.y), acc[t]);
-            acc[t] = f2fma(db, make_float2(x.z, x.w), acc[t]);
-        }
+        ph = __dp4a((int)ws[i], xw(x.h0, x.h1, i), ph);
+        pl = __dp4a((int)ws[i], xw(x.l0, x.l1, i), pl);
     }
-#pragma unroll
-    for (int t = 0; t < NT; ++t) part[t] = acc[t].x + acc[t].y;
+    return ph * 128 + pl;
 }
 
 struct GemvParams {
@@ -104,195 +92,363 @@ struct GemvParams {
     GemvIn in;
 };
 
-// ROWS = 4: a quad of consecutive rows; ROWS = 8: the SwiGLU pair (gate quad, up quad).
-template <int QT, int NT, int ROWS, int EPI, bool OUT16>
-__global__ void __launch_bounds__(256, (NT > 2 ? 1 : 2)) k_gemv(const GemvParams p, const FwdArgs a, const int layer) {
-    extern __shared__ __align__(16) float xs[];   // [NT][nb * 32] swizzled
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int nb = p.nb, K = p.K;
+// The 4 internal rows of a task. SwiGLU tasks take a gate row pair and the matching up pair
+// (128 rows further, in the 128-row chunk layout of the fused gate/up matrix).
+template <int EPI>
+__device__ __forceinline__ int task_row(int task, int r) {
+    if (EPI != EPI_SWIGLU) return task * 4 + r;
+    const int c = task / (kRowTile / 2), qq = task % (kRowTile / 2);
+    return c * 2 * kRowTile + 2 * qq + (r >= 2 ? kRowTile : 0) + (r & 1);
+}
 
-    // ---- prologue: stage (normalised, position-scaled) activations
-    __shared__ float red[8];
-    for (int t = 0; t < NT; ++t) {
-        float *xt = xs + (size_t)t * K;
-        if (t >= p.T) {
-            for (int k = threadIdx.x * 4; k < K; k += blockDim.x * 4) *reinterpret_cast<float4 *>(xt + k) = make_float4(0, 0, 0, 0);
-            continue;
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+// Stage token t: RMS-normalise (when g != NULL) and split every block into hi / lo int8.
+// Run by the 256 consumer threads (warps 0..7), synchronised with named barrier 1.
+template <int QT>
+__device__ void stage_token(const GemvParams &p, const FwdArgs &a, int t, uint8_t *stage_t, float *red) {
+    constexpr int NTHR = 256;
+    const int nb = p.nb, K = p.K;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const float *xr = p.in.x + (size_t)(p.in.x_rows ? p.in.x_rows[t] : t) * K;
+    float rs = 1.f;
+    if (p.in.g) {
+        float ss = 0.f;
+        for (int k = threadIdx.x * 4; k < K; k += NTHR * 4) {
+            const float4 v = *reinterpret_cast<const float4 *>(xr + k);
+            ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
         }
-        const float *xr = p.in.x + (size_t)(p.in.x_rows ? p.in.x_rows[t] : t) * K;
-        float rs = 1.f;
-        if (p.in.g) {
-            float ss = 0.f;
-            for (int k = threadIdx.x * 4; k < K; k += blockDim.x * 4) {
-                const float4 v = *reinterpret_cast<const float4 *>(xr + k);
-                ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
-            }
-            for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-            __syncthreads();
-            if (lane == 0) red[warp] = ss;
-            __syncthreads();
-            float tot = 0.f;
+        for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        consumer_sync();
+        if (lane == 0) red[warp] = ss;
+        consumer_sync();
+        float tot = 0.f;
 #pragma unroll
-            for (int w = 0; w < 8; ++w) tot += red[w];
-            rs = 1.0f / sqrtf(tot / (float)K + a.eps);
-        }
-        for (int k = threadIdx.x * 4; k < K; k += blockDim.x * 4) {
-            float4 v = *reinterpret_cast<const float4 *>(xr + k);
+        for (int w = 0; w < 8; ++w) tot += red[w];
+        rs = 1.0f / sqrtf(tot / (float)K + a.eps);
+    }
+    uint8_t *hp = stage_t, *lp = stage_t + (size_t)nb * 32;
+    float2 *mp = reinterpret_cast<float2 *>(stage_t + (size_t)nb * 64);
+    for (int b = threadIdx.x; b < nb; b += NTHR) {
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+            float4 q = *reinterpret_cast<const float4 *>(xr + b * 32 + j);
             if (p.in.g) {
-                const float4 g = *reinterpret_cast<const float4 *>(p.in.g + k);
-                v.x = v.x * rs * g.x; v.y = v.y * rs * g.y; v.z = v.z * rs * g.z; v.w = v.w * rs * g.w;
+                const float4 g = *reinterpret_cast<const float4 *>(p.in.g + b * 32 + j);
+                q.x = q.x * rs * g.x; q.y = q.y * rs * g.y; q.z = q.z * rs * g.z; q.w = q.w * rs * g.w;
             }
-            const int b = k >> 5, j = (k & 31) >> 2;   // chunk j of block b: elements 4j..4j+3
-            if (QT == Q4) {
-                // element e = 4j + c: e < 16 -> byte e low nibble; else byte e-16 high nibble
-                const int hi = j >= 4;
-                v.x *= __int_as_float((127 - q4_shift(0, hi)) << 23);
-                v.y *= __int_as_float((127 - q4_shift(1, hi)) << 23);
-                v.z *= __int_as_float((127 - q4_shift(2, hi)) << 23);
-                v.w *= __int_as_float((127 - q4_shift(3, hi)) << 23);
-            }
-            *reinterpret_cast<float4 *>(xt + xs_chunk(b, j)) = v;
+            v[j] = q.x; v[j + 1] = q.y; v[j + 2] = q.z; v[j + 3] = q.w;
         }
+        float amax = 0.f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(v[j]));
+        const float s = amax * (1.0f / 127.0f);
+        const float inv = amax > 0.f ? 127.0f / amax : 0.f;
+        uint32_t hw[8], lw[8];
+        int sh = 0, sl = 0;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+            uint32_t hb = 0, lb = 0;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float y = v[4 * w + e] * inv;
+                const float h = fminf(fmaxf(rintf(y), -127.f), 127.f);
+                const float l = fminf(fmaxf(rintf((y - h) * 128.f), -127.f), 127.f);
+                sh += (int)h;
+                sl += (int)l;
+                hb |= ((uint32_t)(int)h & 0xffu) << (8 * e);
+                lb |= ((uint32_t)(int)l & 0xffu) << (8 * e);
+            }
+            hw[w] = hb;
+            lw[w] = lb;
+        }
+        *reinterpret_cast<uint4 *>(hp + plane_chunk_off(b, 0)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        *reinterpret_cast<uint4 *>(hp + plane_chunk_off(b, 1)) = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+        *reinterpret_cast<uint4 *>(lp + plane_chunk_off(b, 0)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        *reinterpret_cast<uint4 *>(lp + plane_chunk_off(b, 1)) = make_uint4(lw[4], lw[5], lw[6], lw[7]);
+        const int C = QT == Q4 ? 8 * (128 * sh + sl) : 0;
+        mp[b] = make_float2(s * (1.0f / 128.0f), __int_as_float(C));
+    }
+}
+
+// ---------------------------------------------------------------- TMA-bulk streaming kernel
+// Warp 8 (one elected lane) streams the weight rows of consecutive "stages" -- TPS tasks of 4
+// rows each, contiguous in the quant and scale planes -- into a ring of S shared-memory slots
+// with cp.async.bulk (mbarrier completion); it starts before the previous kernel's results
+// are needed, since the weights do not depend on them. Warps 0..7 stage the activations, then
+// consume the ring: warp w takes task w / KS of the stage and the w % KS-th slice of its
+// blocks (KS = 8 / TPS), the slices are summed through shared memory and TPS * NT threads
+// apply the epilogue. Every wait is bounded: on a timeout the kernel records an error and
+// returns instead of spinning.
+constexpr int kConsumerWarps = 8;
+constexpr int kMaxStages = 8;
+constexpr uint32_t kSpinLimit = 1u << 24;
+
+struct StagePlan {
+    int tps;            // tasks per stage (4, 2 or 1)
+    int slots;          // ring depth
+    int qs_bytes;       // quant bytes of one stage
+    int sc_bytes;       // scale bytes of one stage
+    int stage_bytes;    // qs + sc, rounded to 128
+    size_t x_bytes;     // staged activations
+    size_t smem;        // total dynamic shared memory
+};
+
+__host__ __device__ inline StagePlan stage_plan(int nb, int qb, int nt, bool swiglu, size_t budget) {
+    StagePlan pl{};
+    const int row = nb * qb;
+    pl.tps = 4;
+    while (pl.tps > (swiglu ? 2 : 1) && pl.tps * 4 * (row + nb * 2) > 40 * 1024) pl.tps /= 2;
+    pl.qs_bytes = pl.tps * 4 * row;
+    pl.sc_bytes = pl.tps * nb * 8;
+    pl.stage_bytes = (pl.qs_bytes + pl.sc_bytes + 127) / 128 * 128;
+    pl.x_bytes = ((size_t)nt * stage_bytes_per_token(nb) + 127) / 128 * 128;
+    const size_t room = budget > pl.x_bytes + 1024 ? budget - pl.x_bytes - 1024 : 0;
+    pl.slots = (int)(room / pl.stage_bytes);
+    if (pl.slots > kMaxStages) pl.slots = kMaxStages;
+    pl.smem = pl.x_bytes + (size_t)pl.slots * pl.stage_bytes + 2 * kMaxStages * 8;
+    return pl;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+// true when the phase with the given parity has completed; false after kSpinLimit polls
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+    const uint32_t a = smem_u32(bar);
+    for (uint32_t i = 0; i < kSpinLimit; ++i) {
+        uint32_t done;
+        asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+                     : "=r"(done) : "r"(a), "r"(parity) : "memory");
+        if (done) return true;
+    }
+    return false;
+}
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
+}
+// First task of stage `st`, and the global rows / scale quads a stage copies.
+template <int EPI>
+__device__ __forceinline__ void stage_rows(int st, int tps, int &row_a, int &row_b) {
+    const int t0 = st * tps;
+    if (EPI != EPI_SWIGLU) {
+        row_a = t0 * 4;
+        row_b = -1;
+    } else {
+        const int c = t0 / (kRowTile / 2), qq = t0 % (kRowTile / 2);
+        row_a = c * 2 * kRowTile + 2 * qq;   // 2 * tps gate rows
+        row_b = row_a + kRowTile;            // 2 * tps up rows
+    }
+}
+
+template <int QT, int NT, int EPI, bool OUT16>
+__global__ void __launch_bounds__(288, 1) k_gemv(const GemvParams p, const FwdArgs a, const int layer) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    constexpr int QB = QT == Q8 ? 32 : 16;
+    const int nb = p.nb;
+    const StagePlan pl = stage_plan(nb, QB, NT, EPI == EPI_SWIGLU, (size_t)kGemvSmemTotal);
+    uint8_t *xstage = smem;
+    uint8_t *ring = smem + pl.x_bytes;
+    uint64_t *full = reinterpret_cast<uint64_t *>(ring + (size_t)pl.slots * pl.stage_bytes);
+    uint64_t *empty = full + kMaxStages;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tps = pl.tps, S = pl.slots;
+    const int n_stages = (p.n_tasks + tps - 1) / tps;
+    const int row_bytes = nb * QB;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < S; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], kConsumerWarps);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
 
-    const float *xs_b[NT];
-#pragma unroll
-    for (int t = 0; t < NT; ++t) xs_b[t] = xs + (size_t)t * K;
+    if (warp == kConsumerWarps) {
+        // ---------------- producer
+        if (lane == 0) {
+            int k = 0;
+            bool ok = true;
+            for (int st = blockIdx.x; st < n_stages; st += gridDim.x, ++k) {
+                const int slot = k % S;
+                if (k >= S && !(ok = mbar_wait(&empty[slot], ((k / S) - 1) & 1))) break;
+                uint8_t *dst = ring + (size_t)slot * pl.stage_bytes;
+                int ra, rb;
+                stage_rows<EPI>(st, tps, ra, rb);
+                const int tasks = min(tps, p.n_tasks - st * tps);   // the last stage may be short
+                const int rows = EPI == EPI_SWIGLU ? 2 * tasks : 4 * tasks;
+                const int quads = EPI == EPI_SWIGLU ? (2 * tasks + 3) / 4 : tasks;
+                const uint32_t qbytes = (uint32_t)rows * row_bytes, sbytes = (uint32_t)quads * nb * 8;
+                const uint32_t tx = (EPI == EPI_SWIGLU ? 2u : 1u) * (qbytes + sbytes);
+                mbar_expect_tx(&full[slot], tx);
+                bulk_g2s(dst, p.qs + (size_t)ra * row_bytes, qbytes, &full[slot]);
+                bulk_g2s(dst + pl.qs_bytes, p.sc + (size_t)(ra >> 2) * nb * 4, sbytes, &full[slot]);
+                if (EPI == EPI_SWIGLU) {
+                    bulk_g2s(dst + pl.qs_bytes / 2, p.qs + (size_t)rb * row_bytes, qbytes, &full[slot]);
+                    bulk_g2s(dst + pl.qs_bytes + pl.sc_bytes / 2, p.sc + (size_t)(rb >> 2) * nb * 4, sbytes, &full[slot]);
+                }
+            }
+            if (!ok) atomicExch(a.err, 1);
+            // drain: every copy this CTA issued must land before the CTA exits
+            const int issued = k;
+            for (int j = (issued > S ? issued - S : 0); j < issued; ++j) mbar_wait(&full[j % S], (j / S) & 1);
+        }
+        return;
+    }
 
+    // ---------------- consumers (256 threads)
+    LCX_PDL_WAIT();
+    LCX_PDL_TRIGGER();
+    __shared__ float red[8];
+    for (int t = 0; t < NT; ++t) {
+        if (t < p.T) {
+            stage_token<QT>(p, a, t, xstage + t * stage_bytes_per_token(nb), red);
+        } else {
+            for (size_t i = threadIdx.x * 16; i < stage_bytes_per_token(nb); i += 256 * 16)
+                *reinterpret_cast<uint4 *>(xstage + t * stage_bytes_per_token(nb) + i) = make_uint4(0, 0, 0, 0);
+        }
+    }
+    consumer_sync();
+
+    const int KS = kConsumerWarps / tps;
+    const int tg = warp / KS, ks = warp % KS;
+    const int nbs = (nb + KS - 1) / KS, b_lo = ks * nbs, b_hi = min(nb, b_lo + nbs);
+    __shared__ float part[2][16][kConsumerWarps][NT];   // [parity][stage row][k-slice][token]
     unsigned long long best[NT];
 #pragma unroll
     for (int t = 0; t < NT; ++t) best[t] = 0ull;
 
-    const int total_warps = gridDim.x * 8;
-    for (int task = blockIdx.x * 8 + warp; task < p.n_tasks; task += total_warps) {
-        int rbase[ROWS / 4];
-        if (ROWS == 4) {
-            rbase[0] = task * 4;
-        } else {
-            const int c = task / (kRowTile / 4), qq = task % (kRowTile / 4);
-            rbase[0] = c * 2 * kRowTile + 4 * qq;
-            rbase[ROWS / 4 - 1] = rbase[0] + kRowTile;
+    // After a timed-out wait a consumer keeps walking the stage loop (so every named barrier
+    // still sees all 256 threads) but skips the waits and the work.
+    bool dead = false;
+    int k = 0;
+    for (int st = blockIdx.x; st < n_stages; st += gridDim.x, ++k) {
+        const int slot = k % S;
+        if (!dead && !mbar_wait(&full[slot], (k / S) & 1)) {
+            dead = true;
+            atomicExch(a.err, 1);
         }
-        float acc[ROWS][NT];
+        const uint8_t *sq = ring + (size_t)slot * pl.stage_bytes;
+        const __half *ss = reinterpret_cast<const __half *>(sq + pl.qs_bytes);
+        // local rows of this warp's task inside the stage, and where their scales sit
+        int lrow[4], sidx[4];
 #pragma unroll
-        for (int r = 0; r < ROWS; ++r)
+        for (int r = 0; r < 4; ++r) {
+            if (EPI != EPI_SWIGLU) {
+                lrow[r] = tg * 4 + r;
+                sidx[r] = tg * nb * 4 + r;                              // + b * 4
+            } else {
+                const int gl = 2 * tg + (r & 1);                        // row within the gate / up half
+                lrow[r] = (r < 2 ? 0 : 2 * tps) + gl;
+                sidx[r] = (r < 2 ? 0 : (tps / 2) * nb * 4) + (gl >> 2) * nb * 4 + (gl & 3);
+            }
+        }
+        float acc[4][NT];
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
 #pragma unroll
             for (int t = 0; t < NT; ++t) acc[r][t] = 0.f;
-
-        // blocks in flight per lane: about 64 registers of weight data
-        constexpr int WORDS = ROWS * (QT == Q8 ? 8 : 4) * NT;
-        constexpr int U = WORDS <= 16 ? 4 : WORDS <= 32 ? 2 : 1;
-        for (int b0 = lane; b0 < nb; b0 += 32 * U) {
-            uint4 wq[U][ROWS][QT == Q8 ? 2 : 1];
-            uint2 sq[U][ROWS / 4];
+        for (int b = b_lo + lane; b < (dead ? b_lo : b_hi); b += 32) {
+            XQ xq[NT];
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int b = b0 + 32 * u;
-                if (b < nb) {
+            for (int t = 0; t < NT; ++t) load_xq(xstage + t * stage_bytes_per_token(nb), nb, b, xq[t]);
 #pragma unroll
-                    for (int r = 0; r < ROWS; ++r) {
-                        const int row = rbase[r / 4] + (r & 3);
-                        const uint4 *src = reinterpret_cast<const uint4 *>(p.qs + ((size_t)row * nb + b) * (QT == Q8 ? 32 : 16));
-                        wq[u][r][0] = __ldg(src);
-                        if (QT == Q8) wq[u][r][QT == Q8 ? 1 : 0] = __ldg(src + 1);
-                    }
+            for (int r = 0; r < 4; ++r) {
+                const uint4 *wp = reinterpret_cast<const uint4 *>(sq + ((size_t)lrow[r] * nb + b) * QB);
+                const uint4 w0 = wp[0];
+                const uint4 w1 = QT == Q8 ? wp[1] : w0;
+                const float d = __half2float(ss[sidx[r] + b * 4]);
 #pragma unroll
-                    for (int g = 0; g < ROWS / 4; ++g)
-                        sq[u][g] = __ldg(reinterpret_cast<const uint2 *>(p.sc + ((size_t)(rbase[g] >> 2) * nb + b) * 4));
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int b = b0 + 32 * u;
-                if (b < nb) {
-#pragma unroll
-                    for (int r = 0; r < ROWS; ++r) {
-                        float part[NT];
-                        if (QT == Q4) q4_block<NT>(wq[u][r][0], xs_b, b, part);
-                        else q8_block<NT>(wq[u][r][0], wq[u][r][QT == Q8 ? 1 : 0], xs_b, b, part);
-                        const uint32_t sbits = (r & 2) ? sq[u][r / 4].y : sq[u][r / 4].x;
-                        const float d = __half2float(__ushort_as_half((unsigned short)((r & 1) ? (sbits >> 16) : (sbits & 0xffffu))));
-#pragma unroll
-                        for (int t = 0; t < NT; ++t) acc[r][t] = fmaf(d, part[t], acc[r][t]);
-                    }
+                for (int t = 0; t < NT; ++t) {
+                    const int P = QT == Q4 ? q4_idot(w0, xq[t]) : q8_idot(w0, w1, xq[t]);
+                    acc[r][t] = fmaf(d * xq[t].s, (float)P, acc[r][t]);
                 }
             }
         }
-        // reduce across lanes
+        // the slot's bytes are no longer read by this warp: hand it back to the producer
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
 #pragma unroll
-        for (int r = 0; r < ROWS; ++r)
+        for (int r = 0; r < 4; ++r)
 #pragma unroll
             for (int t = 0; t < NT; ++t) {
                 float v = acc[r][t];
 #pragma unroll
                 for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-                acc[r][t] = v;
+                if (lane == 0) part[k & 1][tg * 4 + r][ks][t] = v;
             }
-        if (lane < NT && lane < p.T) {
-            const int t = lane;
-            float v0[4], v1[4];
+        consumer_sync();
+        // epilogue: one thread per (task, token)
+        const int e = threadIdx.x;
+        const int tasks = min(tps, p.n_tasks - st * tps);
+        if (!dead && e < tasks * NT) {
+            const int et = e / NT, t = e % NT;
+            if (t < p.T) {
+                float v[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                // select acc[.][t] with a static index
-                float s0 = 0.f, s1 = 0.f;
+                for (int r = 0; r < 4; ++r) {
+                    float sum = 0.f;
+                    for (int q = 0; q < KS; ++q) sum += part[k & 1][et * 4 + r][q][t];
+                    v[r] = sum;
+                }
+                const int task = st * tps + et;
+                if (EPI == EPI_SWIGLU) {
+                    const int c = task / (kRowTile / 2), qq = task % (kRowTile / 2);
+                    const float g2[2] = {v[0], v[1]}, u2[2] = {v[2], v[3]};
+                    epi_swiglu2<OUT16>(a, t, c * kRowTile + 2 * qq, g2, u2);
+                } else {
+                    unsigned long long bk = 0ull;
+                    epi_quad<EPI>(a, layer, t, task * 4, p.N, v, bk);
 #pragma unroll
-                for (int tt = 0; tt < NT; ++tt)
-                    if (tt == t) { s0 = acc[j][tt]; s1 = acc[(ROWS == 8 ? 4 : 0) + j][tt]; }
-                v0[j] = s0;
-                v1[j] = s1;
-            }
-            if (ROWS == 8) {
-                const int c = task / (kRowTile / 4), qq = task % (kRowTile / 4);
-                epi_swiglu<OUT16>(a, t, c * kRowTile + 4 * qq, v0, v1);
-            } else {
-                unsigned long long bk = 0ull;
-                epi_quad<EPI>(a, layer, t, rbase[0], p.N, v0, bk);
-#pragma unroll
-                for (int tt = 0; tt < NT; ++tt)
-                    if (tt == t) best[tt] = bk > best[tt] ? bk : best[tt];
+                    for (int tt = 0; tt < NT; ++tt)
+                        if (tt == t) best[tt] = bk > best[tt] ? bk : best[tt];
+                }
             }
         }
+        // part[k & 1] is rewritten two stages later, after the next consumer_sync
     }
     if (EPI == EPI_LOGITS) {
         __shared__ unsigned long long cbest[NT];
-        __syncthreads();
+        consumer_sync();
         if (threadIdx.x < NT) cbest[threadIdx.x] = 0ull;
-        __syncthreads();
-        if (lane < NT && lane < p.T) {
+        consumer_sync();
 #pragma unroll
-            for (int tt = 0; tt < NT; ++tt)
-                if (tt == lane && best[tt]) atomicMax(&cbest[tt], best[tt]);
-        }
-        __syncthreads();
+        for (int tt = 0; tt < NT; ++tt)
+            if (best[tt]) atomicMax(&cbest[tt], best[tt]);
+        consumer_sync();
         if (threadIdx.x < NT && threadIdx.x < p.T && cbest[threadIdx.x]) atomicMax(&a.amax_key[threadIdx.x], cbest[threadIdx.x]);
     }
 }
 
-template <int QT, int NT, int ROWS, int EPI, bool OUT16>
+template <int QT, int NT, int EPI, bool OUT16>
 cudaError_t run(const GemvParams &p, const FwdArgs &a, int layer, cudaStream_t s) {
-    auto kern = k_gemv<QT, NT, ROWS, EPI, OUT16>;
-    const size_t smem = (size_t)NT * p.K * sizeof(float);
-    static int configured_smem = 0;   // per instantiation
-    if ((int)smem > configured_smem) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemvSmemX + 1024);
-        if (e != cudaSuccess) return e;
-        configured_smem = kGemvSmemX + 1024;
-    }
+    auto kern = k_gemv<QT, NT, EPI, OUT16>;
+    constexpr int QB = QT == Q8 ? 32 : 16;
+    const StagePlan pl = stage_plan(p.nb, QB, NT, EPI == EPI_SWIGLU, (size_t)kGemvSmemTotal);
+    if (pl.slots < 2) return cudaErrorInvalidConfiguration;
     static int n_sm = 0;
     if (!n_sm) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemvSmemTotal);
+        if (e != cudaSuccess) return e;
         int dev = 0;
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
     }
-    int occ = 1;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, 256, smem);
-    if (occ < 1) occ = 1;
-    int grid = (p.n_tasks + 7) / 8;
-    grid = grid < n_sm * occ ? grid : n_sm * occ;
+    const int n_stages = (p.n_tasks + pl.tps - 1) / pl.tps;
+    int grid = n_stages < n_sm ? n_stages : n_sm;
     if (grid < 1) grid = 1;
-    kern<<<grid, 256, smem, s>>>(p, a, layer);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(288), pl.smem, s, p, a, layer);
 }
 
 }  // namespace gemv_detail

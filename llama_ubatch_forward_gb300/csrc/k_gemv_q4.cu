@@ -5,20 +5,20 @@
 namespace lcx {
 namespace gemv_detail {
 
-template <int QT, int EPI, bool OUT16, int ROWS>
+template <int QT, int EPI, bool OUT16>
 static cudaError_t dispatch_nt(const GemvParams &p, const FwdArgs &a, int layer, cudaStream_t s) {
-    if (p.T <= 1) return run<QT, 1, ROWS, EPI, OUT16>(p, a, layer, s);
-    if (p.T <= 2) return run<QT, 2, ROWS, EPI, OUT16>(p, a, layer, s);
-    if (p.T <= 4) return run<QT, 4, ROWS, EPI, OUT16>(p, a, layer, s);
-    return run<QT, 8, ROWS, EPI, OUT16>(p, a, layer, s);
+    if (p.T <= 1) return run<QT, 1, EPI, OUT16>(p, a, layer, s);
+    if (p.T <= 2) return run<QT, 2, EPI, OUT16>(p, a, layer, s);
+    if (p.T <= 4) return run<QT, 4, EPI, OUT16>(p, a, layer, s);
+    return run<QT, 8, EPI, OUT16>(p, a, layer, s);
 }
 
 cudaError_t dispatch_q4(const GemvParams &p, Epi epi, const FwdArgs &a, int layer, cudaStream_t s) {
     switch (epi) {
-        case EPI_QKV: return dispatch_nt<Q4, EPI_QKV, false, 4>(p, a, layer, s);
-        case EPI_RESID: return dispatch_nt<Q4, EPI_RESID, false, 4>(p, a, layer, s);
-        case EPI_SWIGLU: return dispatch_nt<Q4, EPI_SWIGLU, false, 8>(p, a, layer, s);
-        case EPI_LOGITS: return dispatch_nt<Q4, EPI_LOGITS, false, 4>(p, a, layer, s);
+        case EPI_QKV: return dispatch_nt<Q4, EPI_QKV, false>(p, a, layer, s);
+        case EPI_RESID: return dispatch_nt<Q4, EPI_RESID, false>(p, a, layer, s);
+        case EPI_SWIGLU: return dispatch_nt<Q4, EPI_SWIGLU, false>(p, a, layer, s);
+        case EPI_LOGITS: return dispatch_nt<Q4, EPI_LOGITS, false>(p, a, layer, s);
     }
     return cudaErrorInvalidValue;
 }

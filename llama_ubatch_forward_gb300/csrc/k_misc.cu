@@ -83,6 +83,8 @@ cudaError_t launch_rope_table(float2 *tab, int n_pos, int hd, double theta, cuda
 __global__ void k_embed(const uint8_t *__restrict__ table, int type, int d, const int32_t *__restrict__ tok, float *x,
                         const int32_t *__restrict__ pt_upd, int n_upd, int32_t *pt, unsigned long long *keys,
                         int n_out) {
+    LCX_PDL_WAIT();
+    LCX_PDL_TRIGGER();
     const int t = blockIdx.x;
     const int id = tok[t];
     const uint8_t *row = table + (int64_t)id * stored_row_bytes(type, d);
@@ -94,10 +96,9 @@ __global__ void k_embed(const uint8_t *__restrict__ table, int type, int d, cons
 }
 
 cudaError_t launch_embed(const FwdArgs &a, int t_embd, const void *tok_embd, cudaStream_t s, int64_t &launches) {
-    k_embed<<<a.T, 256, 0, s>>>((const uint8_t *)tok_embd, t_embd, a.d, a.tok_src, a.x, a.ub.pt_upd, a.ub.n_upd, a.pt,
-                                a.amax_key, a.n_out);
     ++launches;
-    return cudaGetLastError();
+    return launch_pdl(k_embed, dim3(a.T), dim3(256), 0, s, (const uint8_t *)tok_embd, t_embd, a.d, a.tok_src, a.x,
+                      a.ub.pt_upd, a.ub.n_upd, a.pt, a.amax_key, a.n_out);
 }
 
 __global__ void k_get_rows(const uint8_t *__restrict__ table, int type, int64_t n_cols, const int32_t *__restrict__ ids,
@@ -118,6 +119,8 @@ cudaError_t launch_get_rows(int type, const void *table, int64_t n_cols, const i
 // out[r][:] = f16(x[row r] / sqrt(mean(x^2) + eps) * g); row r of x is rows[r] (or r).
 __global__ void k_rmsnorm_h(const float *__restrict__ x, const int32_t *__restrict__ rows, int d,
                             const float *__restrict__ g, float eps, __half *__restrict__ out) {
+    LCX_PDL_WAIT();
+    LCX_PDL_TRIGGER();
     const int r = blockIdx.x;
     const float *xr = x + (int64_t)(rows ? rows[r] : r) * d;
     float ss = 0.f;
@@ -149,24 +152,25 @@ __global__ void k_rmsnorm_h(const float *__restrict__ x, const int32_t *__restri
 
 cudaError_t launch_rmsnorm_h(const float *x, const int32_t *rows, int T, int d, const float *g, float eps,
                              __half *out, cudaStream_t s, int64_t &launches) {
-    k_rmsnorm_h<<<T, 256, 0, s>>>(x, rows, d, g, eps, out);
     ++launches;
-    return cudaGetLastError();
+    return launch_pdl(k_rmsnorm_h, dim3(T), dim3(256), 0, s, x, rows, d, g, eps, out);
 }
 
 // ------------------------------------------------------------------ argmax
 // keys hold (ordered float bits << 32) | (0xffffffff - index): the max key is the largest
 // logit, ties to the lowest index.
 __global__ void k_argmax_final(const unsigned long long *__restrict__ keys, int n, int32_t *__restrict__ dst) {
+    LCX_PDL_WAIT();
+    LCX_PDL_TRIGGER();
     int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i < n) dst[i] = (int32_t)(0xffffffffu - (uint32_t)(keys[i] & 0xffffffffull));
 }
 
 cudaError_t launch_argmax_final(const FwdArgs &a, int32_t *dst, cudaStream_t s, int64_t &launches) {
     if (a.n_out <= 0) return cudaSuccess;
-    k_argmax_final<<<(a.n_out + 127) / 128, 128, 0, s>>>(a.amax_key, a.n_out, dst);
     ++launches;
-    return cudaGetLastError();
+    return launch_pdl(k_argmax_final, dim3((a.n_out + 127) / 128), dim3(128), 0, s,
+                      (const unsigned long long *)a.amax_key, a.n_out, dst);
 }
 
 }  // namespace lcx

@@ -6,12 +6,15 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace lcx {
 
 constexpr int kPage = 64;            // KV cells per page (all of one sequence)
 constexpr int kRowTile = 128;        // internal row padding of every matrix (tensor-core M tile)
 constexpr int kGemvMaxT = 8;         // largest ubatch the weight-streaming GEMV serves
-constexpr int kGemvSmemX = 160 * 1024;  // bytes of staged activations a GEMV CTA may hold
+constexpr int kGemvSmemX = 96 * 1024;   // bytes of staged activations a GEMV CTA may hold
+constexpr int kGemvSmemTotal = 212 * 1024;  // dynamic shared memory of a GEMV CTA (static use < 12 KB)
 
 enum QType { QF16 = 1, Q4 = 2, Q8 = 8 };
 
@@ -76,6 +79,7 @@ struct FwdArgs {
     float *att_part;   // partial (m, l, acc[hd]) per (token, q head, split)
     int32_t *att_cnt;  // [T][KV] arrival counters, zero between launches
     int att_max_split;
+    int32_t *err;      // device error word: set by a kernel whose bounded wait timed out
     // KV cache
     __half *kc, *vc;   // [L][n_pages][KV][kPage][hd]
     int n_pages;
@@ -119,4 +123,26 @@ int attention_splits(const FwdArgs &a, int max_natt, int *chunk);
 // *counter_offset); 0 when every token fits in a single split.
 size_t attention_scratch_bytes(const FwdArgs &a, int max_natt, size_t *counter_offset);
 
+// Launch with programmatic dependent launch allowed: the kernel may start while the previous
+// kernel on the stream finishes; it must execute griddepcontrol.wait before reading anything
+// the previous kernels wrote (and before writing anything they read).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 }  // namespace lcx
+
+#define LCX_PDL_WAIT() asm volatile("griddepcontrol.wait;" ::: "memory")
+#define LCX_PDL_TRIGGER() asm volatile("griddepcontrol.launch_dependents;")

@@ -328,6 +328,7 @@ extern "C" lcx_ctx *lcx_ctx_create(lcx_model *m, uint32_t n_ctx, uint32_t n_seq_
         part_rows * G * (hd + 2) * 4,        // attention partials
         (size_t)T * KV * 4,                  // attention counters
         (size_t)std::max<int>(T, 4096) * 4,  // argmax per output row
+        256,                                 // device error word
     };
     for (size_t s : sizes) ws += (s + 255) / 256 * 256;
     if (e == cudaSuccess) ok(cudaMalloc(&c->ws, ws), "workspace");
@@ -347,6 +348,7 @@ extern "C" lcx_ctx *lcx_ctx_create(lcx_model *m, uint32_t n_ctx, uint32_t n_seq_
         a.att_part = carve<float>(p, part_rows * G * (hd + 2));
         a.att_cnt = carve<int32_t>(p, (size_t)T * KV);
         c->amax_dev = carve<int32_t>(p, (size_t)std::max<int>(T, 4096));
+        a.err = carve<int32_t>(p, 64);
         a.d = d; a.H = H; a.KV = KV; a.hd = hd; a.F = hp.n_ff; a.F_pad = Fp; a.V = V; a.L = L;
         a.eps = hp.rms_eps;
         a.kc = c->kc; a.vc = c->vc; a.n_pages = c->n_pages;
@@ -639,6 +641,16 @@ cudaError_t run_forward(lcx_ctx *c, FwdArgs &a, int max_natt, double att_cells, 
 
 }  // namespace
 
+// Reads and clears the device error word (a kernel's bounded wait timed out). Synchronizes.
+static bool device_error_raised(lcx_ctx *c) {
+    int32_t v = 0;
+    if (cudaMemcpy(&v, c->base.err, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return true;
+    if (!v) return false;
+    cudaMemset(c->base.err, 0, sizeof(v));
+    set_error_text("a kernel's bounded wait timed out");
+    return true;
+}
+
 extern "C" int32_t lcx_decode(lcx_ctx *c, lcx_batch batch, float *logits_out, int32_t *argmax_out) {
     if (!c) return LCX_INVALID;
     c->n_outputs_last = 0;
@@ -713,6 +725,7 @@ extern "C" int32_t lcx_decode(lcx_ctx *c, lcx_batch batch, float *logits_out, in
             set_err("argmax copy", e);
             return LCX_COMPUTE_FAILED;
         }
+        if (device_error_raised(c)) return LCX_COMPUTE_FAILED;
         std::memcpy(argmax_out, c->amax_host, (size_t)n_out_total * 4);
     }
     c->st.n_decode++;
@@ -789,6 +802,7 @@ extern "C" int32_t lcx_decode_greedy(lcx_ctx *c, int32_t seq, int32_t token, int
             else {
                 e = cudaMemcpyAsync(c->amax_host, c->amax_dev, (size_t)ns * 4, cudaMemcpyDeviceToHost, c->stream);
                 if (e == cudaSuccess) e = cudaStreamSynchronize(c->stream);
+                if (e == cudaSuccess && device_error_raised(c)) e = cudaErrorLaunchFailure;
                 if (e == cudaSuccess) std::memcpy(tokens_out + c0, c->amax_host, (size_t)ns * 4);
             }
         }

@@ -21,9 +21,18 @@ def to_device(a: np.ndarray, device="cuda"):
 
 
 def upload(host, device="cuda") -> Model:
-    """host: an object with cfg, tok_embd, output_norm, output (or None) and layers (dicts)."""
-    layers = [{k: to_device(L[k], device) for k in LAYER_KEYS} for L in host.layers]
+    """host: an object with cfg, tok_embd, output_norm, output (or None) and layers (dicts).
+
+    Matrices are uploaded one layer at a time and released once the model holds its own
+    re-laid-out copy; the embedding table and the norm gains stay referenced by the model."""
+    import torch
     tok = to_device(host.tok_embd, device)
     on = to_device(host.output_norm, device)
     out = None if host.output is None else to_device(host.output, device)
-    return Model(hparams_of(host.cfg, len(host.layers)), tok, on, out, layers)
+    layers = [{k: to_device(L[k], device) for k in LAYER_KEYS} for L in host.layers]
+    m = Model(hparams_of(host.cfg, len(host.layers)), tok, on, out, layers)
+    torch.cuda.synchronize()
+    # keep only what the model reads in place
+    m._keep = (tok, on, None, [{"attn_norm": L["attn_norm"], "ffn_norm": L["ffn_norm"]} for L in layers])
+    del layers, out
+    return m
