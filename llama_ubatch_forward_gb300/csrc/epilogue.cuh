@@ -79,7 +79,7 @@ __device__ __forceinline__ void epi_swiglu(const FwdArgs &a, int t, int f0, cons
         const int f = f0 + j;
         if (f >= a.F) break;
         const float h = silu_f(g[j]) * u[j];
-        if (OUT16) a.h16[(size_t)t * a.F_pad + f] = __float2half_rn(h);
+        if (OUT16) store_split(a.h16, a.h16_lo, (size_t)t * a.F_pad + f, h);
         else a.h32[(size_t)t * a.F_pad + f] = h;
     }
 }
@@ -92,7 +92,7 @@ __device__ __forceinline__ void epi_swiglu2(const FwdArgs &a, int t, int f0, con
         const int f = f0 + j;
         if (f >= a.F) break;
         const float h = silu_f(g[j]) * u[j];
-        if (OUT16) a.h16[(size_t)t * a.F_pad + f] = __float2half_rn(h);
+        if (OUT16) store_split(a.h16, a.h16_lo, (size_t)t * a.F_pad + f, h);
         else a.h32[(size_t)t * a.F_pad + f] = h;
     }
 }

@@ -204,7 +204,7 @@ __global__ void __launch_bounds__(128) k_attn(const FwdArgs a, const int layer, 
         if (single) {
             const float o = A / L;
             const size_t oi = (size_t)t * qw + (size_t)(kvh * G + g) * HD + dd;
-            if (OUT16) a.o16[oi] = __float2half_rn(o);
+            if (OUT16) store_split(a.o16, a.o16_lo, oi, o);
             else a.o32[oi] = o;
         } else {
             float *pr = part + ((prow + sp) * G + g) * (HD + 2);
@@ -265,7 +265,7 @@ __global__ void __launch_bounds__(128) k_attn(const FwdArgs a, const int layer, 
         }
         for (; s2 < ns_t; ++s2) o = fmaf(sw[s2][g], __ldcg(part + ((prow + s2) * G + g) * (HD + 2) + 2 + dd), o);
         const size_t oi = (size_t)t * qw + (size_t)(kvh * G + g) * HD + dd;
-        if (OUT16) a.o16[oi] = __float2half_rn(o);
+        if (OUT16) store_split(a.o16, a.o16_lo, oi, o);
         else a.o32[oi] = o;
     }
     if (threadIdx.x == 0) a.att_cnt[t * a.KV + kvh] = 0;

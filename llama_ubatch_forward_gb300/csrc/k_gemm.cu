@@ -4,6 +4,8 @@
 //
 // This is the CUDA-core tiled version: a CTA computes 16 row tasks (quads, or gate/up quad
 // pairs for SwiGLU) x 32 tokens, with the weight tile dequantised once into shared memory.
+#include <cstdlib>
+
 #include "epilogue.cuh"
 
 namespace lcx {
@@ -25,7 +27,7 @@ __device__ __forceinline__ float deq(const uint8_t *qs, const __half *sc, int nb
 template <int QT, int ROWS, int EPI, bool OUT16>
 __global__ void __launch_bounds__(256) k_gemm_simt(const uint8_t *__restrict__ qs, const __half *__restrict__ sc, int N,
                                                    int nb, int n_tasks, int T, const __half *__restrict__ A,
-                                                   const FwdArgs a, int layer) {
+                                                   const __half *__restrict__ A_lo, const FwdArgs a, int layer) {
     __shared__ float Ws[32][TASKS * ROWS + 1];
     __shared__ float Xs[32][TT + 1];
     LCX_PDL_WAIT();
@@ -51,7 +53,8 @@ __global__ void __launch_bounds__(256) k_gemm_simt(const uint8_t *__restrict__ q
         }
         for (int i = threadIdx.x; i < 32 * TT; i += blockDim.x) {
             const int e = i % 32, tt = i / 32;
-            Xs[e][tt] = tok0 + tt < T ? __half2float(A[(size_t)(tok0 + tt) * K + b * 32 + e]) : 0.f;
+            const size_t ai = (size_t)(tok0 + tt) * K + b * 32 + e;
+            Xs[e][tt] = tok0 + tt < T ? __half2float(A[ai]) + __half2float(A_lo[ai]) : 0.f;
         }
         __syncthreads();
 #pragma unroll 8
@@ -90,30 +93,39 @@ __global__ void __launch_bounds__(256) k_gemm_simt(const uint8_t *__restrict__ q
 }
 
 template <int QT, int ROWS, int EPI, bool OUT16>
-cudaError_t run(const QMat &W, int n_tasks, int T, const __half *A, const FwdArgs &a, int layer, cudaStream_t s) {
+cudaError_t run(const QMat &W, int n_tasks, int T, const __half *A, const __half *A_lo, const FwdArgs &a, int layer,
+               cudaStream_t s) {
     dim3 grid((n_tasks + TASKS - 1) / TASKS, (T + TT - 1) / TT);
     return launch_pdl(k_gemm_simt<QT, ROWS, EPI, OUT16>, grid, dim3(256), 0, s, (const uint8_t *)W.qs,
-                      (const __half *)W.sc, W.N, W.nb, n_tasks, T, A, a, layer);
+                      (const __half *)W.sc, W.N, W.nb, n_tasks, T, A, A_lo, a, layer);
 }
 
 template <int QT>
-cudaError_t dispatch(const QMat &W, Epi epi, int T, const __half *A, const FwdArgs &a, int layer, cudaStream_t s) {
+cudaError_t dispatch(const QMat &W, Epi epi, int T, const __half *A, const __half *A_lo, const FwdArgs &a, int layer,
+                     cudaStream_t s) {
     switch (epi) {
-        case EPI_QKV: return run<QT, 4, EPI_QKV, false>(W, (W.N + 3) / 4, T, A, a, layer, s);
-        case EPI_RESID: return run<QT, 4, EPI_RESID, false>(W, (W.N + 3) / 4, T, A, a, layer, s);
-        case EPI_SWIGLU: return run<QT, 8, EPI_SWIGLU, true>(W, (a.F + 3) / 4, T, A, a, layer, s);
-        case EPI_LOGITS: return run<QT, 4, EPI_LOGITS, false>(W, (W.N + 3) / 4, T, A, a, layer, s);
+        case EPI_QKV: return run<QT, 4, EPI_QKV, false>(W, (W.N + 3) / 4, T, A, A_lo, a, layer, s);
+        case EPI_RESID: return run<QT, 4, EPI_RESID, false>(W, (W.N + 3) / 4, T, A, A_lo, a, layer, s);
+        case EPI_SWIGLU: return run<QT, 8, EPI_SWIGLU, true>(W, (a.F + 3) / 4, T, A, A_lo, a, layer, s);
+        case EPI_LOGITS: return run<QT, 4, EPI_LOGITS, false>(W, (W.N + 3) / 4, T, A, A_lo, a, layer, s);
     }
     return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
-cudaError_t launch_gemm(const QMat &W, Epi epi, int T, const __half *A, const FwdArgs &a, int layer, cudaStream_t s,
-                        int64_t &launches) {
+cudaError_t launch_gemm(const QMat &W, Epi epi, int T, const __half *A, const __half *A_lo, const FwdArgs &a,
+                        int layer, cudaStream_t s, int64_t &launches) {
+    // The tensor-core kernel is the GEMM; LCX_GEMM_SIMT=1 selects this CUDA-core version instead
+    // (same results up to summation order), for cross-checking the two on a device.
+    static const bool simt = [] {
+        const char *e = getenv("LCX_GEMM_SIMT");
+        return e && e[0] == '1';
+    }();
+    if (!simt) return launch_gemm_tc(W, epi, T, A, A_lo, a, layer, s, launches);
     ++launches;
-    if (W.type == Q4) return dispatch<Q4>(W, epi, T, A, a, layer, s);
-    if (W.type == Q8) return dispatch<Q8>(W, epi, T, A, a, layer, s);
+    if (W.type == Q4) return dispatch<Q4>(W, epi, T, A, A_lo, a, layer, s);
+    if (W.type == Q8) return dispatch<Q8>(W, epi, T, A, A_lo, a, layer, s);
     return cudaErrorInvalidValue;
 }
 

@@ -1,0 +1,512 @@
+// Tensor-core GEMM for prefill-sized ubatches on sm_103a (tcgen05 + TMEM + TMA):
+//   out[t][n] = sum_k A[t][k] W[n][k]
+// with A the f16 activations [T][K] (RMS-normed input, attention output or SwiGLU output) and W a
+// Q4_0 / Q8_0 matrix dequantised to f16 on load, f32 accumulation in tensor memory, and the
+// shared epilogues (RoPE + KV append, residual add, SwiGLU, logits + argmax).
+//
+// Prefill is where the work is compute-bound (KV-cache section of the article: prefill loads the
+// compute units), so the contraction runs on the 5th-generation tensor cores. One CTA computes a
+// 128-row weight tile (two for the fused gate/up matrix) against BN tokens:
+//   warp 0      TMA producer: raw quant + scale tiles of the weights (issued before the
+//               grid-dependency wait: the weights do not depend on the previous kernel), then the
+//               activation tiles [BN][64] f16 (high and low parts) with the 128-byte swizzle;
+//   warp 1      allocates the TMEM accumulator and issues tcgen05.mma from one lane -- W A_hi and
+//               W A_lo into the same accumulator, so the activations keep about 22 bits and only
+//               the f16 rounding of the dequantised weights remains; each stage's tcgen05.commit
+//               frees its shared-memory slot;
+//   warps 2..5  dequantise the raw blocks of their row into the K-major SWIZZLE_128B f16 tile the
+//               MMA reads ((q - 8) or q is exact in f16, then one f16 multiply by the block scale),
+//               then run the epilogue from TMEM with tcgen05.ld.
+// All mbarrier waits are bounded; a timeout sets the context's error word and the CTA finishes
+// without further work.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+#include <vector>
+
+#include "epilogue.cuh"
+
+namespace lcx {
+namespace tc {
+
+constexpr int BM = 128;   // weight rows per MMA (tensor-memory lanes)
+constexpr int BK = 64;    // k per stage: 128 bytes of f16
+constexpr uint32_t kSpin = 1u << 22;
+
+__device__ __forceinline__ uint32_t saddr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t *b, uint32_t n) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(saddr(b)), "r"(n));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *b, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(saddr(b)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *b) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(saddr(b)) : "memory");
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t *b, uint32_t parity) {
+    const uint32_t a = saddr(b);
+    for (uint32_t i = 0; i < kSpin; ++i) {
+        uint32_t done;
+        // each poll suspends for at most ~1 us (time hint), so a wait gives up after a few seconds
+        asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 1000;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+                     : "=r"(done) : "r"(a), "r"(parity) : "memory");
+        if (done) return true;
+    }
+    return false;
+}
+__device__ __forceinline__ void tma_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+                 ::"r"(saddr(dst)), "l"((uint64_t)map), "r"(x), "r"(y), "r"(saddr(bar)) : "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major operand tile in the 128-byte swizzle layout:
+// rows of 128 bytes, 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
+    uint64_t d = (uint64_t)((addr >> 4) & 0x3FFFu);
+    d |= (uint64_t)1 << 16;                  // leading byte offset (unused by swizzled K-major)
+    d |= (uint64_t)(1024 >> 4) << 32;        // stride byte offset: next 8-row group
+    d |= (uint64_t)1 << 46;                  // descriptor version of this architecture
+    d |= (uint64_t)2 << 61;                  // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor of kind::f16: f16 A and B, f32 accumulator, both K-major, M x N.
+__host__ __device__ constexpr uint32_t idesc_f16(int m, int n) {
+    return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+                 ::"r"(tmem_d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc));
+}
+__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(saddr(bar)) : "memory");
+}
+
+template <int N>
+struct Regs {
+    uint32_t r[N];
+};
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+                 "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+                 "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+                   "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]),
+                   "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]),
+                   "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]),
+                   "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+template <int QT, int BN, int MT>
+struct Cfg {
+    static constexpr int QB = QT == Q8 ? 32 : 16;          // quant bytes per 32-element block
+    static constexpr int A_BYTES = MT * BM * BK * 2;      // f16 weight tiles
+    static constexpr int B_BYTES = 2 * BN * BK * 2;       // f16 activation tiles: high and low parts
+    static constexpr int RQ_BYTES = MT * BM * QB * 2;     // raw quants: 2 blocks per row
+    static constexpr int RS_BYTES = MT * (BM / 4) * 16;   // raw scales: 2 blocks x 4 rows per quad
+    static constexpr int STAGE = A_BYTES + B_BYTES + ((RQ_BYTES + RS_BYTES + 1023) / 1024) * 1024;
+    static constexpr int S = (220 * 1024) / STAGE < 6 ? (220 * 1024) / STAGE : 6;
+    static constexpr int SMEM = S * STAGE + 1024 /* align */ + 256 /* barriers */;
+    static constexpr int TMEM_COLS = MT * BN <= 32 ? 32 : MT * BN <= 64 ? 64 : MT * BN <= 128 ? 128 : MT * BN <= 256 ? 256 : 512;
+};
+
+struct GemmParams {
+    int N;          // logical rows (outputs) of W
+    int T;          // tokens
+    int nk;         // K / 64
+    int row_base;   // unused (tiles start at blockIdx.x * 128 or, for SwiGLU, chunk c * 256)
+};
+
+// Dequantise row `row` (0..127) of one raw tile into the swizzled f16 tile.
+template <int QT>
+__device__ __forceinline__ void dequant_row(const uint8_t *rq, const uint8_t *rs, uint8_t *atile, int row) {
+    constexpr int QB = QT == Q8 ? 32 : 16;
+    const uint8_t *q = rq + row * QB * 2;
+    const __half *sc = reinterpret_cast<const __half *>(rs + (row >> 2) * 16);
+    uint8_t *dst = atile + row * 128;
+#pragma unroll
+    for (int blk = 0; blk < 2; ++blk) {
+        const __half2 d2 = __half2half2(sc[blk * 4 + (row & 3)]);
+        if (QT == Q4) {
+            const uint4 w = *reinterpret_cast<const uint4 *>(q + blk * 16);
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+            const __half2 off = __float2half2_rn(1032.f);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {   // bytes 0..7 (h = 0) or 8..15 (h = 1)
+                uint32_t lo[4], hi[4];
+#pragma unroll
+                for (int wi = 0; wi < 2; ++wi) {
+                    const uint32_t t0 = __byte_perm(ws[2 * h + wi], 0u, 0x4140u);   // [b0, 0, b1, 0]
+                    const uint32_t t1 = __byte_perm(ws[2 * h + wi], 0u, 0x4342u);   // [b2, 0, b3, 0]
+                    lo[2 * wi] = (t0 & 0x000F000Fu) | 0x64006400u;
+                    lo[2 * wi + 1] = (t1 & 0x000F000Fu) | 0x64006400u;
+                    hi[2 * wi] = ((t0 >> 4) & 0x000F000Fu) | 0x64006400u;
+                    hi[2 * wi + 1] = ((t1 >> 4) & 0x000F000Fu) | 0x64006400u;
+                }
+                uint32_t olo[4], ohi[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    __half2 a = __hmul2(__hsub2(*reinterpret_cast<__half2 *>(&lo[e]), off), d2);
+                    __half2 b = __hmul2(__hsub2(*reinterpret_cast<__half2 *>(&hi[e]), off), d2);
+                    olo[e] = *reinterpret_cast<uint32_t *>(&a);
+                    ohi[e] = *reinterpret_cast<uint32_t *>(&b);
+                }
+                const int c_lo = blk * 4 + h;       // elements 8h .. 8h+7 of the block
+                const int c_hi = blk * 4 + 2 + h;   // elements 16+8h ..
+                *reinterpret_cast<uint4 *>(dst + ((c_lo ^ (row & 7)) << 4)) = make_uint4(olo[0], olo[1], olo[2], olo[3]);
+                *reinterpret_cast<uint4 *>(dst + ((c_hi ^ (row & 7)) << 4)) = make_uint4(ohi[0], ohi[1], ohi[2], ohi[3]);
+            }
+        } else {
+            const __half2 off = __float2half2_rn(1152.f);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {           // chunk c of the block: bytes 8c .. 8c+7
+                const uint2 w = *reinterpret_cast<const uint2 *>(q + blk * 32 + c * 8);
+                const uint32_t ws[2] = {w.x ^ 0x80808080u, w.y ^ 0x80808080u};
+                uint32_t o[4];
+#pragma unroll
+                for (int wi = 0; wi < 2; ++wi) {
+                    uint32_t p0 = __byte_perm(ws[wi], 0x64646464u, 0x4140u);   // (1024 + q0 + 128, 1024 + q1 + 128)
+                    uint32_t p1 = __byte_perm(ws[wi], 0x64646464u, 0x4342u);
+                    __half2 a = __hmul2(__hsub2(*reinterpret_cast<__half2 *>(&p0), off), d2);
+                    __half2 b = __hmul2(__hsub2(*reinterpret_cast<__half2 *>(&p1), off), d2);
+                    o[2 * wi] = *reinterpret_cast<uint32_t *>(&a);
+                    o[2 * wi + 1] = *reinterpret_cast<uint32_t *>(&b);
+                }
+                const int cc = blk * 4 + c;
+                *reinterpret_cast<uint4 *>(dst + ((cc ^ (row & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+        }
+    }
+}
+
+template <int QT, int BN, int EPI>
+__global__ void __launch_bounds__(192, 1)
+    k_gemm_tc(const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_b2,
+              const __grid_constant__ CUtensorMap tm_q,
+              const __grid_constant__ CUtensorMap tm_s, const GemmParams p, const FwdArgs a, const int layer) {
+    constexpr int MT = EPI == EPI_SWIGLU ? 2 : 1;
+    using C = Cfg<QT, BN, MT>;
+    constexpr int S = C::S;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S * C::STAGE);
+    uint64_t *full_w = bars, *full_b = bars + S, *full_a = bars + 2 * S, *empty = bars + 3 * S, *acc_bar = bars + 4 * S;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 4 * S + 1);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m_tile = blockIdx.x, tok0 = blockIdx.y * BN;
+    const int nk = p.nk;
+    // first weight row of each M tile
+    int row0[MT];
+    if (EPI == EPI_SWIGLU) {
+        row0[0] = m_tile * 2 * BM;
+        row0[MT - 1] = m_tile * 2 * BM + BM;
+    } else {
+        row0[0] = m_tile * BM;
+    }
+    auto a_tile = [&](int slot, int mt) { return smem + slot * C::STAGE + mt * BM * BK * 2; };
+    auto b_tile = [&](int slot) { return smem + slot * C::STAGE + C::A_BYTES; };
+    auto rq_tile = [&](int slot, int mt) { return smem + slot * C::STAGE + C::A_BYTES + C::B_BYTES + mt * BM * C::QB * 2; };
+    auto rs_tile = [&](int slot, int mt) {
+        return smem + slot * C::STAGE + C::A_BYTES + C::B_BYTES + C::RQ_BYTES + mt * (BM / 4) * 16;
+    };
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < S; ++i) {
+            mbar_init(&full_w[i], 1);
+            mbar_init(&full_b[i], 1);
+            mbar_init(&full_a[i], 4);
+            mbar_init(&empty[i], 1);
+        }
+        mbar_init(acc_bar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {   // tensor-memory accumulator: MT x BN f32 columns, 128 lanes
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(saddr(tmem_slot)), "r"((uint32_t)C::TMEM_COLS));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------------- producer
+        if (lane == 0) {
+            bool ok = true;
+            auto issue_w = [&](int j) {
+                const int slot = j % S;
+                mbar_expect_tx(&full_w[slot], C::RQ_BYTES + C::RS_BYTES);
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt) {
+                    tma_2d(rq_tile(slot, mt), &tm_q, j * C::QB * 2, row0[mt], &full_w[slot]);
+                    tma_2d(rs_tile(slot, mt), &tm_s, j * 16, row0[mt] / 4, &full_w[slot]);
+                }
+            };
+            auto issue_b = [&](int j) {
+                const int slot = j % S;
+                mbar_expect_tx(&full_b[slot], C::B_BYTES);
+                tma_2d(b_tile(slot), &tm_b, j * BK, tok0, &full_b[slot]);
+                tma_2d(b_tile(slot) + BN * BK * 2, &tm_b2, j * BK, tok0, &full_b[slot]);
+            };
+            const int pre = nk < S ? nk : S;
+            for (int j = 0; j < pre; ++j) issue_w(j);
+            LCX_PDL_WAIT();   // the activations are the previous kernel's output
+            LCX_PDL_TRIGGER();
+            for (int j = 0; j < pre; ++j) issue_b(j);
+            int issued = pre;
+            for (int j = S; j < nk && ok; ++j) {
+                if (!(ok = mbar_wait(&empty[j % S], ((j / S) - 1) & 1))) break;
+                issue_w(j);
+                issue_b(j);
+                issued = j + 1;
+            }
+            if (!ok) atomicExch(a.err, 1);
+            // every copy issued must land before the CTA exits
+            for (int j = (issued > S ? issued - S : 0); j < issued; ++j) {
+                mbar_wait(&full_w[j % S], (j / S) & 1);
+                mbar_wait(&full_b[j % S], (j / S) & 1);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_f16(BM, BN);
+            bool ok = true;
+            for (int j = 0; j < nk; ++j) {
+                const int slot = j % S;
+                const uint32_t ph = (j / S) & 1;
+                if (!(ok = mbar_wait(&full_a[slot], ph) && mbar_wait(&full_b[slot], ph))) break;
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                const uint32_t bbase = saddr(b_tile(slot));
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt) {
+                    const uint32_t abase = saddr(a_tile(slot, mt));
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk) {   // W (A_hi + A_lo) as two MMAs into one accumulator
+                        mma_f16(tmem + mt * BN, sw128_desc(abase + kk * 32), sw128_desc(bbase + kk * 32), idesc,
+                                (j > 0 || kk > 0) ? 1u : 0u);
+                        mma_f16(tmem + mt * BN, sw128_desc(abase + kk * 32), sw128_desc(bbase + BN * BK * 2 + kk * 32),
+                                idesc, 1u);
+                    }
+                }
+                mma_commit(&empty[slot]);   // the slot is free once these MMAs have read it
+            }
+            if (!ok) atomicExch(a.err, 1);
+            mma_commit(acc_bar);
+        }
+    } else {
+        // ---------------------------------------------------------------- dequant, then epilogue
+        const int drow = threadIdx.x - 64;   // 0..127
+        bool ok = true;
+        for (int j = 0; j < nk; ++j) {
+            const int slot = j % S;
+            ok = __all_sync(0xffffffffu, mbar_wait(&full_w[slot], (j / S) & 1));   // warp-uniform
+            if (!ok) break;
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) dequant_row<QT>(rq_tile(slot, mt), rs_tile(slot, mt), a_tile(slot, mt), drow);
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic writes -> tensor-core reads
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&full_a[slot]);
+        }
+        if (!ok) atomicExch(a.err, 1);
+        LCX_PDL_WAIT();
+        LCX_PDL_TRIGGER();
+        const bool acc_ok = __all_sync(0xffffffffu, ok && mbar_wait(acc_bar, 0));
+        if (acc_ok) {
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            const int q = warp & 3;                 // TMEM lane quarter of this warp
+            const int lrow = q * 32 + lane;         // row within the tile
+            const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
+            for (int cb = 0; cb < BN / 32; ++cb) {
+                uint32_t v0[32], v1[32];
+                tmem_ld32(tq + cb * 32, v0);
+                if (EPI == EPI_SWIGLU) tmem_ld32(tq + BN + cb * 32, v1);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int t = tok0 + cb * 32 + i;
+                    const float v = __uint_as_float(v0[i]);
+                    if (EPI == EPI_SWIGLU) {
+                        const int f = m_tile * BM + lrow;
+                        if (t < p.T && f < a.F)
+                            store_split(a.h16, a.h16_lo, (size_t)t * a.F_pad + f, silu_f(v) * __uint_as_float(v1[i]));
+                    } else if (EPI == EPI_RESID) {
+                        const int r = row0[0] + lrow;
+                        if (t < p.T && r < p.N) a.x[(size_t)t * a.d + r] += v;
+                    } else if (EPI == EPI_LOGITS) {
+                        const int r = row0[0] + lrow;
+                        unsigned long long key = 0ull;
+                        if (t < p.T && r < p.N) {
+                            a.logits[(size_t)t * a.V + r] = v;
+                            key = argmax_key(v, r);
+                        }
+#pragma unroll
+                        for (int o = 16; o; o >>= 1) {
+                            const unsigned long long other = __shfl_xor_sync(0xffffffffu, key, o);
+                            key = other > key ? other : key;
+                        }
+                        if (lane == 0 && key) atomicMax(&a.amax_key[t], key);
+                    } else {   // EPI_QKV: rotate (q, k) pairs of adjacent rows, store q f32 and k, v f16
+                        const int r = row0[0] + lrow;
+                        const float partner = __shfl_xor_sync(0xffffffffu, v, 1);
+                        const int qw = a.H * a.hd, kw = a.KV * a.hd;
+                        if (t < p.T && r < qw + 2 * kw && (lane & 1) == 0) {
+                            float y0 = v, y1 = partner;
+                            if (r < qw + kw) {
+                                const int dim = r < qw ? r % a.hd : (r - qw) % a.hd;
+                                const float2 cs = a.rope[(size_t)a.ub.pos[t] * (a.hd / 2) + dim / 2];
+                                const float z0 = y0 * cs.x - y1 * cs.y, z1 = y0 * cs.y + y1 * cs.x;
+                                y0 = z0;
+                                y1 = z1;
+                            }
+                            if (r < qw) {
+                                a.q[(size_t)t * qw + r] = y0;
+                                a.q[(size_t)t * qw + r + 1] = y1;
+                            } else {
+                                const bool isk = r < qw + kw;
+                                const int rr = isk ? r - qw : r - qw - kw;
+                                __half *dst = (isk ? a.kc : a.vc) + kv_off(a, layer, a.ub.cell[t], rr / a.hd, rr % a.hd);
+                                *reinterpret_cast<__half2 *>(dst) = __floats2half2_rn(y0, y1);
+                            }
+                        }
+                    }
+                }
+            }
+        } else if (ok) {
+            atomicExch(a.err, 1);
+        }
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"((uint32_t)C::TMEM_COLS));
+    }
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
+    });
+    return fn;
+}
+
+// 2D map over a row-major byte/half matrix: inner extent `inner` elements, `outer` rows.
+bool make_map_2d(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int esize, uint64_t inner, uint64_t outer,
+                 uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    (void)esize;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {row_stride_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct ActKey {
+    const void *ptr;
+    int K, T, BN;
+};
+struct ActMap {
+    ActKey k;
+    CUtensorMap m;
+};
+
+const CUtensorMap *act_map(const __half *A, int K, int T, int BN) {
+    static std::mutex mu;
+    static std::vector<ActMap *> cache;
+    std::lock_guard<std::mutex> lk(mu);
+    for (ActMap *e : cache)
+        if (e->k.ptr == A && e->k.K == K && e->k.T == T && e->k.BN == BN) return &e->m;
+    ActMap *e = new ActMap;   // kept for the life of the process (a few bytes per shape)
+    e->k = {A, K, T, BN};
+    if (!make_map_2d(&e->m, A, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (uint64_t)K, (uint64_t)T, (uint64_t)K * 2, BK,
+                     (uint32_t)BN, CU_TENSOR_MAP_SWIZZLE_128B)) {
+        delete e;
+        return nullptr;
+    }
+    cache.push_back(e);
+    return &e->m;
+}
+
+template <int QT, int BN, int EPI>
+cudaError_t run(const QMat &W, int T, const __half *A, const __half *A_lo, const FwdArgs &a, int layer, cudaStream_t s) {
+    constexpr int MT = EPI == EPI_SWIGLU ? 2 : 1;
+    using C = Cfg<QT, BN, MT>;
+    auto kern = k_gemm_tc<QT, BN, EPI>;
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    const CUtensorMap *mb = act_map(A, W.K, T, BN), *mb2 = act_map(A_lo, W.K, T, BN);
+    if (!mb || !mb2 || !W.tm_ready) return cudaErrorInvalidValue;
+    GemmParams p{W.N, T, W.K / BK, 0};
+    const int m_tiles = EPI == EPI_SWIGLU ? W.N_pad / (2 * BM) : W.N_pad / BM;
+    dim3 grid(m_tiles, (T + BN - 1) / BN);
+    return launch_pdl(kern, grid, dim3(192), (size_t)C::SMEM, s, *mb, *mb2, *reinterpret_cast<const CUtensorMap *>(W.tm_q),
+                      *reinterpret_cast<const CUtensorMap *>(W.tm_s), p, a, layer);
+}
+
+template <int QT, int BN>
+cudaError_t dispatch(const QMat &W, Epi epi, int T, const __half *A, const __half *A_lo, const FwdArgs &a, int layer,
+                     cudaStream_t s) {
+    switch (epi) {
+        case EPI_QKV: return run<QT, BN, EPI_QKV>(W, T, A, A_lo, a, layer, s);
+        case EPI_RESID: return run<QT, BN, EPI_RESID>(W, T, A, A_lo, a, layer, s);
+        case EPI_SWIGLU: return run<QT, BN, EPI_SWIGLU>(W, T, A, A_lo, a, layer, s);
+        case EPI_LOGITS: return run<QT, BN, EPI_LOGITS>(W, T, A, A_lo, a, layer, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace tc
+
+bool make_weight_maps(QMat &W) {
+    // quants: [N_pad rows][nb * QB bytes]; a stage reads 2 blocks of 128 rows
+    const int qb = W.type == Q8 ? 32 : 16;
+    CUtensorMap *mq = reinterpret_cast<CUtensorMap *>(W.tm_q), *ms = reinterpret_cast<CUtensorMap *>(W.tm_s);
+    W.tm_ready = tc::make_map_2d(mq, W.qs, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)W.nb * qb, (uint64_t)W.N_pad,
+                                 (uint64_t)W.nb * qb, (uint32_t)(2 * qb), (uint32_t)tc::BM, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+                 tc::make_map_2d(ms, W.sc, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)W.nb * 8, (uint64_t)W.N_pad / 4,
+                                 (uint64_t)W.nb * 8, 16u, (uint32_t)(tc::BM / 4), CU_TENSOR_MAP_SWIZZLE_NONE);
+    return W.tm_ready;
+}
+
+cudaError_t launch_gemm_tc(const QMat &W, Epi epi, int T, const __half *A, const __half *A_lo, const FwdArgs &a,
+                           int layer, cudaStream_t s, int64_t &launches) {
+    ++launches;
+    static int n_sm = 0;
+    if (!n_sm) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+    }
+    // 64-token tiles when 128-token tiles would leave SMs idle
+    const int m_tiles = epi == EPI_SWIGLU ? W.N_pad / 256 : W.N_pad / 128;
+    const bool small = (long)m_tiles * ((T + 127) / 128) < (long)n_sm * 3 / 2;
+    if (W.type == Q4)
+        return small ? tc::dispatch<Q4, 64>(W, epi, T, A, A_lo, a, layer, s) : tc::dispatch<Q4, 128>(W, epi, T, A, A_lo, a, layer, s);
+    if (W.type == Q8)
+        return small ? tc::dispatch<Q8, 64>(W, epi, T, A, A_lo, a, layer, s) : tc::dispatch<Q8, 128>(W, epi, T, A, A_lo, a, layer, s);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace lcx

@@ -183,7 +183,7 @@ __device__ void stage_token(const GemvParams &p, const FwdArgs &a, int t, uint8_
 // returns instead of spinning.
 constexpr int kConsumerWarps = 8;
 constexpr int kMaxStages = 8;
-constexpr uint32_t kSpinLimit = 1u << 24;
+constexpr uint32_t kSpinLimit = 1u << 22;
 
 struct StagePlan {
     int tps;            // tasks per stage (4, 2 or 1)
@@ -227,7 +227,8 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
     const uint32_t a = smem_u32(bar);
     for (uint32_t i = 0; i < kSpinLimit; ++i) {
         uint32_t done;
-        asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        // each poll suspends for at most ~1 us (time hint), so a wait gives up after a few seconds
+        asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 1000;\n\tselp.u32 %0, 1, 0, p;\n\t}"
                      : "=r"(done) : "r"(a), "r"(parity) : "memory");
         if (done) return true;
     }

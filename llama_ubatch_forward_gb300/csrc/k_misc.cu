@@ -118,7 +118,7 @@ cudaError_t launch_get_rows(int type, const void *table, int64_t n_cols, const i
 // ------------------------------------------------------------------ RMSNorm -> f16
 // out[r][:] = f16(x[row r] / sqrt(mean(x^2) + eps) * g); row r of x is rows[r] (or r).
 __global__ void k_rmsnorm_h(const float *__restrict__ x, const int32_t *__restrict__ rows, int d,
-                            const float *__restrict__ g, float eps, __half *__restrict__ out) {
+                            const float *__restrict__ g, float eps, __half *__restrict__ out, __half *__restrict__ out_lo) {
     LCX_PDL_WAIT();
     LCX_PDL_TRIGGER();
     const int r = blockIdx.x;
@@ -139,21 +139,21 @@ __global__ void k_rmsnorm_h(const float *__restrict__ x, const int32_t *__restri
     }
     __syncthreads();
     const float rs = 1.0f / sqrtf(red[0] / (float)d + eps);
-    __half *orow = out + (int64_t)r * d;
     for (int i = threadIdx.x * 4; i < d; i += blockDim.x * 4) {
-        float4 v = *reinterpret_cast<const float4 *>(xr + i);
-        float4 gg = *reinterpret_cast<const float4 *>(g + i);
-        __half2 a = __floats2half2_rn(v.x * rs * gg.x, v.y * rs * gg.y);
-        __half2 b = __floats2half2_rn(v.z * rs * gg.z, v.w * rs * gg.w);
-        *reinterpret_cast<__half2 *>(orow + i) = a;
-        *reinterpret_cast<__half2 *>(orow + i + 2) = b;
+        const float4 v = *reinterpret_cast<const float4 *>(xr + i);
+        const float4 gg = *reinterpret_cast<const float4 *>(g + i);
+        const size_t o = (size_t)r * d + i;
+        store_split(out, out_lo, o, v.x * rs * gg.x);
+        store_split(out, out_lo, o + 1, v.y * rs * gg.y);
+        store_split(out, out_lo, o + 2, v.z * rs * gg.z);
+        store_split(out, out_lo, o + 3, v.w * rs * gg.w);
     }
 }
 
 cudaError_t launch_rmsnorm_h(const float *x, const int32_t *rows, int T, int d, const float *g, float eps,
-                             __half *out, cudaStream_t s, int64_t &launches) {
+                             __half *out, __half *out_lo, cudaStream_t s, int64_t &launches) {
     ++launches;
-    return launch_pdl(k_rmsnorm_h, dim3(T), dim3(256), 0, s, x, rows, d, g, eps, out);
+    return launch_pdl(k_rmsnorm_h, dim3(T), dim3(256), 0, s, x, rows, d, g, eps, out, out_lo);
 }
 
 // ------------------------------------------------------------------ argmax

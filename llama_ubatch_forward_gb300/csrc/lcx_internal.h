@@ -29,6 +29,10 @@ struct QMat {
     int K = 0, nb = 0;      // padded input width (nb * 32) and blocks per row
     uint8_t *qs = nullptr;
     __half *sc = nullptr;
+    // TMA descriptors (CUtensorMap) of the quant and scale planes for the tensor-core GEMM
+    alignas(64) unsigned char tm_q[128] = {};
+    alignas(64) unsigned char tm_s[128] = {};
+    bool tm_ready = false;
     size_t qs_row_bytes() const { return (size_t)nb * (type == Q4 ? 16 : 32); }
     size_t bytes() const { return (size_t)N_pad * qs_row_bytes() + (size_t)N_pad * nb * 2; }
 };
@@ -66,12 +70,15 @@ struct FwdArgs {
     const int32_t *tok_src;      // where the embed kernel reads token ids
     // activations
     float *x;          // [T][d] residual stream
-    __half *xh;        // [T][d] normed activations (GEMM path)
+    __half *xh;        // [T][d] normed activations (GEMM path), f16 high part ...
+    __half *xh_lo;     // ... and low part: x = hi + lo to about 22 bits
     float *q;          // [T][H*hd]
     float *o32;        // [T][H*hd]
-    __half *o16;       // [T][H*hd]
+    __half *o16;       // [T][H*hd] (high part)
+    __half *o16_lo;    // [T][H*hd] (low part)
     float *h32;        // [T][F_pad]
-    __half *h16;       // [T][F_pad]
+    __half *h16;       // [T][F_pad] (high part)
+    __half *h16_lo;    // [T][F_pad] (low part)
     float *logits;     // [n_out][V]
     unsigned long long *amax_key;  // [n_out]
     int32_t *amax_out; // [n_out] device
@@ -97,7 +104,7 @@ cudaError_t launch_embed(const FwdArgs &a, int t_embd, const void *tok_embd, cud
 cudaError_t launch_get_rows(int type, const void *table, int64_t n_cols, const int32_t *ids, int n, float *out,
                             cudaStream_t s);
 cudaError_t launch_rmsnorm_h(const float *x, const int32_t *rows, int T, int d, const float *g, float eps,
-                             __half *out, cudaStream_t s, int64_t &launches);
+                             __half *out, __half *out_lo, cudaStream_t s, int64_t &launches);
 cudaError_t launch_argmax_final(const FwdArgs &a, int32_t *dst, cudaStream_t s, int64_t &launches);
 
 // y = W x for T <= kGemvMaxT tokens with the given epilogue; x rows are read from `x`
@@ -111,9 +118,14 @@ cudaError_t launch_gemv(const QMat &W, Epi epi, int T, const GemvIn &in, const F
                         cudaStream_t s, int64_t &launches);
 bool gemv_fits(const QMat &W, int T);
 
-// GEMM for larger T: A = f16 activations [T][K]
-cudaError_t launch_gemm(const QMat &W, Epi epi, int T, const __half *A, const FwdArgs &a, int layer,
-                        cudaStream_t s, int64_t &launches);
+// GEMM for larger T: A = A_hi + A_lo, f16 activations [T][K] split in two parts
+cudaError_t launch_gemm(const QMat &W, Epi epi, int T, const __half *A, const __half *A_lo, const FwdArgs &a,
+                        int layer, cudaStream_t s, int64_t &launches);
+
+// tcgen05 GEMM (k_gemm_tc.cu) and the TMA descriptors of a weight matrix it needs
+cudaError_t launch_gemm_tc(const QMat &W, Epi epi, int T, const __half *A, const __half *A_lo, const FwdArgs &a,
+                           int layer, cudaStream_t s, int64_t &launches);
+bool make_weight_maps(QMat &W);
 
 // attention over the cache for every token of the ubatch; writes o32 (f32) or o16
 cudaError_t launch_attention(const FwdArgs &a, int layer, int max_natt, bool out_f16, cudaStream_t s,
@@ -143,6 +155,14 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
 }
 
 }  // namespace lcx
+
+// f16 high / low split of an f32 value: hi = f16(v), lo = f16(v - hi); hi + lo carries about
+// 22 significant bits of v.
+__device__ __forceinline__ void store_split(__half *hi, __half *lo, size_t i, float v) {
+    const __half h = __float2half_rn(v);
+    hi[i] = h;
+    lo[i] = __float2half_rn(v - __half2float(h));
+}
 
 #define LCX_PDL_WAIT() asm volatile("griddepcontrol.wait;" ::: "memory")
 #define LCX_PDL_TRIGGER() asm volatile("griddepcontrol.launch_dependents;")

@@ -161,6 +161,8 @@ extern "C" lcx_model *lcx_model_create(const lcx_hparams *hp, const lcx_weights 
     if (e == cudaSuccess)
         e = launch_repack(w->output ? w->output : w->tok_embd, t_out, hp->n_vocab, d / 32, m->head, 0, 0, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    for (QMat *q : mats)
+        if (e == cudaSuccess && !make_weight_maps(*q)) e = cudaErrorInvalidValue;
     if (e != cudaSuccess) {
         set_err("model re-layout", e);
         cudaFree(m->arena);
@@ -318,11 +320,14 @@ extern "C" lcx_ctx *lcx_ctx_create(lcx_model *m, uint32_t n_ctx, uint32_t n_seq_
     const size_t sizes[] = {
         (size_t)T * d * 4,                   // x
         (size_t)T * d * 2,                   // xh
+        (size_t)T * d * 2,                   // xh_lo
         (size_t)T * H * hd * 4,              // q
         (size_t)T * H * hd * 4,              // o32
         (size_t)T * H * hd * 2,              // o16
+        (size_t)T * H * hd * 2,              // o16_lo
         (size_t)T * Fp * 4,                  // h32
         (size_t)T * Fp * 2,                  // h16
+        (size_t)T * Fp * 2,                  // h16_lo
         (size_t)T * V * 4,                   // logits scratch
         (size_t)T * 8,                       // argmax keys
         part_rows * G * (hd + 2) * 4,        // attention partials
@@ -338,11 +343,14 @@ extern "C" lcx_ctx *lcx_ctx_create(lcx_model *m, uint32_t n_ctx, uint32_t n_seq_
         FwdArgs &a = c->base;
         a.x = carve<float>(p, (size_t)T * d);
         a.xh = carve<__half>(p, (size_t)T * d);
+        a.xh_lo = carve<__half>(p, (size_t)T * d);
         a.q = carve<float>(p, (size_t)T * H * hd);
         a.o32 = carve<float>(p, (size_t)T * H * hd);
         a.o16 = carve<__half>(p, (size_t)T * H * hd);
+        a.o16_lo = carve<__half>(p, (size_t)T * H * hd);
         a.h32 = carve<float>(p, (size_t)T * Fp);
         a.h16 = carve<__half>(p, (size_t)T * Fp);
+        a.h16_lo = carve<__half>(p, (size_t)T * Fp);
         a.logits = carve<float>(p, (size_t)T * V);
         a.amax_key = carve<unsigned long long>(p, (size_t)T);
         a.att_part = carve<float>(p, part_rows * G * (hd + 2));
@@ -585,12 +593,12 @@ cudaError_t run_forward(lcx_ctx *c, FwdArgs &a, int max_natt, double att_cells, 
         const DevLayer &D = m->layers[l];
         if (!gemv) {
             ProfScope ps(c, PC_OTHER, T * d * 6, 0);
-            e = launch_rmsnorm_h(a.x, nullptr, a.T, a.d, D.attn_norm, a.eps, a.xh, s, nl);
+            e = launch_rmsnorm_h(a.x, nullptr, a.T, a.d, D.attn_norm, a.eps, a.xh, a.xh_lo, s, nl);
         }
         if (e == cudaSuccess) {
             ProfScope ps(c, cls, w_qkv + T * d * ab + T * (qw * 4 + kvw * 4), 2 * T * (qw + 2 * kvw) * d);
             e = gemv ? launch_gemv(D.qkv, EPI_QKV, a.T, GemvIn{a.x, nullptr, D.attn_norm}, a, l, s, nl)
-                     : launch_gemm(D.qkv, EPI_QKV, a.T, a.xh, a, l, s, nl);
+                     : launch_gemm(D.qkv, EPI_QKV, a.T, a.xh, a.xh_lo, a, l, s, nl);
         }
         if (e == cudaSuccess) {
             ProfScope ps(c, PC_ATTN, att_bytes, att_flops);
@@ -599,21 +607,21 @@ cudaError_t run_forward(lcx_ctx *c, FwdArgs &a, int max_natt, double att_cells, 
         if (e == cudaSuccess) {
             ProfScope ps(c, cls, w_o + T * qw * ab + T * d * 8, 2 * T * d * qw);
             e = gemv ? launch_gemv(D.wo, EPI_RESID, a.T, GemvIn{a.o32, nullptr, nullptr}, a, l, s, nl)
-                     : launch_gemm(D.wo, EPI_RESID, a.T, a.o16, a, l, s, nl);
+                     : launch_gemm(D.wo, EPI_RESID, a.T, a.o16, a.o16_lo, a, l, s, nl);
         }
         if (e == cudaSuccess && !gemv) {
             ProfScope ps(c, PC_OTHER, T * d * 6, 0);
-            e = launch_rmsnorm_h(a.x, nullptr, a.T, a.d, D.ffn_norm, a.eps, a.xh, s, nl);
+            e = launch_rmsnorm_h(a.x, nullptr, a.T, a.d, D.ffn_norm, a.eps, a.xh, a.xh_lo, s, nl);
         }
         if (e == cudaSuccess) {
             ProfScope ps(c, cls, w_gu + T * d * ab + T * F * ab, 2 * T * 2 * F * d);
             e = gemv ? launch_gemv(D.gateup, EPI_SWIGLU, a.T, GemvIn{a.x, nullptr, D.ffn_norm}, a, l, s, nl)
-                     : launch_gemm(D.gateup, EPI_SWIGLU, a.T, a.xh, a, l, s, nl);
+                     : launch_gemm(D.gateup, EPI_SWIGLU, a.T, a.xh, a.xh_lo, a, l, s, nl);
         }
         if (e == cudaSuccess) {
             ProfScope ps(c, cls, w_dn + T * F * ab + T * d * 8, 2 * T * d * F);
             e = gemv ? launch_gemv(D.down, EPI_RESID, a.T, GemvIn{a.h32, nullptr, nullptr}, a, l, s, nl)
-                     : launch_gemm(D.down, EPI_RESID, a.T, a.h16, a, l, s, nl);
+                     : launch_gemm(D.down, EPI_RESID, a.T, a.h16, a.h16_lo, a, l, s, nl);
         }
     }
     if (e != cudaSuccess || a.n_out == 0) return e;
@@ -624,12 +632,12 @@ cudaError_t run_forward(lcx_ctx *c, FwdArgs &a, int max_natt, double att_cells, 
     } else {
         {
             ProfScope ps(c, PC_OTHER, no * d * 6, 0);
-            e = launch_rmsnorm_h(a.x, a.ub.out_rows, a.n_out, a.d, m->output_norm, a.eps, a.xh, s, nl);
+            e = launch_rmsnorm_h(a.x, a.ub.out_rows, a.n_out, a.d, m->output_norm, a.eps, a.xh, a.xh_lo, s, nl);
         }
         if (e == cudaSuccess) {
             // the logits GEMM reads the gathered rows as its tokens
             ProfScope ps(c, PC_GEMM, w_head + no * d * 2 + no * a.V * 4, 2 * no * a.V * d);
-            e = launch_gemm(m->head, EPI_LOGITS, a.n_out, a.xh, a, -1, s, nl);
+            e = launch_gemm(m->head, EPI_LOGITS, a.n_out, a.xh, a.xh_lo, a, -1, s, nl);
         }
     }
     if (e == cudaSuccess) {
