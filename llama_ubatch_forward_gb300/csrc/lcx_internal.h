@@ -57,6 +57,8 @@ struct UbDev {
     const int32_t *out_rows; // [n_out] indices of flagged tokens within the ubatch
     const int32_t *pt_upd;   // [n_upd][2] (flat page-table index, page)
     int32_t n_upd;
+    const int4 *qtiles;      // [n_qtiles] query tiles: (first token, tokens <= 64, sequence, first position)
+    int32_t n_qtiles;
 };
 
 // Everything a forward launch needs (device pointers).
@@ -131,6 +133,8 @@ bool make_weight_maps(QMat &W);
 cudaError_t launch_attention(const FwdArgs &a, int layer, int max_natt, bool out_f16, cudaStream_t s,
                              int64_t &launches);
 int attention_splits(const FwdArgs &a, int max_natt, int *chunk);
+// tensor-core attention over the ubatch's query tiles (k_attn_prefill.cu); writes o16 / o16_lo
+cudaError_t launch_attention_prefill(const FwdArgs &a, int layer, cudaStream_t s, int64_t &launches);
 // Scratch bytes one attention launch needs (partials, then arrival counters at
 // *counter_offset); 0 when every token fits in a single split.
 size_t attention_scratch_bytes(const FwdArgs &a, int max_natt, size_t *counter_offset);

@@ -308,6 +308,10 @@ extern "C" lcx_ctx *lcx_ctx_create(lcx_model *m, uint32_t n_ctx, uint32_t n_seq_
     };
     ok(cudaMalloc(&c->kc, kv_elems * sizeof(__half)), "kv cache");
     if (e == cudaSuccess) ok(cudaMalloc(&c->vc, kv_elems * sizeof(__half)), "kv cache");
+    // finite contents everywhere: the prefill attention reads whole pages and gives the cells past
+    // a query's position a weight of exactly 0
+    if (e == cudaSuccess) ok(cudaMemsetAsync(c->kc, 0, kv_elems * sizeof(__half), c->stream), "kv cache");
+    if (e == cudaSuccess) ok(cudaMemsetAsync(c->vc, 0, kv_elems * sizeof(__half), c->stream), "kv cache");
     if (e == cudaSuccess)
         ok(cudaMalloc(&c->pt, (size_t)c->n_seq_max * c->max_pages_per_seq * sizeof(int32_t)), "page table");
     if (e == cudaSuccess) ok(cudaMalloc(&c->rope, (size_t)c->n_ctx * (hd / 2) * sizeof(float2)), "rope table");
@@ -365,7 +369,7 @@ extern "C" lcx_ctx *lcx_ctx_create(lcx_model *m, uint32_t n_ctx, uint32_t n_seq_
         a.att_max_split = c->max_att_split;
     }
     // metadata: per token tok, pos, seq, cell, out_row + up to 2 page-table updates (2 ints each)
-    c->meta_cap = 9 * std::max<int>(T, 4096) + 64;
+    c->meta_cap = 12 * std::max<int>(T, 4096) + 64;
     if (e == cudaSuccess) ok(cudaMalloc(&c->meta_dev, (size_t)c->meta_cap * 4), "metadata");
     if (e == cudaSuccess) ok(cudaHostAlloc((void **)&c->meta_host, (size_t)2 * c->meta_cap * 4, cudaHostAllocDefault), "pinned");
     c->amax_cap = std::max<int>(T, 4096);
@@ -511,7 +515,19 @@ cudaError_t upload_meta(lcx_ctx *c, const Plan &P, const Ub &u, UbDev &ub) {
     std::vector<int> upd;
     for (size_t k = 0; k < P.pt_tok.size(); ++k)
         if (P.pt_tok[k] >= u.i0 && P.pt_tok[k] < u.i0 + T) upd.push_back((int)k);
-    const int need = 5 * T + 2 * (int)upd.size();
+    // query tiles: runs of consecutive positions of one sequence, cut every 64 tokens
+    std::vector<int32_t> tiles;
+    for (int i = 0; i < T;) {
+        int n = 1;
+        while (i + n < T && n < 64 && P.seq[u.i0 + i + n] == P.seq[u.i0 + i] &&
+               P.pos[u.i0 + i + n] == P.pos[u.i0 + i] + n)
+            ++n;
+        tiles.insert(tiles.end(), {i, n, P.seq[u.i0 + i], P.pos[u.i0 + i]});
+        i += n;
+    }
+    const int ntiles = (int)tiles.size() / 4;
+    const int tiles_off = (5 * T + 2 * (int)upd.size() + 3) / 4 * 4;   // int4-aligned
+    const int need = tiles_off + 4 * ntiles;
     if (need > c->meta_cap) return cudaErrorInvalidValue;
     const int slot = c->meta_slot;
     c->meta_slot ^= 1;
@@ -531,6 +547,7 @@ cudaError_t upload_meta(lcx_ctx *c, const Plan &P, const Ub &u, UbDev &ub) {
         pu[2 * k] = P.pt_idx[upd[k]];
         pu[2 * k + 1] = P.pt_page[upd[k]];
     }
+    std::memcpy(h + tiles_off, tiles.data(), tiles.size() * 4);
     e = cudaMemcpyAsync(c->meta_dev, h, (size_t)need * 4, cudaMemcpyHostToDevice, c->stream);
     if (e == cudaSuccess) e = cudaEventRecord(c->meta_ev[slot], c->stream);
     int32_t *d = c->meta_dev;
@@ -541,6 +558,8 @@ cudaError_t upload_meta(lcx_ctx *c, const Plan &P, const Ub &u, UbDev &ub) {
     ub.out_rows = d + 4 * T;
     ub.pt_upd = d + 5 * T;
     ub.n_upd = (int)upd.size();
+    ub.qtiles = reinterpret_cast<const int4 *>(d + tiles_off);
+    ub.n_qtiles = ntiles;
     return e;
 }
 
@@ -602,7 +621,9 @@ cudaError_t run_forward(lcx_ctx *c, FwdArgs &a, int max_natt, double att_cells, 
         }
         if (e == cudaSuccess) {
             ProfScope ps(c, PC_ATTN, att_bytes, att_flops);
-            e = launch_attention(a, l, max_natt, !gemv, s, nl);
+            // long runs of one sequence (prefill): tensor-core tiles; single tokens: split-K
+            const bool tiles = !gemv && a.ub.n_qtiles > 0 && a.ub.n_qtiles * 8 <= a.T;
+            e = tiles ? launch_attention_prefill(a, l, s, nl) : launch_attention(a, l, max_natt, !gemv, s, nl);
         }
         if (e == cudaSuccess) {
             ProfScope ps(c, cls, w_o + T * qw * ab + T * d * 8, 2 * T * d * qw);
