@@ -5,8 +5,8 @@
 // shared epilogues (RoPE + KV append, residual add, SwiGLU, logits + argmax).
 //
 // Prefill is where the work is compute-bound (KV-cache section of the article: prefill loads the
-// compute units), so the contraction runs on the 5th-generation tensor cores. One CTA computes a
-// 128-row weight tile (two for the fused gate/up matrix) against BN tokens:
+// compute units), so the contraction runs on the 5th-generation tensor cores. One CTA computes two
+// 128-row weight tiles (adjacent rows, or a gate chunk and its up chunk) against BN tokens:
 //   warp 0      TMA producer: raw quant + scale tiles of the weights (issued before the
 //               grid-dependency wait: the weights do not depend on the previous kernel), then the
 //               activation tiles [BN][64] f16 (high and low parts) with the 128-byte swizzle;
@@ -190,7 +190,7 @@ __global__ void __launch_bounds__(192, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_b2,
               const __grid_constant__ CUtensorMap tm_q,
               const __grid_constant__ CUtensorMap tm_s, const GemmParams p, const FwdArgs a, const int layer) {
-    constexpr int MT = EPI == EPI_SWIGLU ? 2 : 1;
+    constexpr int MT = 2;   // two 128-row weight tiles share every activation tile
     using C = Cfg<QT, BN, MT>;
     constexpr int S = C::S;
     extern __shared__ uint8_t smem_raw[];
@@ -202,13 +202,8 @@ __global__ void __launch_bounds__(192, 1)
     const int m_tile = blockIdx.x, tok0 = blockIdx.y * BN;
     const int nk = p.nk;
     // first weight row of each M tile
-    int row0[MT];
-    if (EPI == EPI_SWIGLU) {
-        row0[0] = m_tile * 2 * BM;
-        row0[MT - 1] = m_tile * 2 * BM + BM;
-    } else {
-        row0[0] = m_tile * BM;
-    }
+    // gate/up: chunk m_tile's gate rows, then its up rows; otherwise two adjacent row tiles
+    const int row0[MT] = {m_tile * 2 * BM, m_tile * 2 * BM + BM};
     auto a_tile = [&](int slot, int mt) { return smem + slot * C::STAGE + mt * BM * BK * 2; };
     auto b_tile = [&](int slot) { return smem + slot * C::STAGE + C::A_BYTES; };
     auto rq_tile = [&](int slot, int mt) { return smem + slot * C::STAGE + C::A_BYTES + C::B_BYTES + mt * BM * C::QB * 2; };
@@ -327,52 +322,60 @@ __global__ void __launch_bounds__(192, 1)
             for (int cb = 0; cb < BN / 32; ++cb) {
                 uint32_t v0[32], v1[32];
                 tmem_ld32(tq + cb * 32, v0);
-                if (EPI == EPI_SWIGLU) tmem_ld32(tq + BN + cb * 32, v1);
+                tmem_ld32(tq + BN + cb * 32, v1);
+                if (EPI == EPI_SWIGLU) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int t = tok0 + cb * 32 + i;
-                    const float v = __uint_as_float(v0[i]);
-                    if (EPI == EPI_SWIGLU) {
+                    for (int i = 0; i < 32; ++i) {
+                        const int t = tok0 + cb * 32 + i;
                         const int f = m_tile * BM + lrow;
                         if (t < p.T && f < a.F)
-                            store_split(a.h16, a.h16_lo, (size_t)t * a.F_pad + f, silu_f(v) * __uint_as_float(v1[i]));
-                    } else if (EPI == EPI_RESID) {
-                        const int r = row0[0] + lrow;
-                        if (t < p.T && r < p.N) a.x[(size_t)t * a.d + r] += v;
-                    } else if (EPI == EPI_LOGITS) {
-                        const int r = row0[0] + lrow;
-                        unsigned long long key = 0ull;
-                        if (t < p.T && r < p.N) {
-                            a.logits[(size_t)t * a.V + r] = v;
-                            key = argmax_key(v, r);
-                        }
+                            store_split(a.h16, a.h16_lo, (size_t)t * a.F_pad + f,
+                                        silu_f(__uint_as_float(v0[i])) * __uint_as_float(v1[i]));
+                    }
+                    continue;
+                }
 #pragma unroll
-                        for (int o = 16; o; o >>= 1) {
-                            const unsigned long long other = __shfl_xor_sync(0xffffffffu, key, o);
-                            key = other > key ? other : key;
-                        }
-                        if (lane == 0 && key) atomicMax(&a.amax_key[t], key);
-                    } else {   // EPI_QKV: rotate (q, k) pairs of adjacent rows, store q f32 and k, v f16
-                        const int r = row0[0] + lrow;
-                        const float partner = __shfl_xor_sync(0xffffffffu, v, 1);
-                        const int qw = a.H * a.hd, kw = a.KV * a.hd;
-                        if (t < p.T && r < qw + 2 * kw && (lane & 1) == 0) {
-                            float y0 = v, y1 = partner;
-                            if (r < qw + kw) {
-                                const int dim = r < qw ? r % a.hd : (r - qw) % a.hd;
-                                const float2 cs = a.rope[(size_t)a.ub.pos[t] * (a.hd / 2) + dim / 2];
-                                const float z0 = y0 * cs.x - y1 * cs.y, z1 = y0 * cs.y + y1 * cs.x;
-                                y0 = z0;
-                                y1 = z1;
+                for (int mt = 0; mt < MT; ++mt) {
+                    const int r = row0[mt] + lrow;
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int t = tok0 + cb * 32 + i;
+                        const float v = __uint_as_float(mt == 0 ? v0[i] : v1[i]);
+                        if (EPI == EPI_RESID) {
+                            if (t < p.T && r < p.N) a.x[(size_t)t * a.d + r] += v;
+                        } else if (EPI == EPI_LOGITS) {
+                            unsigned long long key = 0ull;
+                            if (t < p.T && r < p.N) {
+                                a.logits[(size_t)t * a.V + r] = v;
+                                key = argmax_key(v, r);
                             }
-                            if (r < qw) {
-                                a.q[(size_t)t * qw + r] = y0;
-                                a.q[(size_t)t * qw + r + 1] = y1;
-                            } else {
-                                const bool isk = r < qw + kw;
-                                const int rr = isk ? r - qw : r - qw - kw;
-                                __half *dst = (isk ? a.kc : a.vc) + kv_off(a, layer, a.ub.cell[t], rr / a.hd, rr % a.hd);
-                                *reinterpret_cast<__half2 *>(dst) = __floats2half2_rn(y0, y1);
+#pragma unroll
+                            for (int o = 16; o; o >>= 1) {
+                                const unsigned long long other = __shfl_xor_sync(0xffffffffu, key, o);
+                                key = other > key ? other : key;
+                            }
+                            if (lane == 0 && key) atomicMax(&a.amax_key[t], key);
+                        } else {   // EPI_QKV: rotate (q, k) pairs of adjacent rows, store q f32 and k, v f16
+                            const float partner = __shfl_xor_sync(0xffffffffu, v, 1);
+                            const int qw = a.H * a.hd, kw = a.KV * a.hd;
+                            if (t < p.T && r < qw + 2 * kw && (lane & 1) == 0) {
+                                float y0 = v, y1 = partner;
+                                if (r < qw + kw) {
+                                    const int dim = r < qw ? r % a.hd : (r - qw) % a.hd;
+                                    const float2 cs = a.rope[(size_t)a.ub.pos[t] * (a.hd / 2) + dim / 2];
+                                    const float z0 = y0 * cs.x - y1 * cs.y, z1 = y0 * cs.y + y1 * cs.x;
+                                    y0 = z0;
+                                    y1 = z1;
+                                }
+                                if (r < qw) {
+                                    a.q[(size_t)t * qw + r] = y0;
+                                    a.q[(size_t)t * qw + r + 1] = y1;
+                                } else {
+                                    const bool isk = r < qw + kw;
+                                    const int rr = isk ? r - qw : r - qw - kw;
+                                    __half *dst = (isk ? a.kc : a.vc) + kv_off(a, layer, a.ub.cell[t], rr / a.hd, rr % a.hd);
+                                    *reinterpret_cast<__half2 *>(dst) = __floats2half2_rn(y0, y1);
+                                }
                             }
                         }
                     }
@@ -447,7 +450,7 @@ const CUtensorMap *act_map(const __half *A, int K, int T, int BN) {
 
 template <int QT, int BN, int EPI>
 cudaError_t run(const QMat &W, int T, const __half *A, const __half *A_lo, const FwdArgs &a, int layer, cudaStream_t s) {
-    constexpr int MT = EPI == EPI_SWIGLU ? 2 : 1;
+    constexpr int MT = 2;
     using C = Cfg<QT, BN, MT>;
     auto kern = k_gemm_tc<QT, BN, EPI>;
     static bool attr = false;
@@ -459,7 +462,7 @@ cudaError_t run(const QMat &W, int T, const __half *A, const __half *A_lo, const
     const CUtensorMap *mb = act_map(A, W.K, T, BN), *mb2 = act_map(A_lo, W.K, T, BN);
     if (!mb || !mb2 || !W.tm_ready) return cudaErrorInvalidValue;
     GemmParams p{W.N, T, W.K / BK, 0};
-    const int m_tiles = EPI == EPI_SWIGLU ? W.N_pad / (2 * BM) : W.N_pad / BM;
+    const int m_tiles = (W.N_pad + 2 * BM - 1) / (2 * BM);   // rows past N_pad read as zeros
     dim3 grid(m_tiles, (T + BN - 1) / BN);
     return launch_pdl(kern, grid, dim3(192), (size_t)C::SMEM, s, *mb, *mb2, *reinterpret_cast<const CUtensorMap *>(W.tm_q),
                       *reinterpret_cast<const CUtensorMap *>(W.tm_s), p, a, layer);
@@ -500,8 +503,8 @@ cudaError_t launch_gemm_tc(const QMat &W, Epi epi, int T, const __half *A, const
         cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
     }
     // 64-token tiles when 128-token tiles would leave SMs idle
-    const int m_tiles = epi == EPI_SWIGLU ? W.N_pad / 256 : W.N_pad / 128;
-    const bool small = (long)m_tiles * ((T + 127) / 128) < (long)n_sm * 3 / 2;
+    const int m_tiles = (W.N_pad + 255) / 256;
+    const bool small = (long)m_tiles * ((T + 127) / 128) < (long)n_sm;
     if (W.type == Q4)
         return small ? tc::dispatch<Q4, 64>(W, epi, T, A, A_lo, a, layer, s) : tc::dispatch<Q4, 128>(W, epi, T, A, A_lo, a, layer, s);
     if (W.type == Q8)
