@@ -150,6 +150,13 @@ int32_t lcx_n_outputs(const lcx_ctx *ctx);
  * the cells of the stopped and later ubatches are released. cb NULL removes it. */
 void lcx_set_abort(lcx_ctx *ctx, int (*cb)(void *), void *user_data);
 
+/* Copies the stored K and V of one cell to HOST memory: k_out, v_out receive n_head_kv *
+ * head_dim f16 values each (the RoPE'd key and the value of layer `layer` at position `pos` of
+ * sequence `seq`, as appended by the forward; KV-cache section: keys and values are kept per
+ * layer and cell). Synchronizes the context's stream. Returns LCX_OK, or LCX_INVALID when the
+ * cell does not exist. */
+int32_t lcx_kv_read(lcx_ctx *ctx, int32_t layer, int32_t seq, int32_t pos, uint16_t *k_out, uint16_t *v_out);
+
 /* Counters of a context, for tests and measurement. */
 typedef struct {
     int64_t n_decode;          /* lcx_decode / lcx_decode_greedy calls that ran */

@@ -20,7 +20,8 @@ LCX_INVALID, LCX_ALLOC_FAILED, LCX_COMPUTE_FAILED = -1, -2, -3
 SYMBOLS = ("lcx_model_create", "lcx_model_free", "lcx_ctx_create", "lcx_ctx_free", "lcx_decode",
            "lcx_decode_greedy", "lcx_kv_clear", "lcx_seq_pos_max", "lcx_n_outputs", "lcx_set_abort",
            "lcx_get_stats", "lcx_ctx_create_host_only", "lcx_get_rows", "lcx_last_error", "lcx_set_profiling",
-           "lcx_get_profile", "lcx_attention_workspace_size", "lcx_attention", "lcx_attention_noalloc")
+           "lcx_get_profile", "lcx_attention_workspace_size", "lcx_attention", "lcx_attention_noalloc",
+           "lcx_kv_read")
 
 
 def build(force: bool = False) -> str:
@@ -105,6 +106,8 @@ def lib():
                                     ctypes.c_size_t, vp]
         L.lcx_attention_noalloc.restype = i32
         L.lcx_attention_noalloc.argtypes = [i32, i32, i32, i32, vp, vp, vp, i32, vp, i32, vp, vp, i32, vp, vp]
+        L.lcx_kv_read.restype = i32
+        L.lcx_kv_read.argtypes = [vp, i32, i32, i32, vp, vp]
         L.lcx_set_profiling.restype = i32
         L.lcx_set_profiling.argtypes = [vp, i32]
         L.lcx_get_profile.restype = i32
@@ -219,6 +222,17 @@ class Context:
         lib().lcx_get_profile(self.h, ctypes.byref(p))
         return {n: {"launches": getattr(p, n).launches, "ms": getattr(p, n).ms, "bytes": getattr(p, n).bytes,
                     "flops": getattr(p, n).flops} for n in ("gemv", "gemm", "attention", "other")}
+
+    def kv_read(self, layer: int, seq: int, pos: int):
+        """(k, v) of one cell as float16 numpy arrays [n_head_kv * head_dim]."""
+        import numpy as np
+        hp = self.model.hp
+        k = np.empty(hp.n_head_kv * hp.head_dim, dtype=np.uint16)
+        v = np.empty_like(k)
+        rc = lib().lcx_kv_read(self.h, layer, seq, pos, k.ctypes.data, v.ctypes.data)
+        if rc != 0:
+            raise IndexError(f"lcx_kv_read -> {rc}")
+        return k.view(np.float16), v.view(np.float16)
 
     def stats(self) -> lcx_stats:
         s = lcx_stats()

@@ -419,6 +419,26 @@ extern "C" void lcx_get_stats(const lcx_ctx *c, lcx_stats *out) {
     out->n_cells_used = c->cells_used;
 }
 
+extern "C" int32_t lcx_kv_read(lcx_ctx *c, int32_t layer, int32_t seq, int32_t pos, uint16_t *k_out, uint16_t *v_out) {
+    if (!c || c->host_only || !k_out || !v_out) return LCX_INVALID;
+    if (layer < 0 || layer >= c->hp.n_layer || seq < 0 || (uint32_t)seq >= c->n_seq_max) return LCX_INVALID;
+    const SeqState &S = c->seqs[seq];
+    if (pos < 0 || pos >= S.len) return LCX_INVALID;
+    const int KV = c->hp.n_head_kv, hd = c->hp.head_dim;
+    const int page = S.pages[pos / kPage], slot = pos % kPage;
+    cudaError_t e = cudaStreamSynchronize(c->stream);
+    for (int h = 0; h < KV && e == cudaSuccess; ++h) {
+        const size_t off = ((((size_t)layer * c->n_pages + page) * KV + h) * kPage + slot) * hd;
+        e = cudaMemcpy(k_out + (size_t)h * hd, c->kc + off, (size_t)hd * 2, cudaMemcpyDeviceToHost);
+        if (e == cudaSuccess) e = cudaMemcpy(v_out + (size_t)h * hd, c->vc + off, (size_t)hd * 2, cudaMemcpyDeviceToHost);
+    }
+    if (e != cudaSuccess) {
+        set_err("kv read", e);
+        return LCX_COMPUTE_FAILED;
+    }
+    return LCX_OK;
+}
+
 extern "C" const char *lcx_last_error(void) {
     std::lock_guard<std::mutex> lk(g_err_mu);
     return g_err.c_str();
