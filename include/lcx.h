@@ -186,6 +186,13 @@ typedef struct {
 } lcx_profile;
 int32_t lcx_set_profiling(lcx_ctx *ctx, int32_t on);
 int32_t lcx_get_profile(lcx_ctx *ctx, lcx_profile *out);
+/* lcx_set_profiling(ctx, 2) instead records an in-kernel timeline of the next matmul-vector and
+ * attention launches (up to 8192): per launch the earliest CTA start, the earliest CTA past the
+ * wait for the previous kernel, the latest CTA done with its set-up (activations staged, or
+ * attention partials computed), and the latest CTA end, as %globaltimer nanoseconds, with no
+ * event between launches. lcx_get_trace synchronizes and copies min(max_slots, recorded) slots
+ * of 4 values to host `out`; it returns the number recorded (-1 when trace mode is off). */
+int32_t lcx_get_trace(lcx_ctx *ctx, unsigned long long *out, int32_t max_slots);
 
 /* A context with no device: every host-side rule of lcx_decode (validation, position and
  * flag filling, cell reservation, ubatch split, abort, return codes) runs, and no kernel is

@@ -21,7 +21,7 @@ SYMBOLS = ("lcx_model_create", "lcx_model_free", "lcx_ctx_create", "lcx_ctx_free
            "lcx_decode_greedy", "lcx_kv_clear", "lcx_seq_pos_max", "lcx_n_outputs", "lcx_set_abort",
            "lcx_get_stats", "lcx_ctx_create_host_only", "lcx_get_rows", "lcx_last_error", "lcx_set_profiling",
            "lcx_get_profile", "lcx_attention_workspace_size", "lcx_attention", "lcx_attention_noalloc",
-           "lcx_kv_read")
+           "lcx_kv_read", "lcx_get_trace")
 
 
 def build(force: bool = False) -> str:
@@ -106,6 +106,8 @@ def lib():
                                     ctypes.c_size_t, vp]
         L.lcx_attention_noalloc.restype = i32
         L.lcx_attention_noalloc.argtypes = [i32, i32, i32, i32, vp, vp, vp, i32, vp, i32, vp, vp, i32, vp, vp]
+        L.lcx_get_trace.restype = i32
+        L.lcx_get_trace.argtypes = [vp, vp, i32]
         L.lcx_kv_read.restype = i32
         L.lcx_kv_read.argtypes = [vp, i32, i32, i32, vp, vp]
         L.lcx_set_profiling.restype = i32
@@ -214,8 +216,18 @@ class Context:
         self._abort = ABORT_CB(lambda _ud: 1 if fn() else 0)
         lib().lcx_set_abort(self.h, self._abort, None)
 
-    def set_profiling(self, on: bool) -> int:
-        return lib().lcx_set_profiling(self.h, 1 if on else 0)
+    def set_profiling(self, on) -> int:
+        """False: off; True: per-launch events; 2: in-kernel timeline (see trace())."""
+        return lib().lcx_set_profiling(self.h, 2 if on == 2 else (1 if on else 0))
+
+    def trace(self):
+        """The recorded timeline as a numpy array [launches][4] (ns)."""
+        import numpy as np
+        n = lib().lcx_get_trace(self.h, None, 0)
+        out = np.zeros((max(n, 0), 4), dtype=np.uint64)
+        if n > 0:
+            lib().lcx_get_trace(self.h, out.ctypes.data, n)
+        return out
 
     def profile(self) -> dict:
         p = lcx_profile()

@@ -26,32 +26,62 @@ __global__ void __launch_bounds__(128) k_attn(const FwdArgs a, const int layer, 
     constexpr int DPV = HD / 32;   // dims per lane in P.V
     const int t = blockIdx.z, kvh = blockIdx.y, sp = blockIdx.x;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    // The ubatch metadata and the page table were written before the preceding kernel ran, and
-    // the cells of earlier positions hold K/V stored by earlier ubatches: pull this CTA's rows
-    // into L2 while the preceding kernel (which writes q and the newest cells) finishes.
+    LCX_TRACE(a, 0);
+    // The ubatch metadata, the page table and the cells of positions <= pos - T (stored by earlier
+    // ubatches) do not depend on the preceding kernel, which writes q and this ubatch's cells: each
+    // warp loads its first 16 cells into registers before waiting for that kernel, and re-reads
+    // afterwards only the cells this ubatch may have written.
     const int pos = a.ub.pos[t], seq = a.ub.seq[t];
     const int n_att = pos + 1;
     const int ns_t = (n_att + chunk - 1) / chunk;
     const int c0 = sp * chunk, c1 = min(c0 + chunk, n_att);
-    if (sp < ns_t) {
-        const int32_t *ptr0 = a.pt + (size_t)seq * a.max_pages_per_seq;
-        constexpr int LPR = HD * 2 / 128;   // 128-byte lines per K or V row
-        for (int i = threadIdx.x; i < (c1 - c0) * LPR; i += blockDim.x) {
-            const int j = c0 + i / LPR;
-            const size_t row = (((size_t)layer * a.n_pages + ptr0[j / kPage]) * a.KV + kvh) * kPage + (j % kPage);
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(a.kc + row * HD + (i % LPR) * 64));
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(a.vc + row * HD + (i % LPR) * 64));
+    const int sub = lane & 7, cgrp = lane >> 3;
+    const int32_t *ptrow = a.pt + (size_t)seq * a.max_pages_per_seq;
+    const size_t layer_base = (size_t)layer * a.n_pages;
+    const int fresh = n_att - a.T;   // cells at positions >= fresh may come from this ubatch
+    uint4 kraw[4][DPL / 8];
+    uint2 vraw[16];
+    // K/V of the super-group of 16 cells at j0 (inside one page); `only_fresh` re-reads just the
+    // cells this ubatch may have written
+    auto load_sg = [&](int j0, bool only_fresh) {
+        const int page = ptrow[j0 / kPage];
+        const size_t row0 = ((layer_base + page) * a.KV + kvh) * kPage + (j0 % kPage);
+#pragma unroll
+        for (int g4 = 0; g4 < 4; ++g4) {
+            const int j = j0 + 4 * g4 + cgrp;
+            if (only_fresh && (j < fresh || j >= c1)) continue;
+            if (j < c1) {
+                const __half *kp = a.kc + (row0 + 4 * g4 + cgrp) * HD + sub * DPL;
+#pragma unroll
+                for (int i = 0; i < DPL / 8; ++i) kraw[g4][i] = *reinterpret_cast<const uint4 *>(kp + 8 * i);
+            } else {
+#pragma unroll
+                for (int i = 0; i < DPL / 8; ++i) kraw[g4][i] = make_uint4(0, 0, 0, 0);
+            }
         }
-    }
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+            const int j = j0 + c;
+            if (only_fresh && j < fresh) continue;
+            if (j < c1) {
+                const __half *vp = a.vc + (row0 + c) * HD + lane * DPV;
+                if (DPV == 4) vraw[c] = *reinterpret_cast<const uint2 *>(vp);
+                else vraw[c] = make_uint2(*reinterpret_cast<const uint32_t *>(vp), 0u);
+            }
+        }
+    };
+    const int j_first = c0 + warp * 16;
+    if (sp < ns_t && j_first < c1) load_sg(j_first, false);
     LCX_PDL_WAIT();
     LCX_PDL_TRIGGER();
+    LCX_TRACE(a, 1);
     if (sp >= ns_t) return;
+    if (j_first < c1 && j_first + 16 > fresh) load_sg(j_first, true);
     const int qw = a.H * HD;
     const float scale = rsqrtf((float)HD);
 
     // this lane's Q slice for the QK step: dims (lane % 8) * DPL .. + DPL, pre-scaled
     float qr[G][DPL];
-    const int sub = lane & 7, cgrp = lane >> 3;
 #pragma unroll
     for (int g = 0; g < G; ++g) {
         const float *qp = a.q + (size_t)t * qw + (size_t)(kvh * G + g) * HD + sub * DPL;
@@ -69,36 +99,11 @@ __global__ void __launch_bounds__(128) k_attn(const FwdArgs a, const int layer, 
 #pragma unroll
         for (int i = 0; i < DPV; ++i) acc[g][i] = 0.f;
     }
-    const int32_t *ptrow = a.pt + (size_t)seq * a.max_pages_per_seq;
-    const size_t layer_base = (size_t)layer * a.n_pages;
 
     // Each warp takes super-groups of 16 consecutive cells (inside one 64-cell page): all K and
     // V loads of a super-group are issued before any of them is used.
-    for (int j0 = c0 + warp * 16; j0 < c1; j0 += 64) {
-        const int page = ptrow[j0 / kPage];
-        const int row0 = (int)(((layer_base + page) * a.KV + kvh) * kPage + (j0 % kPage));
-        uint4 kraw[4][DPL / 8];
-        uint2 vraw[16];
-#pragma unroll
-        for (int g4 = 0; g4 < 4; ++g4) {
-            const int j = j0 + 4 * g4 + cgrp;
-            if (j < c1) {
-                const __half *kp = a.kc + (size_t)(row0 + 4 * g4 + cgrp) * HD + sub * DPL;
-#pragma unroll
-                for (int i = 0; i < DPL / 8; ++i) kraw[g4][i] = *reinterpret_cast<const uint4 *>(kp + 8 * i);
-            } else {
-#pragma unroll
-                for (int i = 0; i < DPL / 8; ++i) kraw[g4][i] = make_uint4(0, 0, 0, 0);
-            }
-        }
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-            if (j0 + c < c1) {
-                const __half *vp = a.vc + (size_t)(row0 + c) * HD + lane * DPV;
-                if (DPV == 4) vraw[c] = *reinterpret_cast<const uint2 *>(vp);
-                else vraw[c] = make_uint2(*reinterpret_cast<const uint32_t *>(vp), 0u);
-            }
-        }
+    for (int j0 = j_first; j0 < c1; j0 += 64) {
+        if (j0 != j_first) load_sg(j0, false);
 #pragma unroll
         for (int g4 = 0; g4 < 4; ++g4) {
             if (j0 + 4 * g4 >= c1) break;
@@ -175,6 +180,7 @@ __global__ void __launch_bounds__(128) k_attn(const FwdArgs a, const int layer, 
         }
     }
 
+    LCX_TRACE(a, 2);
     // ---- merge the 4 warps
     __shared__ float sm_m[4][G], sm_l[4][G];
     __shared__ float sm_acc[4][G][HD];
@@ -212,7 +218,10 @@ __global__ void __launch_bounds__(128) k_attn(const FwdArgs a, const int layer, 
             if (dd == 0) { pr[0] = M; pr[1] = L; }
         }
     }
-    if (single) return;
+    if (single) {
+        LCX_TRACE(a, 3);
+        return;
+    }
 
     // ---- split merge by the last CTA to arrive
     __shared__ int last;
@@ -223,7 +232,10 @@ __global__ void __launch_bounds__(128) k_attn(const FwdArgs a, const int layer, 
         last = prev == ns_t - 1;
     }
     __syncthreads();
-    if (!last) return;
+    if (!last) {
+        LCX_TRACE(a, 3);
+        return;
+    }
     __threadfence();
     // merge weights of the splits: w_s = exp(M_s - M*) / L*, one warp per query head
     __shared__ float sw[64][G];
@@ -269,11 +281,17 @@ __global__ void __launch_bounds__(128) k_attn(const FwdArgs a, const int layer, 
         else a.o32[oi] = o;
     }
     if (threadIdx.x == 0) a.att_cnt[t * a.KV + kvh] = 0;
+    LCX_TRACE(a, 3);
 }
 
 template <int HD, int G>
 cudaError_t run(const FwdArgs &a, int layer, int chunk, int ns, bool out16, cudaStream_t s) {
     dim3 grid(ns, a.KV, a.T);
+    if (!a.pdl) {   // stand-alone call: fully ordered after the caller's preceding work
+        if (out16) k_attn<HD, G, true><<<grid, 128, 0, s>>>(a, layer, chunk, ns);
+        else k_attn<HD, G, false><<<grid, 128, 0, s>>>(a, layer, chunk, ns);
+        return cudaGetLastError();
+    }
     if (out16) return launch_pdl(k_attn<HD, G, true>, grid, dim3(128), 0, s, a, layer, chunk, ns);
     return launch_pdl(k_attn<HD, G, false>, grid, dim3(128), 0, s, a, layer, chunk, ns);
 }
@@ -298,7 +316,9 @@ int attention_splits(const FwdArgs &a, int max_natt, int *chunk) {
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
     }
-    const int target = 4 * n_sm;
+    // one CTA per SM: the next kernel's CTAs (started early, waiting for this one) leave room for
+    // about one attention CTA per SM, so a second wave would double the latency
+    const int target = n_sm;
     const int units = a.T * a.KV;
     int ns = units >= target ? 1 : (target + units - 1) / units;
     int by_len = (max_natt + 63) / 64;

@@ -103,53 +103,45 @@ __device__ __forceinline__ int task_row(int task, int r) {
 
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
-// Stage token t: RMS-normalise (when g != NULL) and split every block into hi / lo int8.
-// Run by the 256 consumer threads (warps 0..7), synchronised with named barrier 1.
+// Stage token t: split every 32-element block of x * g (g = the RMSNorm gains, or 1) into
+// hi / lo int8 parts, and leave this thread's share of sum(x^2) in red[t][warp]. The RMS factor
+// is a positive scalar, so the block split does not depend on it: it multiplies each row's dot
+// product in the epilogue instead, and the sum of squares is reduced while the blocks are being
+// split. Two adjacent lanes share a block (16 elements each). Run by the 256 consumer threads.
 template <int QT>
-__device__ void stage_token(const GemvParams &p, const FwdArgs &a, int t, uint8_t *stage_t, float *red) {
+__device__ void stage_token(const GemvParams &p, int t, uint8_t *stage_t, float (*red)[8]) {
     constexpr int NTHR = 256;
     const int nb = p.nb, K = p.K;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const float *xr = p.in.x + (size_t)(p.in.x_rows ? p.in.x_rows[t] : t) * K;
-    float rs = 1.f;
-    if (p.in.g) {
-        float ss = 0.f;
-        for (int k = threadIdx.x * 4; k < K; k += NTHR * 4) {
-            const float4 v = *reinterpret_cast<const float4 *>(xr + k);
-            ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
-        }
-        for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-        consumer_sync();
-        if (lane == 0) red[warp] = ss;
-        consumer_sync();
-        float tot = 0.f;
-#pragma unroll
-        for (int w = 0; w < 8; ++w) tot += red[w];
-        rs = 1.0f / sqrtf(tot / (float)K + a.eps);
-    }
     uint8_t *hp = stage_t, *lp = stage_t + (size_t)nb * 32;
     float2 *mp = reinterpret_cast<float2 *>(stage_t + (size_t)nb * 64);
-    for (int b = threadIdx.x; b < nb; b += NTHR) {
-        float v[32];
+    float ss = 0.f;
+    const int n_half = 2 * nb, iters = (n_half + NTHR - 1) / NTHR;   // same trip count in every lane
+    for (int it = 0; it < iters; ++it) {
+        const int hb = it * NTHR + threadIdx.x, b = hb >> 1, half = hb & 1;
+        const bool active = hb < n_half;
+        float v[16];
 #pragma unroll
-        for (int j = 0; j < 32; j += 4) {
-            float4 q = *reinterpret_cast<const float4 *>(xr + b * 32 + j);
-            if (p.in.g) {
-                const float4 g = *reinterpret_cast<const float4 *>(p.in.g + b * 32 + j);
-                q.x = q.x * rs * g.x; q.y = q.y * rs * g.y; q.z = q.z * rs * g.z; q.w = q.w * rs * g.w;
+        for (int j = 0; j < 16; j += 4) {
+            float4 q = active ? *reinterpret_cast<const float4 *>(xr + b * 32 + half * 16 + j) : make_float4(0, 0, 0, 0);
+            ss += q.x * q.x + q.y * q.y + q.z * q.z + q.w * q.w;
+            if (p.in.g && active) {
+                const float4 gg = *reinterpret_cast<const float4 *>(p.in.g + b * 32 + half * 16 + j);
+                q.x *= gg.x; q.y *= gg.y; q.z *= gg.z; q.w *= gg.w;
             }
             v[j] = q.x; v[j + 1] = q.y; v[j + 2] = q.z; v[j + 3] = q.w;
         }
         float amax = 0.f;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(v[j]));
-        const float s = amax * (1.0f / 127.0f);
+        for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(v[j]));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));   // the partner holds the other half
         const float inv = amax > 0.f ? 127.0f / amax : 0.f;
-        uint32_t hw[8], lw[8];
+        uint32_t hw[4], lw[4];
         int sh = 0, sl = 0;
 #pragma unroll
-        for (int w = 0; w < 8; ++w) {
-            uint32_t hb = 0, lb = 0;
+        for (int w = 0; w < 4; ++w) {
+            uint32_t hbits = 0, lbits = 0;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const float y = v[4 * w + e] * inv;
@@ -157,19 +149,35 @@ __device__ void stage_token(const GemvParams &p, const FwdArgs &a, int t, uint8_
                 const float l = fminf(fmaxf(rintf((y - h) * 128.f), -127.f), 127.f);
                 sh += (int)h;
                 sl += (int)l;
-                hb |= ((uint32_t)(int)h & 0xffu) << (8 * e);
-                lb |= ((uint32_t)(int)l & 0xffu) << (8 * e);
+                hbits |= ((uint32_t)(int)h & 0xffu) << (8 * e);
+                lbits |= ((uint32_t)(int)l & 0xffu) << (8 * e);
             }
-            hw[w] = hb;
-            lw[w] = lb;
+            hw[w] = hbits;
+            lw[w] = lbits;
         }
-        *reinterpret_cast<uint4 *>(hp + plane_chunk_off(b, 0)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-        *reinterpret_cast<uint4 *>(hp + plane_chunk_off(b, 1)) = make_uint4(hw[4], hw[5], hw[6], hw[7]);
-        *reinterpret_cast<uint4 *>(lp + plane_chunk_off(b, 0)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-        *reinterpret_cast<uint4 *>(lp + plane_chunk_off(b, 1)) = make_uint4(lw[4], lw[5], lw[6], lw[7]);
-        const int C = QT == Q4 ? 8 * (128 * sh + sl) : 0;
-        mp[b] = make_float2(s * (1.0f / 128.0f), __int_as_float(C));
+        sh += __shfl_xor_sync(0xffffffffu, sh, 1);
+        sl += __shfl_xor_sync(0xffffffffu, sl, 1);
+        if (active) {
+            *reinterpret_cast<uint4 *>(hp + plane_chunk_off(b, half)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4 *>(lp + plane_chunk_off(b, half)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            if (half == 0) {
+                const int C = QT == Q4 ? 8 * (128 * sh + sl) : 0;
+                mp[b] = make_float2(amax * (1.0f / (127.0f * 128.0f)), __int_as_float(C));
+            }
+        }
     }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (lane == 0) red[t][warp] = ss;
+}
+
+// RMS factor of token t from the partial sums left by stage_token (1 without norm gains).
+__device__ __forceinline__ float token_rs(const GemvParams &p, const FwdArgs &a, float (*red)[8], int t) {
+    if (!p.in.g) return 1.f;
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) tot += red[t][w];
+    return 1.0f / sqrtf(tot / (float)p.K + a.eps);
 }
 
 // ---------------------------------------------------------------- TMA-bulk streaming kernel
@@ -266,6 +274,7 @@ __global__ void __launch_bounds__(288, 1) k_gemv(const GemvParams p, const FwdAr
     const int tps = pl.tps, S = pl.slots;
     const int n_stages = (p.n_tasks + tps - 1) / tps;
     const int row_bytes = nb * QB;
+    LCX_TRACE(a, 0);
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
@@ -309,18 +318,24 @@ __global__ void __launch_bounds__(288, 1) k_gemv(const GemvParams p, const FwdAr
     }
 
     // ---------------- consumers (256 threads)
+    if (p.in.g) {   // the norm gains are weights: bring them close before waiting
+        for (int l = threadIdx.x; l < p.K / 32; l += 256)
+            asm volatile("prefetch.global.L1 [%0];" ::"l"(p.in.g + 32 * l));
+    }
     LCX_PDL_WAIT();
     LCX_PDL_TRIGGER();
-    __shared__ float red[8];
+    LCX_TRACE(a, 1);
+    __shared__ float red[NT][8];
     for (int t = 0; t < NT; ++t) {
         if (t < p.T) {
-            stage_token<QT>(p, a, t, xstage + t * stage_bytes_per_token(nb), red);
+            stage_token<QT>(p, t, xstage + t * stage_bytes_per_token(nb), red);
         } else {
             for (size_t i = threadIdx.x * 16; i < stage_bytes_per_token(nb); i += 256 * 16)
                 *reinterpret_cast<uint4 *>(xstage + t * stage_bytes_per_token(nb) + i) = make_uint4(0, 0, 0, 0);
         }
     }
     consumer_sync();
+    LCX_TRACE(a, 2);
 
     const int KS = kConsumerWarps / tps;
     const int tg = warp / KS, ks = warp % KS;
@@ -398,10 +413,11 @@ __global__ void __launch_bounds__(288, 1) k_gemv(const GemvParams p, const FwdAr
             if (t < p.T) {
                 float v[4];
 #pragma unroll
+                const float rs = token_rs(p, a, red, t);
                 for (int r = 0; r < 4; ++r) {
                     float sum = 0.f;
                     for (int q = 0; q < KS; ++q) sum += part[k & 1][et * 4 + r][q][t];
-                    v[r] = sum;
+                    v[r] = sum * rs;
                 }
                 const int task = st * tps + et;
                 if (EPI == EPI_SWIGLU) {
@@ -419,6 +435,7 @@ __global__ void __launch_bounds__(288, 1) k_gemv(const GemvParams p, const FwdAr
         }
         // part[k & 1] is rewritten two stages later, after the next consumer_sync
     }
+    LCX_TRACE(a, 3);
     if (EPI == EPI_LOGITS) {
         __shared__ unsigned long long cbest[NT];
         consumer_sync();

@@ -89,6 +89,9 @@ struct FwdArgs {
     int32_t *att_cnt;  // [T][KV] arrival counters, zero between launches
     int att_max_split;
     int32_t *err;      // device error word: set by a kernel whose bounded wait timed out
+    unsigned long long *trace;   // NULL, or [slots][4] timestamps (first start, first past wait, last staged, last end)
+    bool pdl;                    // launched inside the forward's chain of dependent launches
+    int trace_slot;              // this launch's slot
     // KV cache
     __half *kc, *vc;   // [L][n_pages][KV][kPage][hd]
     int n_pages;
@@ -142,9 +145,21 @@ size_t attention_scratch_bytes(const FwdArgs &a, int max_natt, size_t *counter_o
 // Launch with programmatic dependent launch allowed: the kernel may start while the previous
 // kernel on the stream finishes; it must execute griddepcontrol.wait before reading anything
 // the previous kernels wrote (and before writing anything they read).
+// Every kernel of the forward asks for the largest shared-memory carveout, so consecutive kernels
+// never make an SM re-split its L1 and shared memory between launches.
+template <typename F>
+inline void prefer_max_shared(F *kern) {
+    static bool done = false;   // one per kernel instantiation
+    if (!done) {
+        cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+        done = true;
+    }
+}
+
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
                               Args &&...args) {
+    prefer_max_shared(kern);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
@@ -167,6 +182,20 @@ __device__ __forceinline__ void store_split(__half *hi, __half *lo, size_t i, fl
     hi[i] = h;
     lo[i] = __float2half_rn(v - __half2float(h));
 }
+
+__device__ __forceinline__ unsigned long long lcx_gtime() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// Launch timeline for measurement (off when a.trace == NULL): thread 0 of every CTA records.
+#define LCX_TRACE(a, which)                                                                     \
+    do {                                                                                        \
+        if ((a).trace && threadIdx.x == 0) {                                                    \
+            unsigned long long *t_ = (a).trace + 4 * (a).trace_slot + (which);                  \
+            if ((which) >= 2) atomicMax(t_, lcx_gtime()); else atomicMin(t_, lcx_gtime());      \
+        }                                                                                       \
+    } while (0)
 
 #define LCX_PDL_WAIT() asm volatile("griddepcontrol.wait;" ::: "memory")
 #define LCX_PDL_TRIGGER() asm volatile("griddepcontrol.launch_dependents;")

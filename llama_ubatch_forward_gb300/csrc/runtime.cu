@@ -231,13 +231,18 @@ struct lcx_ctx {
     struct ProfRec { int cls; double bytes, flops; };
     std::vector<ProfRec> prof_rec;
     lcx_profile prof{};
+    // in-kernel launch timeline (lcx_set_profiling mode 2)
+    unsigned long long *trace = nullptr;
+    int trace_cap = 0, trace_used = 0;
 };
 
 static void prof_resolve(lcx_ctx *c);
+static int32_t trace_on(lcx_ctx *c);
 
 static void free_ctx_device(lcx_ctx *c) {
     for (auto e : c->prof_ev) cudaEventDestroy(e);
     c->prof_ev.clear();
+    if (c->trace) cudaFree(c->trace);
     if (c->kc) cudaFree(c->kc);
     if (c->vc) cudaFree(c->vc);
     if (c->pt) cudaFree(c->pt);
@@ -367,6 +372,7 @@ extern "C" lcx_ctx *lcx_ctx_create(lcx_model *m, uint32_t n_ctx, uint32_t n_seq_
         a.pt = c->pt; a.max_pages_per_seq = c->max_pages_per_seq;
         a.rope = c->rope;
         a.att_max_split = c->max_att_split;
+        a.pdl = true;
     }
     // metadata: per token tok, pos, seq, cell, out_row + up to 2 page-table updates (2 ints each)
     c->meta_cap = 12 * std::max<int>(T, 4096) + 64;
@@ -585,12 +591,21 @@ cudaError_t upload_meta(lcx_ctx *c, const Plan &P, const Ub &u, UbDev &ub) {
 
 enum { PC_GEMV = 0, PC_GEMM = 1, PC_ATTN = 2, PC_OTHER = 3 };
 
-// Brackets one launch with events when profiling is on.
+// Brackets one launch with events when profiling is on; in trace mode gives the launch a slot of
+// the in-kernel timeline instead.
 struct ProfScope {
     lcx_ctx *c;
     int cls;
     double bytes, flops;
-    ProfScope(lcx_ctx *c_, int cls_, double bytes_, double flops_) : c(c_), cls(cls_), bytes(bytes_), flops(flops_) {
+    ProfScope(lcx_ctx *c_, int cls_, double bytes_, double flops_, FwdArgs *a = nullptr)
+        : c(c_), cls(cls_), bytes(bytes_), flops(flops_) {
+        if (a) {
+            a->trace = nullptr;
+            if (c->trace && c->trace_used < c->trace_cap) {
+                a->trace = c->trace;
+                a->trace_slot = c->trace_used++;
+            }
+        }
         if (!c->prof_on) return;
         if (c->prof_rec.size() * 2 + 2 > c->prof_ev.size()) prof_resolve(c);
         cudaEventRecord(c->prof_ev[c->prof_rec.size() * 2], c->stream);
@@ -635,18 +650,18 @@ cudaError_t run_forward(lcx_ctx *c, FwdArgs &a, int max_natt, double att_cells, 
             e = launch_rmsnorm_h(a.x, nullptr, a.T, a.d, D.attn_norm, a.eps, a.xh, a.xh_lo, s, nl);
         }
         if (e == cudaSuccess) {
-            ProfScope ps(c, cls, w_qkv + T * d * ab + T * (qw * 4 + kvw * 4), 2 * T * (qw + 2 * kvw) * d);
+            ProfScope ps(c, cls, w_qkv + T * d * ab + T * (qw * 4 + kvw * 4), 2 * T * (qw + 2 * kvw) * d, &a);
             e = gemv ? launch_gemv(D.qkv, EPI_QKV, a.T, GemvIn{a.x, nullptr, D.attn_norm}, a, l, s, nl)
                      : launch_gemm(D.qkv, EPI_QKV, a.T, a.xh, a.xh_lo, a, l, s, nl);
         }
         if (e == cudaSuccess) {
-            ProfScope ps(c, PC_ATTN, att_bytes, att_flops);
+            ProfScope ps(c, PC_ATTN, att_bytes, att_flops, &a);
             // long runs of one sequence (prefill): tensor-core tiles; single tokens: split-K
             const bool tiles = !gemv && a.ub.n_qtiles > 0 && a.ub.n_qtiles * 8 <= a.T;
             e = tiles ? launch_attention_prefill(a, l, s, nl) : launch_attention(a, l, max_natt, !gemv, s, nl);
         }
         if (e == cudaSuccess) {
-            ProfScope ps(c, cls, w_o + T * qw * ab + T * d * 8, 2 * T * d * qw);
+            ProfScope ps(c, cls, w_o + T * qw * ab + T * d * 8, 2 * T * d * qw, &a);
             e = gemv ? launch_gemv(D.wo, EPI_RESID, a.T, GemvIn{a.o32, nullptr, nullptr}, a, l, s, nl)
                      : launch_gemm(D.wo, EPI_RESID, a.T, a.o16, a.o16_lo, a, l, s, nl);
         }
@@ -655,12 +670,12 @@ cudaError_t run_forward(lcx_ctx *c, FwdArgs &a, int max_natt, double att_cells, 
             e = launch_rmsnorm_h(a.x, nullptr, a.T, a.d, D.ffn_norm, a.eps, a.xh, a.xh_lo, s, nl);
         }
         if (e == cudaSuccess) {
-            ProfScope ps(c, cls, w_gu + T * d * ab + T * F * ab, 2 * T * 2 * F * d);
+            ProfScope ps(c, cls, w_gu + T * d * ab + T * F * ab, 2 * T * 2 * F * d, &a);
             e = gemv ? launch_gemv(D.gateup, EPI_SWIGLU, a.T, GemvIn{a.x, nullptr, D.ffn_norm}, a, l, s, nl)
                      : launch_gemm(D.gateup, EPI_SWIGLU, a.T, a.xh, a.xh_lo, a, l, s, nl);
         }
         if (e == cudaSuccess) {
-            ProfScope ps(c, cls, w_dn + T * F * ab + T * d * 8, 2 * T * d * F);
+            ProfScope ps(c, cls, w_dn + T * F * ab + T * d * 8, 2 * T * d * F, &a);
             e = gemv ? launch_gemv(D.down, EPI_RESID, a.T, GemvIn{a.h32, nullptr, nullptr}, a, l, s, nl)
                      : launch_gemm(D.down, EPI_RESID, a.T, a.h16, a.h16_lo, a, l, s, nl);
         }
@@ -668,7 +683,7 @@ cudaError_t run_forward(lcx_ctx *c, FwdArgs &a, int max_natt, double att_cells, 
     if (e != cudaSuccess || a.n_out == 0) return e;
     const double no = a.n_out, w_head = qmat_bytes(m->head, a.V, a.d);
     if (gemv_fits(m->head, a.n_out)) {
-        ProfScope ps(c, PC_GEMV, w_head + no * d * 4 + no * a.V * 4, 2 * no * a.V * d);
+        ProfScope ps(c, PC_GEMV, w_head + no * d * 4 + no * a.V * 4, 2 * no * a.V * d, &a);
         e = launch_gemv(m->head, EPI_LOGITS, a.n_out, GemvIn{a.x, a.ub.out_rows, m->output_norm}, a, -1, s, nl);
     } else {
         {
@@ -894,6 +909,15 @@ extern "C" int32_t lcx_set_profiling(lcx_ctx *c, int32_t on) {
     if (!c || c->host_only) return LCX_INVALID;
     prof_resolve(c);
     c->prof = lcx_profile{};
+    if (on == 2) {
+        c->prof_on = false;
+        return trace_on(c);
+    }
+    if (c->trace) {   // leaving trace mode
+        cudaStreamSynchronize(c->stream);
+        cudaFree(c->trace);
+        c->trace = nullptr;
+    }
     c->prof_on = on != 0;
     if (c->prof_on && c->prof_ev.empty()) {
         c->prof_ev.resize(2 * 4096);
@@ -901,6 +925,27 @@ extern "C" int32_t lcx_set_profiling(lcx_ctx *c, int32_t on) {
             if (cudaEventCreate(&e) != cudaSuccess) return LCX_ALLOC_FAILED;
     }
     return LCX_OK;
+}
+
+// mode 2: record the in-kernel timeline of the next launches (up to 8192) instead of events
+static int32_t trace_on(lcx_ctx *c) {
+    if (!c->trace) {
+        c->trace_cap = 8192;
+        if (cudaMalloc(&c->trace, (size_t)c->trace_cap * 4 * 8) != cudaSuccess) return LCX_ALLOC_FAILED;
+    }
+    std::vector<unsigned long long> init((size_t)c->trace_cap * 4);
+    for (size_t i = 0; i < init.size(); ++i) init[i] = i % 4 >= 2 ? 0ull : ~0ull;
+    cudaMemcpy(c->trace, init.data(), init.size() * 8, cudaMemcpyHostToDevice);
+    c->trace_used = 0;
+    return LCX_OK;
+}
+
+extern "C" int32_t lcx_get_trace(lcx_ctx *c, unsigned long long *out, int32_t max_slots) {
+    if (!c || c->host_only || !c->trace) return -1;
+    cudaStreamSynchronize(c->stream);
+    const int n = std::min(max_slots, c->trace_used);
+    if (out && n > 0) cudaMemcpy(out, c->trace, (size_t)n * 4 * 8, cudaMemcpyDeviceToHost);
+    return c->trace_used;
 }
 
 extern "C" int32_t lcx_get_profile(lcx_ctx *c, lcx_profile *out) {
