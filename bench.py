@@ -30,10 +30,10 @@ import numpy as np  # noqa: E402
 
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
-# dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant GEMV (gate/up,
-# Q4_0, 8B shape, T = 1) from the committed ncu summary; None until captured for the
-# current kernel.
-GEMV_NCU_TRAFFIC_BYTES = None
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the weight-streaming
+# GEMV averaged over the 129 launches of one 8B decode token, from an ncu capture of the current
+# kernel: QKV 14.24 MB, O 9.51, gate/up 66.41, down 33.15 per layer, head 558.81 once.
+GEMV_NCU_TRAFFIC_BYTES = (32 * (14.24 + 9.51 + 66.41 + 33.15) + 558.81) / 129 * 1e6
 
 
 def log(*a):
