@@ -23,15 +23,48 @@ __device__ __forceinline__ size_t kv_off(const FwdArgs &a, int layer, int cell, 
     return ((((size_t)layer * a.n_pages + page) * a.KV + kvh) * kPage + slot) * a.hd + dim;
 }
 
-// Epilogue of 4 consecutive rows r0..r0+3 (r0 % 4 == 0) of token t.
+// Operands an epilogue reads from memory, loaded ahead of the dot products that feed it: the
+// residual rows (through L2: other CTAs of the same launch may have written them), or the
+// token's cache cell and the RoPE (cos, sin) pairs of the quad.
+struct EpiIn {
+    float4 x;
+    float4 cs;     // (cos, sin) of pair r0 / 2 and of pair r0 / 2 + 1 within the head
+    int cell;
+};
+
 template <int EPI>
-__device__ __forceinline__ void epi_quad(const FwdArgs &a, int layer, int t, int r0, int N, const float v[4],
-                                         unsigned long long &best) {
+__device__ __forceinline__ EpiIn epi_load(const FwdArgs &a, int t, int r0, int N) {
+    EpiIn in{};
+    if (EPI == EPI_RESID) {
+        const float *xr = a.x + (size_t)t * a.d + r0;
+        if (r0 + 3 < N) {
+            in.x = __ldcg(reinterpret_cast<const float4 *>(xr));
+        } else {
+            in.x.x = r0 < N ? __ldcg(xr) : 0.f;
+            in.x.y = r0 + 1 < N ? __ldcg(xr + 1) : 0.f;
+            in.x.z = r0 + 2 < N ? __ldcg(xr + 2) : 0.f;
+        }
+    } else if (EPI == EPI_QKV) {
+        const int qw = a.H * a.hd, kw = a.KV * a.hd;
+        in.cell = a.ub.cell[t];
+        if (r0 < qw + kw) {   // q or k rows: the quad lies inside one head (hd % 4 == 0)
+            const int dim = r0 < qw ? r0 % a.hd : (r0 - qw) % a.hd;
+            in.cs = *reinterpret_cast<const float4 *>(a.rope + (size_t)a.ub.pos[t] * (a.hd / 2) + dim / 2);
+        }
+    }
+    return in;
+}
+
+// Epilogue of 4 consecutive rows r0..r0+3 (r0 % 4 == 0) of token t, with its operands loaded.
+template <int EPI>
+__device__ __forceinline__ void epi_quad_in(const FwdArgs &a, int layer, int t, int r0, int N, const float v[4],
+                                            const EpiIn &in, unsigned long long &best) {
     if (EPI == EPI_RESID) {
         float *xr = a.x + (size_t)t * a.d;
+        const float xo[4] = {in.x.x, in.x.y, in.x.z, in.x.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-            if (r0 + j < N) xr[r0 + j] += v[j];
+            if (r0 + j < N) xr[r0 + j] = xo[j] + v[j];
     } else if (EPI == EPI_LOGITS) {
         float *lr = a.logits + (size_t)t * a.V;
 #pragma unroll
@@ -43,16 +76,14 @@ __device__ __forceinline__ void epi_quad(const FwdArgs &a, int layer, int t, int
             }
     } else if (EPI == EPI_QKV) {
         const int qw = a.H * a.hd, kw = a.KV * a.hd;
-        const int pos = a.ub.pos[t];
 #pragma unroll
         for (int p = 0; p < 2; ++p) {
             const int r = r0 + 2 * p;
             if (r >= qw + 2 * kw) break;
             float y0 = v[2 * p], y1 = v[2 * p + 1];
             if (r < qw + kw) {   // q or k: rotate the pair
-                const int dim = r < qw ? r % a.hd : (r - qw) % a.hd;
-                const float2 cs = a.rope[(size_t)pos * (a.hd / 2) + dim / 2];
-                const float z0 = y0 * cs.x - y1 * cs.y, z1 = y0 * cs.y + y1 * cs.x;
+                const float c = p ? in.cs.z : in.cs.x, sn = p ? in.cs.w : in.cs.y;
+                const float z0 = y0 * c - y1 * sn, z1 = y0 * sn + y1 * c;
                 y0 = z0;
                 y1 = z1;
             }
@@ -64,11 +95,18 @@ __device__ __forceinline__ void epi_quad(const FwdArgs &a, int layer, int t, int
                 const bool isk = r < qw + kw;
                 const int rr = isk ? r - qw : r - qw - kw;
                 const int kvh = rr / a.hd, dim = rr % a.hd;
-                __half *dst = (isk ? a.kc : a.vc) + kv_off(a, layer, a.ub.cell[t], kvh, dim);
+                __half *dst = (isk ? a.kc : a.vc) + kv_off(a, layer, in.cell, kvh, dim);
                 *reinterpret_cast<__half2 *>(dst) = __floats2half2_rn(y0, y1);
             }
         }
     }
+}
+
+// Epilogue of 4 consecutive rows r0..r0+3 (r0 % 4 == 0) of token t.
+template <int EPI>
+__device__ __forceinline__ void epi_quad(const FwdArgs &a, int layer, int t, int r0, int N, const float v[4],
+                                         unsigned long long &best) {
+    epi_quad_in<EPI>(a, layer, t, r0, N, v, epi_load<EPI>(a, t, r0, N), best);
 }
 
 // SwiGLU epilogue: features f0..f0+3 of token t from gate g[4] and up u[4].

@@ -15,17 +15,21 @@ namespace {
 constexpr int TT = 32;     // tokens per CTA
 constexpr int TASKS = 16;  // row tasks per CTA
 
-template <int QT, int ROWS>
-__device__ __forceinline__ float deq(const uint8_t *qs, const __half *sc, int nb, int row, int b, int e) {
-    const float d = __half2float(sc[((size_t)(row >> 2) * nb + b) * 4 + (row & 3)]);
-    if (QT == Q8) return d * (float)(int8_t)qs[((size_t)row * nb + b) * 32 + e];
-    const uint8_t byte = qs[((size_t)row * nb + b) * 16 + (e & 15)];
-    const int q = e < 16 ? (byte & 15) : (byte >> 4);
-    return d * (float)(q - 8);
+// element e of block b of row `row` in the quad-interleaved storage (QMat)
+template <int QT>
+__device__ __forceinline__ float deq(const uint8_t *w, int nb, int row, int b, int e) {
+    constexpr int QB = QT == Q8 ? 32 : 16;
+    const uint8_t *quad = w + (size_t)(row >> 2) * (nb / 2) * pair_bytes_of(QB);
+    const float d = __half2float(*reinterpret_cast<const __half *>(quad + quad_s_off(QB, b) + 2 * (row & 3)));
+    const uint8_t *q = quad + quad_q_off(QB, row & 3, b);
+    if (QT == Q8) return d * (float)(int8_t)q[e];
+    const uint8_t byte = q[e & 15];
+    const int v = e < 16 ? (byte & 15) : (byte >> 4);
+    return d * (float)(v - 8);
 }
 
 template <int QT, int ROWS, int EPI, bool OUT16>
-__global__ void __launch_bounds__(256) k_gemm_simt(const uint8_t *__restrict__ qs, const __half *__restrict__ sc, int N,
+__global__ void __launch_bounds__(256) k_gemm_simt(const uint8_t *__restrict__ w, int N,
                                                    int nb, int n_tasks, int T, const __half *__restrict__ A,
                                                    const __half *__restrict__ A_lo, const FwdArgs a, int layer) {
     __shared__ float Ws[32][TASKS * ROWS + 1];
@@ -39,17 +43,14 @@ __global__ void __launch_bounds__(256) k_gemm_simt(const uint8_t *__restrict__ q
 #pragma unroll
     for (int r = 0; r < ROWS; ++r) acc[r][0] = acc[r][1] = 0.f;
 
-    auto task_row = [&](int task, int r) -> int {
-        if (ROWS == 4) return task * 4 + r;
-        const int c = task / (kRowTile / 4), qq = task % (kRowTile / 4);
-        return c * 2 * kRowTile + 4 * qq + (r >= 4 ? kRowTile : 0) + (r & 3);
-    };
+    // a SwiGLU task (ROWS 8) is a gate quad and the up quad after it: rows 8 task .. 8 task + 7
+    auto task_row = [&](int task, int r) -> int { return task * ROWS + r; };
 
     for (int b = 0; b < nb; ++b) {
         for (int i = threadIdx.x; i < 32 * TASKS * ROWS; i += blockDim.x) {
             const int e = i % 32, rr = i / 32;   // rr = local row (task * ROWS + r)
             const int task = task0 + rr / ROWS;
-            Ws[e][rr] = task < n_tasks ? deq<QT, ROWS>(qs, sc, nb, task_row(task, rr % ROWS), b, e) : 0.f;
+            Ws[e][rr] = task < n_tasks ? deq<QT>(w, nb, task_row(task, rr % ROWS), b, e) : 0.f;
         }
         for (int i = threadIdx.x; i < 32 * TT; i += blockDim.x) {
             const int e = i % 32, tt = i / 32;
@@ -83,8 +84,7 @@ __global__ void __launch_bounds__(256) k_gemm_simt(const uint8_t *__restrict__ q
             v1[r] = acc[(ROWS == 8 ? 4 : 0) + r][j];
         }
         if (ROWS == 8) {
-            const int c = task / (kRowTile / 4), qq = task % (kRowTile / 4);
-            epi_swiglu<OUT16>(a, t, c * kRowTile + 4 * qq, v0, v1);
+            epi_swiglu<OUT16>(a, t, 4 * task, v0, v1);
         } else {
             epi_quad<EPI>(a, layer, t, task * 4, N, v0, best[j]);
             if (EPI == EPI_LOGITS && best[j]) atomicMax(&a.amax_key[t], best[j]);
@@ -96,8 +96,8 @@ template <int QT, int ROWS, int EPI, bool OUT16>
 cudaError_t run(const QMat &W, int n_tasks, int T, const __half *A, const __half *A_lo, const FwdArgs &a, int layer,
                cudaStream_t s) {
     dim3 grid((n_tasks + TASKS - 1) / TASKS, (T + TT - 1) / TT);
-    return launch_pdl(k_gemm_simt<QT, ROWS, EPI, OUT16>, grid, dim3(256), 0, s, (const uint8_t *)W.qs,
-                      (const __half *)W.sc, W.N, W.nb, n_tasks, T, A, A_lo, a, layer);
+    return launch_pdl(k_gemm_simt<QT, ROWS, EPI, OUT16>, grid, dim3(256), 0, s, (const uint8_t *)W.w, W.N, W.nb,
+                      n_tasks, T, A, A_lo, a, layer);
 }
 
 template <int QT>

@@ -108,9 +108,9 @@ struct Cfg {
     static constexpr int QB = QT == Q8 ? 32 : 16;          // quant bytes per 32-element block
     static constexpr int A_BYTES = MT * BM * BK * 2;      // f16 weight tiles
     static constexpr int B_BYTES = 2 * BN * BK * 2;       // f16 activation tiles: high and low parts
-    static constexpr int RQ_BYTES = MT * BM * QB * 2;     // raw quants: 2 blocks per row
-    static constexpr int RS_BYTES = MT * (BM / 4) * 16;   // raw scales: 2 blocks x 4 rows per quad
-    static constexpr int STAGE = A_BYTES + B_BYTES + ((RQ_BYTES + RS_BYTES + 1023) / 1024) * 1024;
+    static constexpr int PB = 8 * QB + 16;                // one block pair of a row quad (QMat)
+    static constexpr int RQ_BYTES = MT * (BM / 4) * PB;   // raw tiles: 32 quads x one block pair
+    static constexpr int STAGE = A_BYTES + B_BYTES + ((RQ_BYTES + 1023) / 1024) * 1024;
     static constexpr int S = (220 * 1024) / STAGE < 6 ? (220 * 1024) / STAGE : 6;
     static constexpr int SMEM = S * STAGE + 1024 /* align */ + 256 /* barriers */;
     static constexpr int TMEM_COLS = MT * BN <= 32 ? 32 : MT * BN <= 64 ? 64 : MT * BN <= 128 ? 128 : MT * BN <= 256 ? 256 : 512;
@@ -123,12 +123,13 @@ struct GemmParams {
     int row_base;   // unused (tiles start at blockIdx.x * 128 or, for SwiGLU, chunk c * 256)
 };
 
-// Dequantise row `row` (0..127) of one raw tile into the swizzled f16 tile.
+// Dequantise row `row` (0..127) of one raw tile -- 32 row quads x one block pair, as stored
+// (QMat) -- into the swizzled f16 tile.
 template <int QT>
-__device__ __forceinline__ void dequant_row(const uint8_t *rq, const uint8_t *rs, uint8_t *atile, int row) {
-    constexpr int QB = QT == Q8 ? 32 : 16;
-    const uint8_t *q = rq + row * QB * 2;
-    const __half *sc = reinterpret_cast<const __half *>(rs + (row >> 2) * 16);
+__device__ __forceinline__ void dequant_row(const uint8_t *rq, uint8_t *atile, int row) {
+    constexpr int QB = QT == Q8 ? 32 : 16, PB = 8 * QB + 16;
+    const uint8_t *q = rq + (row >> 2) * PB + (row & 3) * 2 * QB;
+    const __half *sc = reinterpret_cast<const __half *>(rq + (row >> 2) * PB + 8 * QB);
     uint8_t *dst = atile + row * 128;
 #pragma unroll
     for (int blk = 0; blk < 2; ++blk) {
@@ -188,8 +189,7 @@ __device__ __forceinline__ void dequant_row(const uint8_t *rq, const uint8_t *rs
 template <int QT, int BN, int EPI>
 __global__ void __launch_bounds__(192, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_b2,
-              const __grid_constant__ CUtensorMap tm_q,
-              const __grid_constant__ CUtensorMap tm_s, const GemmParams p, const FwdArgs a, const int layer) {
+              const __grid_constant__ CUtensorMap tm_w, const GemmParams p, const FwdArgs a, const int layer) {
     constexpr int MT = 2;   // two 128-row weight tiles share every activation tile
     using C = Cfg<QT, BN, MT>;
     constexpr int S = C::S;
@@ -201,15 +201,12 @@ __global__ void __launch_bounds__(192, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m_tile = blockIdx.x, tok0 = blockIdx.y * BN;
     const int nk = p.nk;
-    // first weight row of each M tile
-    // gate/up: chunk m_tile's gate rows, then its up rows; otherwise two adjacent row tiles
+    // first weight row of each M tile: two adjacent 128-row tiles (for gate/up each holds 16
+    // gate quads interleaved with their 16 up quads)
     const int row0[MT] = {m_tile * 2 * BM, m_tile * 2 * BM + BM};
     auto a_tile = [&](int slot, int mt) { return smem + slot * C::STAGE + mt * BM * BK * 2; };
     auto b_tile = [&](int slot) { return smem + slot * C::STAGE + C::A_BYTES; };
-    auto rq_tile = [&](int slot, int mt) { return smem + slot * C::STAGE + C::A_BYTES + C::B_BYTES + mt * BM * C::QB * 2; };
-    auto rs_tile = [&](int slot, int mt) {
-        return smem + slot * C::STAGE + C::A_BYTES + C::B_BYTES + C::RQ_BYTES + mt * (BM / 4) * 16;
-    };
+    auto rq_tile = [&](int slot, int mt) { return smem + slot * C::STAGE + C::A_BYTES + C::B_BYTES + mt * (BM / 4) * C::PB; };
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
@@ -237,12 +234,10 @@ __global__ void __launch_bounds__(192, 1)
             bool ok = true;
             auto issue_w = [&](int j) {
                 const int slot = j % S;
-                mbar_expect_tx(&full_w[slot], C::RQ_BYTES + C::RS_BYTES);
+                mbar_expect_tx(&full_w[slot], C::RQ_BYTES);
 #pragma unroll
-                for (int mt = 0; mt < MT; ++mt) {
-                    tma_2d(rq_tile(slot, mt), &tm_q, j * C::QB * 2, row0[mt], &full_w[slot]);
-                    tma_2d(rs_tile(slot, mt), &tm_s, j * 16, row0[mt] / 4, &full_w[slot]);
-                }
+                for (int mt = 0; mt < MT; ++mt)   // quants and scales of 32 quads: one box
+                    tma_2d(rq_tile(slot, mt), &tm_w, j * (C::PB / 4), row0[mt] / 4, &full_w[slot]);
             };
             auto issue_b = [&](int j) {
                 const int slot = j % S;
@@ -305,7 +300,7 @@ __global__ void __launch_bounds__(192, 1)
             ok = __all_sync(0xffffffffu, mbar_wait(&full_w[slot], (j / S) & 1));   // warp-uniform
             if (!ok) break;
 #pragma unroll
-            for (int mt = 0; mt < MT; ++mt) dequant_row<QT>(rq_tile(slot, mt), rs_tile(slot, mt), a_tile(slot, mt), drow);
+            for (int mt = 0; mt < MT; ++mt) dequant_row<QT>(rq_tile(slot, mt), a_tile(slot, mt), drow);
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic writes -> tensor-core reads
             __syncwarp();
             if (lane == 0) mbar_arrive(&full_a[slot]);
@@ -323,14 +318,19 @@ __global__ void __launch_bounds__(192, 1)
                 uint32_t v0[32], v1[32];
                 tmem_ld32(tq + cb * 32, v0);
                 tmem_ld32(tq + BN + cb * 32, v1);
-                if (EPI == EPI_SWIGLU) {
+                if (EPI == EPI_SWIGLU) {   // rows 8f'..8f'+3 gate, 8f'+4..8f'+7 up of features 4f'..
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int t = tok0 + cb * 32 + i;
-                        const int f = m_tile * BM + lrow;
-                        if (t < p.T && f < a.F)
-                            store_split(a.h16, a.h16_lo, (size_t)t * a.F_pad + f,
-                                        silu_f(__uint_as_float(v0[i])) * __uint_as_float(v1[i]));
+                    for (int mt = 0; mt < MT; ++mt) {
+                        const int f = ((row0[mt] + lrow) >> 3) * 4 + (lrow & 3);
+                        const bool gate = (lane & 7) < 4;
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const float g = __uint_as_float(mt == 0 ? v0[i] : v1[i]);
+                            const float u = __shfl_down_sync(0xffffffffu, g, 4);
+                            const int t = tok0 + cb * 32 + i;
+                            if (gate && t < p.T && f < a.F)
+                                store_split(a.h16, a.h16_lo, (size_t)t * a.F_pad + f, silu_f(g) * u);
+                        }
                     }
                     continue;
                 }
@@ -464,8 +464,8 @@ cudaError_t run(const QMat &W, int T, const __half *A, const __half *A_lo, const
     GemmParams p{W.N, T, W.K / BK, 0};
     const int m_tiles = (W.N_pad + 2 * BM - 1) / (2 * BM);   // rows past N_pad read as zeros
     dim3 grid(m_tiles, (T + BN - 1) / BN);
-    return launch_pdl(kern, grid, dim3(192), (size_t)C::SMEM, s, *mb, *mb2, *reinterpret_cast<const CUtensorMap *>(W.tm_q),
-                      *reinterpret_cast<const CUtensorMap *>(W.tm_s), p, a, layer);
+    return launch_pdl(kern, grid, dim3(192), (size_t)C::SMEM, s, *mb, *mb2, *reinterpret_cast<const CUtensorMap *>(W.tm_w),
+                      p, a, layer);
 }
 
 template <int QT, int BN>
@@ -483,13 +483,12 @@ cudaError_t dispatch(const QMat &W, Epi epi, int T, const __half *A, const __hal
 }  // namespace tc
 
 bool make_weight_maps(QMat &W) {
-    // quants: [N_pad rows][nb * QB bytes]; a stage reads 2 blocks of 128 rows
-    const int qb = W.type == Q8 ? 32 : 16;
-    CUtensorMap *mq = reinterpret_cast<CUtensorMap *>(W.tm_q), *ms = reinterpret_cast<CUtensorMap *>(W.tm_s);
-    W.tm_ready = tc::make_map_2d(mq, W.qs, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)W.nb * qb, (uint64_t)W.N_pad,
-                                 (uint64_t)W.nb * qb, (uint32_t)(2 * qb), (uint32_t)tc::BM, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-                 tc::make_map_2d(ms, W.sc, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)W.nb * 8, (uint64_t)W.N_pad / 4,
-                                 (uint64_t)W.nb * 8, 16u, (uint32_t)(tc::BM / 4), CU_TENSOR_MAP_SWIZZLE_NONE);
+    // the storage as [N_pad / 4 quads][quad_bytes] in 4-byte units; a box is one block pair
+    // (quants and scales) of 32 quads
+    const int pb = W.pair_bytes();
+    CUtensorMap *m = reinterpret_cast<CUtensorMap *>(W.tm_w);
+    W.tm_ready = tc::make_map_2d(m, W.w, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, W.quad_bytes() / 4, (uint64_t)W.N_pad / 4,
+                                 W.quad_bytes(), (uint32_t)(pb / 4), (uint32_t)(tc::BM / 4), CU_TENSOR_MAP_SWIZZLE_NONE);
     return W.tm_ready;
 }
 

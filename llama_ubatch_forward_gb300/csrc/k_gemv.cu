@@ -18,8 +18,7 @@ bool gemv_fits(const QMat &W, int T) {
 cudaError_t launch_gemv(const QMat &W, Epi epi, int T, const GemvIn &in, const FwdArgs &a, int layer, cudaStream_t s,
                         int64_t &launches) {
     gemv_detail::GemvParams p;
-    p.qs = W.qs;
-    p.sc = W.sc;
+    p.w = W.w;
     p.N = W.N;
     p.nb = W.nb;
     p.K = W.K;

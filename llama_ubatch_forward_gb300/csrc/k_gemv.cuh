@@ -3,9 +3,9 @@
 // Decode is bound by reading the weights once (KV-cache section of the article: decode loads
 // memory, prefill loads the compute units), so the kernel is built to keep HBM busy with as
 // few instructions per weight as possible:
-//   * each warp owns a task of 4 rows and its lanes stride over the rows' 32-element blocks,
-//     so every load instruction of a warp reads 512 contiguous bytes (16 B of nibbles or
-//     2 x 16 B of int8 per lane); a row quad's 4 block scales arrive in one 8-byte load;
+//   * each warp owns a task of 4 rows and its lanes take the rows' 32-element blocks, 32 at a
+//     time in an order that makes every quarter-warp's 16-byte loads hit 8 distinct bank groups
+//     of the quad-interleaved layout (QMat); a row quad's 4 block scales arrive in one 8-byte load;
 //   * the activations are staged once per CTA in shared memory with the RMSNorm fused in, and
 //     each 32-element block of them is split into two int8 parts, x ~= s (hi + lo / 128) with
 //     s = max|x| / 127 (hi = round(x / s), lo = round(128 (x / s - hi))): about 14 bits of
@@ -16,7 +16,10 @@
 //     per block instead of one float FMA per weight;
 //   * row sums are reduced with warp shuffles; epilogues (RoPE + KV append, residual add,
 //     SwiGLU, logits + argmax) are fused.
-// The weight rows stream through a shared-memory ring filled by TMA bulk copies (see k_gemv).
+// The weight rows stream through a shared-memory ring filled by TMA bulk copies, one copy per
+// stage: a stage is a run of consecutive row quads, contiguous in the quad-interleaved layout.
+// (The copy engine's cost is per copy much more than per byte: copies of about 32 KB keep HBM
+// near its peak, copies of a few KB cap a CTA far below it.)
 #pragma once
 #include "epilogue.cuh"
 
@@ -24,12 +27,18 @@ namespace lcx {
 namespace gemv_detail {
 
 // ---------------------------------------------------------------- staged activations
-// Per token: hi plane [nb][32 B], lo plane [nb][32 B] (16-byte chunk c of block b stored at
-// chunk c ^ ((b >> 2) & 1): 8 lanes reading 8 consecutive blocks hit 8 distinct bank groups),
-// then meta [nb] (s / 128, C) with C = 8 (128 sum hi + sum lo) for Q4_0 and 0 for Q8_0.
+// Per token: hi plane [nb][32 B], lo plane [nb][32 B], then meta [nb] (s / 128, C) with
+// C = 8 (128 sum hi + sum lo) for Q4_0 and 0 for Q8_0. Block b sits at position xpos(b): even
+// blocks first, then odd ones, matching the lanes' block order (block_of_lane); 16-byte chunk c
+// of position i is stored at chunk c ^ ((i >> 2) & 1), so 8 lanes reading 8 consecutive
+// positions hit 8 distinct bank groups.
 __host__ __device__ constexpr size_t stage_bytes_per_token(int nb) { return (size_t)nb * 72; }
 
-__device__ __forceinline__ int plane_chunk_off(int b, int c) { return b * 32 + ((c ^ ((b >> 2) & 1)) << 4); }
+__device__ __forceinline__ int xpos(int nb, int b) { return (b & 1) * (nb >> 1) + (b >> 1); }
+__device__ __forceinline__ int plane_chunk_off(int i, int c) { return i * 32 + ((c ^ ((i >> 2) & 1)) << 4); }
+// block a lane takes in a run of 32 blocks starting at an even block: lanes 0-7 the even blocks
+// 0, 2, .., 14, lanes 8-15 the odd blocks 1, .., 15, lanes 16-31 the same for blocks 16..31
+__device__ __forceinline__ int block_of_lane(int lane) { return 2 * ((lane & 7) + 8 * (lane >> 4)) + ((lane >> 3) & 1); }
 
 struct XQ {          // one block of one token, in registers
     int4 h0, h1;     // hi words 0..3, 4..7
@@ -41,11 +50,12 @@ struct XQ {          // one block of one token, in registers
 __device__ __forceinline__ void load_xq(const uint8_t *stage_t, int nb, int b, XQ &x) {
     const uint8_t *hp = stage_t, *lp = stage_t + (size_t)nb * 32;
     const float2 *mp = reinterpret_cast<const float2 *>(stage_t + (size_t)nb * 64);
-    x.h0 = *reinterpret_cast<const int4 *>(hp + plane_chunk_off(b, 0));
-    x.h1 = *reinterpret_cast<const int4 *>(hp + plane_chunk_off(b, 1));
-    x.l0 = *reinterpret_cast<const int4 *>(lp + plane_chunk_off(b, 0));
-    x.l1 = *reinterpret_cast<const int4 *>(lp + plane_chunk_off(b, 1));
-    const float2 m = mp[b];
+    const int i = xpos(nb, b);
+    x.h0 = *reinterpret_cast<const int4 *>(hp + plane_chunk_off(i, 0));
+    x.h1 = *reinterpret_cast<const int4 *>(hp + plane_chunk_off(i, 1));
+    x.l0 = *reinterpret_cast<const int4 *>(lp + plane_chunk_off(i, 0));
+    x.l1 = *reinterpret_cast<const int4 *>(lp + plane_chunk_off(i, 1));
+    const float2 m = mp[i];
     x.s = m.x;
     x.C = __float_as_int(m.y);
 }
@@ -84,22 +94,12 @@ __device__ __forceinline__ int q8_idot(const uint4 w0, const uint4 w1, const XQ 
 }
 
 struct GemvParams {
-    const uint8_t *qs;
-    const __half *sc;
+    const uint8_t *w;   // quad-interleaved storage (QMat)
     int N, nb, K;
     int n_tasks;
     int T;
     GemvIn in;
 };
-
-// The 4 internal rows of a task. SwiGLU tasks take a gate row pair and the matching up pair
-// (128 rows further, in the 128-row chunk layout of the fused gate/up matrix).
-template <int EPI>
-__device__ __forceinline__ int task_row(int task, int r) {
-    if (EPI != EPI_SWIGLU) return task * 4 + r;
-    const int c = task / (kRowTile / 2), qq = task % (kRowTile / 2);
-    return c * 2 * kRowTile + 2 * qq + (r >= 2 ? kRowTile : 0) + (r & 1);
-}
 
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
@@ -108,9 +108,23 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 256;
 // is a positive scalar, so the block split does not depend on it: it multiplies each row's dot
 // product in the epilogue instead, and the sum of squares is reduced while the blocks are being
 // split. Two adjacent lanes share a block (16 elements each). Run by the 256 consumer threads.
+// x is read through L2 only (it may have been written by other CTAs of the same launch); the
+// loads of up to 4 iterations are issued together. gpre, if given, holds this thread's gains of
+// the first iteration, loaded earlier by the caller (stage_gains).
+constexpr int kStageThreads = 256;
+
+__device__ __forceinline__ void stage_gains(const float *g, int nb, float4 (&gpre)[4]) {
+    const int hb = threadIdx.x, b = hb >> 1, half = hb & 1;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        gpre[j] = g && hb < 2 * nb ? *reinterpret_cast<const float4 *>(g + b * 32 + half * 16 + 4 * j)
+                                   : make_float4(1.f, 1.f, 1.f, 1.f);
+}
+
 template <int QT>
-__device__ void stage_token(const GemvParams &p, int t, uint8_t *stage_t, float (*red)[8]) {
-    constexpr int NTHR = 256;
+__device__ void stage_token(const GemvParams &p, int t, uint8_t *stage_t, float (*red)[8],
+                            const float4 (*gpre)[4] = nullptr) {
+    constexpr int NTHR = kStageThreads, U = 4;
     const int nb = p.nb, K = p.K;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const float *xr = p.in.x + (size_t)(p.in.x_rows ? p.in.x_rows[t] : t) * K;
@@ -118,51 +132,68 @@ __device__ void stage_token(const GemvParams &p, int t, uint8_t *stage_t, float 
     float2 *mp = reinterpret_cast<float2 *>(stage_t + (size_t)nb * 64);
     float ss = 0.f;
     const int n_half = 2 * nb, iters = (n_half + NTHR - 1) / NTHR;   // same trip count in every lane
-    for (int it = 0; it < iters; ++it) {
-        const int hb = it * NTHR + threadIdx.x, b = hb >> 1, half = hb & 1;
-        const bool active = hb < n_half;
-        float v[16];
+    for (int it0 = 0; it0 < iters; it0 += U) {
+        float4 xv[U][4];
 #pragma unroll
-        for (int j = 0; j < 16; j += 4) {
-            float4 q = active ? *reinterpret_cast<const float4 *>(xr + b * 32 + half * 16 + j) : make_float4(0, 0, 0, 0);
-            ss += q.x * q.x + q.y * q.y + q.z * q.z + q.w * q.w;
-            if (p.in.g && active) {
-                const float4 gg = *reinterpret_cast<const float4 *>(p.in.g + b * 32 + half * 16 + j);
-                q.x *= gg.x; q.y *= gg.y; q.z *= gg.z; q.w *= gg.w;
-            }
-            v[j] = q.x; v[j + 1] = q.y; v[j + 2] = q.z; v[j + 3] = q.w;
+        for (int u = 0; u < U; ++u) {
+            const int hb = (it0 + u) * NTHR + threadIdx.x;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                xv[u][j] = it0 + u < iters && hb < n_half
+                               ? __ldcg(reinterpret_cast<const float4 *>(xr + (hb >> 1) * 32 + (hb & 1) * 16 + 4 * j))
+                               : make_float4(0, 0, 0, 0);
         }
-        float amax = 0.f;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(v[j]));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));   // the partner holds the other half
-        const float inv = amax > 0.f ? 127.0f / amax : 0.f;
-        uint32_t hw[4], lw[4];
-        int sh = 0, sl = 0;
+        for (int u = 0; u < U; ++u) {
+            if (it0 + u >= iters) break;   // uniform over the CTA
+            const int hb = (it0 + u) * NTHR + threadIdx.x, b = hb >> 1, half = hb & 1;
+            const bool active = hb < n_half;
+            float v[16];
 #pragma unroll
-        for (int w = 0; w < 4; ++w) {
-            uint32_t hbits = 0, lbits = 0;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float y = v[4 * w + e] * inv;
-                const float h = fminf(fmaxf(rintf(y), -127.f), 127.f);
-                const float l = fminf(fmaxf(rintf((y - h) * 128.f), -127.f), 127.f);
-                sh += (int)h;
-                sl += (int)l;
-                hbits |= ((uint32_t)(int)h & 0xffu) << (8 * e);
-                lbits |= ((uint32_t)(int)l & 0xffu) << (8 * e);
+            for (int j = 0; j < 4; ++j) {
+                float4 q = xv[u][j];
+                ss += q.x * q.x + q.y * q.y + q.z * q.z + q.w * q.w;
+                if (p.in.g && active) {
+                    const float4 gg = gpre && it0 + u == 0
+                                          ? (*gpre)[j]
+                                          : *reinterpret_cast<const float4 *>(p.in.g + b * 32 + half * 16 + 4 * j);
+                    q.x *= gg.x; q.y *= gg.y; q.z *= gg.z; q.w *= gg.w;
+                }
+                v[4 * j] = q.x; v[4 * j + 1] = q.y; v[4 * j + 2] = q.z; v[4 * j + 3] = q.w;
             }
-            hw[w] = hbits;
-            lw[w] = lbits;
-        }
-        sh += __shfl_xor_sync(0xffffffffu, sh, 1);
-        sl += __shfl_xor_sync(0xffffffffu, sl, 1);
-        if (active) {
-            *reinterpret_cast<uint4 *>(hp + plane_chunk_off(b, half)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-            *reinterpret_cast<uint4 *>(lp + plane_chunk_off(b, half)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-            if (half == 0) {
-                const int C = QT == Q4 ? 8 * (128 * sh + sl) : 0;
-                mp[b] = make_float2(amax * (1.0f / (127.0f * 128.0f)), __int_as_float(C));
+            float amax = 0.f;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(v[j]));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));   // the partner holds the other half
+            const float inv = amax > 0.f ? 127.0f / amax : 0.f;
+            uint32_t hw[4], lw[4];
+            int sh = 0, sl = 0;
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                uint32_t hbits = 0, lbits = 0;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float y = v[4 * w + e] * inv;
+                    const float h = fminf(fmaxf(rintf(y), -127.f), 127.f);
+                    const float l = fminf(fmaxf(rintf((y - h) * 128.f), -127.f), 127.f);
+                    sh += (int)h;
+                    sl += (int)l;
+                    hbits |= ((uint32_t)(int)h & 0xffu) << (8 * e);
+                    lbits |= ((uint32_t)(int)l & 0xffu) << (8 * e);
+                }
+                hw[w] = hbits;
+                lw[w] = lbits;
+            }
+            sh += __shfl_xor_sync(0xffffffffu, sh, 1);
+            sl += __shfl_xor_sync(0xffffffffu, sl, 1);
+            if (active) {
+                const int i = xpos(nb, b);
+                *reinterpret_cast<uint4 *>(hp + plane_chunk_off(i, half)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                *reinterpret_cast<uint4 *>(lp + plane_chunk_off(i, half)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                if (half == 0) {
+                    const int C = QT == Q4 ? 8 * (128 * sh + sl) : 0;
+                    mp[i] = make_float2(amax * (1.0f / (127.0f * 128.0f)), __int_as_float(C));
+                }
             }
         }
     }
@@ -194,27 +225,27 @@ constexpr int kMaxStages = 8;
 constexpr uint32_t kSpinLimit = 1u << 22;
 
 struct StagePlan {
-    int tps;            // tasks per stage (4, 2 or 1)
+    int tps;            // tasks per stage (4, 2 or 1): row quads per stage
     int slots;          // ring depth
-    int qs_bytes;       // quant bytes of one stage
-    int sc_bytes;       // scale bytes of one stage
-    int stage_bytes;    // qs + sc, rounded to 128
+    int quad_bytes;     // bytes of one row quad (quants and scales)
+    int stage_bytes;    // tps row quads, rounded to 128
     size_t x_bytes;     // staged activations
     size_t smem;        // total dynamic shared memory
 };
 
+// Stages of about 32-40 KB (one bulk copy each); a SwiGLU stage keeps at least 2 tasks (the gate
+// and up halves of one feature quad). Ring depth: at most 4 slots -- deeper rings add queueing
+// in front of the CTA's own loads without adding bandwidth.
 __host__ __device__ inline StagePlan stage_plan(int nb, int qb, int nt, bool swiglu, size_t budget) {
     StagePlan pl{};
-    const int row = nb * qb;
+    pl.quad_bytes = (nb / 2) * (8 * qb + 16);
     pl.tps = 4;
-    while (pl.tps > (swiglu ? 2 : 1) && pl.tps * 4 * (row + nb * 2) > 40 * 1024) pl.tps /= 2;
-    pl.qs_bytes = pl.tps * 4 * row;
-    pl.sc_bytes = pl.tps * nb * 8;
-    pl.stage_bytes = (pl.qs_bytes + pl.sc_bytes + 127) / 128 * 128;
+    while (pl.tps > (swiglu ? 2 : 1) && pl.tps * pl.quad_bytes > 40 * 1024) pl.tps /= 2;
+    pl.stage_bytes = (pl.tps * pl.quad_bytes + 127) / 128 * 128;
     pl.x_bytes = ((size_t)nt * stage_bytes_per_token(nb) + 127) / 128 * 128;
     const size_t room = budget > pl.x_bytes + 1024 ? budget - pl.x_bytes - 1024 : 0;
     pl.slots = (int)(room / pl.stage_bytes);
-    if (pl.slots > kMaxStages) pl.slots = kMaxStages;
+    if (pl.slots > 4) pl.slots = 4;
     pl.smem = pl.x_bytes + (size_t)pl.slots * pl.stage_bytes + 2 * kMaxStages * 8;
     return pl;
 }
@@ -246,18 +277,150 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                  ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
 }
-// First task of stage `st`, and the global rows / scale quads a stage copies.
+// Producer side: one bulk copy of stage `st` of matrix p -- its row quads st * tps.. (a SwiGLU
+// stage's tasks cover half feature quads, so its quad count is rounded up to even) -- into the
+// ring slot at dst, completing on `bar` (one elected thread).
 template <int EPI>
-__device__ __forceinline__ void stage_rows(int st, int tps, int &row_a, int &row_b) {
-    const int t0 = st * tps;
-    if (EPI != EPI_SWIGLU) {
-        row_a = t0 * 4;
-        row_b = -1;
-    } else {
-        const int c = t0 / (kRowTile / 2), qq = t0 % (kRowTile / 2);
-        row_a = c * 2 * kRowTile + 2 * qq;   // 2 * tps gate rows
-        row_b = row_a + kRowTile;            // 2 * tps up rows
+__device__ __forceinline__ void issue_stage(const GemvParams &p, const StagePlan &pl, int st, uint8_t *dst,
+                                            uint64_t *bar) {
+    const int tasks = min(pl.tps, p.n_tasks - st * pl.tps);   // the last stage may be short
+    const int quads = EPI == EPI_SWIGLU ? tasks + (tasks & 1) : tasks;
+    const uint32_t bytes = (uint32_t)quads * (uint32_t)pl.quad_bytes;
+    mbar_expect_tx(bar, bytes);
+    bulk_g2s(dst, p.w + (size_t)st * pl.tps * pl.quad_bytes, bytes, bar);
+}
+
+template <int NT>
+using PartBuf = float[2][16][kConsumerWarps][NT];   // [parity][stage row][k-slice][token]
+
+// Consumer side of one landed stage (the 256 consumer threads): warp w takes task w / KS of the
+// stage and the w % KS-th slice of its blocks, releases the slot to the producer, and after the
+// slices are summed in part[k & 1], tps * NT threads apply the epilogue. `dead` skips the work
+// (after a timed-out wait) but keeps every barrier. best[t] collects the logits argmax keys.
+template <int QT, int NT, int EPI, bool OUT16>
+__device__ __forceinline__ void consume_stage(const GemvParams &p, const FwdArgs &a, int layer, const StagePlan &pl,
+                                              const uint8_t *sq, const uint8_t *xstage, int st, int k, bool dead,
+                                              uint64_t *empty_bar, PartBuf<NT> &part, float (*red)[8],
+                                              unsigned long long (&best)[NT]) {
+    constexpr int QB = QT == Q8 ? 32 : 16;
+    const int nb = p.nb, tps = pl.tps, QBY = pl.quad_bytes;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int KS = kConsumerWarps / tps;
+    const int tg = warp / KS, ks = warp % KS;
+    const int nbs = ((nb + KS - 1) / KS + 1) & ~1;   // even, so runs of 32 start on block pairs
+    const int b_lo = min(nb, ks * nbs), b_hi = min(nb, b_lo + nbs);
+    // quad (within the stage) and row within it of this warp's 4 rows: a plain task is one quad;
+    // a SwiGLU task is rows 2h, 2h+1 of a gate quad and of the up quad after it (h = tg & 1)
+    int qd[4], rr[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        if (EPI != EPI_SWIGLU) {
+            qd[r] = tg;
+            rr[r] = r;
+        } else {
+            qd[r] = 2 * (tg >> 1) + (r >> 1);
+            rr[r] = 2 * (tg & 1) + (r & 1);
+        }
     }
+    // the epilogue threads' memory operands, loaded while the dot products run
+    const int e = threadIdx.x;
+    const int tasks = min(tps, p.n_tasks - st * tps);
+    const bool epi_thread = !dead && e < tasks * NT && e % NT < p.T;
+    EpiIn ein{};
+    if ((EPI == EPI_RESID || EPI == EPI_QKV) && epi_thread) ein = epi_load<EPI>(a, e % NT, (st * tps + e / NT) * 4, p.N);
+    float acc[4][NT];
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int t = 0; t < NT; ++t) acc[r][t] = 0.f;
+    const int lb = block_of_lane(lane);
+    for (int b0 = b_lo; b0 < (dead ? b_lo : b_hi); b0 += 32) {
+        const int b = b0 + lb;
+        if (b >= b_hi) continue;
+        XQ xq[NT];
+#pragma unroll
+        for (int t = 0; t < NT; ++t) load_xq(xstage + t * stage_bytes_per_token(nb), nb, b, xq[t]);
+        float d[4];
+        if (EPI != EPI_SWIGLU) {
+            const uint2 s4 = *reinterpret_cast<const uint2 *>(sq + qd[0] * QBY + quad_s_off(QB, b));
+            const float2 d01 = __half22float2(*reinterpret_cast<const __half2 *>(&s4.x));
+            const float2 d23 = __half22float2(*reinterpret_cast<const __half2 *>(&s4.y));
+            d[0] = d01.x; d[1] = d01.y; d[2] = d23.x; d[3] = d23.y;
+        } else {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const uint32_t s2 = *reinterpret_cast<const uint32_t *>(sq + qd[2 * h] * QBY + quad_s_off(QB, b) + 2 * rr[2 * h]);
+                const float2 dd = __half22float2(*reinterpret_cast<const __half2 *>(&s2));
+                d[2 * h] = dd.x;
+                d[2 * h + 1] = dd.y;
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const uint4 *wp = reinterpret_cast<const uint4 *>(sq + qd[r] * QBY + quad_q_off(QB, rr[r], b));
+            const uint4 w0 = wp[0];
+            const uint4 w1 = QT == Q8 ? wp[1] : w0;
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+                const int P = QT == Q4 ? q4_idot(w0, xq[t]) : q8_idot(w0, w1, xq[t]);
+                acc[r][t] = fmaf(d[r] * xq[t].s, (float)P, acc[r][t]);
+            }
+        }
+    }
+    // the slot's bytes are no longer read by this warp: hand it back to the producer (a NULL
+    // barrier: the slot is refilled after the CTA-wide barrier below instead)
+    __syncwarp();
+    if (lane == 0 && empty_bar) mbar_arrive(empty_bar);
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            float v = acc[r][t];
+#pragma unroll
+            for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+            if (lane == 0) part[k & 1][tg * 4 + r][ks][t] = v;
+        }
+    consumer_sync();
+    // epilogue: one thread per (task, token)
+    if (epi_thread) {
+        const int et = e / NT, t = e % NT;
+        {
+            float v[4];
+            const float rs = token_rs(p, a, red, t);
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                float sum = 0.f;
+                for (int q = 0; q < KS; ++q) sum += part[k & 1][et * 4 + r][q][t];
+                v[r] = sum * rs;
+            }
+            const int task = st * tps + et;
+            if (EPI == EPI_SWIGLU) {   // features 4 (task / 2) + 2 (task & 1) + {0, 1}
+                const float g2[2] = {v[0], v[1]}, u2[2] = {v[2], v[3]};
+                epi_swiglu2<OUT16>(a, t, 4 * (task >> 1) + 2 * (task & 1), g2, u2);
+            } else {
+                unsigned long long bk = 0ull;
+                epi_quad_in<EPI>(a, layer, t, task * 4, p.N, v, ein, bk);
+#pragma unroll
+                for (int tt = 0; tt < NT; ++tt)
+                    if (tt == t) best[tt] = bk > best[tt] ? bk : best[tt];
+            }
+        }
+    }
+    // part[k & 1] is rewritten two stages later, after the next consumer_sync
+}
+
+// The CTA's largest logits keys, one atomicMax per token into a.amax_key (consumer threads).
+template <int NT>
+__device__ __forceinline__ void logits_cta_reduce(const FwdArgs &a, int T, const unsigned long long (&best)[NT]) {
+    __shared__ unsigned long long cbest[NT];
+    consumer_sync();
+    if (threadIdx.x < NT) cbest[threadIdx.x] = 0ull;
+    consumer_sync();
+#pragma unroll
+    for (int tt = 0; tt < NT; ++tt)
+        if (best[tt]) atomicMax(&cbest[tt], best[tt]);
+    consumer_sync();
+    if (threadIdx.x < NT && threadIdx.x < T && cbest[threadIdx.x]) atomicMax(&a.amax_key[threadIdx.x], cbest[threadIdx.x]);
 }
 
 template <int QT, int NT, int EPI, bool OUT16>
@@ -271,9 +434,8 @@ __global__ void __launch_bounds__(288, 1) k_gemv(const GemvParams p, const FwdAr
     uint64_t *full = reinterpret_cast<uint64_t *>(ring + (size_t)pl.slots * pl.stage_bytes);
     uint64_t *empty = full + kMaxStages;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tps = pl.tps, S = pl.slots;
-    const int n_stages = (p.n_tasks + tps - 1) / tps;
-    const int row_bytes = nb * QB;
+    const int S = pl.slots;
+    const int n_stages = (p.n_tasks + pl.tps - 1) / pl.tps;
     LCX_TRACE(a, 0);
 
     if (threadIdx.x == 0) {
@@ -286,28 +448,15 @@ __global__ void __launch_bounds__(288, 1) k_gemv(const GemvParams p, const FwdAr
     __syncthreads();
 
     if (warp == kConsumerWarps) {
-        // ---------------- producer
+        // ---------------- producer: the weights do not depend on earlier kernels, so streaming
+        // starts before the dependency wait
         if (lane == 0) {
             int k = 0;
             bool ok = true;
             for (int st = blockIdx.x; st < n_stages; st += gridDim.x, ++k) {
                 const int slot = k % S;
                 if (k >= S && !(ok = mbar_wait(&empty[slot], ((k / S) - 1) & 1))) break;
-                uint8_t *dst = ring + (size_t)slot * pl.stage_bytes;
-                int ra, rb;
-                stage_rows<EPI>(st, tps, ra, rb);
-                const int tasks = min(tps, p.n_tasks - st * tps);   // the last stage may be short
-                const int rows = EPI == EPI_SWIGLU ? 2 * tasks : 4 * tasks;
-                const int quads = EPI == EPI_SWIGLU ? (2 * tasks + 3) / 4 : tasks;
-                const uint32_t qbytes = (uint32_t)rows * row_bytes, sbytes = (uint32_t)quads * nb * 8;
-                const uint32_t tx = (EPI == EPI_SWIGLU ? 2u : 1u) * (qbytes + sbytes);
-                mbar_expect_tx(&full[slot], tx);
-                bulk_g2s(dst, p.qs + (size_t)ra * row_bytes, qbytes, &full[slot]);
-                bulk_g2s(dst + pl.qs_bytes, p.sc + (size_t)(ra >> 2) * nb * 4, sbytes, &full[slot]);
-                if (EPI == EPI_SWIGLU) {
-                    bulk_g2s(dst + pl.qs_bytes / 2, p.qs + (size_t)rb * row_bytes, qbytes, &full[slot]);
-                    bulk_g2s(dst + pl.qs_bytes + pl.sc_bytes / 2, p.sc + (size_t)(rb >> 2) * nb * 4, sbytes, &full[slot]);
-                }
+                issue_stage<EPI>(p, pl, st, ring + (size_t)slot * pl.stage_bytes, &full[slot]);
             }
             if (!ok) atomicExch(a.err, 1);
             // drain: every copy this CTA issued must land before the CTA exits
@@ -337,10 +486,7 @@ __global__ void __launch_bounds__(288, 1) k_gemv(const GemvParams p, const FwdAr
     consumer_sync();
     LCX_TRACE(a, 2);
 
-    const int KS = kConsumerWarps / tps;
-    const int tg = warp / KS, ks = warp % KS;
-    const int nbs = (nb + KS - 1) / KS, b_lo = ks * nbs, b_hi = min(nb, b_lo + nbs);
-    __shared__ float part[2][16][kConsumerWarps][NT];   // [parity][stage row][k-slice][token]
+    __shared__ PartBuf<NT> part;
     unsigned long long best[NT];
 #pragma unroll
     for (int t = 0; t < NT; ++t) best[t] = 0ull;
@@ -355,98 +501,11 @@ __global__ void __launch_bounds__(288, 1) k_gemv(const GemvParams p, const FwdAr
             dead = true;
             atomicExch(a.err, 1);
         }
-        const uint8_t *sq = ring + (size_t)slot * pl.stage_bytes;
-        const __half *ss = reinterpret_cast<const __half *>(sq + pl.qs_bytes);
-        // local rows of this warp's task inside the stage, and where their scales sit
-        int lrow[4], sidx[4];
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            if (EPI != EPI_SWIGLU) {
-                lrow[r] = tg * 4 + r;
-                sidx[r] = tg * nb * 4 + r;                              // + b * 4
-            } else {
-                const int gl = 2 * tg + (r & 1);                        // row within the gate / up half
-                lrow[r] = (r < 2 ? 0 : 2 * tps) + gl;
-                sidx[r] = (r < 2 ? 0 : (tps / 2) * nb * 4) + (gl >> 2) * nb * 4 + (gl & 3);
-            }
-        }
-        float acc[4][NT];
-#pragma unroll
-        for (int r = 0; r < 4; ++r)
-#pragma unroll
-            for (int t = 0; t < NT; ++t) acc[r][t] = 0.f;
-        for (int b = b_lo + lane; b < (dead ? b_lo : b_hi); b += 32) {
-            XQ xq[NT];
-#pragma unroll
-            for (int t = 0; t < NT; ++t) load_xq(xstage + t * stage_bytes_per_token(nb), nb, b, xq[t]);
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const uint4 *wp = reinterpret_cast<const uint4 *>(sq + ((size_t)lrow[r] * nb + b) * QB);
-                const uint4 w0 = wp[0];
-                const uint4 w1 = QT == Q8 ? wp[1] : w0;
-                const float d = __half2float(ss[sidx[r] + b * 4]);
-#pragma unroll
-                for (int t = 0; t < NT; ++t) {
-                    const int P = QT == Q4 ? q4_idot(w0, xq[t]) : q8_idot(w0, w1, xq[t]);
-                    acc[r][t] = fmaf(d * xq[t].s, (float)P, acc[r][t]);
-                }
-            }
-        }
-        // the slot's bytes are no longer read by this warp: hand it back to the producer
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[slot]);
-#pragma unroll
-        for (int r = 0; r < 4; ++r)
-#pragma unroll
-            for (int t = 0; t < NT; ++t) {
-                float v = acc[r][t];
-#pragma unroll
-                for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-                if (lane == 0) part[k & 1][tg * 4 + r][ks][t] = v;
-            }
-        consumer_sync();
-        // epilogue: one thread per (task, token)
-        const int e = threadIdx.x;
-        const int tasks = min(tps, p.n_tasks - st * tps);
-        if (!dead && e < tasks * NT) {
-            const int et = e / NT, t = e % NT;
-            if (t < p.T) {
-                float v[4];
-#pragma unroll
-                const float rs = token_rs(p, a, red, t);
-                for (int r = 0; r < 4; ++r) {
-                    float sum = 0.f;
-                    for (int q = 0; q < KS; ++q) sum += part[k & 1][et * 4 + r][q][t];
-                    v[r] = sum * rs;
-                }
-                const int task = st * tps + et;
-                if (EPI == EPI_SWIGLU) {
-                    const int c = task / (kRowTile / 2), qq = task % (kRowTile / 2);
-                    const float g2[2] = {v[0], v[1]}, u2[2] = {v[2], v[3]};
-                    epi_swiglu2<OUT16>(a, t, c * kRowTile + 2 * qq, g2, u2);
-                } else {
-                    unsigned long long bk = 0ull;
-                    epi_quad<EPI>(a, layer, t, task * 4, p.N, v, bk);
-#pragma unroll
-                    for (int tt = 0; tt < NT; ++tt)
-                        if (tt == t) best[tt] = bk > best[tt] ? bk : best[tt];
-                }
-            }
-        }
-        // part[k & 1] is rewritten two stages later, after the next consumer_sync
+        consume_stage<QT, NT, EPI, OUT16>(p, a, layer, pl, ring + (size_t)slot * pl.stage_bytes, xstage, st, k, dead,
+                                          &empty[slot], part, red, best);
     }
     LCX_TRACE(a, 3);
-    if (EPI == EPI_LOGITS) {
-        __shared__ unsigned long long cbest[NT];
-        consumer_sync();
-        if (threadIdx.x < NT) cbest[threadIdx.x] = 0ull;
-        consumer_sync();
-#pragma unroll
-        for (int tt = 0; tt < NT; ++tt)
-            if (best[tt]) atomicMax(&cbest[tt], best[tt]);
-        consumer_sync();
-        if (threadIdx.x < NT && threadIdx.x < p.T && cbest[threadIdx.x]) atomicMax(&a.amax_key[threadIdx.x], cbest[threadIdx.x]);
-    }
+    if (EPI == EPI_LOGITS) logits_cta_reduce<NT>(a, p.T, best);
 }
 
 template <int QT, int NT, int EPI, bool OUT16>

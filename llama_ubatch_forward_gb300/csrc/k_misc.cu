@@ -31,30 +31,33 @@ __host__ __device__ inline int64_t stored_row_bytes(int type, int64_t k) {
 }
 
 // ------------------------------------------------------------------ repack
-// One thread per (source row, block): copies the block's quant bytes into the qs plane and
-// its scale into the scale plane at the destination row. gateup_chunked maps source row r of
-// the gate (row_offset 0) or up (row_offset 128) matrix to (r / 128) * 256 + row_offset + r % 128.
-__global__ void k_repack(const uint8_t *__restrict__ src, int type, int N_src, int nb_src, uint8_t *__restrict__ qs,
-                         __half *__restrict__ sc, int nb_dst, int row_offset, int gateup_chunked) {
+// One thread per (source row, block): copies the block's quant bytes and its scale to the
+// destination row's place in the quad-interleaved storage (QMat). With `gateup`, source row r
+// of the gate (row_offset 0) or up (row_offset 4) matrix goes to row 8 (r / 4) + row_offset + r % 4:
+// the gate and up rows of features 4f..4f+3 form the consecutive quads 2f, 2f+1.
+__global__ void k_repack(const uint8_t *__restrict__ src, int type, int N_src, int nb_src, uint8_t *__restrict__ w,
+                         int nb_dst, int row_offset, int gateup) {
     int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= (int64_t)N_src * nb_src) return;
     int r = (int)(idx / nb_src), b = (int)(idx % nb_src);
-    int dr = gateup_chunked ? (r / kRowTile) * (2 * kRowTile) + row_offset + (r % kRowTile) : r + row_offset;
+    int dr = gateup ? 8 * (r / 4) + row_offset + (r % 4) : r + row_offset;
     const int bb = type == Q8 ? 34 : 18, qb = type == Q8 ? 32 : 16;
+    const size_t quad = (size_t)(dr >> 2) * (size_t)(nb_dst / 2) * pair_bytes_of(qb);
     const uint8_t *blk = src + ((int64_t)r * nb_src + b) * bb;
-    uint8_t *dq = qs + ((int64_t)dr * nb_dst + b) * qb;
+    uint8_t *dq = w + quad + quad_q_off(qb, dr & 3, b);
     for (int i = 0; i < qb; ++i) dq[i] = blk[2 + i];
-    uint16_t dbits = (uint16_t)(blk[0] | (blk[1] << 8));
-    sc[((int64_t)(dr >> 2) * nb_dst + b) * 4 + (dr & 3)] = __ushort_as_half(dbits);
+    uint8_t *ds = w + quad + quad_s_off(qb, b) + 2 * (dr & 3);
+    ds[0] = blk[0];
+    ds[1] = blk[1];
 }
 
-cudaError_t launch_repack(const void *src, int type, int N_src, int nb_src, QMat &dst, int row_offset,
-                          int gateup_chunked, cudaStream_t s) {
+cudaError_t launch_repack(const void *src, int type, int N_src, int nb_src, QMat &dst, int row_offset, int gateup,
+                          cudaStream_t s) {
     int64_t n = (int64_t)N_src * nb_src;
     int threads = 256;
     int64_t blocks = (n + threads - 1) / threads;
-    k_repack<<<(unsigned)blocks, threads, 0, s>>>((const uint8_t *)src, type, N_src, nb_src, dst.qs, dst.sc, dst.nb,
-                                                 row_offset, gateup_chunked);
+    k_repack<<<(unsigned)blocks, threads, 0, s>>>((const uint8_t *)src, type, N_src, nb_src, dst.w, dst.nb, row_offset,
+                                                 gateup);
     return cudaGetLastError();
 }
 

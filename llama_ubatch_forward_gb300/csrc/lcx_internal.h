@@ -18,30 +18,41 @@ constexpr int kGemvSmemTotal = 212 * 1024;  // dynamic shared memory of a GEMV C
 
 enum QType { QF16 = 1, Q4 = 2, Q8 = 8 };
 
-// A weight matrix re-laid out for the kernels: N_pad rows of nb 32-element blocks.
-//   qs:  [N_pad][nb][16 B] (Q4_0 nibbles, GGUF order kept) or [N_pad][nb][32 B] (Q8_0 int8)
-//   sc:  [N_pad/4][nb][4] fp16 scales: the scales of 4 consecutive rows for one block are
-//        adjacent, so one 8-byte load brings a row quad's scales.
-// Rows >= N and blocks past the stored ones are zero (scale 0).
+// A weight matrix re-laid out for the kernels: N_pad rows (a multiple of 128) of nb 32-element
+// blocks (nb even), stored by row quads so that any run of consecutive quads -- quants and scales
+// together -- is one contiguous range (one bulk copy per decode stage, one tensor-map box per
+// prefill tile). Quad q (rows 4q..4q+3) takes quad_bytes() at q * quad_bytes(), as nb / 2 block
+// pairs of pair_bytes() each; pair p (blocks 2p, 2p+1) holds
+//   [row 0: block 2p quants, block 2p+1 quants] ... [row 3: ...]   (4 x 2 x QB bytes)
+//   [block 2p: f16 scales of rows 0..3] [block 2p+1: scales of rows 0..3]   (16 bytes)
+// with QB = 16 (Q4_0 nibbles, GGUF order kept) or 32 (Q8_0 int8). Rows >= N and blocks past the
+// stored ones are zero (scale 0).
 struct QMat {
     int type = 0;
     int N = 0, N_pad = 0;   // logical and padded rows
     int K = 0, nb = 0;      // padded input width (nb * 32) and blocks per row
-    uint8_t *qs = nullptr;
-    __half *sc = nullptr;
-    // TMA descriptors (CUtensorMap) of the quant and scale planes for the tensor-core GEMM
-    alignas(64) unsigned char tm_q[128] = {};
-    alignas(64) unsigned char tm_s[128] = {};
+    uint8_t *w = nullptr;   // the quad-interleaved storage
+    // TMA descriptor (CUtensorMap) of the storage for the tensor-core GEMM
+    alignas(64) unsigned char tm_w[128] = {};
     bool tm_ready = false;
-    size_t qs_row_bytes() const { return (size_t)nb * (type == Q4 ? 16 : 32); }
-    size_t bytes() const { return (size_t)N_pad * qs_row_bytes() + (size_t)N_pad * nb * 2; }
+    int qb() const { return type == Q4 ? 16 : 32; }
+    int pair_bytes() const { return 8 * qb() + 16; }
+    size_t quad_bytes() const { return (size_t)(nb / 2) * pair_bytes(); }
+    size_t bytes() const { return (size_t)(N_pad / 4) * quad_bytes(); }
 };
+
+// Byte offsets inside the quad-interleaved storage (host and device).
+__host__ __device__ inline int pair_bytes_of(int qb) { return 8 * qb + 16; }
+// quants of row rr (0..3) of a quad, block b, relative to the quad
+__host__ __device__ inline int quad_q_off(int qb, int rr, int b) { return (b >> 1) * pair_bytes_of(qb) + rr * 2 * qb + (b & 1) * qb; }
+// the 4 f16 scales (rows 0..3) of block b, relative to the quad
+__host__ __device__ inline int quad_s_off(int qb, int b) { return (b >> 1) * pair_bytes_of(qb) + 8 * qb + (b & 1) * 8; }
 
 struct DevLayer {
     const float *attn_norm, *ffn_norm;
     QMat qkv;      // rows [Wq; Wk; Wv]
     QMat wo;
-    QMat gateup;   // chunks of 128 rows: gate rows c*128.., then up rows c*128.. (F padded to 128)
+    QMat gateup;   // row quads alternate: gate rows 4f..4f+3 at quad 2f, up rows 4f..4f+3 at quad 2f+1
     QMat down;     // K = F padded to 128
 };
 
@@ -103,7 +114,7 @@ struct FwdArgs {
 // ---------------------------------------------------------------- launchers (kernels *.cu)
 // All return cudaGetLastError() after the launch(es); `launches` counts kernels issued.
 cudaError_t launch_repack(const void *src, int type, int N_src, int nb_src, QMat &dst, int row_offset,
-                          int gateup_chunked, cudaStream_t s);
+                          int gateup, cudaStream_t s);
 cudaError_t launch_rope_table(float2 *tab, int n_pos, int hd, double theta, cudaStream_t s);
 cudaError_t launch_embed(const FwdArgs &a, int t_embd, const void *tok_embd, cudaStream_t s, int64_t &launches);
 cudaError_t launch_get_rows(int type, const void *table, int64_t n_cols, const int32_t *ids, int n, float *out,
@@ -141,6 +152,31 @@ cudaError_t launch_attention_prefill(const FwdArgs &a, int layer, cudaStream_t s
 // Scratch bytes one attention launch needs (partials, then arrival counters at
 // *counter_offset); 0 when every token fits in a single split.
 size_t attention_scratch_bytes(const FwdArgs &a, int max_natt, size_t *counter_offset);
+
+// Persistent one-token decode step (k_decode_step.cu): one cooperative launch runs the whole
+// forward of a 1-token ubatch. Prepared once per context; `ok` is false where it does not apply
+// (block types or shapes without an instantiation, too little shared memory), and the forward
+// then runs as separate launches.
+struct DecodeStep {
+    bool ok = false;
+    bool tried = false;
+    void *ph = nullptr;          // device array of the phases
+    unsigned int *sync = nullptr;// 2 counters, zero between launches
+    const void *kern = nullptr;
+    int slot_bytes = 0, slots = 0, x_bytes = 0;
+    size_t smem = 0;
+    int grid = 0;
+    int n_ph = 0;
+    double weight_bytes = 0;     // stored weight bytes one step streams (without the head)
+    double head_bytes = 0;
+};
+cudaError_t decode_step_prepare(DecodeStep &ds, const DevLayer *layers, int n_layer, const QMat &head,
+                                const float *output_norm, const FwdArgs &a);
+void decode_step_release(DecodeStep &ds);
+// resets the step's counters (after a launch that reported an error)
+cudaError_t decode_step_reset(const DecodeStep &ds, const FwdArgs &a, cudaStream_t s);
+cudaError_t launch_decode_step(const DecodeStep &ds, const FwdArgs &a, const void *tok_embd, int t_embd,
+                               int32_t *amax_dst, int n_att, cudaStream_t s, int64_t &launches);
 
 // Launch with programmatic dependent launch allowed: the kernel may start while the previous
 // kernel on the stream finishes; it must execute griddepcontrol.wait before reading anything

@@ -140,8 +140,7 @@ extern "C" lcx_model *lcx_model_create(const lcx_hparams *hp, const lcx_weights 
     m->arena_bytes = total;
     uint8_t *p = (uint8_t *)m->arena;
     for (QMat *q : mats) {
-        q->qs = p;
-        q->sc = (__half *)(p + (size_t)q->N_pad * q->qs_row_bytes());
+        q->w = p;
         p += (q->bytes() + 255) / 256 * 256;
     }
     cudaStream_t s = nullptr;
@@ -155,7 +154,7 @@ extern "C" lcx_model *lcx_model_create(const lcx_hparams *hp, const lcx_weights 
         if (e == cudaSuccess) e = launch_repack(L.wv, hp->t_linear, KV * hd, nbd, D.qkv, (H + KV) * hd, 0, s);
         if (e == cudaSuccess) e = launch_repack(L.wo, hp->t_linear, d, (H * hd) / 32, D.wo, 0, 0, s);
         if (e == cudaSuccess) e = launch_repack(L.w_gate, hp->t_linear, F, nbd, D.gateup, 0, 1, s);
-        if (e == cudaSuccess) e = launch_repack(L.w_up, hp->t_linear, F, nbd, D.gateup, kRowTile, 1, s);
+        if (e == cudaSuccess) e = launch_repack(L.w_up, hp->t_linear, F, nbd, D.gateup, 4, 1, s);
         if (e == cudaSuccess) e = launch_repack(L.w_down, hp->t_linear, d, (F + 31) / 32, D.down, 0, 0, s);
     }
     if (e == cudaSuccess)
@@ -225,6 +224,7 @@ struct lcx_ctx {
     int32_t *amax_host = nullptr;  // pinned argmax staging
     int amax_cap = 0;
     int max_att_split = 64;
+    DecodeStep step;             // persistent one-token decode step, prepared at first use
     // profiling
     bool prof_on = false;
     std::vector<cudaEvent_t> prof_ev;      // pairs
@@ -240,6 +240,7 @@ static void prof_resolve(lcx_ctx *c);
 static int32_t trace_on(lcx_ctx *c);
 
 static void free_ctx_device(lcx_ctx *c) {
+    decode_step_release(c->step);
     for (auto e : c->prof_ev) cudaEventDestroy(e);
     c->prof_ev.clear();
     if (c->trace) cudaFree(c->trace);
@@ -629,6 +630,30 @@ cudaError_t run_forward(lcx_ctx *c, FwdArgs &a, int max_natt, double att_cells, 
     int64_t &nl = c->st.n_kernels;
     const double T = a.T, d = a.d, qw = (double)a.H * a.hd, kvw = (double)a.KV * a.hd, F = a.F;
     cudaError_t e;
+    // a one-token ubatch runs as one persistent launch where the step kernel applies
+    if (a.T == 1 && a.n_out <= 1) {
+        if (!c->step.tried) {
+            e = decode_step_prepare(c->step, m->layers.data(), hp.n_layer, m->head, m->output_norm, c->base);
+            if (e != cudaSuccess) return e;
+        }
+        if (c->step.ok) {
+            const double kvw = (double)a.KV * a.hd;
+            const double bytes = c->step.weight_bytes + (a.n_out ? c->step.head_bytes : 0.0) +
+                                 att_cells * kvw * 2 * 2 * hp.n_layer;
+            const double flops = 2.0 * (c->step.weight_bytes + (a.n_out ? c->step.head_bytes : 0.0)) * 32.0 /
+                                     (m->layers[0].qkv.type == Q4 ? 18.0 : 34.0) +
+                                 att_cells * 4.0 * a.H * a.hd * hp.n_layer;
+            a.trace = nullptr;
+            const int n_slots = 5 * hp.n_layer + 2;
+            if (c->trace && c->trace_used + n_slots <= c->trace_cap) {
+                a.trace = c->trace;
+                a.trace_slot = c->trace_used;
+                c->trace_used += n_slots;
+            }
+            ProfScope ps(c, PC_GEMV, bytes, flops);
+            return launch_decode_step(c->step, a, m->tok_embd, hp.t_embd, amax_dst, max_natt, s, nl);
+        }
+    }
     {
         ProfScope ps(c, PC_OTHER, T * (d * (hp.t_embd == LCX_F16 ? 2.0 : 34.0 / 32.0) + d * 4), 0);
         e = launch_embed(a, hp.t_embd, m->tok_embd, s, nl);
@@ -711,6 +736,8 @@ static bool device_error_raised(lcx_ctx *c) {
     if (cudaMemcpy(&v, c->base.err, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return true;
     if (!v) return false;
     cudaMemset(c->base.err, 0, sizeof(v));
+    decode_step_reset(c->step, c->base, c->stream);   // counters a stopped step may have left
+    cudaStreamSynchronize(c->stream);
     set_error_text("a kernel's bounded wait timed out");
     return true;
 }
