@@ -15,7 +15,9 @@ __device__ __forceinline__ unsigned long long argmax_key(float v, int idx) {
     return ((unsigned long long)b << 32) | (unsigned long long)(0xffffffffu - (uint32_t)idx);
 }
 
-__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
+// SiLU with the fast exponential and division (relative error about 1e-6; the exponential
+// saturates to inf for very negative g, where the quotient is then 0)
+__device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
 // cache address of (layer, cell, kv head, dim) in [L][n_pages][KV][kPage][hd]
 __device__ __forceinline__ size_t kv_off(const FwdArgs &a, int layer, int cell, int kvh, int dim) {
@@ -48,7 +50,7 @@ __device__ __forceinline__ EpiIn epi_load(const FwdArgs &a, int t, int r0, int N
         const int qw = a.H * a.hd, kw = a.KV * a.hd;
         in.cell = a.ub.cell[t];
         if (r0 < qw + kw) {   // q or k rows: the quad lies inside one head (hd % 4 == 0)
-            const int dim = r0 < qw ? r0 % a.hd : (r0 - qw) % a.hd;
+            const int dim = (r0 < qw ? r0 : r0 - qw) & (a.hd - 1);   // hd is 64 or 128
             in.cs = *reinterpret_cast<const float4 *>(a.rope + (size_t)a.ub.pos[t] * (a.hd / 2) + dim / 2);
         }
     }
@@ -94,7 +96,8 @@ __device__ __forceinline__ void epi_quad_in(const FwdArgs &a, int layer, int t, 
             } else {
                 const bool isk = r < qw + kw;
                 const int rr = isk ? r - qw : r - qw - kw;
-                const int kvh = rr / a.hd, dim = rr % a.hd;
+                const int sh = __ffs(a.hd) - 1;   // hd is a power of two
+                const int kvh = rr >> sh, dim = rr & (a.hd - 1);
                 __half *dst = (isk ? a.kc : a.vc) + kv_off(a, layer, in.cell, kvh, dim);
                 *reinterpret_cast<__half2 *>(dst) = __floats2half2_rn(y0, y1);
             }

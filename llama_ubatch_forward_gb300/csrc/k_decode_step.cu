@@ -93,7 +93,10 @@ cudaError_t decode_step_prepare(DecodeStep &ds, const DevLayer *layers, int n_la
     }
     ph.push_back(phase_for(head, false, (head.N + 3) / 4, GemvIn{a.x, nullptr, output_norm}, cap));
     max_nb = std::max(max_nb, head.nb);
-    for (const StepPhase &P : ph) slot = std::max(slot, P.pl.stage_bytes);
+    for (const StepPhase &P : ph) {
+        slot = std::max(slot, P.pl.stage_bytes);
+        if (gemv_map(P.pl.tps, P.p.nb).NBT > 2) return cudaSuccess;   // rows wider than 16384: separate launches
+    }
 
     // shared memory: staged activations (or attention scratch), then the ring and its barriers
     int dev = 0, optin = 0, n_sm = 0, coop = 0;
@@ -107,7 +110,8 @@ cudaError_t decode_step_prepare(DecodeStep &ds, const DevLayer *layers, int n_la
     if (e != cudaSuccess) return e;
     const int x_bytes =
         (std::max<int>((int)stage_bytes_per_token(max_nb), attn_scratch_bytes(a.hd, G)) + 127) / 128 * 128;
-    const int bars = 2 * kMaxStages * 8;
+    // barriers, then the phase table and the attention unit's page ids
+    const int bars = kMaxStages * 8 + (int)(ph.size() * sizeof(StepPhase)) + kMaxUnitPages * 4;
     const long room = (long)optin - (long)fa.sharedSizeBytes - x_bytes - bars - 64;
     // 4 slots: enough copies in flight to keep HBM streaming, few enough that the CTA's own
     // loads (activations, attention) do not queue behind many of them
@@ -170,6 +174,7 @@ cudaError_t launch_decode_step(const DecodeStep &ds, const FwdArgs &a, const voi
     if (!ds.ok || a.T != 1 || a.n_out > 1) return cudaErrorInvalidValue;
     StepArgs sa{};
     sa.ph = reinterpret_cast<const StepPhase *>(ds.ph);
+    sa.n_ph_all = ds.n_ph;
     sa.slot_bytes = ds.slot_bytes;
     sa.slots = ds.slots;
     sa.x_bytes = ds.x_bytes;

@@ -23,6 +23,13 @@
 //     cached K/V lines are prefetched into L2 at the start of the layer, before QKV runs.
 // Every wait is bounded: a timed-out wait sets the error word, the CTA stops, and the others
 // see the error word and stop at their next barrier.
+//
+// Code size matters as much as data movement here: with HBM saturated, every instruction-cache
+// miss costs a loaded memory round trip (microseconds), so a kernel whose per-layer code does not
+// stay cached pays them at every phase of every layer. The GEMV of all layer matrices is one
+// non-inlined routine (epilogue chosen at run time), the activation staging and the attention
+// loops are rolled, and the phase table lives in shared memory (the 28 KB L1 left next to the
+// ring does not keep it).
 #pragma once
 #include <math_constants.h>
 
@@ -34,7 +41,7 @@ namespace step_detail {
 using namespace gemv_detail;
 
 // One weight-streaming phase: the matrix, its input vector and gains, and its stage plan.
-struct StepPhase {
+struct alignas(16) StepPhase {
     GemvParams p;
     StagePlan pl;
     int n_stages;
@@ -42,6 +49,7 @@ struct StepPhase {
 
 struct StepArgs {
     const StepPhase *ph;   // [4 * n_layer + 1]: per layer QKV, O, gate/up, down; then the head
+    int n_ph_all;          // 4 * n_layer + 1 (the table copied to shared memory)
     int slot_bytes;        // ring slot size (>= every phase's stage bytes)
     int slots;
     int x_bytes;           // staged activations / attention scratch at the start of shared memory
@@ -134,79 +142,87 @@ __device__ __forceinline__ float embd_elem(int type, const uint8_t *row, int i) 
 // L2 prefetch of the cached K/V lines of this CTA's attention unit (cells [c0, c1) of KV head
 // kvh, at most 512 cells); the cell the step itself appends is written later and not fetched.
 template <int HD>
-__device__ __forceinline__ void attn_prefetch(const FwdArgs &a, int layer, int kvh, int c0, int c1) {
+__device__ __forceinline__ void attn_prefetch(const FwdArgs &a, int layer, int kvh, int c0, int c1, const int *pages,
+                                              int page0) {
     constexpr int LINES = HD * 2 / 128;   // 128-byte lines of one K (or V) row
-    const int seq = a.ub.seq[0];
     const int n_att = a.ub.pos[0] + 1;
     c1 = min(min(c1, n_att - 1), c0 + 512);
-    const int32_t *ptrow = a.pt + (size_t)seq * a.max_pages_per_seq;
     for (int i = threadIdx.x; i < (c1 - c0) * 2 * LINES; i += 256) {
         const int j = c0 + i / (2 * LINES), w = i % (2 * LINES);
-        const int page = __ldcg(ptrow + j / kPage);
+        const int page = pages[(j >> 6) - page0];
         const size_t row = (((size_t)layer * a.n_pages + page) * a.KV + kvh) * kPage + (j % kPage);
         const __half *base = (w < LINES ? a.kc : a.vc) + row * HD + (w % LINES) * 64;
         asm volatile("prefetch.global.L2 [%0];" ::"l"(base));
     }
 }
 
-// K/V of one 16-cell super-group of a warp, in registers: lanes 8c..8c+7 hold dims of cell
-// 4 g4 + c of K (DPL = HD / 8 per lane), lane l holds dims l * HD / 32.. of every V row.
+// ---------------------------------------------------------------- attention
+constexpr int kMaxUnitPages = 64;   // page ids of an attention unit kept in shared memory
+
+// K and V of 4 consecutive cells (inside one page), in registers: lanes 8c..8c+7 hold K dims
+// (lane & 7) * HD / 8 .. of cell c; lane l holds V dims l * HD / 32 .. of cells 0..3.
 template <int HD>
-struct AttnRegs {
-    uint4 kraw[4][HD / 64];
-    uint2 vraw[16];
+struct KVGroup {
+    uint4 k[HD / 64];
+    uint2 v[4];
 };
 
-// Loads the super-group of 16 cells at j0 (inside one page) of KV head kvh, cells >= c1 as
-// zeros; only_fresh re-reads just the cells at positions >= fresh (written by this step).
+// page of cell j of the unit's sequence (ids of the unit's pages in shared memory)
+__device__ __forceinline__ int unit_page(const FwdArgs &a, const int *pages, int page0, int j) {
+    const int i = (j >> 6) - page0;
+    return i < kMaxUnitPages ? pages[i] : __ldcg(a.pt + (size_t)a.ub.seq[0] * a.max_pages_per_seq + (j >> 6));
+}
+
+// loads the group of cells j..j+3 (j % 4 == 0) of KV head kvh; cells >= c1 as zeros
 template <int HD>
-__device__ __forceinline__ void attn_load_sg(const FwdArgs &a, int layer, int kvh, int j0, int c1, int fresh,
-                                             bool only_fresh, AttnRegs<HD> &R) {
+__device__ __forceinline__ void kv_group_load(const FwdArgs &a, int layer, int kvh, int page, int j, int c1,
+                                              KVGroup<HD> &g) {
     constexpr int DPL = HD / 8, DPV = HD / 32;
-    const int lane = threadIdx.x & 31, sub = lane & 7, cgrp = lane >> 3;
-    if (j0 >= c1) return;
-    const int32_t *ptrow = a.pt + (size_t)a.ub.seq[0] * a.max_pages_per_seq;
-    const int page = __ldcg(ptrow + j0 / kPage);
-    const size_t row0 = (((size_t)layer * a.n_pages + page) * a.KV + kvh) * kPage + (j0 % kPage);
+    const int lane = threadIdx.x & 31, sub = lane & 7, cg = lane >> 3;
+    const size_t row0 = (((size_t)layer * a.n_pages + page) * a.KV + kvh) * kPage + (j % kPage);
+    const __half *kp = a.kc + (row0 + cg) * HD + sub * DPL;
 #pragma unroll
-    for (int g4 = 0; g4 < 4; ++g4) {
-        const int j = j0 + 4 * g4 + cgrp;
-        if (only_fresh && j < fresh) continue;
-        const __half *kp = a.kc + (row0 + 4 * g4 + cgrp) * HD + sub * DPL;
+    for (int i = 0; i < DPL / 8; ++i)
+        g.k[i] = j + cg < c1 ? __ldcg(reinterpret_cast<const uint4 *>(kp + 8 * i)) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-        for (int i = 0; i < DPL / 8; ++i)
-            R.kraw[g4][i] = j < c1 ? __ldcg(reinterpret_cast<const uint4 *>(kp + 8 * i)) : make_uint4(0, 0, 0, 0);
-    }
-#pragma unroll
-    for (int c = 0; c < 16; ++c) {
-        if (only_fresh && j0 + c < fresh) continue;
+    for (int c = 0; c < 4; ++c) {
         const __half *vp = a.vc + (row0 + c) * HD + lane * DPV;
-        if (j0 + c < c1) {
-            if (DPV == 4) R.vraw[c] = __ldcg(reinterpret_cast<const uint2 *>(vp));
-            else R.vraw[c] = make_uint2(__ldcg(reinterpret_cast<const unsigned int *>(vp)), 0u);
+        if (j + c < c1) {
+            if (DPV == 4) g.v[c] = __ldcg(reinterpret_cast<const uint2 *>(vp));
+            else g.v[c] = make_uint2(__ldcg(reinterpret_cast<const unsigned int *>(vp)), 0u);
         } else {
-            R.vraw[c] = make_uint2(0u, 0u);
+            g.v[c] = make_uint2(0u, 0u);
         }
     }
 }
 
-// One attention unit: query token 0 against cells [c0, c1) of KV head kvh, by the 8 consumer
-// warps (the math of k_attn with 8 warps instead of 4): warp w takes the super-groups at
-// c0 + 16 w + 128 i, the first of them already in R (loaded before this step's K/V were
-// appended; the appended cell is re-read here). With one split the result goes to o32;
-// otherwise the partial (max, sum, acc) is written and the last CTA of the KV head to arrive
-// merges the splits in order. scr: shared scratch of at least attn_scratch_bytes(HD, G).
+// One attention unit: query token 0 against cells [c0, c1) of KV head kvh by the 8 warps (the
+// math of k_attn): warp w takes the 4-cell groups at c0 + 4 w + 32 i. A queue of 4 groups
+// in registers keeps the next groups' K/V in flight while one is used; it was filled before this
+// step's K/V were appended (the group holding the appended cell is re-read here). With one split
+// the result goes to o32; otherwise the partial (max, sum, acc) is written and the last CTA of
+// the KV head to arrive merges the splits in order. scr: attn_scratch_bytes(HD, G) of shared memory.
 template <int HD, int G>
-__device__ __forceinline__ void attn_unit(const FwdArgs &a, int layer, int kvh, int sp, int chunk, int ns, float *scr,
-                                          AttnRegs<HD> &R, int trace_phase) {
+__device__ __forceinline__ void step_attention(const FwdArgs &a, int layer, int kvh, int sp, int chunk, int ns,
+                                               float *scr, const int *pages, int page0, KVGroup<HD> (&q)[4],
+                                               int trace_phase) {
     constexpr int NW = 8, DPL = HD / 8, DPV = HD / 32;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int n_att = a.ub.pos[0] + 1;
     const int c0 = sp * chunk, c1 = min(c0 + chunk, n_att);
-    const int sub = lane & 7, cgrp = lane >> 3;
+    const int sub = lane & 7, cg = lane >> 3;
     const float scale = rsqrtf((float)HD);
-    const int j_first = c0 + 16 * warp;
-    if (j_first < c1 && j_first + 16 > n_att - 1) attn_load_sg<HD>(a, layer, kvh, j_first, c1, n_att - 1, true, R);
+    const int j_first = c0 + 4 * warp;
+    {   // re-read the queued group that holds the appended cell (warp-uniform)
+        const int jf = (n_att - 1) & ~3, i = (jf - j_first) >> 5;
+        if (jf >= j_first && ((jf - j_first) & 31) == 0 && i < 4) {
+            const int pg = unit_page(a, pages, page0, jf);
+            if (i == 0) kv_group_load<HD>(a, layer, kvh, pg, jf, c1, q[0]);
+            else if (i == 1) kv_group_load<HD>(a, layer, kvh, pg, jf, c1, q[1]);
+            else if (i == 2) kv_group_load<HD>(a, layer, kvh, pg, jf, c1, q[2]);
+            else kv_group_load<HD>(a, layer, kvh, pg, jf, c1, q[3]);
+        }
+    }
 
     float qr[G][DPL];
 #pragma unroll
@@ -226,79 +242,85 @@ __device__ __forceinline__ void attn_unit(const FwdArgs &a, int layer, int kvh, 
 #pragma unroll
         for (int i = 0; i < DPV; ++i) acc[g][i] = 0.f;
     }
-    for (int j0 = j_first; j0 < c1; j0 += 16 * NW) {
-        if (j0 != j_first) attn_load_sg<HD>(a, layer, kvh, j0, c1, 0, false, R);
+#pragma unroll 1
+    for (int j = j_first; j < c1; j += 4 * NW) {
+        const KVGroup<HD> cur = q[0];
+        q[0] = q[1];
+        q[1] = q[2];
+        q[2] = q[3];
+        const int jn = j + 16 * NW;   // 4 groups ahead
+        if (jn < c1) kv_group_load<HD>(a, layer, kvh, unit_page(a, pages, page0, jn), jn, c1, q[3]);
+        const bool valid = j + cg < c1;
+        float s[G];
+        {
+            float kf[DPL];
 #pragma unroll
-        for (int g4 = 0; g4 < 4; ++g4) {
-            if (j0 + 4 * g4 >= c1) break;
-            const int j = j0 + 4 * g4 + cgrp;
-            const bool valid = j < c1;
-            float s[G];
-            {
-                float kf[DPL];
+            for (int i = 0; i < DPL / 8; ++i) {
+                const __half2 *h2 = reinterpret_cast<const __half2 *>(&cur.k[i]);
 #pragma unroll
-                for (int i = 0; i < DPL / 8; ++i) {
-                    const __half2 *h2 = reinterpret_cast<const __half2 *>(&R.kraw[g4][i]);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 f = __half22float2(h2[e]);
-                        kf[8 * i + 2 * e] = f.x;
-                        kf[8 * i + 2 * e + 1] = f.y;
-                    }
-                }
-#pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    float d = 0.f;
-#pragma unroll
-                    for (int i = 0; i < DPL; ++i) d = fmaf(qr[g][i], kf[i], d);
-                    d += __shfl_xor_sync(0xffffffffu, d, 1);
-                    d += __shfl_xor_sync(0xffffffffu, d, 2);
-                    d += __shfl_xor_sync(0xffffffffu, d, 4);
-                    s[g] = valid ? d : -CUDART_INF_F;
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = __half22float2(h2[e]);
+                    kf[8 * i + 2 * e] = f.x;
+                    kf[8 * i + 2 * e + 1] = f.y;
                 }
             }
-            float p[G];
+#pragma unroll
+            for (int g = 0; g < G; ++g) {   // two partial sums per head: shorter dependent chains
+                float d0 = 0.f, d1 = 0.f;
+#pragma unroll
+                for (int i = 0; i < DPL; i += 2) {
+                    d0 = fmaf(qr[g][i], kf[i], d0);
+                    d1 = fmaf(qr[g][i + 1], kf[i + 1], d1);
+                }
+                float d = d0 + d1;
+                d += __shfl_xor_sync(0xffffffffu, d, 1);
+                d += __shfl_xor_sync(0xffffffffu, d, 2);
+                d += __shfl_xor_sync(0xffffffffu, d, 4);
+                s[g] = valid ? d : -CUDART_INF_F;
+            }
+        }
+        float p[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {   // online softmax over the group's 4 cells
+            float mx = s[g];
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+            const float mn = fmaxf(m[g], mx);
+            const float alpha = expf(m[g] - mn);
+            p[g] = expf(s[g] - mn);
+            float ps = p[g];
+            ps += __shfl_xor_sync(0xffffffffu, ps, 8);
+            ps += __shfl_xor_sync(0xffffffffu, ps, 16);
+            l[g] = l[g] * alpha + ps;
+            m[g] = mn;
+#pragma unroll
+            for (int i = 0; i < DPV; ++i) acc[g][i] *= alpha;
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {   // P.V; cells past c1 have p = 0 and zero V
+            const uint2 raw = cur.v[c];
+            float vf[DPV];
+            const float2 f0 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.x));
+            vf[0] = f0.x;
+            vf[1 % DPV] = f0.y;
+            if (DPV == 4) {
+                const float2 f1 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.y));
+                vf[2 % DPV] = f1.x;
+                vf[3 % DPV] = f1.y;
+            }
 #pragma unroll
             for (int g = 0; g < G; ++g) {
-                float mx = s[g];
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-                const float mn = fmaxf(m[g], mx);
-                const float alpha = expf(m[g] - mn);
-                p[g] = expf(s[g] - mn);
-                float ps = p[g];
-                ps += __shfl_xor_sync(0xffffffffu, ps, 8);
-                ps += __shfl_xor_sync(0xffffffffu, ps, 16);
-                l[g] = l[g] * alpha + ps;
-                m[g] = mn;
+                const float pc = __shfl_sync(0xffffffffu, p[g], 8 * c);
 #pragma unroll
-                for (int i = 0; i < DPV; ++i) acc[g][i] *= alpha;
-            }
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                if (j0 + 4 * g4 + c >= c1) break;
-                const uint2 raw = R.vraw[4 * g4 + c];
-                float vf[DPV];
-                const float2 f0 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.x));
-                vf[0] = f0.x;
-                vf[1 % DPV] = f0.y;
-                if (DPV == 4) {
-                    const float2 f1 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.y));
-                    vf[2 % DPV] = f1.x;
-                    vf[3 % DPV] = f1.y;
-                }
-#pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    const float pc = __shfl_sync(0xffffffffu, p[g], 8 * c);
-#pragma unroll
-                    for (int i = 0; i < DPV; ++i) acc[g][i] = fmaf(pc, vf[i], acc[g][i]);
-                }
+                for (int i = 0; i < DPV; ++i) acc[g][i] = fmaf(pc, vf[i], acc[g][i]);
             }
         }
     }
 
-    // ---- merge the 8 warps
-    float *sm_m = scr, *sm_l = scr + NW * G, *sm_acc = scr + 2 * NW * G;   // [NW][G], [NW][G], [NW][G][HD]
+    // ---- merge the 8 warps: per query head the max, the sum and the 8 warps' weights once
+    float *sm_m = scr, *sm_l = scr + NW * G, *fac = scr + 2 * NW * G, *sM = scr + 3 * NW * G, *sL = sM + G;
+    int *flag = reinterpret_cast<int *>(sL + G);
+    float *sm_acc = scr + 3 * NW * G + 2 * G + 4;   // [NW][G][HD]
 #pragma unroll
     for (int g = 0; g < G; ++g) {
         if (lane == 0) {
@@ -309,29 +331,39 @@ __device__ __forceinline__ void attn_unit(const FwdArgs &a, int layer, int kvh, 
         for (int i = 0; i < DPV; ++i) sm_acc[(warp * G + g) * HD + lane * DPV + i] = acc[g][i];
     }
     consumer_sync();
-    float *part = a.att_part;
-    const size_t prow = (size_t)kvh * ns;   // partial rows of this KV head (token 0)
-    for (int idx = threadIdx.x; idx < G * HD; idx += 256) {
-        const int g = idx / HD, dd = idx % HD;
+    if (threadIdx.x < G) {
+        const int g = threadIdx.x;
         float M = -CUDART_INF_F;
 #pragma unroll
         for (int w = 0; w < NW; ++w) M = fmaxf(M, sm_m[w * G + g]);
-        float L = 0.f, A = 0.f;
+        float L = 0.f;
 #pragma unroll
         for (int w = 0; w < NW; ++w) {
             const float mw = sm_m[w * G + g];
             const float f = mw == -CUDART_INF_F ? 0.f : expf(mw - M);
+            fac[w * G + g] = f;
             L += sm_l[w * G + g] * f;
-            A += sm_acc[(w * G + g) * HD + dd] * f;
         }
+        sM[g] = M;
+        sL[g] = L;
+    }
+    consumer_sync();
+    float *part = a.att_part;
+    const size_t prow = (size_t)kvh * ns;   // partial rows of this KV head (token 0)
+#pragma unroll 1
+    for (int idx = threadIdx.x; idx < G * HD; idx += 256) {
+        const int g = idx / HD, dd = idx % HD;
+        float A = 0.f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) A = fmaf(sm_acc[(w * G + g) * HD + dd], fac[w * G + g], A);
         if (ns == 1) {
-            a.o32[(size_t)(kvh * G + g) * HD + dd] = A / L;
+            a.o32[(size_t)(kvh * G + g) * HD + dd] = A / sL[g];
         } else {
             float *pr = part + ((prow + sp) * G + g) * (HD + 2);
             pr[2 + dd] = A;
             if (dd == 0) {
-                pr[0] = M;
-                pr[1] = L;
+                pr[0] = sM[g];
+                pr[1] = sL[g];
             }
         }
     }
@@ -342,74 +374,63 @@ __device__ __forceinline__ void attn_unit(const FwdArgs &a, int layer, int kvh, 
     // ---- split merge by the last CTA of this KV head to arrive: the barrier orders the CTA's
     // partial stores before thread 0's acq_rel arrival, which publishes them and, for the last
     // CTA, acquires the others'
-    int *last = reinterpret_cast<int *>(sm_m);   // sm_m is no longer read after the barrier below
     consumer_sync();
     if (threadIdx.x == 0) {
         unsigned prev;
         asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(prev) : "l"(a.att_cnt + kvh) : "memory");
-        *last = prev == (unsigned)(ns - 1);
+        *flag = prev == (unsigned)(ns - 1);
     }
     consumer_sync();
-    if (!*last) return;
-    // every thread's partial sums first (up to 32 splits in flight at once), then the weights
-    // w_s = exp(M_s - M*) / L* per query head (one warp per head, lanes over splits)
-    constexpr int PER = (G * HD + 255) / 256;   // outputs per thread
-    float av[PER][32];
-    for (int s0 = 0; s0 < ns; s0 += 32) {
+    if (!*flag) return;
+    // weights w_s = exp(M_s - M*) / L* per query head (one warp per head, lanes over splits)
+    float *sw = sm_acc;   // [64][G]
+    for (int g = warp; g < G; g += NW) {
+        float ms[2], ls[2];
 #pragma unroll
-        for (int q = 0; q < PER; ++q) {
-            const int idx = threadIdx.x + 256 * q;
-            const int g = idx / HD, dd = idx % HD;
-#pragma unroll
-            for (int u = 0; u < 32; ++u)
-                av[q][u] = idx < G * HD && s0 + u < ns ? __ldcg(part + ((prow + s0 + u) * G + g) * (HD + 2) + 2 + dd) : 0.f;
+        for (int h = 0; h < 2; ++h) {
+            const int s2 = lane + 32 * h;
+            const float *pr = part + ((prow + s2) * G + g) * (HD + 2);
+            ms[h] = s2 < ns ? __ldcg(pr) : -CUDART_INF_F;
+            ls[h] = s2 < ns ? __ldcg(pr + 1) : 0.f;
         }
-        if (s0 == 0) {
-            float *sw = sm_acc;   // [64][G]
-            for (int g = warp; g < G; g += NW) {
-                float ms[2], ls[2];
+        float M = fmaxf(ms[0], ms[1]);
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int s2 = lane + 32 * h;
-                    const float *pr = part + ((prow + s2) * G + g) * (HD + 2);
-                    ms[h] = s2 < ns ? __ldcg(pr) : -CUDART_INF_F;
-                    ls[h] = s2 < ns ? __ldcg(pr + 1) : 0.f;
-                }
-                float M = fmaxf(ms[0], ms[1]);
+        for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        float e[2], L = 0.f;
 #pragma unroll
-                for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-                float e[2], L = 0.f;
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    e[h] = lane + 32 * h < ns ? expf(ms[h] - M) : 0.f;
-                    L += e[h] * ls[h];
-                }
-#pragma unroll
-                for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-#pragma unroll
-                for (int h = 0; h < 2; ++h)
-                    if (lane + 32 * h < ns) sw[(lane + 32 * h) * G + g] = e[h] / L;
-            }
-            consumer_sync();
+        for (int h = 0; h < 2; ++h) {
+            e[h] = lane + 32 * h < ns ? expf(ms[h] - M) : 0.f;
+            L += e[h] * ls[h];
         }
 #pragma unroll
-        for (int q = 0; q < PER; ++q) {
-            const int idx = threadIdx.x + 256 * q;
-            if (idx >= G * HD) continue;
-            const int g = idx / HD, dd = idx % HD;
-            float *o = a.o32 + (size_t)(kvh * G + g) * HD + dd;
-            float acc_o = s0 == 0 ? 0.f : *o;
+        for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
 #pragma unroll
-            for (int u = 0; u < 32; ++u)
-                if (s0 + u < ns) acc_o = fmaf(sm_acc[(s0 + u) * G + g], av[q][u], acc_o);
-            *o = acc_o;
+        for (int h = 0; h < 2; ++h)
+            if (lane + 32 * h < ns) sw[(lane + 32 * h) * G + g] = e[h] / L;
+    }
+    consumer_sync();
+#pragma unroll 1
+    for (int idx = threadIdx.x; idx < G * HD; idx += 256) {
+        const int g = idx / HD, dd = idx % HD;
+        float o = 0.f;
+#pragma unroll 1
+        for (int s0 = 0; s0 < ns; s0 += 16) {   // 16 independent loads in flight
+            float v[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u)
+                v[u] = s0 + u < ns ? __ldcg(part + ((prow + s0 + u) * G + g) * (HD + 2) + 2 + dd) : 0.f;
+#pragma unroll
+            for (int u = 0; u < 16; ++u)
+                if (s0 + u < ns) o = fmaf(sw[(s0 + u) * G + g], v[u], o);
         }
+        a.o32[(size_t)(kvh * G + g) * HD + dd] = o;
     }
     if (threadIdx.x == 0) a.att_cnt[kvh] = 0;
 }
 
-__host__ __device__ constexpr int attn_scratch_bytes(int hd, int g) { return (2 * 8 * g + 8 * g * hd) * 4; }
+__host__ __device__ constexpr int attn_scratch_bytes(int hd, int g) { return (3 * 8 * g + 2 * g + 4 + 8 * g * hd) * 4; }
 
+// ---------------------------------------------------------------- weight streaming
 // The ring's refill cursor (used by one thread, kFeedThread): the next stage of the step's
 // sequence -- phase `ph`, stage `st` of it -- and the number of stages issued so far.
 constexpr int kFeedThread = 255;
@@ -418,56 +439,370 @@ struct Feeder {
 };
 
 // Issues the cursor's stage into ring slot issued % slots and advances the cursor; nothing once
-// the sequence is exhausted.
-template <int QL, int QH>
-__device__ __forceinline__ void feed_one(const StepArgs &s, int n_ph, int L, Feeder &f, uint8_t *ring, uint64_t *full) {
-    while (f.ph < n_ph && f.st >= s.ph[f.ph].n_stages) {
+// the sequence is exhausted. tab: the phase table (shared memory).
+__device__ __forceinline__ void feed_one(const StepArgs &s, const StepPhase *tab, int n_ph, int L, Feeder &f,
+                                         uint8_t *ring, uint64_t *full) {
+    while (f.ph < n_ph && f.st >= tab[f.ph].n_stages) {
         ++f.ph;
         f.st = blockIdx.x;
     }
     if (f.ph >= n_ph) return;
-    const StepPhase &P = s.ph[f.ph];
-    const bool head = f.ph == 4 * L;
+    const StepPhase &P = tab[f.ph];
     const int slot = f.issued % s.slots;
     uint8_t *dst = ring + (size_t)slot * s.slot_bytes;
-    if (!head && f.ph % 4 == PH_GU) issue_stage<EPI_SWIGLU>(P.p, P.pl, f.st, dst, &full[slot]);
+    if (f.ph != 4 * L && f.ph % 4 == PH_GU) issue_stage<EPI_SWIGLU>(P.p, P.pl, f.st, dst, &full[slot]);
     else issue_stage<EPI_RESID>(P.p, P.pl, f.st, dst, &full[slot]);
     f.st += gridDim.x;
     ++f.issued;
 }
 
-// One weight-streaming phase: stage the input vector, then consume this CTA's stages of the
-// matrix from the ring (k counts ring uses over the whole step), refilling each slot.
-template <int QL, int QH, int QT, int EPI>
-__device__ __forceinline__ void gemv_phase(const StepArgs &s, const StepPhase &P, const FwdArgs &a, int layer,
-                                           uint8_t *xs, uint8_t *ring, uint64_t *full, int &k, Feeder &f, int n_ph,
-                                           bool &dead, PartBuf<1> &part, float (*red)[8],
-                                           unsigned long long (&best)[1], int trace_phase,
-                                           const float4 (*gpre)[4] = nullptr) {
-    if (!dead) stage_token<QT>(P.p, 0, xs, red, 2 * P.p.nb <= kStageThreads ? gpre : nullptr);
+// Stages x (token 0) for a matrix with nb blocks: as stage_token, in a rolled loop over pairs of
+// half-block iterations, the next pair's values loading while the current ones are split (two
+// independent chains per thread). gpre: this thread's gains of the first iteration, loaded
+// before the barrier (or NULL).
+template <int QT>
+__device__ __forceinline__ void stage_x(const GemvParams &p, uint8_t *stage_t, float *red, const float4 *gpre) {
+    constexpr int NTHR = 256;
+    const int nb = p.nb;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const float *xr = p.in.x;
+    uint8_t *hp = stage_t, *lp = stage_t + (size_t)nb * 32;
+    float2 *mp = reinterpret_cast<float2 *>(stage_t + (size_t)nb * 64);
+    float ss = 0.f;
+    const int n_half = 2 * nb, iters = (n_half + NTHR - 1) / NTHR;
+    float4 nx[2][4];
+    auto load = [&](int it, float4 (&dst)[4]) {
+        const int hb = it * NTHR + threadIdx.x;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            dst[j] = it < iters && hb < n_half
+                         ? __ldcg(reinterpret_cast<const float4 *>(xr + (hb >> 1) * 32 + (hb & 1) * 16 + 4 * j))
+                         : make_float4(0, 0, 0, 0);
+    };
+    // split one half block (16 values of iteration it) into the hi / lo planes and the meta
+    auto split = [&](int it, const float4 (&xv)[4]) {
+        const int hb = it * NTHR + threadIdx.x, b = hb >> 1, half = hb & 1;
+        const bool active = hb < n_half;
+        float v[16];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            float4 q = xv[j];
+            ss += q.x * q.x + q.y * q.y + q.z * q.z + q.w * q.w;
+            if (p.in.g && active) {
+                const float4 gg = gpre && it == 0 ? gpre[j]
+                                                  : *reinterpret_cast<const float4 *>(p.in.g + b * 32 + half * 16 + 4 * j);
+                q.x *= gg.x; q.y *= gg.y; q.z *= gg.z; q.w *= gg.w;
+            }
+            v[4 * j] = q.x; v[4 * j + 1] = q.y; v[4 * j + 2] = q.z; v[4 * j + 3] = q.w;
+        }
+        float amax = 0.f;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(v[j]));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));   // the partner holds the other half
+        const float inv = amax > 0.f ? 127.0f / amax : 0.f;
+        uint32_t hw[4], lw[4];
+        int sh = 0, sl = 0;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            uint32_t hbits = 0, lbits = 0;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float y = v[4 * w + e] * inv;
+                const float h = fminf(fmaxf(rintf(y), -127.f), 127.f);
+                const float l = fminf(fmaxf(rintf((y - h) * 128.f), -127.f), 127.f);
+                sh += (int)h;
+                sl += (int)l;
+                hbits |= ((uint32_t)(int)h & 0xffu) << (8 * e);
+                lbits |= ((uint32_t)(int)l & 0xffu) << (8 * e);
+            }
+            hw[w] = hbits;
+            lw[w] = lbits;
+        }
+        sh += __shfl_xor_sync(0xffffffffu, sh, 1);
+        sl += __shfl_xor_sync(0xffffffffu, sl, 1);
+        if (active) {
+            const int i = xpos(nb, b);
+            *reinterpret_cast<uint4 *>(hp + plane_chunk_off(i, half)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4 *>(lp + plane_chunk_off(i, half)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            if (half == 0) {
+                const int C = QT == Q4 ? 8 * (128 * sh + sl) : 0;
+                mp[i] = make_float2(amax * (1.0f / (127.0f * 128.0f)), __int_as_float(C));
+            }
+        }
+    };
+    load(0, nx[0]);
+    load(1, nx[1]);
+#pragma unroll 1
+    for (int it = 0; it < iters; it += 2) {
+        float4 c0[4], c1[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            c0[j] = nx[0][j];
+            c1[j] = nx[1][j];
+        }
+        if (it + 2 < iters) {
+            load(it + 2, nx[0]);
+            load(it + 3, nx[1]);
+        }
+        split(it, c0);
+        if (it + 1 < iters) split(it + 1, c1);   // uniform over the CTA
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (lane == 0) red[warp] = ss;
+}
+
+// How one phase's stages map onto the 256 threads. The R = 4 tps rows of a stage are split into
+// G row groups of NR = R / G rows; the 256 / G threads of a group (whole warps) take the nb
+// blocks of the row, NBT <= 2 blocks each, fixed for the whole phase: a thread keeps its blocks'
+// staged activations in registers and multiplies them with the NR rows of every stage, so the
+// shared-memory traffic of a stage is its weights alone.
+struct GemvMap {
+    int G, NR, NBT;
+};
+__host__ __device__ inline GemvMap gemv_map(int tps, int nb) {
+    const int R = 4 * tps;
+    int g = 1;
+    while (g * 2 <= R && g * 2 <= 8 && nb * g * 2 <= 256) g *= 2;
+    GemvMap m;
+    m.G = g;
+    m.NR = R / g;
+    m.NBT = (nb + 256 / g - 1) / (256 / g);
+    return m;
+}
+
+// Sums v over the 32 lanes of a warp, scattering the NR row sums: afterwards every lane holds the
+// sum of row `row` (the lanes whose bits 16, 8, .. select it), 4 + 2 + 1 + 1 + 1 shuffles for 8 rows.
+template <int NR>
+__device__ __forceinline__ float warp_reduce_rows(float (&v)[NR], int lane, int &row) {
+    int base = 0;
+#pragma unroll
+    for (int st = 0; st < 5; ++st) {
+        const int m = 16 >> st;
+        const int n = NR >> st;   // rows still held (a constant once unrolled)
+        if (n >= 2) {
+            const bool up = lane & m;
+#pragma unroll
+            for (int i = 0; i < NR / 2; ++i) {
+                if (i < n / 2) {
+                    const float send = up ? v[i] : v[i + n / 2];
+                    const float keep = up ? v[i + n / 2] : v[i];
+                    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+                }
+            }
+            if (up) base += n / 2;
+        } else {
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], m);
+        }
+    }
+    row = base;
+    return v[0];
+}
+
+// The dot products of one landed stage for this thread's NR rows and NBT blocks, reduced over
+// the warp and left in part[stage row * 8 + warp within the row group].
+template <int QT, int NR>
+__device__ __forceinline__ void stage_dots(const uint8_t *sq, int QBY, int nb, const XQ (&xq)[2], const int (&bk)[2],
+                                           int nbt, int grp, int wg, float *pk) {
+    constexpr int QB = QT == Q8 ? 32 : 16;
+    const int lane = threadIdx.x & 31;
+    float acc[NR];
+#pragma unroll
+    for (int r = 0; r < NR; ++r) acc[r] = 0.f;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        if (i >= nbt) break;
+        const int b = bk[i];
+        if (b >= nb) continue;
+        float d[NR];
+#pragma unroll
+        for (int r = 0; r < NR; r += 4) {   // scales of whole quads (NR >= 4) ...
+            if (NR >= 4) {
+                const int sr = grp * NR + r;
+                const uint2 s4 = *reinterpret_cast<const uint2 *>(sq + (sr >> 2) * QBY + quad_s_off(QB, b));
+                const float2 d01 = __half22float2(*reinterpret_cast<const __half2 *>(&s4.x));
+                const float2 d23 = __half22float2(*reinterpret_cast<const __half2 *>(&s4.y));
+                d[r] = d01.x; d[(r + 1) % NR] = d01.y; d[(r + 2) % NR] = d23.x; d[(r + 3) % NR] = d23.y;
+            }
+        }
+        if (NR < 4) {   // ... or of single rows
+#pragma unroll
+            for (int r = 0; r < NR; ++r) {
+                const int sr = grp * NR + r;
+                d[r] = __half2float(*reinterpret_cast<const __half *>(sq + (sr >> 2) * QBY + quad_s_off(QB, b) + 2 * (sr & 3)));
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+            const int sr = grp * NR + r;
+            const uint4 *wp = reinterpret_cast<const uint4 *>(sq + (sr >> 2) * QBY + quad_q_off(QB, sr & 3, b));
+            const uint4 w0 = wp[0];
+            const uint4 w1 = QT == Q8 ? wp[1] : w0;
+            const int Pd = QT == Q4 ? q4_idot(w0, xq[i]) : q8_idot(w0, w1, xq[i]);
+            acc[r] = fmaf(d[r] * xq[i].s, (float)Pd, acc[r]);
+        }
+    }
+    int row;
+    const float sum = warp_reduce_rows<NR>(acc, lane, row);
+    if ((lane & (32 / NR - 1)) == 0) pk[(grp * NR + row) * 8 + wg] = sum;
+}
+
+// The dot products of one landed stage (all 256 threads; one copy of the loop per row count),
+// left in pk[stage row * 8 + warp of the row group].
+template <int QT>
+__device__ __forceinline__ void dots_rt(const StepPhase &P, const GemvMap &mp, const uint8_t *sq, const XQ (&xq)[2],
+                                        const int (&bk)[2], float *pk) {
+    const int per_grp = 256 / mp.G;   // threads of a row group
+    const int grp = threadIdx.x / per_grp, wg = (threadIdx.x % per_grp) >> 5;
+    switch (mp.NR) {
+        case 8: stage_dots<QT, 8>(sq, P.pl.quad_bytes, P.p.nb, xq, bk, mp.NBT, grp, wg, pk); break;
+        case 4: stage_dots<QT, 4>(sq, P.pl.quad_bytes, P.p.nb, xq, bk, mp.NBT, grp, wg, pk); break;
+        case 2: stage_dots<QT, 2>(sq, P.pl.quad_bytes, P.p.nb, xq, bk, mp.NBT, grp, wg, pk); break;
+        default: stage_dots<QT, 1>(sq, P.pl.quad_bytes, P.p.nb, xq, bk, mp.NBT, grp, wg, pk); break;
+    }
+}
+
+// Epilogue of task e of stage st (one thread), epilogue kind chosen at run time: a task is a row
+// quad, or for SwiGLU the gate and up rows of 2 features.
+__device__ __forceinline__ void epilogue_rt(const StepPhase &P, const GemvMap &mp, int epi, const FwdArgs &a,
+                                            int layer, int st, int e, const float *pk, float rs, const EpiIn &ein,
+                                            unsigned long long &best) {
+    const GemvParams &p = P.p;
+    const int n_wg = 8 / mp.G;   // warps of a row group: partial sums per row
+    const bool swiglu = epi == EPI_SWIGLU;
+    float v[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        // stage row of output r: the task's quad, or gate (r < 2) / up rows of its feature pair
+        const int sr = swiglu ? (2 * (e >> 1) + (r >> 1)) * 4 + 2 * (e & 1) + (r & 1) : 4 * e + r;
+        const float4 lo = *reinterpret_cast<const float4 *>(pk + sr * 8);
+        const float4 hi = *reinterpret_cast<const float4 *>(pk + sr * 8 + 4);
+        float sum = lo.x;
+        if (n_wg > 1) sum += lo.y;
+        if (n_wg > 2) sum += lo.z + lo.w;
+        if (n_wg > 4) sum += hi.x + hi.y + hi.z + hi.w;
+        v[r] = sum * rs;
+    }
+    const int task = st * P.pl.tps + e, r0 = 4 * task;
+    unsigned long long bkey = 0ull;
+    switch (epi) {
+        case EPI_SWIGLU: {   // features 4 (task / 2) + 2 (task & 1) + {0, 1}
+            const float g2[2] = {v[0], v[1]}, u2[2] = {v[2], v[3]};
+            epi_swiglu2<false>(a, 0, 4 * (task >> 1) + 2 * (task & 1), g2, u2);
+            break;
+        }
+        case EPI_QKV: epi_quad_in<EPI_QKV>(a, layer, 0, r0, p.N, v, ein, bkey); break;
+        case EPI_RESID: epi_quad_in<EPI_RESID>(a, layer, 0, r0, p.N, v, ein, bkey); break;
+        default: epi_quad_in<EPI_LOGITS>(a, layer, 0, r0, p.N, v, ein, bkey); break;
+    }
+    best = bkey > best ? bkey : best;
+}
+
+// State the GEMV routine carries from phase to phase.
+struct GemvState {
+    int k;                    // ring uses so far
+    Feeder f;                 // refill cursor (kFeedThread)
+    bool dead;
+    unsigned long long best;  // logits argmax key of this thread
+};
+
+// One weight-streaming phase (all 256 threads): stage x, then consume this CTA's stages of the
+// phase's matrix from the ring, refilling each slot with the stage S ahead in the sequence.
+template <int QT>
+__device__ __noinline__ void step_gemv(const StepArgs &s, const StepPhase *tab, int ph, int n_ph, int epi,
+                                       const FwdArgs &a, int layer, uint8_t *xs, uint8_t *ring, uint64_t *full,
+                                       GemvState &gs, float *part, float *red, const float4 *gpre, int trace_phase) {
+    const StepPhase &P = tab[ph];
+    if (!gs.dead) stage_x<QT>(P.p, xs, red, 2 * P.p.nb <= 256 ? gpre : nullptr);
     consumer_sync();
+    float rs = 1.f;   // RMS factor of the phase's input (1 without norm gains)
+    if (P.p.in.g) {
+        float tot = 0.f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) tot += red[w];
+        rs = 1.0f / sqrtf(tot / (float)P.p.K + a.eps);
+    }
+    // this thread's blocks and their staged activations, for the whole phase
+    const GemvMap mp = gemv_map(P.pl.tps, P.p.nb);
+    XQ xq[2];
+    int bk[2];
+    {
+        const int per_grp = 256 / mp.G, wg = (threadIdx.x % per_grp) >> 5;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            bk[i] = 32 * wg + block_of_lane(threadIdx.x & 31) + i * per_grp;
+            if (i < mp.NBT && bk[i] < P.p.nb) load_xq(xs, P.p.nb, bk[i], xq[i]);
+        }
+    }
     step_trace(a, trace_phase, 1);
     step_trace(a, trace_phase, 2);
-    for (int st = blockIdx.x; st < P.n_stages; st += gridDim.x, ++k) {
-        const int slot = k % s.slots;
-        if (!dead && !mbar_wait(&full[slot], (k / s.slots) & 1)) {
+    int k = gs.k;
+    bool dead = gs.dead;
+    unsigned long long best = gs.best;
+    Feeder f = gs.f;
+    const int tps = P.pl.tps, n_tasks = P.p.n_tasks;
+    // stages in pairs: both stages' dot products, one barrier, then warp 0 and warp 1 apply the
+    // two epilogues side by side, and both slots are refilled
+    int bi = 0;   // pair index: the partial sums alternate between two buffers
+#pragma unroll 1
+    for (int st = blockIdx.x; st < P.n_stages; st += 2 * gridDim.x, ++bi) {
+        const int st2 = st + gridDim.x;
+        const bool two = st2 < P.n_stages;
+        const int slot0 = k % s.slots, slot1 = (k + 1) % s.slots;
+        float *pk0 = part + (bi & 1) * 256, *pk1 = pk0 + 128;
+        // this thread's epilogue, if any: warp 0 takes the tasks of the first stage, warp 1 the second's
+        const int my_st = threadIdx.x < 32 ? st : st2, e = threadIdx.x & 31;
+        const bool epi_thread = !dead && threadIdx.x < 64 && (threadIdx.x < 32 || two) &&
+                                e < min(tps, n_tasks - my_st * tps);
+        EpiIn ein{};
+        if (epi_thread && epi == EPI_RESID) ein = epi_load<EPI_RESID>(a, 0, (my_st * tps + e) * 4, P.p.N);
+        if (epi_thread && epi == EPI_QKV) ein = epi_load<EPI_QKV>(a, 0, (my_st * tps + e) * 4, P.p.N);
+        if (!dead && !mbar_wait(&full[slot0], (k / s.slots) & 1)) {
             dead = true;
             atomicExch(a.err, 1);
         }
-        consume_stage<QT, 1, EPI, false>(P.p, a, layer, P.pl, ring + (size_t)slot * s.slot_bytes, xs, st, k, dead,
-                                         nullptr, part, red, best);
-        // every warp is past its reads of the slot (the barrier inside consume_stage): refill it
-        if (threadIdx.x == kFeedThread && !dead) feed_one<QL, QH>(s, n_ph, a.L, f, ring, full);
+        if (!dead) dots_rt<QT>(P, mp, ring + (size_t)slot0 * s.slot_bytes, xq, bk, pk0);
+        if (two) {
+            if (!dead && !mbar_wait(&full[slot1], ((k + 1) / s.slots) & 1)) {
+                dead = true;
+                atomicExch(a.err, 1);
+            }
+            if (!dead) dots_rt<QT>(P, mp, ring + (size_t)slot1 * s.slot_bytes, xq, bk, pk1);
+        }
+        consumer_sync();
+        if (epi_thread) epilogue_rt(P, mp, epi, a, layer, my_st, e, threadIdx.x < 32 ? pk0 : pk1, rs, ein, best);
+        // every warp is past its reads of the slots (the barrier above): refill them
+        if (threadIdx.x == kFeedThread && !dead) {
+            feed_one(s, tab, n_ph, a.L, f, ring, full);
+            if (two) feed_one(s, tab, n_ph, a.L, f, ring, full);
+        }
+        k += two ? 2 : 1;
     }
+    gs.k = k;
+    gs.dead = dead;
+    gs.best = best;
+    gs.f = f;
     step_trace(a, trace_phase, 3);
 }
 
+// this thread's gains of the first staging iteration of a phase (loaded before its barrier)
+__device__ __forceinline__ void gains_of(const StepPhase &P, float4 (&g)[4]) {
+    const int hb = threadIdx.x, b = hb >> 1, half = hb & 1;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        g[j] = P.p.in.g && hb < 2 * P.p.nb ? *reinterpret_cast<const float4 *>(P.p.in.g + b * 32 + half * 16 + 4 * j)
+                                           : make_float4(1.f, 1.f, 1.f, 1.f);
+}
+
 template <int QL, int QH, int HD, int G>
-__global__ void __launch_bounds__(256, 1) k_decode_step(const StepArgs s, const FwdArgs a) {
+__global__ void __launch_bounds__(256, 1) k_decode_step(const __grid_constant__ StepArgs s,
+                                                        const __grid_constant__ FwdArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t *xs = smem;
     uint8_t *ring = smem + s.x_bytes;
     uint64_t *full = reinterpret_cast<uint64_t *>(ring + (size_t)s.slots * s.slot_bytes);
+    StepPhase *tab = reinterpret_cast<StepPhase *>(full + kMaxStages);
+    int *pages = reinterpret_cast<int *>(tab + s.n_ph_all);
     const int L = a.L;
     const int n_ph = 4 * L + (a.n_out > 0 ? 1 : 0);
 
@@ -475,20 +810,23 @@ __global__ void __launch_bounds__(256, 1) k_decode_step(const StepArgs s, const 
         for (int i = 0; i < s.slots; ++i) mbar_init(&full[i], 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    {   // the phase table, into shared memory
+        const uint4 *src = reinterpret_cast<const uint4 *>(s.ph);
+        uint4 *dst = reinterpret_cast<uint4 *>(tab);
+        const int n16 = (int)(s.n_ph_all * sizeof(StepPhase) / 16);
+        for (int i = threadIdx.x; i < n16; i += 256) dst[i] = src[i];
+    }
     __syncthreads();
+    GemvState gs{0, Feeder{0, (int)blockIdx.x, 0}, false, 0ull};
     // fill the ring: the weights do not depend on anything this step computes
-    Feeder f{0, (int)blockIdx.x, 0};
     if (threadIdx.x == kFeedThread)
-        for (int i = 0; i < s.slots; ++i) feed_one<QL, QH>(s, n_ph, L, f, ring, full);
+        for (int i = 0; i < s.slots; ++i) feed_one(s, tab, n_ph, L, gs.f, ring, full);
 
-    __shared__ float red[1][8];
-    __shared__ PartBuf<1> part;
+    __shared__ float red[8];
+    __shared__ __align__(16) float part[2 * 2 * 16 * 8];   // [batch parity][stage of the pair][16 rows][8]
     __shared__ int s_ok;
-    unsigned long long best[1] = {0ull};
     unsigned *bar = s.sync;
     unsigned n_bar = 0;
-    int k = 0;
-    bool dead = false;
     const int units = a.KV * s.att_ns;
     const bool has_unit = (int)blockIdx.x < units;
     const int u_kvh = blockIdx.x % a.KV, u_sp = blockIdx.x / a.KV;
@@ -510,59 +848,71 @@ __global__ void __launch_bounds__(256, 1) k_decode_step(const StepArgs s, const 
     // this token's attention unit: cells [ac0, ac1) of KV head u_kvh
     const int n_att = a.ub.pos[0] + 1;
     const int ac0 = u_sp * s.att_chunk, ac1 = min(ac0 + s.att_chunk, n_att);
-    AttnRegs<HD> R;
-    // the norm gains of the next phase that has them, loaded before the barrier it waits on
+    const int page0 = ac0 >> 6;
+    KVGroup<HD> kvq[4];   // this warp's first 4 groups of the unit, loaded before each attention barrier
     float4 gpre[4];
-    stage_gains(s.ph[0].p.in.g, s.ph[0].p.nb, gpre);
-    dead = !grid_sync(a, bar, ++n_bar, dead, &s_ok);
+    gains_of(tab[0], gpre);
+    gs.dead = !grid_sync(a, bar, ++n_bar, gs.dead, &s_ok);
+    if (has_unit) {   // the unit's page ids (the page table is complete after the barrier)
+        const int n_pg = min(kMaxUnitPages, ((max(ac1, ac0 + 1) - 1) >> 6) - page0 + 1);
+        const int32_t *ptrow = a.pt + (size_t)a.ub.seq[0] * a.max_pages_per_seq;
+        for (int i = threadIdx.x; i < n_pg; i += 256) pages[i] = __ldcg(ptrow + page0 + i);
+        consumer_sync();
+    }
 
-    for (int l = 0; l < L && !dead; ++l) {
+    for (int l = 0; l < L && !gs.dead; ++l) {
         const int tp = 1 + 5 * l;
-        const StepPhase &Pq = s.ph[4 * l + PH_QKV], &Po = s.ph[4 * l + PH_O], &Pg = s.ph[4 * l + PH_GU],
-                        &Pd = s.ph[4 * l + PH_DOWN];
         // QKV (the attention unit's cached K/V lines go to L2 meanwhile)
         step_trace(a, tp, 0);
-        if (has_unit) attn_prefetch<HD>(a, l, u_kvh, ac0, ac1);
-        gemv_phase<QL, QH, QL, EPI_QKV>(s, Pq, a, l, xs, ring, full, k, f, n_ph, dead, part, red, best, tp, &gpre);
-        if (has_unit) attn_load_sg<HD>(a, l, u_kvh, ac0 + 16 * (threadIdx.x >> 5), ac1, 0, false, R);
-        dead = !grid_sync(a, bar, ++n_bar, dead, &s_ok);
-        if (dead) break;
+        if (has_unit) attn_prefetch<HD>(a, l, u_kvh, ac0, ac1, pages, page0);
+        step_gemv<QL>(s, tab, 4 * l + PH_QKV, n_ph, EPI_QKV, a, l, xs, ring, full, gs, part, red, gpre, tp);
+        if (has_unit) {
+            const int jf = ac0 + 4 * (threadIdx.x >> 5);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                if (jf + 32 * i < ac1)
+                    kv_group_load<HD>(a, l, u_kvh, unit_page(a, pages, page0, jf + 32 * i), jf + 32 * i, ac1, kvq[i]);
+        }
+        gs.dead = !grid_sync(a, bar, ++n_bar, gs.dead, &s_ok);
+        if (gs.dead) break;
         // attention
         step_trace(a, tp + 1, 0);
-        if (has_unit) attn_unit<HD, G>(a, l, u_kvh, u_sp, s.att_chunk, s.att_ns, reinterpret_cast<float *>(xs), R, tp + 1);
+        if (has_unit)
+            step_attention<HD, G>(a, l, u_kvh, u_sp, s.att_chunk, s.att_ns, reinterpret_cast<float *>(xs), pages, page0,
+                                  kvq, tp + 1);
         step_trace(a, tp + 1, 3);
-        dead = !grid_sync(a, bar, ++n_bar, dead, &s_ok);
-        if (dead) break;
+        gs.dead = !grid_sync(a, bar, ++n_bar, gs.dead, &s_ok);
+        if (gs.dead) break;
         // output projection + residual
         step_trace(a, tp + 2, 0);
-        gemv_phase<QL, QH, QL, EPI_RESID>(s, Po, a, l, xs, ring, full, k, f, n_ph, dead, part, red, best, tp + 2);
-        stage_gains(Pg.p.in.g, Pg.p.nb, gpre);
-        dead = !grid_sync(a, bar, ++n_bar, dead, &s_ok);
-        if (dead) break;
+        step_gemv<QL>(s, tab, 4 * l + PH_O, n_ph, EPI_RESID, a, l, xs, ring, full, gs, part, red, nullptr, tp + 2);
+        gains_of(tab[4 * l + PH_GU], gpre);
+        gs.dead = !grid_sync(a, bar, ++n_bar, gs.dead, &s_ok);
+        if (gs.dead) break;
         // gate/up + SwiGLU
         step_trace(a, tp + 3, 0);
-        gemv_phase<QL, QH, QL, EPI_SWIGLU>(s, Pg, a, l, xs, ring, full, k, f, n_ph, dead, part, red, best, tp + 3, &gpre);
-        dead = !grid_sync(a, bar, ++n_bar, dead, &s_ok);
-        if (dead) break;
+        step_gemv<QL>(s, tab, 4 * l + PH_GU, n_ph, EPI_SWIGLU, a, l, xs, ring, full, gs, part, red, gpre, tp + 3);
+        gs.dead = !grid_sync(a, bar, ++n_bar, gs.dead, &s_ok);
+        if (gs.dead) break;
         // down + residual
         step_trace(a, tp + 4, 0);
-        gemv_phase<QL, QH, QL, EPI_RESID>(s, Pd, a, l, xs, ring, full, k, f, n_ph, dead, part, red, best, tp + 4);
-        const StepPhase &Pn = s.ph[4 * l + 4];   // next layer's QKV, or the head
-        stage_gains(Pn.p.in.g, Pn.p.nb, gpre);
-        dead = !grid_sync(a, bar, ++n_bar, dead, &s_ok);
+        step_gemv<QL>(s, tab, 4 * l + PH_DOWN, n_ph, EPI_RESID, a, l, xs, ring, full, gs, part, red, nullptr, tp + 4);
+        gains_of(tab[4 * l + 4], gpre);   // next layer's QKV, or the head
+        gs.dead = !grid_sync(a, bar, ++n_bar, gs.dead, &s_ok);
     }
-    if (dead) {
+    if (gs.dead) {
         // copies still in flight must land before the CTA's shared memory is released
         if (threadIdx.x == kFeedThread)
-            for (int j = f.issued > s.slots ? f.issued - s.slots : 0; j < f.issued; ++j)
+            for (int j = gs.f.issued > s.slots ? gs.f.issued - s.slots : 0; j < gs.f.issued; ++j)
                 mbar_wait(&full[j % s.slots], (j / s.slots) & 1);
         return;
     }
     if (a.n_out > 0) {
         const int tp = 1 + 5 * L;
         step_trace(a, tp, 0);
-        gemv_phase<QL, QH, QH, EPI_LOGITS>(s, s.ph[4 * L], a, -1, xs, ring, full, k, f, n_ph, dead, part, red, best, tp, &gpre);
-        logits_cta_reduce<1>(a, 1, best);
+        step_gemv<QH>(s, tab, 4 * L, n_ph, EPI_LOGITS, a, -1, xs, ring, full, gs, part, red, gpre, tp);
+        const unsigned long long bst[1] = {gs.best};
+        logits_cta_reduce<1>(a, 1, bst);
     }
     // the last CTA to finish writes the argmax and resets the step's counters: every other CTA
     // is past its last barrier by then
