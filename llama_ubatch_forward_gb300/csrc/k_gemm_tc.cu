@@ -7,16 +7,21 @@
 // Prefill is where the work is compute-bound (KV-cache section of the article: prefill loads the
 // compute units), so the contraction runs on the 5th-generation tensor cores. One CTA computes two
 // 128-row weight tiles (adjacent rows, or a gate chunk and its up chunk) against BN tokens:
-//   warp 0      TMA producer: raw quant + scale tiles of the weights (issued before the
-//               grid-dependency wait: the weights do not depend on the previous kernel), then the
-//               activation tiles [BN][64] f16 (high and low parts) with the 128-byte swizzle;
+//   warp 0      TMA producer: one box per stage holds the quants and scales of both weight tiles
+//               (64 row quads of the quad-interleaved layout; issued before the grid-dependency
+//               wait: the weights do not depend on the previous kernel);
 //   warp 1      allocates the TMEM accumulator and issues tcgen05.mma from one lane -- W A_hi and
 //               W A_lo into the same accumulator, so the activations keep about 22 bits and only
 //               the f16 rounding of the dequantised weights remains; each stage's tcgen05.commit
 //               frees its shared-memory slot;
-//   warps 2..5  dequantise the raw blocks of their row into the K-major SWIZZLE_128B f16 tile the
-//               MMA reads ((q - 8) or q is exact in f16, then one f16 multiply by the block scale),
-//               then run the epilogue from TMEM with tcgen05.ld.
+//   warps 2..9  load the activation tiles [BN][64] f16 (high and low parts) with cp.async, S - 1
+//               stages ahead, writing the 128-byte swizzle themselves; dequantise the raw blocks of
+//               their row (warps 2..5 tile 0, warps 6..9 tile 1) into the K-major SWIZZLE_128B f16
+//               tile the MMA reads ((q - 8) or q is exact in f16, then one f16 multiply by the
+//               block scale); then run their tile's epilogue from TMEM with tcgen05.ld.
+// The copy engine's cost is per copy (about 0.4 us each, whatever the size up to several KB) and
+// per 128-byte row, so the activation tiles -- 4 bytes per element, re-read by every weight tile
+// pair -- go through the load/store path instead, and the engine moves one box per stage.
 // All mbarrier waits are bounded; a timeout sets the context's error word and the CTA finishes
 // without further work.
 #include <cudaTypedefs.h>
@@ -103,17 +108,25 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// Shared memory: a ring of S stages, each the raw weight box and the activation tiles of one K
+// step, and a separate ring of 2 dequantised f16 weight tiles (the largest part of a stage), so
+// the TMA and activation loads can run S - 1 stages ahead while the f16 tiles are double-buffered.
 template <int QT, int BN, int MT>
 struct Cfg {
     static constexpr int QB = QT == Q8 ? 32 : 16;          // quant bytes per 32-element block
-    static constexpr int A_BYTES = MT * BM * BK * 2;      // f16 weight tiles
+    static constexpr int A_BYTES = MT * BM * BK * 2;      // f16 weight tiles (one slot of the A ring)
     static constexpr int B_BYTES = 2 * BN * BK * 2;       // f16 activation tiles: high and low parts
     static constexpr int PB = 8 * QB + 16;                // one block pair of a row quad (QMat)
     static constexpr int RQ_BYTES = MT * (BM / 4) * PB;   // raw tiles: 32 quads x one block pair
-    static constexpr int STAGE = A_BYTES + B_BYTES + ((RQ_BYTES + 1023) / 1024) * 1024;
-    static constexpr int S = (220 * 1024) / STAGE < 6 ? (220 * 1024) / STAGE : 6;
-    static constexpr int SMEM = S * STAGE + 1024 /* align */ + 256 /* barriers */;
-    static constexpr int TMEM_COLS = MT * BN <= 32 ? 32 : MT * BN <= 64 ? 64 : MT * BN <= 128 ? 128 : MT * BN <= 256 ? 256 : 512;
+    static constexpr int STAGE = B_BYTES + ((RQ_BYTES + 1023) / 1024) * 1024;
+    static constexpr int SA = 2;                          // dequantised tiles in flight
+    static constexpr int S_FIT = (220 * 1024 - SA * A_BYTES) / STAGE;
+    static constexpr int S = S_FIT < 6 ? S_FIT : 6;
+    static_assert(S >= 2, "the activation prefetch needs at least two stages");
+    static constexpr int SMEM = SA * A_BYTES + S * STAGE + 1024 /* align */ + 512 /* barriers */;
+    // per weight tile, W A_hi and W A_lo side by side: one MMA of N = 2 BN over the stacked tiles
+    static constexpr int TMEM_COLS = MT * 2 * BN <= 128 ? 128 : MT * 2 * BN <= 256 ? 256 : 512;
+    static_assert(MT * 2 * BN <= 512, "tensor memory holds 512 columns");
 };
 
 struct GemmParams {
@@ -187,33 +200,40 @@ __device__ __forceinline__ void dequant_row(const uint8_t *rq, uint8_t *atile, i
 }
 
 template <int QT, int BN, int EPI>
-__global__ void __launch_bounds__(192, 1)
-    k_gemm_tc(const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_b2,
+__global__ void __launch_bounds__(320, 1)
+    k_gemm_tc(const __half *__restrict__ A_hi, const __half *__restrict__ A_lo, const int K,
               const __grid_constant__ CUtensorMap tm_w, const GemmParams p, const FwdArgs a, const int layer) {
     constexpr int MT = 2;   // two 128-row weight tiles share every activation tile
     using C = Cfg<QT, BN, MT>;
     constexpr int S = C::S;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S * C::STAGE);
-    uint64_t *full_w = bars, *full_b = bars + S, *full_a = bars + 2 * S, *empty = bars + 3 * S, *acc_bar = bars + 4 * S;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 4 * S + 1);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::SA * C::A_BYTES + S * C::STAGE);
+    // full_w: raw weights landed; full_b: activations landed; empty: the stage's MMAs are done
+    // (raw and activation slot free); full_a / empty_a: the A ring's dequantised tile written / read
+    uint64_t *full_w = bars, *full_b = bars + S, *empty = bars + 2 * S, *full_a = bars + 3 * S,
+             *empty_a = full_a + C::SA, *acc_bar = empty_a + C::SA;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_bar + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m_tile = blockIdx.x, tok0 = blockIdx.y * BN;
     const int nk = p.nk;
     // first weight row of each M tile: two adjacent 128-row tiles (for gate/up each holds 16
     // gate quads interleaved with their 16 up quads)
     const int row0[MT] = {m_tile * 2 * BM, m_tile * 2 * BM + BM};
-    auto a_tile = [&](int slot, int mt) { return smem + slot * C::STAGE + mt * BM * BK * 2; };
-    auto b_tile = [&](int slot) { return smem + slot * C::STAGE + C::A_BYTES; };
-    auto rq_tile = [&](int slot, int mt) { return smem + slot * C::STAGE + C::A_BYTES + C::B_BYTES + mt * (BM / 4) * C::PB; };
+    auto a_tile = [&](int aslot, int mt) { return smem + aslot * C::A_BYTES + mt * BM * BK * 2; };
+    uint8_t *ring = smem + C::SA * C::A_BYTES;
+    auto b_tile = [&](int slot) { return ring + slot * C::STAGE; };
+    auto rq_tile = [&](int slot, int mt) { return ring + slot * C::STAGE + C::B_BYTES + mt * (BM / 4) * C::PB; };
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
             mbar_init(&full_w[i], 1);
-            mbar_init(&full_b[i], 1);
-            mbar_init(&full_a[i], 4);
+            mbar_init(&full_b[i], 8);   // one arrival per loading warp
             mbar_init(&empty[i], 1);
+        }
+        for (int i = 0; i < C::SA; ++i) {
+            mbar_init(&full_a[i], 8);   // one arrival per dequantising warp
+            mbar_init(&empty_a[i], 1);
         }
         mbar_init(acc_bar, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -232,118 +252,161 @@ __global__ void __launch_bounds__(192, 1)
         // ---------------------------------------------------------------- producer
         if (lane == 0) {
             bool ok = true;
-            auto issue_w = [&](int j) {
+            auto issue_w = [&](int j) {   // quants and scales of the 64 quads of both tiles: one box
                 const int slot = j % S;
                 mbar_expect_tx(&full_w[slot], C::RQ_BYTES);
-#pragma unroll
-                for (int mt = 0; mt < MT; ++mt)   // quants and scales of 32 quads: one box
-                    tma_2d(rq_tile(slot, mt), &tm_w, j * (C::PB / 4), row0[mt] / 4, &full_w[slot]);
-            };
-            auto issue_b = [&](int j) {
-                const int slot = j % S;
-                mbar_expect_tx(&full_b[slot], C::B_BYTES);
-                tma_2d(b_tile(slot), &tm_b, j * BK, tok0, &full_b[slot]);
-                tma_2d(b_tile(slot) + BN * BK * 2, &tm_b2, j * BK, tok0, &full_b[slot]);
+                tma_2d(rq_tile(slot, 0), &tm_w, j * (C::PB / 4), row0[0] / 4, &full_w[slot]);
             };
             const int pre = nk < S ? nk : S;
             for (int j = 0; j < pre; ++j) issue_w(j);
-            LCX_PDL_WAIT();   // the activations are the previous kernel's output
             LCX_PDL_TRIGGER();
-            for (int j = 0; j < pre; ++j) issue_b(j);
             int issued = pre;
             for (int j = S; j < nk && ok; ++j) {
                 if (!(ok = mbar_wait(&empty[j % S], ((j / S) - 1) & 1))) break;
                 issue_w(j);
-                issue_b(j);
                 issued = j + 1;
             }
             if (!ok) atomicExch(a.err, 1);
             // every copy issued must land before the CTA exits
-            for (int j = (issued > S ? issued - S : 0); j < issued; ++j) {
-                mbar_wait(&full_w[j % S], (j / S) & 1);
-                mbar_wait(&full_b[j % S], (j / S) & 1);
-            }
+            for (int j = (issued > S ? issued - S : 0); j < issued; ++j) mbar_wait(&full_w[j % S], (j / S) & 1);
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_f16(BM, BN);
+            constexpr uint32_t idesc = idesc_f16(BM, 2 * BN);   // the high and low parts stacked: N = 2 BN
             bool ok = true;
             for (int j = 0; j < nk; ++j) {
-                const int slot = j % S;
-                const uint32_t ph = (j / S) & 1;
-                if (!(ok = mbar_wait(&full_a[slot], ph) && mbar_wait(&full_b[slot], ph))) break;
+                const int slot = j % S, aslot = j % C::SA;
+                if (!(ok = mbar_wait(&full_a[aslot], (j / C::SA) & 1) && mbar_wait(&full_b[slot], (j / S) & 1))) break;
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                 const uint32_t bbase = saddr(b_tile(slot));
+                // the activation tile's high rows then low rows form one K-major operand of 2 BN
+                // rows, so each MMA computes W A_hi and W A_lo into adjacent accumulator columns;
+                // the two weight tiles alternate so consecutive MMAs use different accumulators
 #pragma unroll
-                for (int mt = 0; mt < MT; ++mt) {
-                    const uint32_t abase = saddr(a_tile(slot, mt));
+                for (int kk = 0; kk < BK / 16; ++kk) {
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk) {   // W (A_hi + A_lo) as two MMAs into one accumulator
-                        mma_f16(tmem + mt * BN, sw128_desc(abase + kk * 32), sw128_desc(bbase + kk * 32), idesc,
+                    for (int mt = 0; mt < MT; ++mt) {
+                        const uint32_t abase = saddr(a_tile(aslot, mt));
+                        mma_f16(tmem + mt * 2 * BN, sw128_desc(abase + kk * 32), sw128_desc(bbase + kk * 32), idesc,
                                 (j > 0 || kk > 0) ? 1u : 0u);
-                        mma_f16(tmem + mt * BN, sw128_desc(abase + kk * 32), sw128_desc(bbase + BN * BK * 2 + kk * 32),
-                                idesc, 1u);
                     }
                 }
-                mma_commit(&empty[slot]);   // the slot is free once these MMAs have read it
+                mma_commit(&empty[slot]);     // the stage's slot is free once these MMAs have read it
+                mma_commit(&empty_a[aslot]);  // and so is the A slot
             }
             if (!ok) atomicExch(a.err, 1);
             mma_commit(acc_bar);
         }
     } else {
-        // ---------------------------------------------------------------- dequant, then epilogue
-        const int drow = threadIdx.x - 64;   // 0..127
-        bool ok = true;
-        for (int j = 0; j < nk; ++j) {
-            const int slot = j % S;
-            ok = __all_sync(0xffffffffu, mbar_wait(&full_w[slot], (j / S) & 1));   // warp-uniform
-            if (!ok) break;
+        // ---------------------------------------------------------------- activations, dequant, epilogue
+        // 8 warps: warps 2..5 own weight tile 0, warps 6..9 tile 1 (dequant and epilogue); all 8
+        // load the activation tiles
+        const int wt = threadIdx.x - 64;           // 0..255
+        const int my_mt = wt >> 7, drow = wt & 127;
+        // activation tile of stage j: 2 parts x BN rows x 8 chunks of 16 bytes; thread wt copies
+        // chunk wt % 8 of rows wt / 8 + 32 u, each to its 128-byte-swizzled place; rows past the
+        // last token are zero-filled
+        auto load_act = [&](int j) {
+            uint8_t *bt = b_tile(j % S);
+            const int c = wt & 7;
 #pragma unroll
-            for (int mt = 0; mt < MT; ++mt) dequant_row<QT>(rq_tile(slot, mt), a_tile(slot, mt), drow);
+            for (int hl = 0; hl < 2; ++hl) {
+                const __half *src0 = hl ? A_lo : A_hi;
+#pragma unroll
+                for (int u = 0; u < BN / 32; ++u) {
+                    const int r = (wt >> 3) + 32 * u, t = tok0 + r;
+                    const __half *src = src0 + (size_t)(t < p.T ? t : 0) * K + j * BK + c * 8;
+                    const uint32_t dst = saddr(bt + hl * BN * BK * 2 + r * 128 + ((c ^ (r & 7)) << 4));
+                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+                                 "r"(t < p.T ? 16 : 0) : "memory");
+                }
+            }
+        };
+        bool ok = true;
+        LCX_PDL_WAIT();   // the activations are the previous kernel's output
+        LCX_PDL_TRIGGER();
+        for (int j = 0; j < S - 1; ++j) {   // stages 0 .. S-2 ahead (their slots start free)
+            if (j < nk) load_act(j);
+            asm volatile("cp.async.commit_group;" ::: "memory");
+        }
+        for (int j = 0; j < nk; ++j) {
+            const int slot = j % S, aslot = j % C::SA;
+            ok = __all_sync(0xffffffffu, mbar_wait(&full_w[slot], (j / S) & 1));   // warp-uniform
+            // the A slot is free once the MMAs of stage j - SA are done
+            if (ok && j >= C::SA) ok = __all_sync(0xffffffffu, mbar_wait(&empty_a[aslot], ((j / C::SA) - 1) & 1));
+            if (!ok) break;
+            dequant_row<QT>(rq_tile(slot, my_mt), a_tile(aslot, my_mt), drow);
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic writes -> tensor-core reads
             __syncwarp();
-            if (lane == 0) mbar_arrive(&full_a[slot]);
+            if (lane == 0) mbar_arrive(&full_a[aslot]);
+            // stage j's activation copies have landed: of the S - 1 + j groups committed so far,
+            // all but the S - 2 newest
+            asm volatile("cp.async.wait_group %0;" ::"n"(S - 2) : "memory");
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&full_b[slot]);
+            // prefetch stage j + S - 1 into the slot stage j - 1 used, once its MMAs are done
+            const int jn = j + S - 1;
+            if (jn < nk) {
+                if (jn >= S) ok = __all_sync(0xffffffffu, mbar_wait(&empty[jn % S], ((jn / S) - 1) & 1));
+                if (!ok) break;
+                load_act(jn);
+            }
+            asm volatile("cp.async.commit_group;" ::: "memory");
         }
+        asm volatile("cp.async.wait_all;" ::: "memory");   // nothing in flight when the CTA ends
         if (!ok) atomicExch(a.err, 1);
-        LCX_PDL_WAIT();
-        LCX_PDL_TRIGGER();
         const bool acc_ok = __all_sync(0xffffffffu, ok && mbar_wait(acc_bar, 0));
         if (acc_ok) {
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             const int q = warp & 3;                 // TMEM lane quarter of this warp
             const int lrow = q * 32 + lane;         // row within the tile
-            const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
+            const int r = row0[my_mt] + lrow;       // weight row
+            const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16) + my_mt * 2 * BN;
             for (int cb = 0; cb < BN / 32; ++cb) {
-                uint32_t v0[32], v1[32];
-                tmem_ld32(tq + cb * 32, v0);
-                tmem_ld32(tq + BN + cb * 32, v1);
+                uint32_t vv[32];   // W (A_hi + A_lo): the high-part columns plus the low-part columns
+                {
+                    uint32_t lo[32];
+                    tmem_ld32(tq + cb * 32, vv);
+                    tmem_ld32(tq + BN + cb * 32, lo);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) vv[i] = __float_as_uint(__uint_as_float(vv[i]) + __uint_as_float(lo[i]));
+                }
                 if (EPI == EPI_SWIGLU) {   // rows 8f'..8f'+3 gate, 8f'+4..8f'+7 up of features 4f'..
+                    const int f = (r >> 3) * 4 + (lrow & 3);
+                    const bool gate = (lane & 7) < 4;
 #pragma unroll
-                    for (int mt = 0; mt < MT; ++mt) {
-                        const int f = ((row0[mt] + lrow) >> 3) * 4 + (lrow & 3);
-                        const bool gate = (lane & 7) < 4;
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            const float g = __uint_as_float(mt == 0 ? v0[i] : v1[i]);
-                            const float u = __shfl_down_sync(0xffffffffu, g, 4);
-                            const int t = tok0 + cb * 32 + i;
-                            if (gate && t < p.T && f < a.F)
-                                store_split(a.h16, a.h16_lo, (size_t)t * a.F_pad + f, silu_f(g) * u);
-                        }
+                    for (int i = 0; i < 32; ++i) {
+                        const float g = __uint_as_float(vv[i]);
+                        const float u = __shfl_down_sync(0xffffffffu, g, 4);
+                        const int t = tok0 + cb * 32 + i;
+                        if (gate && t < p.T && f < a.F)
+                            store_split(a.h16, a.h16_lo, (size_t)t * a.F_pad + f, silu_f(g) * u);
                     }
                     continue;
                 }
+                // every load of a 16-token group is issued before its first store: a store may
+                // alias a later load, so mixing them would serialise one L2 round trip per element
 #pragma unroll
-                for (int mt = 0; mt < MT; ++mt) {
-                    const int r = row0[mt] + lrow;
+                for (int h = 0; h < 2; ++h) {
+                    if (EPI == EPI_RESID) {
+                        float xo[16];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int t = tok0 + cb * 32 + i;
-                        const float v = __uint_as_float(mt == 0 ? v0[i] : v1[i]);
-                        if (EPI == EPI_RESID) {
-                            if (t < p.T && r < p.N) a.x[(size_t)t * a.d + r] += v;
-                        } else if (EPI == EPI_LOGITS) {
+                        for (int i = 0; i < 16; ++i) {
+                            const int t = tok0 + cb * 32 + 16 * h + i;
+                            xo[i] = t < p.T && r < p.N ? __ldcg(a.x + (size_t)t * a.d + r) : 0.f;
+                        }
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const int t = tok0 + cb * 32 + 16 * h + i;
+                            if (t < p.T && r < p.N) a.x[(size_t)t * a.d + r] = xo[i] + __uint_as_float(vv[16 * h + i]);
+                        }
+                    } else if (EPI == EPI_LOGITS) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const int t = tok0 + cb * 32 + 16 * h + i;
+                            const float v = __uint_as_float(vv[16 * h + i]);
                             unsigned long long key = 0ull;
                             if (t < p.T && r < p.N) {
                                 a.logits[(size_t)t * a.V + r] = v;
@@ -355,25 +418,39 @@ __global__ void __launch_bounds__(192, 1)
                                 key = other > key ? other : key;
                             }
                             if (lane == 0 && key) atomicMax(&a.amax_key[t], key);
-                        } else {   // EPI_QKV: rotate (q, k) pairs of adjacent rows, store q f32 and k, v f16
+                        }
+                    } else {   // EPI_QKV: rotate (q, k) pairs of adjacent rows, store q f32 and k, v f16
+                        const int qw = a.H * a.hd, kw = a.KV * a.hd;
+                        const bool rot = r < qw + kw;
+                        const int dim = (r < qw ? r : r - qw) & (a.hd - 1);   // hd is 64 or 128
+                        int cell[16];
+                        float2 cs[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {   // token metadata and RoPE pairs, all loads first
+                            const int t = tok0 + cb * 32 + 16 * h + i;
+                            const int pos = t < p.T ? __ldg(a.ub.pos + t) : 0;
+                            cell[i] = t < p.T ? __ldg(a.ub.cell + t) : 0;
+                            cs[i] = rot ? __ldg(a.rope + (size_t)pos * (a.hd / 2) + dim / 2) : make_float2(1.f, 0.f);
+                        }
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const int t = tok0 + cb * 32 + 16 * h + i;
+                            const float v = __uint_as_float(vv[16 * h + i]);
                             const float partner = __shfl_xor_sync(0xffffffffu, v, 1);
-                            const int qw = a.H * a.hd, kw = a.KV * a.hd;
                             if (t < p.T && r < qw + 2 * kw && (lane & 1) == 0) {
                                 float y0 = v, y1 = partner;
-                                if (r < qw + kw) {
-                                    const int dim = r < qw ? r % a.hd : (r - qw) % a.hd;
-                                    const float2 cs = a.rope[(size_t)a.ub.pos[t] * (a.hd / 2) + dim / 2];
-                                    const float z0 = y0 * cs.x - y1 * cs.y, z1 = y0 * cs.y + y1 * cs.x;
+                                if (rot) {
+                                    const float z0 = y0 * cs[i].x - y1 * cs[i].y, z1 = y0 * cs[i].y + y1 * cs[i].x;
                                     y0 = z0;
                                     y1 = z1;
                                 }
                                 if (r < qw) {
-                                    a.q[(size_t)t * qw + r] = y0;
-                                    a.q[(size_t)t * qw + r + 1] = y1;
+                                    *reinterpret_cast<float2 *>(a.q + (size_t)t * qw + r) = make_float2(y0, y1);
                                 } else {
                                     const bool isk = r < qw + kw;
                                     const int rr = isk ? r - qw : r - qw - kw;
-                                    __half *dst = (isk ? a.kc : a.vc) + kv_off(a, layer, a.ub.cell[t], rr / a.hd, rr % a.hd);
+                                    const int sh = __ffs(a.hd) - 1;
+                                    __half *dst = (isk ? a.kc : a.vc) + kv_off(a, layer, cell[i], rr >> sh, rr & (a.hd - 1));
                                     *reinterpret_cast<__half2 *>(dst) = __floats2half2_rn(y0, y1);
                                 }
                             }
@@ -422,32 +499,6 @@ bool make_map_2d(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int e
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-struct ActKey {
-    const void *ptr;
-    int K, T, BN;
-};
-struct ActMap {
-    ActKey k;
-    CUtensorMap m;
-};
-
-const CUtensorMap *act_map(const __half *A, int K, int T, int BN) {
-    static std::mutex mu;
-    static std::vector<ActMap *> cache;
-    std::lock_guard<std::mutex> lk(mu);
-    for (ActMap *e : cache)
-        if (e->k.ptr == A && e->k.K == K && e->k.T == T && e->k.BN == BN) return &e->m;
-    ActMap *e = new ActMap;   // kept for the life of the process (a few bytes per shape)
-    e->k = {A, K, T, BN};
-    if (!make_map_2d(&e->m, A, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (uint64_t)K, (uint64_t)T, (uint64_t)K * 2, BK,
-                     (uint32_t)BN, CU_TENSOR_MAP_SWIZZLE_128B)) {
-        delete e;
-        return nullptr;
-    }
-    cache.push_back(e);
-    return &e->m;
-}
-
 template <int QT, int BN, int EPI>
 cudaError_t run(const QMat &W, int T, const __half *A, const __half *A_lo, const FwdArgs &a, int layer, cudaStream_t s) {
     constexpr int MT = 2;
@@ -459,13 +510,12 @@ cudaError_t run(const QMat &W, int T, const __half *A, const __half *A_lo, const
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    const CUtensorMap *mb = act_map(A, W.K, T, BN), *mb2 = act_map(A_lo, W.K, T, BN);
-    if (!mb || !mb2 || !W.tm_ready) return cudaErrorInvalidValue;
+    if (!W.tm_ready) return cudaErrorInvalidValue;
     GemmParams p{W.N, T, W.K / BK, 0};
     const int m_tiles = (W.N_pad + 2 * BM - 1) / (2 * BM);   // rows past N_pad read as zeros
     dim3 grid(m_tiles, (T + BN - 1) / BN);
-    return launch_pdl(kern, grid, dim3(192), (size_t)C::SMEM, s, *mb, *mb2, *reinterpret_cast<const CUtensorMap *>(W.tm_w),
-                      p, a, layer);
+    return launch_pdl(kern, grid, dim3(320), (size_t)C::SMEM, s, A, A_lo, W.K,
+                      *reinterpret_cast<const CUtensorMap *>(W.tm_w), p, a, layer);
 }
 
 template <int QT, int BN>
@@ -484,11 +534,11 @@ cudaError_t dispatch(const QMat &W, Epi epi, int T, const __half *A, const __hal
 
 bool make_weight_maps(QMat &W) {
     // the storage as [N_pad / 4 quads][quad_bytes] in 4-byte units; a box is one block pair
-    // (quants and scales) of 32 quads
+    // (quants and scales) of 64 quads: both 128-row tiles of a CTA
     const int pb = W.pair_bytes();
     CUtensorMap *m = reinterpret_cast<CUtensorMap *>(W.tm_w);
     W.tm_ready = tc::make_map_2d(m, W.w, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, W.quad_bytes() / 4, (uint64_t)W.N_pad / 4,
-                                 W.quad_bytes(), (uint32_t)(pb / 4), (uint32_t)(tc::BM / 4), CU_TENSOR_MAP_SWIZZLE_NONE);
+                                 W.quad_bytes(), (uint32_t)(pb / 4), (uint32_t)(tc::BM / 2), CU_TENSOR_MAP_SWIZZLE_NONE);
     return W.tm_ready;
 }
 
