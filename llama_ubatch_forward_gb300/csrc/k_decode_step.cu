@@ -62,7 +62,7 @@ cudaError_t decode_step_prepare(DecodeStep &ds, const DevLayer *layers, int n_la
         if (e && e[0] == '0') return cudaSuccess;
     }
     const int ql = layers[0].qkv.type, G = a.H / a.KV;
-    if (head.type != Q8) return cudaSuccess;
+    if (head.type != Q8 || a.KV > 48) return cudaSuccess;   // per-head counters: 48 in the sync block
     const void *kern = ql == Q4 ? step_kernel_q4(a.hd, G) : ql == Q8 ? step_kernel_q8(a.hd, G) : nullptr;
     if (!kern) return cudaSuccess;
 
@@ -113,9 +113,9 @@ cudaError_t decode_step_prepare(DecodeStep &ds, const DevLayer *layers, int n_la
     // barriers, then the phase table and the attention unit's page ids
     const int bars = kMaxStages * 8 + (int)(ph.size() * sizeof(StepPhase)) + kMaxUnitPages * 4;
     const long room = (long)optin - (long)fa.sharedSizeBytes - x_bytes - bars - 64;
-    // 4 slots: enough copies in flight to keep HBM streaming, few enough that the CTA's own
-    // loads (activations, attention) do not queue behind many of them
-    const int slots = (int)std::min<long>(4, room > 0 ? room / slot : 0);
+    // 5 slots where they fit: stages are consumed in pairs, so a pair is in flight while one is
+    // used; few enough that the CTA's own loads (activations, attention) do not queue behind many
+    const int slots = (int)std::min<long>(5, room > 0 ? room / slot : 0);
     if (slots < 3) return cudaSuccess;
     const size_t smem = (size_t)x_bytes + (size_t)slots * slot + bars;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -128,8 +128,8 @@ cudaError_t decode_step_prepare(DecodeStep &ds, const DevLayer *layers, int n_la
 
     e = cudaMalloc(&ds.ph, ph.size() * sizeof(StepPhase));
     if (e == cudaSuccess) e = cudaMemcpy(ds.ph, ph.data(), ph.size() * sizeof(StepPhase), cudaMemcpyHostToDevice);
-    if (e == cudaSuccess) e = cudaMalloc(&ds.sync, 64);
-    if (e == cudaSuccess) e = cudaMemset(ds.sync, 0, 64);
+    if (e == cudaSuccess) e = cudaMalloc(&ds.sync, 256);
+    if (e == cudaSuccess) e = cudaMemset(ds.sync, 0, 256);
     if (e != cudaSuccess) {
         decode_step_release(ds);
         return e;
@@ -163,7 +163,7 @@ void decode_step_release(DecodeStep &ds) {
 
 cudaError_t decode_step_reset(const DecodeStep &ds, const FwdArgs &a, cudaStream_t s) {
     if (!ds.sync) return cudaSuccess;
-    cudaError_t e = cudaMemsetAsync(ds.sync, 0, 64, s);
+    cudaError_t e = cudaMemsetAsync(ds.sync, 0, 256, s);
     if (e == cudaSuccess) e = cudaMemsetAsync(a.att_cnt, 0, (size_t)a.KV * sizeof(int32_t), s);
     return e;
 }
@@ -189,6 +189,7 @@ cudaError_t launch_decode_step(const DecodeStep &ds, const FwdArgs &a, const voi
     ns = (n_att + chunk - 1) / chunk;
     sa.att_ns = ns;
     sa.att_chunk = chunk;
+    sa.kvh_quads = (a.H / a.KV + 2) * a.hd / 4;
     sa.tok_embd = reinterpret_cast<const uint8_t *>(tok_embd);
     sa.t_embd = t_embd;   // the ABI type codes equal QType
     sa.amax_dst = amax_dst;

@@ -20,7 +20,9 @@
 //     polling); data written inside the step is read through L2 (ld.cg), never from L1;
 //   * attention over the cache is split into (KV head, cell range) units, one per CTA, each
 //     merged in the CTA and across splits by the last CTA of a KV head to arrive; the unit's
-//     cached K/V lines are prefetched into L2 at the start of the layer, before QKV runs.
+//     cached K/V lines are prefetched into L2 at the start of the layer, before QKV runs. A
+//     unit does not wait for the whole QKV phase: each QKV epilogue publishes its row quad on a
+//     per-KV-head counter (release), and the unit starts once its head's q, k and v rows are in.
 // Every wait is bounded: a timed-out wait sets the error word, the CTA stops, and the others
 // see the error word and stop at their next barrier.
 //
@@ -53,8 +55,10 @@ struct StepArgs {
     int slot_bytes;        // ring slot size (>= every phase's stage bytes)
     int slots;
     int x_bytes;           // staged activations / attention scratch at the start of shared memory
-    unsigned int *sync;    // [0] barrier arrivals, [1] arrivals at the end; zero between launches
+    unsigned int *sync;    // [0] barrier arrivals, [1] arrivals at the end, [16 + h] QKV quads of KV
+                           // head h written so far; zero between launches
     int att_ns, att_chunk; // attention splits of this token: att_ns ranges of att_chunk cells
+    int kvh_quads;         // QKV row quads per KV head and layer: (n_head / n_head_kv + 2) head_dim / 4
     const uint8_t *tok_embd;
     int t_embd;
     int32_t *amax_dst;     // argmax of the logits row (n_out == 1)
@@ -382,7 +386,19 @@ __device__ __forceinline__ void step_attention(const FwdArgs &a, int layer, int 
     }
     consumer_sync();
     if (!*flag) return;
-    // weights w_s = exp(M_s - M*) / L* per query head (one warp per head, lanes over splits)
+    // the partial sums of this thread's outputs for the first 24 splits are loaded first, so their
+    // round trip overlaps the one of the weights w_s = exp(M_s - M*) / L* (one warp per query
+    // head, lanes over splits)
+    constexpr int PER = (G * HD + 255) / 256, NB = 24;
+    float av[PER][NB];
+#pragma unroll
+    for (int q = 0; q < PER; ++q) {
+        const int idx = threadIdx.x + 256 * q;
+        const int g = idx / HD, dd = idx % HD;
+#pragma unroll
+        for (int u = 0; u < NB; ++u)
+            av[q][u] = idx < G * HD && u < ns ? __ldcg(part + ((prow + u) * G + g) * (HD + 2) + 2 + dd) : 0.f;
+    }
     float *sw = sm_acc;   // [64][G]
     for (int g = warp; g < G; g += NW) {
         float ms[2], ls[2];
@@ -409,20 +425,18 @@ __device__ __forceinline__ void step_attention(const FwdArgs &a, int layer, int 
             if (lane + 32 * h < ns) sw[(lane + 32 * h) * G + g] = e[h] / L;
     }
     consumer_sync();
-#pragma unroll 1
-    for (int idx = threadIdx.x; idx < G * HD; idx += 256) {
+#pragma unroll
+    for (int q = 0; q < PER; ++q) {
+        const int idx = threadIdx.x + 256 * q;
+        if (idx >= G * HD) continue;
         const int g = idx / HD, dd = idx % HD;
         float o = 0.f;
+#pragma unroll
+        for (int u = 0; u < NB; ++u)
+            if (u < ns) o = fmaf(sw[u * G + g], av[q][u], o);
 #pragma unroll 1
-        for (int s0 = 0; s0 < ns; s0 += 16) {   // 16 independent loads in flight
-            float v[16];
-#pragma unroll
-            for (int u = 0; u < 16; ++u)
-                v[u] = s0 + u < ns ? __ldcg(part + ((prow + s0 + u) * G + g) * (HD + 2) + 2 + dd) : 0.f;
-#pragma unroll
-            for (int u = 0; u < 16; ++u)
-                if (s0 + u < ns) o = fmaf(sw[(s0 + u) * G + g], v[u], o);
-        }
+        for (int s0 = NB; s0 < ns; ++s0)   // splits past the first 24 (long contexts of small models)
+            o = fmaf(sw[s0 * G + g], __ldcg(part + ((prow + s0) * G + g) * (HD + 2) + 2 + dd), o);
         a.o32[(size_t)(kvh * G + g) * HD + dd] = o;
     }
     if (threadIdx.x == 0) a.att_cnt[kvh] = 0;
@@ -666,7 +680,7 @@ __device__ __forceinline__ void dots_rt(const StepPhase &P, const GemvMap &mp, c
 // quad, or for SwiGLU the gate and up rows of 2 features.
 __device__ __forceinline__ void epilogue_rt(const StepPhase &P, const GemvMap &mp, int epi, const FwdArgs &a,
                                             int layer, int st, int e, const float *pk, float rs, const EpiIn &ein,
-                                            unsigned long long &best) {
+                                            unsigned long long &best, unsigned *kvh_cnt) {
     const GemvParams &p = P.p;
     const int n_wg = 8 / mp.G;   // warps of a row group: partial sums per row
     const bool swiglu = epi == EPI_SWIGLU;
@@ -691,7 +705,17 @@ __device__ __forceinline__ void epilogue_rt(const StepPhase &P, const GemvMap &m
             epi_swiglu2<false>(a, 0, 4 * (task >> 1) + 2 * (task & 1), g2, u2);
             break;
         }
-        case EPI_QKV: epi_quad_in<EPI_QKV>(a, layer, 0, r0, p.N, v, ein, bkey); break;
+        case EPI_QKV: {
+            epi_quad_in<EPI_QKV>(a, layer, 0, r0, p.N, v, ein, bkey);
+            // publish the quad on its KV head's counter (release: after this thread's stores)
+            const int qw = a.H * a.hd, kw = a.KV * a.hd;
+            if (r0 < qw + 2 * kw) {
+                const int sh = __ffs(a.hd) - 1;
+                const int kvh = r0 < qw ? (r0 >> sh) / (a.H / a.KV) : ((r0 - qw) >> sh) % a.KV;
+                asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(kvh_cnt + kvh) : "memory");
+            }
+            break;
+        }
         case EPI_RESID: epi_quad_in<EPI_RESID>(a, layer, 0, r0, p.N, v, ein, bkey); break;
         default: epi_quad_in<EPI_LOGITS>(a, layer, 0, r0, p.N, v, ein, bkey); break;
     }
@@ -770,7 +794,7 @@ __device__ __noinline__ void step_gemv(const StepArgs &s, const StepPhase *tab, 
             if (!dead) dots_rt<QT>(P, mp, ring + (size_t)slot1 * s.slot_bytes, xq, bk, pk1);
         }
         consumer_sync();
-        if (epi_thread) epilogue_rt(P, mp, epi, a, layer, my_st, e, threadIdx.x < 32 ? pk0 : pk1, rs, ein, best);
+        if (epi_thread) epilogue_rt(P, mp, epi, a, layer, my_st, e, threadIdx.x < 32 ? pk0 : pk1, rs, ein, best, s.sync + 16);
         // every warp is past its reads of the slots (the barrier above): refill them
         if (threadIdx.x == kFeedThread && !dead) {
             feed_one(s, tab, n_ph, a.L, f, ring, full);
@@ -873,8 +897,26 @@ __global__ void __launch_bounds__(256, 1) k_decode_step(const __grid_constant__ 
                 if (jf + 32 * i < ac1)
                     kv_group_load<HD>(a, l, u_kvh, unit_page(a, pages, page0, jf + 32 * i), jf + 32 * i, ac1, kvq[i]);
         }
-        gs.dead = !grid_sync(a, bar, ++n_bar, gs.dead, &s_ok);
-        if (gs.dead) break;
+        if (has_unit) {   // this unit's KV head: all its q, k and v quads of layer l written
+            if (threadIdx.x == 0) {
+                const unsigned target = (unsigned)(l + 1) * (unsigned)s.kvh_quads;
+                bool ok = !gs.dead;
+                if (ok) {
+                    ok = false;
+                    for (uint32_t i = 0; i < kSpinLimit; ++i) {
+                        if (ld_acquire_u32(s.sync + 16 + u_kvh) >= target) {
+                            ok = true;
+                            break;
+                        }
+                        if ((i & 255u) == 255u && ld_volatile_i32(a.err)) break;
+                    }
+                    if (!ok) atomicExch(a.err, 1);
+                }
+                s_ok = ok;
+            }
+            consumer_sync();
+            gs.dead = !s_ok;
+        }
         // attention
         step_trace(a, tp + 1, 0);
         if (has_unit)
@@ -927,6 +969,7 @@ __global__ void __launch_bounds__(256, 1) k_decode_step(const __grid_constant__ 
             }
             bar[0] = 0u;
             bar[1] = 0u;
+            for (int h = 0; h < a.KV; ++h) bar[16 + h] = 0u;
         }
     }
 }
