@@ -30,10 +30,12 @@ import numpy as np  # noqa: E402
 
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
-# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the weight-streaming
-# GEMV averaged over the 129 launches of one 8B decode token, from an ncu capture of the current
-# kernel: QKV 14.24 MB, O 9.51, gate/up 66.41, down 33.15 per layer, head 558.81 once.
-GEMV_NCU_TRAFFIC_BYTES = (32 * (14.24 + 9.51 + 66.41 + 33.15) + 558.81) / 129 * 1e6
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the persistent
+# decode step on the 8B shape, from the ncu launch list of the current kernel (decode at ~520
+# attended positions): 4645.03 MB, of which the K/V of those positions are 68.2 MB. The K/V part
+# is rescaled to the context of the run being reported.
+STEP_NCU_TRAFFIC_BYTES = 4645.03e6
+STEP_NCU_KV_POSITIONS = 520.5
 
 
 def log(*a):
@@ -101,8 +103,12 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------------- workload
 def workload_args(a):
+    import dataclasses
+
     import synth
     cfg = synth.CONFIGS[a.config]
+    if a.layers:   # a shallower model of the same shape (the first layers of the same draws), for profiling
+        cfg = dataclasses.replace(cfg, n_layer=a.layers)
     return cfg, a.prompt, a.decode_steps, a.n_ubatch
 
 
@@ -248,15 +254,16 @@ def run_lcx(a, rank, world):
     g = prof["gemv"]
     # one launch per decode token: the persistent step kernel (weights, KV and head in one launch)
     step_kernel = g["launches"] == n_dec and prof["attention"]["launches"] == 0
+    kv_pos_bytes = cfg.n_layer * cfg.n_head_kv * cfg.head_dim * 2 * 2   # K and V of one position, all layers
     if step_kernel:
         dom_kernel = "k_decode_step (persistent: every matmul, attention and the head of a token in one launch)"
         dom_traffic = None
+        if cfg.name == "8b" and not a.layers:
+            avg_pos = n_prompt + (n_dec + 1) / 2.0
+            dom_traffic = round(STEP_NCU_TRAFFIC_BYTES + kv_pos_bytes * (avg_pos - STEP_NCU_KV_POSITIONS))
     else:
         dom_kernel = "gemv (weight-streaming, all decode matmuls)"
-        dom_traffic = GEMV_NCU_TRAFFIC_BYTES
-    gemv_gbs = g["bytes"] / (g["ms"] / 1e3) / 1e9 if g["ms"] else 0.0
-    gm_ = prof_pre["gemm"]
-    gemm_tf = gm_["flops"] / (gm_["ms"] / 1e3) / 1e12 if gm_["ms"] else 0.0
+        dom_traffic = None   # separate launches (LCX_DECODE_STEP=0): no current counters
     dec_bytes = decode_bytes_per_step(cfg, host, n_prompt, n_dec)
     dec_gbs = dec_bytes / (sum(dec_ms) / a.steps / 1e3) / 1e9
     pf = prefill_flops(cfg, n_prompt)
@@ -278,7 +285,7 @@ def run_lcx(a, rank, world):
         "config": {"workload": f"{cfg.name}: {n_prompt}-token prompt in ubatches of {n_ub}, then {n_dec} greedy "
                                f"decode steps", "n_ctx": cfg.n_ctx, "n_ubatch": n_ub,
                    "l2": "inputs larger than L2 (4.5 GB of weights streamed per decode step)",
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": f"replicas x{world}", **({"layers": cfg.n_layer} if a.layers else {})},
         "prefill": {"value": round(prefill_tps, 1), "unit": "tokens/s",
                     "achieved_tflops": round(pre_tf, 2),
                     "roofline_frac": round(pre_tf / bf16, 4)},
@@ -363,6 +370,8 @@ def main():
     ap.add_argument("--n-ubatch", type=int, default=512)
     ap.add_argument("--n-ctx", type=int, default=0, help="override the context size (0: the config's)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="profiling only: the first N layers of the model (0: all); the line is then not the workload's")
     a = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
