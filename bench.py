@@ -112,6 +112,14 @@ def workload_args(a):
     return cfg, a.prompt, a.decode_steps, a.n_ubatch
 
 
+def workload_config(a, cfg, n_prompt, n_dec, n_ub, world):
+    """The `config` of the JSON line, the same for both arms."""
+    return {"workload": f"{cfg.name}: {n_prompt}-token prompt in ubatches of {n_ub}, then {n_dec} greedy "
+                        f"decode steps", "n_ctx": a.n_ctx or cfg.n_ctx, "n_ubatch": n_ub,
+            "l2": "inputs larger than L2 (4.5 GB of weights streamed per decode step)",
+            "parallelism": f"replicas x{world}", **({"layers": cfg.n_layer} if a.layers else {})}
+
+
 def decode_bytes_per_step(cfg, host, pos0, n_steps):
     """Algorithmic HBM bytes of the decode steps: all weights as stored (the embedding row only)
     plus the K/V of every attended cell."""
@@ -282,10 +290,7 @@ def run_lcx(a, rank, world):
         "vs_baseline": None,
         "dtype": "q4_0 weights x f32 (decode GEMV), f16 x f16 -> f32 (prefill matmul)",
         "data": "synthetic (seeded N(0,0.02) weights, uniform token ids)",
-        "config": {"workload": f"{cfg.name}: {n_prompt}-token prompt in ubatches of {n_ub}, then {n_dec} greedy "
-                               f"decode steps", "n_ctx": cfg.n_ctx, "n_ubatch": n_ub,
-                   "l2": "inputs larger than L2 (4.5 GB of weights streamed per decode step)",
-                   "parallelism": f"replicas x{world}", **({"layers": cfg.n_layer} if a.layers else {})},
+        "config": workload_config(a, cfg, n_prompt, n_dec, n_ub, world),
         "prefill": {"value": round(prefill_tps, 1), "unit": "tokens/s",
                     "achieved_tflops": round(pre_tf, 2),
                     "roofline_frac": round(pre_tf / bf16, 4)},
@@ -352,7 +357,7 @@ def run_reference(a, rank, world):
         "value": round(v, 4), "unit": "tokens/s", "n_gpus": world, "steps": a.steps, "warmup": a.warmup,
         "ms_per_step": round(1e3 * sum(times) / a.steps, 1), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,0.02) weights, uniform token ids)",
-        "config": {"workload": f"{cfg.name}: bounded sample of the decode workload", "n_ctx": cfg.n_ctx},
+        "config": workload_config(a, cfg, n_prompt, n_dec, n_ub, world),
         "cpu_baseline": {"value": round(v, 4), "unit": "tokens/s", "cores": n, "kind": "oracle", "sample": sample},
         "e2e": {"value": round(v, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
