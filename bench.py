@@ -272,6 +272,9 @@ def run_lcx(a, rank, world):
     else:
         dom_kernel = "gemv (weight-streaming, all decode matmuls)"
         dom_traffic = None   # separate launches (LCX_DECODE_STEP=0): no current counters
+    gemv_gbs = g["bytes"] / (g["ms"] / 1e3) / 1e9 if g["ms"] else 0.0
+    gm_ = prof_pre["gemm"]
+    gemm_tf = gm_["flops"] / (gm_["ms"] / 1e3) / 1e12 if gm_["ms"] else 0.0
     dec_bytes = decode_bytes_per_step(cfg, host, n_prompt, n_dec)
     dec_gbs = dec_bytes / (sum(dec_ms) / a.steps / 1e3) / 1e9
     pf = prefill_flops(cfg, n_prompt)

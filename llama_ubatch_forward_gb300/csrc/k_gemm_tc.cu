@@ -14,8 +14,8 @@
 //               W A_lo into the same accumulator, so the activations keep about 22 bits and only
 //               the f16 rounding of the dequantised weights remains; each stage's tcgen05.commit
 //               frees its shared-memory slot;
-//   warps 2..9  load the activation tiles [BN][64] f16 (high and low parts) with cp.async, S - 1
-//               stages ahead, writing the 128-byte swizzle themselves; dequantise the raw blocks of
+//   warps 2..9  load the activation tiles [BN][64] f16 (high and low parts) with cp.async, S - 2
+//               (S - 1 with fewer than 5 slots) stages ahead, writing the 128-byte swizzle themselves; dequantise the raw blocks of
 //               their row (warps 2..5 tile 0, warps 6..9 tile 1) into the K-major SWIZZLE_128B f16
 //               tile the MMA reads ((q - 8) or q is exact in f16, then one f16 multiply by the
 //               block scale); then run their tile's epilogue from TMEM with tcgen05.ld.
@@ -151,6 +151,7 @@ __device__ __forceinline__ void dequant_row(const uint8_t *rq, uint8_t *atile, i
             const uint4 w = *reinterpret_cast<const uint4 *>(q + blk * 16);
             const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
             const __half2 off = __float2half2_rn(1032.f);
+            const __half2 sixteenth = __float2half2_rn(0.0625f), m72 = __float2half2_rn(-72.f);
 #pragma unroll
             for (int h = 0; h < 2; ++h) {   // bytes 0..7 (h = 0) or 8..15 (h = 1)
                 uint32_t lo[4], hi[4];
@@ -158,16 +159,18 @@ __device__ __forceinline__ void dequant_row(const uint8_t *rq, uint8_t *atile, i
                 for (int wi = 0; wi < 2; ++wi) {
                     const uint32_t t0 = __byte_perm(ws[2 * h + wi], 0u, 0x4140u);   // [b0, 0, b1, 0]
                     const uint32_t t1 = __byte_perm(ws[2 * h + wi], 0u, 0x4342u);   // [b2, 0, b3, 0]
+                    // low nibbles as f16 1024 + q, high nibbles as 1024 + 16 q (no shift needed)
                     lo[2 * wi] = (t0 & 0x000F000Fu) | 0x64006400u;
                     lo[2 * wi + 1] = (t1 & 0x000F000Fu) | 0x64006400u;
-                    hi[2 * wi] = ((t0 >> 4) & 0x000F000Fu) | 0x64006400u;
-                    hi[2 * wi + 1] = ((t1 >> 4) & 0x000F000Fu) | 0x64006400u;
+                    hi[2 * wi] = (t0 & 0x00F000F0u) | 0x64006400u;
+                    hi[2 * wi + 1] = (t1 & 0x00F000F0u) | 0x64006400u;
                 }
                 uint32_t olo[4], ohi[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     __half2 a = __hmul2(__hsub2(*reinterpret_cast<__half2 *>(&lo[e]), off), d2);
-                    __half2 b = __hmul2(__hsub2(*reinterpret_cast<__half2 *>(&hi[e]), off), d2);
+                    // (1024 + 16 q) / 16 - 72 = q - 8, exact in one fused multiply-add
+                    __half2 b = __hmul2(__hfma2(*reinterpret_cast<__half2 *>(&hi[e]), sixteenth, m72), d2);
                     olo[e] = *reinterpret_cast<uint32_t *>(&a);
                     ohi[e] = *reinterpret_cast<uint32_t *>(&b);
                 }
@@ -323,10 +326,14 @@ __global__ void __launch_bounds__(320, 1)
                 }
             }
         };
+        // activations run D steps ahead: with 5 or more slots, into the slot of step j - 2 (free
+        // once the A slot of step j - 2 is, so no wait on the MMAs of step j - 1 delays the
+        // dequantisation); with fewer, into the slot of step j - 1
+        constexpr int D = S >= 5 ? S - 2 : S - 1;
         bool ok = true;
         LCX_PDL_WAIT();   // the activations are the previous kernel's output
         LCX_PDL_TRIGGER();
-        for (int j = 0; j < S - 1; ++j) {   // stages 0 .. S-2 ahead (their slots start free)
+        for (int j = 0; j < D; ++j) {   // stages 0 .. D-1 ahead (their slots start free)
             if (j < nk) load_act(j);
             asm volatile("cp.async.commit_group;" ::: "memory");
         }
@@ -340,14 +347,14 @@ __global__ void __launch_bounds__(320, 1)
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic writes -> tensor-core reads
             __syncwarp();
             if (lane == 0) mbar_arrive(&full_a[aslot]);
-            // stage j's activation copies have landed: of the S - 1 + j groups committed so far,
-            // all but the S - 2 newest
-            asm volatile("cp.async.wait_group %0;" ::"n"(S - 2) : "memory");
+            // stage j's activation copies have landed: of the D + j groups committed so far, all
+            // but the D - 1 newest
+            asm volatile("cp.async.wait_group %0;" ::"n"(D - 1) : "memory");
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
             if (lane == 0) mbar_arrive(&full_b[slot]);
-            // prefetch stage j + S - 1 into the slot stage j - 1 used, once its MMAs are done
-            const int jn = j + S - 1;
+            // prefetch stage j + D into the slot stage j + D - S used, once its MMAs are done
+            const int jn = j + D;
             if (jn < nk) {
                 if (jn >= S) ok = __all_sync(0xffffffffu, mbar_wait(&empty[jn % S], ((jn / S) - 1) & 1));
                 if (!ok) break;
