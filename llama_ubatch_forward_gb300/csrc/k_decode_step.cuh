@@ -781,17 +781,15 @@ __device__ __noinline__ void step_gemv(const StepArgs &s, const StepPhase *tab, 
         EpiIn ein{};
         if (epi_thread && epi == EPI_RESID) ein = epi_load<EPI_RESID>(a, 0, (my_st * tps + e) * 4, P.p.N);
         if (epi_thread && epi == EPI_QKV) ein = epi_load<EPI_QKV>(a, 0, (my_st * tps + e) * 4, P.p.N);
-        if (!dead && !mbar_wait(&full[slot0], (k / s.slots) & 1)) {
-            dead = true;
-            atomicExch(a.err, 1);
-        }
-        if (!dead) dots_rt<QT>(P, mp, ring + (size_t)slot0 * s.slot_bytes, xq, bk, pk0);
-        if (two) {
-            if (!dead && !mbar_wait(&full[slot1], ((k + 1) / s.slots) & 1)) {
+        // the pair's two stages through one copy of the dot-product code (instruction cache)
+#pragma unroll 1
+        for (int u = 0; u < (two ? 2 : 1); ++u) {
+            const int slot = u ? slot1 : slot0;
+            if (!dead && !mbar_wait(&full[slot], ((k + u) / s.slots) & 1)) {
                 dead = true;
                 atomicExch(a.err, 1);
             }
-            if (!dead) dots_rt<QT>(P, mp, ring + (size_t)slot1 * s.slot_bytes, xq, bk, pk1);
+            if (!dead) dots_rt<QT>(P, mp, ring + (size_t)slot * s.slot_bytes, xq, bk, u ? pk1 : pk0);
         }
         consumer_sync();
         if (epi_thread) epilogue_rt(P, mp, epi, a, layer, my_st, e, threadIdx.x < 32 ? pk0 : pk1, rs, ein, best, s.sync + 16);
