@@ -162,6 +162,39 @@ def cpu_baseline(host, cfg, n_prompt=4, n_decode=2):
 
 host_prompt_cache = {}
 
+SAMPLER_CHAIN = dict(top_k=40, top_p=0.95, min_p=0.05, temp=0.8)
+
+
+def time_sampler(n_vocab, stream, iters=50):
+    """Device time of lcx_sample (the sampler chain) on logits rows of the model's vocabulary:
+    one row (a batch-1 decode step) and 64 rows (one per sequence of the multi-sequence
+    workload), CUDA events on the launching stream after warm-up. Not part of the greedy
+    workload's timed region."""
+    import torch
+
+    import llama_ubatch_forward_gb300 as lcx
+    import synth
+    out = {"chain": "top_k 40, top_p 0.95, min_p 0.05, temp 0.8 (the draw: u uniform)", "n_vocab": n_vocab}
+    for rows in (1, 64):
+        x = synth.normal(0x5A11, 1, rows * n_vocab, 0.0, 2.0).reshape(rows, n_vocab).astype(np.float32)
+        x[:, :: max(1, n_vocab // 7)] += 8.0           # a few strong candidates over the background
+        dx = torch.from_numpy(x).to("cuda")
+        du = torch.from_numpy((synth.uniform_int(0x5A11, 2, rows, 0, 1 << 24) / float(1 << 24)).astype(np.float32)).cuda()
+        tok = torch.empty(rows, dtype=torch.int32, device="cuda")
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                lcx.sample(dx, du, tokens_out=tok, stream=stream, **SAMPLER_CHAIN)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(iters):
+                rc, _ = lcx.sample(dx, du, tokens_out=tok, stream=stream, **SAMPLER_CHAIN)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        assert rc == 0, rc
+        out[f"us_per_call_{rows}_rows"] = round(e0.elapsed_time(e1) * 1e3 / iters, 2)
+    return out
+
 
 def run_lcx(a, rank, world):
     import torch
@@ -257,6 +290,7 @@ def run_lcx(a, rank, world):
             tok = int(am[0])
         t_e2e += time.perf_counter() - s
     e2e_tps = world * e2e_steps * n_dec / t_e2e
+    sampler = time_sampler(cfg.n_vocab, stream)
 
     hbm, bf16, bf16_sus, src = peaks()
     g = prof["gemv"]
@@ -317,6 +351,7 @@ def run_lcx(a, rank, world):
                 "d2h_bytes_per_step": 4 * (1 + n_dec),
                 "how": "lcx_decode per token with host token ids and host argmax (one sync per token)"},
         "gpu_launches": int(launches_per_step * a.steps),
+        "sampler": sampler,
         "clocks": clk,
     }
     if rank == 0:

@@ -250,6 +250,43 @@ int32_t lcx_attention_noalloc(int32_t T, int32_t n_head, int32_t n_head_kv, int3
                               int32_t max_pages, const int32_t *pos, const int32_t *seq, int32_t max_pos, float *out,
                               void *cuda_stream);
 
+/* Parameters of the sampler chain (article, "Sampler chain", after step 14: a repeat penalty,
+ * then the cut-offs top-k, top-p and min-p, then temperature, then one token is chosen).
+ *   penalty_repeat: > 0; 1 = off. Each distinct history token's logit is divided by it when
+ *                   positive and multiplied by it otherwise (both lower it for a value > 1).
+ *   top_k:          keep the k largest logits; <= 0 or >= n_vocab = off.
+ *   top_p:          keep the shortest run of candidates, largest logit first, whose softmax
+ *                   probability over the candidates left by top-k reaches top_p (at least
+ *                   one); >= 1 = off.
+ *   min_p:          keep the candidates whose probability is >= min_p times the leader's, i.e.
+ *                   logit >= max + ln(min_p); <= 0 = off.
+ *   temp:           <= 0: greedy (the largest logit, lowest id on ties). Otherwise the token is
+ *                   drawn from the remaining candidates with weights exp((logit - max) / temp). */
+typedef struct {
+    float penalty_repeat;
+    int32_t top_k;
+    float top_p;
+    float min_p;
+    float temp;
+} lcx_sampler;
+
+/* Runs the sampler chain on the device over n_rows logits rows and writes one token per row
+ * (the sampler running on the backend: only the token leaves the kernel).
+ *   logits:     DEVICE float32 [n_rows][n_vocab] (as lcx_decode writes them); finite values.
+ *   history:    DEVICE int32 [n_rows][n_history] tokens for the repeat penalty (entries outside
+ *               [0, n_vocab) are ignored), or NULL with n_history == 0.
+ *   u:          DEVICE float32 [n_rows], the random numbers of the draws, in [0, 1); may be NULL
+ *               when temp <= 0. The draw walks the remaining candidates in increasing token id
+ *               and returns the first whose running weight exceeds u times the total weight.
+ *   tokens_out: DEVICE int32 [n_rows].
+ * Candidates are ordered by logit, lower token id first among equal logits. Decisions are
+ * taken in float32: a token within float32 rounding of a top-p, min-p or draw boundary may
+ * fall on either side of it. n_vocab <= 262144; n_rows == 0 is a no-op. Stream-ordered on cuda_stream; allocates
+ * nothing. Returns LCX_OK, LCX_INVALID or LCX_COMPUTE_FAILED. */
+int32_t lcx_sample(const lcx_sampler *params, const float *logits, int32_t n_rows, int32_t n_vocab,
+                   const int32_t *history, int32_t n_history, const float *u, int32_t *tokens_out,
+                   void *cuda_stream);
+
 /* Last CUDA error string seen by the library in this process ("" if none). */
 const char *lcx_last_error(void);
 

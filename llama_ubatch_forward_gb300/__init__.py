@@ -21,7 +21,7 @@ SYMBOLS = ("lcx_model_create", "lcx_model_free", "lcx_ctx_create", "lcx_ctx_free
            "lcx_decode_greedy", "lcx_kv_clear", "lcx_seq_pos_max", "lcx_n_outputs", "lcx_set_abort",
            "lcx_get_stats", "lcx_ctx_create_host_only", "lcx_get_rows", "lcx_last_error", "lcx_set_profiling",
            "lcx_get_profile", "lcx_attention_workspace_size", "lcx_attention", "lcx_attention_noalloc",
-           "lcx_kv_read", "lcx_get_trace")
+           "lcx_kv_read", "lcx_get_trace", "lcx_sample")
 
 
 def build(force: bool = False) -> str:
@@ -49,6 +49,11 @@ class lcx_weights(ctypes.Structure):
 class lcx_batch(ctypes.Structure):
     _fields_ = [("n_tokens", ctypes.c_int32), ("token", ctypes.c_void_p), ("pos", ctypes.c_void_p),
                 ("seq_id", ctypes.c_void_p), ("logits", ctypes.c_void_p)]
+
+
+class lcx_sampler(ctypes.Structure):
+    _fields_ = [("penalty_repeat", ctypes.c_float), ("top_k", ctypes.c_int32), ("top_p", ctypes.c_float),
+                ("min_p", ctypes.c_float), ("temp", ctypes.c_float)]
 
 
 class lcx_stats(ctypes.Structure):
@@ -106,6 +111,8 @@ def lib():
                                     ctypes.c_size_t, vp]
         L.lcx_attention_noalloc.restype = i32
         L.lcx_attention_noalloc.argtypes = [i32, i32, i32, i32, vp, vp, vp, i32, vp, i32, vp, vp, i32, vp, vp]
+        L.lcx_sample.restype = i32
+        L.lcx_sample.argtypes = [ctypes.POINTER(lcx_sampler), vp, i32, i32, vp, i32, vp, vp, vp]
         L.lcx_get_trace.restype = i32
         L.lcx_get_trace.argtypes = [vp, vp, i32]
         L.lcx_kv_read.restype = i32
@@ -283,3 +290,19 @@ def attention_noalloc(q, k_cache, v_cache, page_table, pos, seq, max_pos: int, o
     return lib().lcx_attention_noalloc(T, H, n_kv, hd, _ptr(q), _ptr(k_cache), _ptr(v_cache), n_pages,
                                        _ptr(page_table), int(page_table.shape[1]), _ptr(pos), _ptr(seq), max_pos,
                                        _ptr(out), s)
+
+
+def sample(logits, u=None, history=None, penalty_repeat: float = 1.0, top_k: int = 0, top_p: float = 1.0,
+           min_p: float = 0.0, temp: float = 1.0, tokens_out=None, stream=None):
+    """lcx_sample over torch device tensors: logits [n_rows][n_vocab] f32, u [n_rows] f32,
+    history [n_rows][n_history] i32 or None; returns (rc, tokens_out [n_rows] i32)."""
+    import torch
+    n_rows, n_vocab = (int(x) for x in logits.shape)
+    if tokens_out is None:
+        tokens_out = torch.empty(n_rows, dtype=torch.int32, device=logits.device)
+    prm = lcx_sampler(penalty_repeat, top_k, top_p, min_p, temp)
+    n_hist = 0 if history is None else int(history.shape[1])
+    s = None if stream is None else (stream if isinstance(stream, int) else stream.cuda_stream)
+    rc = lib().lcx_sample(ctypes.byref(prm), _ptr(logits), n_rows, n_vocab, _ptr(history), n_hist, _ptr(u),
+                          _ptr(tokens_out), s)
+    return rc, tokens_out
