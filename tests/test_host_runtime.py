@@ -128,3 +128,26 @@ def test_rules_match_the_oracle_on_random_streams():
                 assert hc.n_outputs() == ro[1].shape[0]
             for s in range(3):
                 assert hc.seq_pos_max(s) == oc.seq_pos_max(s)
+
+
+def test_sample_checks_arguments_before_any_device_work():
+    """lcx_sample's host-side checks: each call below returns before touching the device (the
+    pointers are never dereferenced), so it runs without a GPU."""
+    import ctypes
+    L = lcx.lib()
+    P = lcx.lcx_sampler
+    ok = P(1.0, 40, 0.95, 0.05, 0.8)
+    fake = 16
+    by = ctypes.byref
+    assert L.lcx_sample(None, fake, 1, 100, None, 0, fake, fake, None) == lcx.LCX_INVALID        # no parameters
+    assert L.lcx_sample(by(ok), fake, -1, 100, None, 0, fake, fake, None) == lcx.LCX_INVALID     # rows < 0
+    assert L.lcx_sample(by(ok), fake, 1, 0, None, 0, fake, fake, None) == lcx.LCX_INVALID        # empty vocabulary
+    assert L.lcx_sample(by(ok), fake, 1, (1 << 18) + 1, None, 0, fake, fake, None) == lcx.LCX_INVALID
+    assert L.lcx_sample(by(ok), fake, 1, 100, None, -1, fake, fake, None) == lcx.LCX_INVALID     # history < 0
+    for pen in (0.0, -1.0, float("nan"), float("inf")):
+        assert L.lcx_sample(by(P(pen, 40, 0.95, 0.05, 0.8)), fake, 1, 100, None, 0, fake, fake, None) == lcx.LCX_INVALID
+    assert L.lcx_sample(by(ok), None, 0, 100, None, 0, None, None, None) == lcx.LCX_OK         # no rows: no-op
+    assert L.lcx_sample(by(ok), None, 1, 100, None, 0, fake, fake, None) == lcx.LCX_INVALID      # no logits
+    assert L.lcx_sample(by(ok), fake, 1, 100, None, 0, fake, None, None) == lcx.LCX_INVALID      # no output
+    assert L.lcx_sample(by(ok), fake, 1, 100, None, 3, fake, fake, None) == lcx.LCX_INVALID      # history missing
+    assert L.lcx_sample(by(ok), fake, 1, 100, None, 0, None, fake, None) == lcx.LCX_INVALID      # a draw needs u
