@@ -120,6 +120,20 @@ def workload_config(a, cfg, n_prompt, n_dec, n_ub, world):
             "parallelism": f"replicas x{world}", **({"layers": cfg.n_layer} if a.layers else {})}
 
 
+def linear_type(cfg):
+    return {2: "Q4_0", 8: "Q8_0"}.get(cfg.t_linear, str(cfg.t_linear))
+
+
+def max_over_ranks(values, device, world):
+    """Element-wise maximum of the ranks' values (the slowest replica's times) when world > 1;
+    the values themselves otherwise."""
+    import torch
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return t.tolist()
+
+
 def decode_bytes_per_step(cfg, host, pos0, n_steps):
     """Algorithmic HBM bytes of the decode steps: all weights as stored (the embedding row only)
     plus the K/V of every attended cell."""
@@ -252,10 +266,7 @@ def run_lcx(a, rank, world):
     total_ms = g0.elapsed_time(g1)
     pre_ms = [e[0].elapsed_time(e[1]) for e in evs]
     dec_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    times = torch.tensor([total_ms, sum(pre_ms), sum(dec_ms)], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(times, op=torch.distributed.ReduceOp.MAX)
-    total_ms, pre_sum, dec_sum = times.tolist()
+    total_ms, pre_sum, dec_sum = max_over_ranks([total_ms, sum(pre_ms), sum(dec_ms)], dev, world)
     decode_tps = world * a.steps * n_dec / (dec_sum / 1e3)
     prefill_tps = world * a.steps * n_prompt / (pre_sum / 1e3)
 
@@ -314,7 +325,7 @@ def run_lcx(a, rank, world):
     pf = prefill_flops(cfg, n_prompt)
     pre_tf = pf / (sum(pre_ms) / a.steps / 1e3) / 1e12
     res = {
-        "metric": f"decode tokens/s ({cfg.name}-shape Llama, Q4_0 linears, batch 1, {n_dec} greedy steps after a "
+        "metric": f"decode tokens/s ({cfg.name}-shape Llama, {linear_type(cfg)} linears, batch 1, {n_dec} greedy steps after a "
                   f"{n_prompt}-token prefill)",
         "value": round(decode_tps, 2),
         "unit": "tokens/s",
@@ -390,7 +401,7 @@ def run_reference(a, rank, world):
     v = a.steps * per / sum(times)
     sample = f"{cfg.name} model, fp64 oracle: 4-token prompt then {per} decode steps per step"
     print(json.dumps({
-        "impl": "reference", "metric": f"decode tokens/s ({cfg.name}-shape Llama, Q4_0 linears, batch 1, {n_dec} "
+        "impl": "reference", "metric": f"decode tokens/s ({cfg.name}-shape Llama, {linear_type(cfg)} linears, batch 1, {n_dec} "
                                        f"greedy steps after a {n_prompt}-token prefill)",
         "value": round(v, 4), "unit": "tokens/s", "n_gpus": world, "steps": a.steps, "warmup": a.warmup,
         "ms_per_step": round(1e3 * sum(times) / a.steps, 1), "higher_is_better": True, "scaling": "weak",
