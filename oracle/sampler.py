@@ -1,7 +1,7 @@
 """ORACLE -- test infrastructure only.
 
-The sampler chain applied to one logits row, in plain numpy. Only ``tests/`` and the bench's
-CPU-baseline leg use it; the product library never loads it and shares no code with it.
+The sampler chain applied to one logits row, in plain numpy. Only ``tests/`` use it; the
+product library never loads it and shares no code with it.
 
 The article ("llama.cpp AI LLM Engine -- how it works", section "Sampler chain", after step 14
 on ``llama_get_logits_ith``) describes sampling as a sequence of steps over one row of logits:
