@@ -179,6 +179,46 @@ host_prompt_cache = {}
 SAMPLER_CHAIN = dict(top_k=40, top_p=0.95, min_p=0.05, temp=0.8)
 
 
+PHASES = ("QKV", "attention", "O", "gate/up", "down")
+
+
+def step_timeline(ctx, prompt, am_host, cfg, n_tok):
+    """Per-phase timeline of the persistent decode step over n_tok greedy tokens after the
+    prompt, from the in-kernel %globaltimer trace (lcx_set_profiling(ctx, 2)): per phase kind the
+    mean span (first CTA in -> last CTA done), set-up (first CTA in -> last CTA done staging its
+    input, or with its attention partial) and the gap to the next phase (next phase's first CTA in
+    -> this phase's last CTA done; negative when they overlap), in microseconds."""
+    import torch
+    L = cfg.n_layer
+    per = 5 * L + 2
+    n_tok = max(1, min(n_tok, 8192 // per))
+    ctx.kv_clear()
+    assert ctx.decode(prompt, argmax_out=am_host) == 0
+    gen = torch.zeros(n_tok, dtype=torch.int32, device="cuda")
+    assert ctx.set_profiling(2) == 0
+    assert ctx.decode_greedy(0, int(am_host[0]), n_tok, gen) == 0
+    tr = ctx.trace().astype(np.float64)
+    ctx.set_profiling(False)
+    n = tr.shape[0] // per
+    tr = tr[: n * per].reshape(n, per, 4)
+    seq = tr[:, 1:1 + 5 * L]                                # [token][phase of the step][4]
+    gap = np.concatenate([seq[:, 1:, 0] - seq[:, :-1, 3], tr[:, -1:, 0] - seq[:, -1:, 3]], axis=1)
+    lay = seq.reshape(n, L, 5, 4)
+    gl = gap.reshape(n, L, 5)
+    out = {"tokens": n}
+    for i, name in enumerate(PHASES):
+        ph = lay[:, :, i]
+        out[name] = {"span_us": round(float(np.mean(ph[..., 3] - ph[..., 0])) / 1e3, 2),
+                     "setup_us": round(float(np.mean(ph[..., 2] - ph[..., 0])) / 1e3, 2),
+                     "gap_after_us": round(float(np.mean(gl[:, :, i])) / 1e3, 2)}
+    out["layer_us"] = round(float(np.mean(seq[:, -1, 3] - seq[:, 0, 0])) / L / 1e3, 2)
+    out["embed_us"] = round(float(np.mean(tr[:, 0, 3] - tr[:, 0, 0])) / 1e3, 2)
+    out["head_us"] = round(float(np.mean(tr[:, -1, 3] - tr[:, -1, 0])) / 1e3, 2)
+    out["token_us"] = round(float(np.mean(tr[:, -1, 3] - tr[:, 0, 0])) / 1e3, 2)
+    log("[bench] decode-step timeline (us, mean over %d tokens): %s" % (n, json.dumps(out)))
+    return out
+
+
 def time_sampler(n_vocab, stream, iters=50):
     """Device time of lcx_sample (the sampler chain) on logits rows of the model's vocabulary:
     one row (a batch-1 decode step) and 64 rows (one per sequence of the multi-sequence
@@ -302,6 +342,12 @@ def run_lcx(a, rank, world):
         t_e2e += time.perf_counter() - s
     e2e_tps = world * e2e_steps * n_dec / t_e2e
     sampler = time_sampler(cfg.n_vocab, stream)
+    timeline = None
+    if a.timeline > 0:
+        try:
+            timeline = step_timeline(ctx, prompt, am_host, cfg, a.timeline)
+        except Exception as ex:  # diagnostics only: never costs the bench line
+            timeline = {"error": str(ex)}
 
     hbm, bf16, bf16_sus, src = peaks()
     g = prof["gemv"]
@@ -363,6 +409,7 @@ def run_lcx(a, rank, world):
                 "how": "lcx_decode per token with host token ids and host argmax (one sync per token)"},
         "gpu_launches": int(launches_per_step * a.steps),
         "sampler": sampler,
+        **({"timeline": timeline} if timeline is not None else {}),
         "clocks": clk,
     }
     if rank == 0:
@@ -424,6 +471,8 @@ def main():
     ap.add_argument("--n-ubatch", type=int, default=512)
     ap.add_argument("--n-ctx", type=int, default=0, help="override the context size (0: the config's)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--timeline", type=int, default=0,
+                    help="diagnostics: per-phase timeline of the decode step over this many tokens (0: off)")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling only: the first N layers of the model (0: all); the line is then not the workload's")
     a = ap.parse_args()
