@@ -32,7 +32,9 @@
  *   n_tokens <= 0, a token outside [0, n_vocab), a sequence outside [0, n_seq_max), or
  *   positions of a sequence that do not continue from its last position by +1 -> -1;
  *   positions NULL -> filled from the sequence's last position + 1; logits flags NULL ->
- *   only the last token; more new cells than the cache has free -> 1, nothing committed.
+ *   only the last token; more new cells than the cache has free -> 1, nothing committed;
+ *   a flagged token whose logits are not all finite -> -3, the cells of its ubatch (consecutive
+ *   chunks of n_ubatch tokens) removed again and the rows of earlier ubatches kept.
  *
  * Readings where the pages are silent (each is a choice of this implementation):
  *   Q8_0 block = fp16 d + int8 q[32], w = d*q; Q4_0 block = fp16 d + 16 bytes, element j in
@@ -330,6 +332,22 @@ void forward_token(Ctx &c, int32_t tok, int32_t pos, int32_t seq, double *logits
     }
 }
 
+/* Removes the cells appended by tokens i0..i1 of a batch (each token appended the cell at its
+ * position of its sequence; a sequence's cells stay positions 0..n-1). */
+void rollback(Ctx &c, int32_t i0, int32_t i1, const int32_t *seq, const int32_t *pos) {
+    const int64_t W = kv_width(c.m->hp);
+    for (int32_t j = i0; j <= i1; ++j) {
+        Seq &s = c.seqs[seq[j]];
+        if (pos[j] < s.n) s.n = pos[j];
+        c.used -= 1;
+    }
+    for (auto &s : c.seqs)
+        for (size_t l = 0; l < s.k.size(); ++l) {
+            if ((int64_t)s.k[l].size() > s.n * W) s.k[l].resize((size_t)(s.n * W));
+            if ((int64_t)s.v[l].size() > s.n * W) s.v[l].resize((size_t)(s.n * W));
+        }
+}
+
 }  // namespace
 
 /* ====================================================================== C API */
@@ -430,8 +448,9 @@ int32_t orc_decode(void *cv, int32_t n_tokens, const int32_t *token, const int32
         flag[i] = flags_in ? (flags_in[i] != 0) : (int8_t)(i == n_tokens - 1);
     }
     if (c->used + n_tokens > (int64_t)c->n_ctx) return 1;
-    int32_t row = 0;
+    int32_t row = 0, row_ub = 0;
     for (int32_t i = 0; i < n_tokens; ++i) {
+        if (i % (int32_t)c->n_ubatch == 0) row_ub = row;   /* first token of a ubatch (split_simple) */
         double *lg = nullptr;
         std::vector<double> tmp;
         int32_t am = -1;
@@ -441,6 +460,14 @@ int32_t orc_decode(void *cv, int32_t n_tokens, const int32_t *token, const int32
         }
         forward_token(*c, token[i], pos[i], seq[i], lg, &am);
         if (flag[i]) {
+            /* a logit that is not finite fails the ubatch (step 13, a failed compute: its cells
+             * are removed again); earlier ubatches stay */
+            for (int32_t j = 0; j < hp.n_vocab; ++j)
+                if (!std::isfinite(lg[j])) {
+                    rollback(*c, i - i % (int32_t)c->n_ubatch, i, seq.data(), pos.data());
+                    if (n_out) *n_out = row_ub;
+                    return -3;
+                }
             if (argmax_out) argmax_out[row] = am;
             ++row;
         }

@@ -368,3 +368,28 @@ def test_default_flags_select_last_token(tiny_model):
     assert rc == 0 and lg.shape[0] == 1 and np.array_equal(lg[0], all_rows[-1])
     rc, lg, _ = _ctx(tiny_model).decode(toks, logits=[0, 1, 0, 0, 1, 0])
     assert np.array_equal(lg, all_rows[[1, 4]])            # flagged rows, in batch order
+
+
+def test_non_finite_logits_fail_their_ubatch():
+    """A flagged row whose logits are not finite is a failed compute (-3): the cells of its
+    ubatch are removed again, earlier ubatches and their rows stay."""
+    import dataclasses
+    cfg = synth.CONFIGS["tiny"]
+    host = synth.make_model(cfg)
+    bad = 7
+    emb = host.tok_embd.copy()
+    emb[bad].view(np.uint16)[:] = 0x7E00                   # an f16 NaN embedding row
+    om = oracle.Model(dataclasses.replace(host, tok_embd=emb))
+    # the bad token itself flagged: its own ubatch (the first) fails, nothing stays
+    octx = oracle.Context(om, cfg.n_ctx, 1, 2)
+    rc, lg, am = octx.decode([1, bad], logits=[1, 1])
+    assert rc == -3 and lg.shape[0] == 0 and octx.seq_pos_max(0) == -1
+    # ubatches [1, 2] [3, bad] [5]: the bad token's K/V reach token 5, whose row fails; the
+    # first two ubatches stay (positions 0..3) with the row of token 2
+    octx = oracle.Context(om, cfg.n_ctx, 1, 2)
+    rc, lg, am = octx.decode([1, 2, 3, bad, 5], logits=[0, 1, 0, 0, 1])
+    assert rc == -3 and lg.shape[0] == 1 and np.all(np.isfinite(lg))
+    assert octx.seq_pos_max(0) == 3
+    ok = oracle.Context(oracle.Model(host), cfg.n_ctx, 1, 2)
+    rc2, lg2, _ = ok.decode([1, 2], logits=[0, 1])
+    assert rc2 == 0 and np.array_equal(lg[0], lg2[0])
