@@ -200,6 +200,13 @@ int32_t lcx_get_trace(lcx_ctx *ctx, unsigned long long *out, int32_t max_slots);
  * runtime on machines without a GPU. */
 lcx_ctx *lcx_ctx_create_host_only(const lcx_hparams *hp, uint32_t n_ctx, uint32_t n_seq_max, uint32_t n_ubatch);
 
+/* Host-only contexts: ubatch `ubatch` (0-based, in split order) of the next lcx_decode fails the
+ * way a failed launch does -- LCX_COMPUTE_FAILED, the cells of that ubatch and of the later ones
+ * released, earlier ubatches kept (step 13: the positions of a failed computation are removed
+ * from the cache again) -- so the rollback can be tested without making a GPU fail. -1 cancels.
+ * Returns LCX_INVALID for a context with a device. */
+int32_t lcx_ctx_inject_failure(lcx_ctx *ctx, int32_t ubatch);
+
 /* Row gather with dequantisation to float32 (step 13b, ggml_get_rows on the token
  * embeddings): out[i][:] = the n_cols values of row ids[i] of `table` (stored type `type`).
  * ids and out are DEVICE pointers; runs on cuda_stream. Returns LCX_OK or LCX_INVALID /

@@ -21,7 +21,7 @@ SYMBOLS = ("lcx_model_create", "lcx_model_free", "lcx_ctx_create", "lcx_ctx_free
            "lcx_decode_greedy", "lcx_kv_clear", "lcx_seq_pos_max", "lcx_n_outputs", "lcx_set_abort",
            "lcx_get_stats", "lcx_ctx_create_host_only", "lcx_get_rows", "lcx_last_error", "lcx_set_profiling",
            "lcx_get_profile", "lcx_attention_workspace_size", "lcx_attention", "lcx_attention_noalloc",
-           "lcx_kv_read", "lcx_get_trace", "lcx_sample")
+           "lcx_kv_read", "lcx_get_trace", "lcx_sample", "lcx_ctx_inject_failure")
 
 
 def build(force: bool = False) -> str:
@@ -111,6 +111,8 @@ def lib():
                                     ctypes.c_size_t, vp]
         L.lcx_attention_noalloc.restype = i32
         L.lcx_attention_noalloc.argtypes = [i32, i32, i32, i32, vp, vp, vp, i32, vp, i32, vp, vp, i32, vp, vp]
+        L.lcx_ctx_inject_failure.restype = i32
+        L.lcx_ctx_inject_failure.argtypes = [vp, i32]
         L.lcx_sample.restype = i32
         L.lcx_sample.argtypes = [ctypes.POINTER(lcx_sampler), vp, i32, i32, vp, i32, vp, vp, vp]
         L.lcx_get_trace.restype = i32
@@ -207,6 +209,10 @@ class Context:
 
     def kv_clear(self):
         lib().lcx_kv_clear(self.h)
+
+    def inject_failure(self, ubatch: int) -> int:
+        """Host-only contexts: ubatch `ubatch` of the next decode fails as a failed launch would."""
+        return lib().lcx_ctx_inject_failure(self.h, ubatch)
 
     def seq_pos_max(self, seq: int) -> int:
         return lib().lcx_seq_pos_max(self.h, seq)

@@ -198,6 +198,7 @@ struct lcx_ctx {
     lcx_model *m = nullptr;
     lcx_hparams hp{};
     bool host_only = false;
+    int fail_ubatch = -1;   // host-only contexts: this ubatch of the next lcx_decode fails (-3)
     uint32_t n_ctx = 0, n_seq_max = 0, n_ubatch = 0;
     cudaStream_t stream = nullptr;
     int n_pages = 0, max_pages_per_seq = 0;
@@ -284,6 +285,12 @@ extern "C" lcx_ctx *lcx_ctx_create_host_only(const lcx_hparams *hp, uint32_t n_c
     lcx_ctx *c = make_ctx_common(hp, n_ctx, n_seq_max, n_ubatch);
     if (c) c->host_only = true;
     return c;
+}
+
+extern "C" int32_t lcx_ctx_inject_failure(lcx_ctx *c, int32_t ubatch) {
+    if (!c || !c->host_only) return LCX_INVALID;
+    c->fail_ubatch = ubatch;
+    return LCX_OK;
 }
 
 template <class T>
@@ -783,6 +790,11 @@ extern "C" int32_t lcx_decode(lcx_ctx *c, lcx_batch batch, float *logits_out, in
             c->st.n_outputs_last = u.row0;
             c->n_outputs_last = u.row0;
             return LCX_ABORTED;
+        }
+        if (c->host_only && (int)k == c->fail_ubatch) {   // as a failed launch below
+            c->fail_ubatch = -1;
+            release_cells(c, P, u.i0);
+            return LCX_COMPUTE_FAILED;
         }
         if (!c->host_only) {
             FwdArgs a = c->base;

@@ -34,7 +34,7 @@
  *   positions NULL -> filled from the sequence's last position + 1; logits flags NULL ->
  *   only the last token; more new cells than the cache has free -> 1, nothing committed;
  *   a flagged token whose logits are not all finite -> -3, the cells of its ubatch (consecutive
- *   chunks of n_ubatch tokens) removed again and the rows of earlier ubatches kept.
+ *   chunks of n_ubatch tokens) removed again, earlier ubatches kept, no rows reported.
  *
  * Readings where the pages are silent (each is a choice of this implementation):
  *   Q8_0 block = fp16 d + int8 q[32], w = d*q; Q4_0 block = fp16 d + 16 bytes, element j in
@@ -448,9 +448,8 @@ int32_t orc_decode(void *cv, int32_t n_tokens, const int32_t *token, const int32
         flag[i] = flags_in ? (flags_in[i] != 0) : (int8_t)(i == n_tokens - 1);
     }
     if (c->used + n_tokens > (int64_t)c->n_ctx) return 1;
-    int32_t row = 0, row_ub = 0;
+    int32_t row = 0;
     for (int32_t i = 0; i < n_tokens; ++i) {
-        if (i % (int32_t)c->n_ubatch == 0) row_ub = row;   /* first token of a ubatch (split_simple) */
         double *lg = nullptr;
         std::vector<double> tmp;
         int32_t am = -1;
@@ -465,7 +464,6 @@ int32_t orc_decode(void *cv, int32_t n_tokens, const int32_t *token, const int32
             for (int32_t j = 0; j < hp.n_vocab; ++j)
                 if (!std::isfinite(lg[j])) {
                     rollback(*c, i - i % (int32_t)c->n_ubatch, i, seq.data(), pos.data());
-                    if (n_out) *n_out = row_ub;
                     return -3;
                 }
             if (argmax_out) argmax_out[row] = am;

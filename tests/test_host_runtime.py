@@ -151,3 +151,34 @@ def test_sample_checks_arguments_before_any_device_work():
     assert L.lcx_sample(by(ok), fake, 1, 100, None, 0, fake, None, None) == lcx.LCX_INVALID      # no output
     assert L.lcx_sample(by(ok), fake, 1, 100, None, 3, fake, fake, None) == lcx.LCX_INVALID      # history missing
     assert L.lcx_sample(by(ok), fake, 1, 100, None, 0, None, fake, None) == lcx.LCX_INVALID      # a draw needs u
+
+
+def test_failed_ubatch_rolls_back_like_the_oracle():
+    """A failed ubatch (-3) releases its cells and those of the later ubatches; earlier ubatches
+    stay. The failure is made on the host (a host-only context's injected launch failure) and
+    compared with the oracle's rule (a non-finite logit fails its ubatch)."""
+    import dataclasses
+    hp = hparams_of(TINY)
+    c = lcx.Context(None, 256, 2, 2, host_only_hp=hp)
+    assert c.inject_failure(1) == 0
+    # tokens of two sequences, ubatches of 2: [s0 p0, s1 p0] [s0 p1, s1 p1] [s0 p2]
+    toks, seqs = [1, 2, 3, 4, 5], [0, 1, 0, 1, 0]
+    assert c.decode(toks, seq_id=seqs) == lcx.LCX_COMPUTE_FAILED
+    assert (c.seq_pos_max(0), c.seq_pos_max(1), c.n_outputs()) == (0, 0, 0)
+    assert c.stats().n_cells_used == 2
+    assert c.decode([6, 7], seq_id=[0, 1]) == 0              # the failure was one-shot
+    assert (c.seq_pos_max(0), c.seq_pos_max(1)) == (1, 1)
+    assert c.inject_failure(0) == 0
+    assert c.decode([8], seq_id=[1]) == lcx.LCX_COMPUTE_FAILED and c.seq_pos_max(1) == 1
+    # the oracle: the flagged row of a NaN-embedding token in ubatch 1 fails it
+    host = synth.make_model(TINY)
+    bad = 11
+    emb = host.tok_embd.copy()
+    emb[bad].view(np.uint16)[:] = 0x7E00
+    octx = oracle.Context(oracle.Model(dataclasses.replace(host, tok_embd=emb)), 256, 2, 2)
+    rc, _, _ = octx.decode([1, 2, bad, 4, 5], seq=seqs, logits=[0, 0, 1, 0, 0])
+    assert rc == -3 and (octx.seq_pos_max(0), octx.seq_pos_max(1)) == (0, 0)
+
+
+def test_inject_failure_needs_a_host_only_context():
+    assert lcx.lib().lcx_ctx_inject_failure(None, 0) == lcx.LCX_INVALID
