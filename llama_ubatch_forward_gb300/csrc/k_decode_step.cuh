@@ -722,12 +722,13 @@ __device__ __forceinline__ void epilogue_rt(const StepPhase &P, const GemvMap &m
         }
         case EPI_QKV: {
             epi_quad_in<EPI_QKV>(a, layer, 0, r0, p.N, v, ein, bkey);
-            // publish the quad on its KV head's counter (release: after this thread's stores)
+            // count the quad for its KV head (shared memory); the CTA publishes the counts once,
+            // after its last QKV stage
             const int qw = a.H * a.hd, kw = a.KV * a.hd;
             if (r0 < qw + 2 * kw) {
                 const int sh = __ffs(a.hd) - 1;
                 const int kvh = r0 < qw ? (r0 >> sh) / (a.H / a.KV) : ((r0 - qw) >> sh) % a.KV;
-                asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(kvh_cnt + kvh) : "memory");
+                atomicAdd(kvh_cnt + kvh, 1u);
             }
             break;
         }
@@ -743,6 +744,7 @@ __device__ __forceinline__ void epilogue_rt(const StepPhase &P, const GemvMap &m
 struct StepConst {
     const float2 *rope;   // [head_dim / 2]
     int cell;
+    unsigned *pub;        // [n_head_kv] QKV quads of this CTA per KV head, not yet published
 };
 
 __device__ __forceinline__ EpiIn qkv_in(const FwdArgs &a, int r0, const StepConst &sc) {
@@ -827,7 +829,7 @@ __device__ __noinline__ void step_gemv(const StepArgs &s, const StepPhase *tab, 
             if (!dead) dots_rt<QT>(P, mp, ring + (size_t)slot * s.slot_bytes, xq, bk, u ? pk1 : pk0);
         }
         consumer_sync();
-        if (epi_thread) epilogue_rt(P, mp, epi, a, layer, my_st, e, threadIdx.x < 32 ? pk0 : pk1, rs, ein, best, s.sync + 16);
+        if (epi_thread) epilogue_rt(P, mp, epi, a, layer, my_st, e, threadIdx.x < 32 ? pk0 : pk1, rs, ein, best, sc.pub);
         // every warp is past its reads of the slots (the barrier above): refill them
         if (threadIdx.x == kFeedThread && !dead) {
             feed_one(s, tab, n_ph, a.L, f, ring, full);
@@ -839,6 +841,16 @@ __device__ __noinline__ void step_gemv(const StepArgs &s, const StepPhase *tab, 
     gs.dead = dead;
     gs.best = best;
     gs.f = f;
+    if (epi == EPI_QKV) {
+        // publish this CTA's quads, one release reduction per KV head: the barrier orders every
+        // epilogue thread's stores before it
+        consumer_sync();
+        if ((int)threadIdx.x < a.KV) {
+            const unsigned n = sc.pub[threadIdx.x];
+            if (n && !dead) asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(s.sync + 16 + threadIdx.x), "r"(n) : "memory");
+            sc.pub[threadIdx.x] = 0u;
+        }
+    }
     step_trace(a, trace_phase, 3);
 }
 
@@ -867,13 +879,15 @@ __global__ void __launch_bounds__(256, 1) k_decode_step(const __grid_constant__ 
     }
     __shared__ __align__(16) float2 s_rope[128];   // head_dim <= 256
     __shared__ int s_cell;
+    __shared__ unsigned s_pub[48];                  // n_head_kv <= 48
     {   // the token's constants (written by the host before the launch)
         const int pos0 = a.ub.pos[0];
         for (int i = threadIdx.x; i < a.hd / 2; i += 256) s_rope[i] = a.rope[(size_t)pos0 * (a.hd / 2) + i];
         if (threadIdx.x == 0) s_cell = a.ub.cell[0];
+        if (threadIdx.x < 48) s_pub[threadIdx.x] = 0u;
     }
     __syncthreads();
-    const StepConst sc{s_rope, s_cell};
+    const StepConst sc{s_rope, s_cell, s_pub};
     GemvState gs{0, Feeder{0, (int)blockIdx.x, 0}, false, 0ull};
     // fill the ring: the weights do not depend on anything this step computes
     if (threadIdx.x == kFeedThread)
