@@ -81,17 +81,32 @@ __device__ __forceinline__ bool consumer_any(bool v) {
     return r != 0;
 }
 
+// this thread's gains of the first staging iteration of a phase (constant inputs of the step)
+__device__ __forceinline__ void gains_of(const StepPhase &P, float4 (&g)[4]) {
+    const int hb = threadIdx.x, b = hb >> 1, half = hb & 1;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        g[j] = P.p.in.g && hb < 2 * P.p.nb ? *reinterpret_cast<const float4 *>(P.p.in.g + b * 32 + half * 16 + 4 * j)
+                                           : make_float4(1.f, 1.f, 1.f, 1.f);
+}
+
 // Grid barrier among the consumers of all CTAs: barrier number n (1-based) completes when the
 // counter reaches n * gridDim.x. Returns false (and the error word is set) if this CTA or any
-// other gave up.
-__device__ __forceinline__ bool grid_sync(const FwdArgs &a, unsigned *cnt, unsigned n, bool dead, int *s_ok) {
+// other gave up. With `next`, every thread loads its gains of that phase while the barrier
+// completes: after this CTA's arrival (a release orders the loads issued before it too, so
+// loading them earlier would delay the arrival by their round trip).
+__device__ __forceinline__ bool grid_sync(const FwdArgs &a, unsigned *cnt, unsigned n, bool dead, int *s_ok,
+                                          const StepPhase *next = nullptr, float4 (*gpre)[4] = nullptr) {
     const bool any_dead = consumer_any(dead);
+    if (next && threadIdx.x != 0) gains_of(*next, *gpre);
     if (threadIdx.x == 0) {
         bool ok = !any_dead;
+        if (!ok && next) gains_of(*next, *gpre);
         if (ok) {
             // release: this CTA's writes (ordered before by the barrier above) become visible
             // to the CTAs whose acquire load sees the count
             asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(cnt) : "memory");
+            if (next) gains_of(*next, *gpre);
             const unsigned target = n * gridDim.x;
             ok = false;
             for (uint32_t i = 0; i < kSpinLimit; ++i) {
@@ -707,12 +722,13 @@ __device__ __forceinline__ void epilogue_rt(const StepPhase &P, const GemvMap &m
         }
         case EPI_QKV: {
             epi_quad_in<EPI_QKV>(a, layer, 0, r0, p.N, v, ein, bkey);
-            // publish the quad on its KV head's counter (release: after this thread's stores)
+            // count the quad for its KV head (shared memory); the CTA publishes the counts once,
+            // after its last QKV stage
             const int qw = a.H * a.hd, kw = a.KV * a.hd;
             if (r0 < qw + 2 * kw) {
                 const int sh = __ffs(a.hd) - 1;
                 const int kvh = r0 < qw ? (r0 >> sh) / (a.H / a.KV) : ((r0 - qw) >> sh) % a.KV;
-                asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(kvh_cnt + kvh) : "memory");
+                atomicAdd(kvh_cnt + kvh, 1u);
             }
             break;
         }
@@ -720,6 +736,26 @@ __device__ __forceinline__ void epilogue_rt(const StepPhase &P, const GemvMap &m
         default: epi_quad_in<EPI_LOGITS>(a, layer, 0, r0, p.N, v, ein, bkey); break;
     }
     best = bkey > best ? bkey : best;
+}
+
+// The token's constants for the whole step, in shared memory from the launch on: its cache cell
+// and the RoPE (cos, sin) row of its position. The QKV epilogue reads them there instead of
+// a dependent chain of global loads (position, then the row it indexes) at every stage pair.
+struct StepConst {
+    const float2 *rope;   // [head_dim / 2]
+    int cell;
+    unsigned *pub;        // [n_head_kv] QKV quads of this CTA per KV head, not yet published
+};
+
+__device__ __forceinline__ EpiIn qkv_in(const FwdArgs &a, int r0, const StepConst &sc) {
+    EpiIn in{};
+    in.cell = sc.cell;
+    const int qw = a.H * a.hd, kw = a.KV * a.hd;
+    if (r0 < qw + kw) {   // q or k rows: the quad lies inside one head (hd % 4 == 0)
+        const int dim = (r0 < qw ? r0 : r0 - qw) & (a.hd - 1);
+        in.cs = *reinterpret_cast<const float4 *>(sc.rope + dim / 2);
+    }
+    return in;
 }
 
 // State the GEMV routine carries from phase to phase.
@@ -735,7 +771,8 @@ struct GemvState {
 template <int QT>
 __device__ __noinline__ void step_gemv(const StepArgs &s, const StepPhase *tab, int ph, int n_ph, int epi,
                                        const FwdArgs &a, int layer, uint8_t *xs, uint8_t *ring, uint64_t *full,
-                                       GemvState &gs, float *part, float *red, const float4 *gpre, int trace_phase) {
+                                       GemvState &gs, float *part, float *red, const float4 *gpre, int trace_phase,
+                                       StepConst sc) {
     const StepPhase &P = tab[ph];
     if (!gs.dead) stage_x<QT>(P.p, xs, red, 2 * P.p.nb <= 256 ? gpre : nullptr);
     consumer_sync();
@@ -780,7 +817,7 @@ __device__ __noinline__ void step_gemv(const StepArgs &s, const StepPhase *tab, 
                                 e < min(tps, n_tasks - my_st * tps);
         EpiIn ein{};
         if (epi_thread && epi == EPI_RESID) ein = epi_load<EPI_RESID>(a, 0, (my_st * tps + e) * 4, P.p.N);
-        if (epi_thread && epi == EPI_QKV) ein = epi_load<EPI_QKV>(a, 0, (my_st * tps + e) * 4, P.p.N);
+        if (epi_thread && epi == EPI_QKV) ein = qkv_in(a, (my_st * tps + e) * 4, sc);
         // the pair's two stages through one copy of the dot-product code (instruction cache)
 #pragma unroll 1
         for (int u = 0; u < (two ? 2 : 1); ++u) {
@@ -792,7 +829,7 @@ __device__ __noinline__ void step_gemv(const StepArgs &s, const StepPhase *tab, 
             if (!dead) dots_rt<QT>(P, mp, ring + (size_t)slot * s.slot_bytes, xq, bk, u ? pk1 : pk0);
         }
         consumer_sync();
-        if (epi_thread) epilogue_rt(P, mp, epi, a, layer, my_st, e, threadIdx.x < 32 ? pk0 : pk1, rs, ein, best, s.sync + 16);
+        if (epi_thread) epilogue_rt(P, mp, epi, a, layer, my_st, e, threadIdx.x < 32 ? pk0 : pk1, rs, ein, best, sc.pub);
         // every warp is past its reads of the slots (the barrier above): refill them
         if (threadIdx.x == kFeedThread && !dead) {
             feed_one(s, tab, n_ph, a.L, f, ring, full);
@@ -804,17 +841,19 @@ __device__ __noinline__ void step_gemv(const StepArgs &s, const StepPhase *tab, 
     gs.dead = dead;
     gs.best = best;
     gs.f = f;
+    if (epi == EPI_QKV) {
+        // publish this CTA's quads, one release reduction per KV head: the barrier orders every
+        // epilogue thread's stores before it
+        consumer_sync();
+        if ((int)threadIdx.x < a.KV) {
+            const unsigned n = sc.pub[threadIdx.x];
+            if (n && !dead) asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(s.sync + 16 + threadIdx.x), "r"(n) : "memory");
+            sc.pub[threadIdx.x] = 0u;
+        }
+    }
     step_trace(a, trace_phase, 3);
 }
 
-// this thread's gains of the first staging iteration of a phase (loaded before its barrier)
-__device__ __forceinline__ void gains_of(const StepPhase &P, float4 (&g)[4]) {
-    const int hb = threadIdx.x, b = hb >> 1, half = hb & 1;
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-        g[j] = P.p.in.g && hb < 2 * P.p.nb ? *reinterpret_cast<const float4 *>(P.p.in.g + b * 32 + half * 16 + 4 * j)
-                                           : make_float4(1.f, 1.f, 1.f, 1.f);
-}
 
 template <int QL, int QH, int HD, int G>
 __global__ void __launch_bounds__(256, 1) k_decode_step(const __grid_constant__ StepArgs s,
@@ -838,7 +877,17 @@ __global__ void __launch_bounds__(256, 1) k_decode_step(const __grid_constant__ 
         const int n16 = (int)(s.n_ph_all * sizeof(StepPhase) / 16);
         for (int i = threadIdx.x; i < n16; i += 256) dst[i] = src[i];
     }
+    __shared__ __align__(16) float2 s_rope[128];   // head_dim <= 256
+    __shared__ int s_cell;
+    __shared__ unsigned s_pub[48];                  // n_head_kv <= 48
+    {   // the token's constants (written by the host before the launch)
+        const int pos0 = a.ub.pos[0];
+        for (int i = threadIdx.x; i < a.hd / 2; i += 256) s_rope[i] = a.rope[(size_t)pos0 * (a.hd / 2) + i];
+        if (threadIdx.x == 0) s_cell = a.ub.cell[0];
+        if (threadIdx.x < 48) s_pub[threadIdx.x] = 0u;
+    }
     __syncthreads();
+    const StepConst sc{s_rope, s_cell, s_pub};
     GemvState gs{0, Feeder{0, (int)blockIdx.x, 0}, false, 0ull};
     // fill the ring: the weights do not depend on anything this step computes
     if (threadIdx.x == kFeedThread)
@@ -873,8 +922,7 @@ __global__ void __launch_bounds__(256, 1) k_decode_step(const __grid_constant__ 
     const int page0 = ac0 >> 6;
     KVGroup<HD> kvq[4];   // this warp's first 4 groups of the unit, loaded before each attention barrier
     float4 gpre[4];
-    gains_of(tab[0], gpre);
-    gs.dead = !grid_sync(a, bar, ++n_bar, gs.dead, &s_ok);
+    gs.dead = !grid_sync(a, bar, ++n_bar, gs.dead, &s_ok, &tab[0], &gpre);
     if (has_unit) {   // the unit's page ids (the page table is complete after the barrier)
         const int n_pg = min(kMaxUnitPages, ((max(ac1, ac0 + 1) - 1) >> 6) - page0 + 1);
         const int32_t *ptrow = a.pt + (size_t)a.ub.seq[0] * a.max_pages_per_seq;
@@ -887,7 +935,7 @@ __global__ void __launch_bounds__(256, 1) k_decode_step(const __grid_constant__ 
         // QKV (the attention unit's cached K/V lines go to L2 meanwhile)
         step_trace(a, tp, 0);
         if (has_unit) attn_prefetch<HD>(a, l, u_kvh, ac0, ac1, pages, page0);
-        step_gemv<QL>(s, tab, 4 * l + PH_QKV, n_ph, EPI_QKV, a, l, xs, ring, full, gs, part, red, gpre, tp);
+        step_gemv<QL>(s, tab, 4 * l + PH_QKV, n_ph, EPI_QKV, a, l, xs, ring, full, gs, part, red, gpre, tp, sc);
         if (has_unit) {
             const int jf = ac0 + 4 * (threadIdx.x >> 5);
 #pragma unroll
@@ -925,20 +973,19 @@ __global__ void __launch_bounds__(256, 1) k_decode_step(const __grid_constant__ 
         if (gs.dead) break;
         // output projection + residual
         step_trace(a, tp + 2, 0);
-        step_gemv<QL>(s, tab, 4 * l + PH_O, n_ph, EPI_RESID, a, l, xs, ring, full, gs, part, red, nullptr, tp + 2);
-        gains_of(tab[4 * l + PH_GU], gpre);
-        gs.dead = !grid_sync(a, bar, ++n_bar, gs.dead, &s_ok);
+        step_gemv<QL>(s, tab, 4 * l + PH_O, n_ph, EPI_RESID, a, l, xs, ring, full, gs, part, red, nullptr, tp + 2, sc);
+        gs.dead = !grid_sync(a, bar, ++n_bar, gs.dead, &s_ok, &tab[4 * l + PH_GU], &gpre);
         if (gs.dead) break;
         // gate/up + SwiGLU
         step_trace(a, tp + 3, 0);
-        step_gemv<QL>(s, tab, 4 * l + PH_GU, n_ph, EPI_SWIGLU, a, l, xs, ring, full, gs, part, red, gpre, tp + 3);
+        step_gemv<QL>(s, tab, 4 * l + PH_GU, n_ph, EPI_SWIGLU, a, l, xs, ring, full, gs, part, red, gpre, tp + 3, sc);
         gs.dead = !grid_sync(a, bar, ++n_bar, gs.dead, &s_ok);
         if (gs.dead) break;
         // down + residual
         step_trace(a, tp + 4, 0);
-        step_gemv<QL>(s, tab, 4 * l + PH_DOWN, n_ph, EPI_RESID, a, l, xs, ring, full, gs, part, red, nullptr, tp + 4);
-        gains_of(tab[4 * l + 4], gpre);   // next layer's QKV, or the head
-        gs.dead = !grid_sync(a, bar, ++n_bar, gs.dead, &s_ok);
+        step_gemv<QL>(s, tab, 4 * l + PH_DOWN, n_ph, EPI_RESID, a, l, xs, ring, full, gs, part, red, nullptr, tp + 4, sc);
+        // next layer's QKV, or the head
+        gs.dead = !grid_sync(a, bar, ++n_bar, gs.dead, &s_ok, &tab[4 * l + 4], &gpre);
     }
     if (gs.dead) {
         // copies still in flight must land before the CTA's shared memory is released
@@ -950,7 +997,7 @@ __global__ void __launch_bounds__(256, 1) k_decode_step(const __grid_constant__ 
     if (a.n_out > 0) {
         const int tp = 1 + 5 * L;
         step_trace(a, tp, 0);
-        step_gemv<QH>(s, tab, 4 * L, n_ph, EPI_LOGITS, a, -1, xs, ring, full, gs, part, red, gpre, tp);
+        step_gemv<QH>(s, tab, 4 * L, n_ph, EPI_LOGITS, a, -1, xs, ring, full, gs, part, red, gpre, tp, sc);
         const unsigned long long bst[1] = {gs.best};
         logits_cta_reduce<1>(a, 1, bst);
     }

@@ -3,8 +3,8 @@
 The step is the one kernel whose CTAs wait on one another, so its protocol is checked as a model:
 each CTA runs as a coroutine over the kernel's flow -- the stage ring filled at launch and refilled
 after every consumed pair (slot k % slots, barrier parity (k / slots) & 1), the grid barriers
-(a monotonic arrival counter), the per-KV-head counters the QKV epilogues publish on and the
-attention units wait for, the split merge by the last unit of a head (an arrival counter), and
+(a monotonic arrival counter), the per-KV-head counters each CTA publishes its QKV quads on
+after its last QKV stage and the attention units wait for, the split merge by the last unit of a head (an arrival counter), and
 the reset by the last CTA to finish -- with every bulk copy landing after a random delay and the
 CTAs scheduled in random order. Over two launches in a row it checks that every consumed slot
 holds the stage the consumer expects and none is refilled early, that each phase's input is
@@ -101,6 +101,7 @@ def model(grid, slots, L, H, KV, hd, d, F, V, tps, ns, n_out, seed, launches=2):
                     yield
 
             k = [0]
+            pub = [0] * KV                                          # quads not yet published
 
             def gemv(ph, prev_done):
                 assert prev_done(), ("phase input incomplete when staged", ph, c)
@@ -124,7 +125,7 @@ def model(grid, slots, L, H, KV, hd, d, F, V, tps, ns, n_out, seed, launches=2):
                                 task = s_ * tps[0] + e
                                 if task < tasks[0]:                # one epilogue thread per quad
                                     quads[l][kvh_of(4 * task)] += 1
-                                    shared["cnt"][kvh_of(4 * task)] += 1
+                                    pub[kvh_of(4 * task)] += 1     # counted in shared memory
                                     yield
                         written[ph] += 1
                     feed_one()
@@ -132,6 +133,13 @@ def model(grid, slots, L, H, KV, hd, d, F, V, tps, ns, n_out, seed, launches=2):
                         feed_one()
                     k[0] += 2 if two else 1
                     st += 2 * grid
+                if ph < 4 * L and ph % 4 == 0:                     # publish once per KV head
+                    yield                                           # the CTA barrier
+                    for h in range(KV):
+                        if pub[h]:
+                            shared["cnt"][h] += pub[h]
+                            pub[h] = 0
+                            yield
 
             def done_all(ph):
                 return lambda: written[ph] == n_st[ph]
@@ -221,7 +229,7 @@ def test_decode_step_protocol(shape):
 
 
 @pytest.mark.parametrize("wrong,right", [
-    ("target = (l + 1) * kvh_quads", "target = (l + 1) * kvh_quads - 1"),       # a unit starts one quad early
+    ("target = (l + 1) * kvh_quads", "target = l * kvh_quads + 1"),             # a unit starts on the first quads
     ('                shared["cnt"] = [0] * KV\n', ""),                          # counters left for the next launch
 ])
 def test_model_catches_planted_mistakes(wrong, right):
