@@ -108,9 +108,13 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// Shared memory: a ring of S stages, each the raw weight box and the activation tiles of one K
-// step, and a separate ring of 2 dequantised f16 weight tiles (the largest part of a stage), so
-// the TMA and activation loads can run S - 1 stages ahead while the f16 tiles are double-buffered.
+// Shared memory: three rings. The dequantised f16 weight tiles (SA slots, the largest part of a
+// step); the activation tiles (SB slots, freed by the MMAs that read them); the raw weight boxes
+// (SR slots, freed by the dequantising warps as soon as they have read them -- not by the MMA, so
+// the next boxes stream in while the tensor pipe works). With SA = 3 the dequantisation of step j
+// waits only for the MMAs of step j - 3, so it overlaps the MMAs of steps j - 2 and j - 1; the
+// activations run DB steps ahead into the slot freed by the MMAs of step j + DB - SB, which are
+// never later than those the A ring waits for.
 template <int QT, int BN, int MT>
 struct Cfg {
     static constexpr int QB = QT == Q8 ? 32 : 16;          // quant bytes per 32-element block
@@ -118,12 +122,15 @@ struct Cfg {
     static constexpr int B_BYTES = 2 * BN * BK * 2;       // f16 activation tiles: high and low parts
     static constexpr int PB = 8 * QB + 16;                // one block pair of a row quad (QMat)
     static constexpr int RQ_BYTES = MT * (BM / 4) * PB;   // raw tiles: 32 quads x one block pair
-    static constexpr int STAGE = B_BYTES + ((RQ_BYTES + 1023) / 1024) * 1024;
-    static constexpr int SA = 2;                          // dequantised tiles in flight
-    static constexpr int S_FIT = (220 * 1024 - SA * A_BYTES) / STAGE;
-    static constexpr int S = S_FIT < 6 ? S_FIT : 6;
-    static_assert(S >= 2, "the activation prefetch needs at least two stages");
-    static constexpr int SMEM = SA * A_BYTES + S * STAGE + 1024 /* align */ + 512 /* barriers */;
+    static constexpr int RQ_SLOT = ((RQ_BYTES + 1023) / 1024) * 1024;
+    static constexpr int SA = (QT == Q4 && BN == 64) ? 3 : 2;
+    static constexpr int SR = (QT == Q8 && BN == 128) ? 2 : 3;
+    static constexpr int SB_FIT = (220 * 1024 - SA * A_BYTES - SR * RQ_SLOT) / B_BYTES;
+    static constexpr int SB = SB_FIT < 6 ? SB_FIT : 6;
+    static constexpr int DB = SB - SA >= 2 ? SB - SA : SB - 1;   // activation prefetch distance
+    static_assert(SB >= 2 && DB >= 1, "the activation prefetch needs at least two slots");
+    static constexpr int SMEM = SA * A_BYTES + SB * B_BYTES + SR * RQ_SLOT + 1024 /* align */ + 512 /* barriers */;
+    static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
     // per weight tile, W A_hi and W A_lo side by side: one MMA of N = 2 BN over the stacked tiles
     static constexpr int TMEM_COLS = MT * 2 * BN <= 128 ? 128 : MT * 2 * BN <= 256 ? 256 : 512;
     static_assert(MT * 2 * BN <= 512, "tensor memory holds 512 columns");
@@ -208,14 +215,17 @@ __global__ void __launch_bounds__(320, 1)
               const __grid_constant__ CUtensorMap tm_w, const GemmParams p, const FwdArgs a, const int layer) {
     constexpr int MT = 2;   // two 128-row weight tiles share every activation tile
     using C = Cfg<QT, BN, MT>;
-    constexpr int S = C::S;
+    constexpr int SA = C::SA, SB = C::SB, SR = C::SR;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::SA * C::A_BYTES + S * C::STAGE);
-    // full_w: raw weights landed; full_b: activations landed; empty: the stage's MMAs are done
-    // (raw and activation slot free); full_a / empty_a: the A ring's dequantised tile written / read
-    uint64_t *full_w = bars, *full_b = bars + S, *empty = bars + 2 * S, *full_a = bars + 3 * S,
-             *empty_a = full_a + C::SA, *acc_bar = empty_a + C::SA;
+    uint8_t *act_ring = smem + SA * C::A_BYTES;
+    uint8_t *raw_ring = act_ring + SB * C::B_BYTES;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(raw_ring + SR * C::RQ_SLOT);
+    // full_w / empty_w: a raw weight box landed / read by the dequantising warps; full_b / empty_b:
+    // an activation tile landed / read by the MMAs; full_a / empty_a: a dequantised tile written /
+    // read by the MMAs
+    uint64_t *full_w = bars, *empty_w = full_w + SR, *full_b = empty_w + SR, *empty_b = full_b + SB,
+             *full_a = empty_b + SB, *empty_a = full_a + SA, *acc_bar = empty_a + SA;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_bar + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m_tile = blockIdx.x, tok0 = blockIdx.y * BN;
@@ -224,17 +234,19 @@ __global__ void __launch_bounds__(320, 1)
     // gate quads interleaved with their 16 up quads)
     const int row0[MT] = {m_tile * 2 * BM, m_tile * 2 * BM + BM};
     auto a_tile = [&](int aslot, int mt) { return smem + aslot * C::A_BYTES + mt * BM * BK * 2; };
-    uint8_t *ring = smem + C::SA * C::A_BYTES;
-    auto b_tile = [&](int slot) { return ring + slot * C::STAGE; };
-    auto rq_tile = [&](int slot, int mt) { return ring + slot * C::STAGE + C::B_BYTES + mt * (BM / 4) * C::PB; };
+    auto b_tile = [&](int slot) { return act_ring + slot * C::B_BYTES; };
+    auto rq_tile = [&](int slot, int mt) { return raw_ring + slot * C::RQ_SLOT + mt * (BM / 4) * C::PB; };
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < S; ++i) {
+        for (int i = 0; i < SR; ++i) {
             mbar_init(&full_w[i], 1);
-            mbar_init(&full_b[i], 8);   // one arrival per loading warp
-            mbar_init(&empty[i], 1);
+            mbar_init(&empty_w[i], 8);   // one arrival per dequantising warp
         }
-        for (int i = 0; i < C::SA; ++i) {
+        for (int i = 0; i < SB; ++i) {
+            mbar_init(&full_b[i], 8);    // one arrival per loading warp
+            mbar_init(&empty_b[i], 1);
+        }
+        for (int i = 0; i < SA; ++i) {
             mbar_init(&full_a[i], 8);   // one arrival per dequantising warp
             mbar_init(&empty_a[i], 1);
         }
@@ -256,22 +268,22 @@ __global__ void __launch_bounds__(320, 1)
         if (lane == 0) {
             bool ok = true;
             auto issue_w = [&](int j) {   // quants and scales of the 64 quads of both tiles: one box
-                const int slot = j % S;
+                const int slot = j % SR;
                 mbar_expect_tx(&full_w[slot], C::RQ_BYTES);
                 tma_2d(rq_tile(slot, 0), &tm_w, j * (C::PB / 4), row0[0] / 4, &full_w[slot]);
             };
-            const int pre = nk < S ? nk : S;
+            const int pre = nk < SR ? nk : SR;
             for (int j = 0; j < pre; ++j) issue_w(j);
             LCX_PDL_TRIGGER();
             int issued = pre;
-            for (int j = S; j < nk && ok; ++j) {
-                if (!(ok = mbar_wait(&empty[j % S], ((j / S) - 1) & 1))) break;
+            for (int j = SR; j < nk && ok; ++j) {
+                if (!(ok = mbar_wait(&empty_w[j % SR], ((j / SR) - 1) & 1))) break;
                 issue_w(j);
                 issued = j + 1;
             }
             if (!ok) atomicExch(a.err, 1);
             // every copy issued must land before the CTA exits
-            for (int j = (issued > S ? issued - S : 0); j < issued; ++j) mbar_wait(&full_w[j % S], (j / S) & 1);
+            for (int j = (issued > SR ? issued - SR : 0); j < issued; ++j) mbar_wait(&full_w[j % SR], (j / SR) & 1);
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
@@ -279,8 +291,8 @@ __global__ void __launch_bounds__(320, 1)
             constexpr uint32_t idesc = idesc_f16(BM, 2 * BN);   // the high and low parts stacked: N = 2 BN
             bool ok = true;
             for (int j = 0; j < nk; ++j) {
-                const int slot = j % S, aslot = j % C::SA;
-                if (!(ok = mbar_wait(&full_a[aslot], (j / C::SA) & 1) && mbar_wait(&full_b[slot], (j / S) & 1))) break;
+                const int slot = j % SB, aslot = j % SA;
+                if (!(ok = mbar_wait(&full_a[aslot], (j / SA) & 1) && mbar_wait(&full_b[slot], (j / SB) & 1))) break;
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                 const uint32_t bbase = saddr(b_tile(slot));
                 // the activation tile's high rows then low rows form one K-major operand of 2 BN
@@ -295,7 +307,7 @@ __global__ void __launch_bounds__(320, 1)
                                 (j > 0 || kk > 0) ? 1u : 0u);
                     }
                 }
-                mma_commit(&empty[slot]);     // the stage's slot is free once these MMAs have read it
+                mma_commit(&empty_b[slot]);   // the activation slot is free once these MMAs have read it
                 mma_commit(&empty_a[aslot]);  // and so is the A slot
             }
             if (!ok) atomicExch(a.err, 1);
@@ -311,7 +323,7 @@ __global__ void __launch_bounds__(320, 1)
         // chunk wt % 8 of rows wt / 8 + 32 u, each to its 128-byte-swizzled place; rows past the
         // last token are zero-filled
         auto load_act = [&](int j) {
-            uint8_t *bt = b_tile(j % S);
+            uint8_t *bt = b_tile(j % SB);
             const int c = wt & 7;
 #pragma unroll
             for (int hl = 0; hl < 2; ++hl) {
@@ -326,10 +338,9 @@ __global__ void __launch_bounds__(320, 1)
                 }
             }
         };
-        // activations run D steps ahead: with 5 or more slots, into the slot of step j - 2 (free
-        // once the A slot of step j - 2 is, so no wait on the MMAs of step j - 1 delays the
-        // dequantisation); with fewer, into the slot of step j - 1
-        constexpr int D = S >= 5 ? S - 2 : S - 1;
+        // activations run D steps ahead, into the slot the MMAs of step j + D - SB read (no later
+        // than the step whose A slot the dequantisation of step j waits for, when DB = SB - SA)
+        constexpr int D = C::DB;
         bool ok = true;
         LCX_PDL_WAIT();   // the activations are the previous kernel's output
         LCX_PDL_TRIGGER();
@@ -338,25 +349,28 @@ __global__ void __launch_bounds__(320, 1)
             asm volatile("cp.async.commit_group;" ::: "memory");
         }
         for (int j = 0; j < nk; ++j) {
-            const int slot = j % S, aslot = j % C::SA;
-            ok = __all_sync(0xffffffffu, mbar_wait(&full_w[slot], (j / S) & 1));   // warp-uniform
-            // the A slot is free once the MMAs of stage j - SA are done
-            if (ok && j >= C::SA) ok = __all_sync(0xffffffffu, mbar_wait(&empty_a[aslot], ((j / C::SA) - 1) & 1));
+            const int rslot = j % SR, bslot = j % SB, aslot = j % SA;
+            ok = __all_sync(0xffffffffu, mbar_wait(&full_w[rslot], (j / SR) & 1));   // warp-uniform
+            // the A slot is free once the MMAs of step j - SA are done
+            if (ok && j >= SA) ok = __all_sync(0xffffffffu, mbar_wait(&empty_a[aslot], ((j / SA) - 1) & 1));
             if (!ok) break;
-            dequant_row<QT>(rq_tile(slot, my_mt), a_tile(aslot, my_mt), drow);
+            dequant_row<QT>(rq_tile(rslot, my_mt), a_tile(aslot, my_mt), drow);
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic writes -> tensor-core reads
             __syncwarp();
-            if (lane == 0) mbar_arrive(&full_a[aslot]);
-            // stage j's activation copies have landed: of the D + j groups committed so far, all
+            if (lane == 0) {
+                mbar_arrive(&full_a[aslot]);
+                mbar_arrive(&empty_w[rslot]);   // this warp's rows of the raw box are read
+            }
+            // step j's activation copies have landed: of the D + j groups committed so far, all
             // but the D - 1 newest
             asm volatile("cp.async.wait_group %0;" ::"n"(D - 1) : "memory");
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
-            if (lane == 0) mbar_arrive(&full_b[slot]);
-            // prefetch stage j + D into the slot stage j + D - S used, once its MMAs are done
+            if (lane == 0) mbar_arrive(&full_b[bslot]);
+            // prefetch step j + D into the slot step j + D - SB used, once its MMAs are done
             const int jn = j + D;
             if (jn < nk) {
-                if (jn >= S) ok = __all_sync(0xffffffffu, mbar_wait(&empty[jn % S], ((jn / S) - 1) & 1));
+                if (jn >= SB) ok = __all_sync(0xffffffffu, mbar_wait(&empty_b[jn % SB], ((jn / SB) - 1) & 1));
                 if (!ok) break;
                 load_act(jn);
             }

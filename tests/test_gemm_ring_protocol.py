@@ -43,19 +43,21 @@ class Bar:
         return (self.phase & 1) != parity
 
 
-def run(S, SA, D, nk, seed):
-    """One CTA's K loop: S stage slots (raw weight box + activation tile, freed by the MMA
-    commit), SA dequantised-tile slots, activations D steps ahead."""
+def run(SA, SB, SR, D, nk, seed):
+    """One CTA's K loop: SR raw-box slots (freed by the dequantising warps), SB activation slots
+    (freed by the MMA commit), SA dequantised-tile slots, activations D steps ahead."""
     rnd = random.Random(seed)
-    full_w = [Bar(1) for _ in range(S)]
-    full_b = [Bar(8) for _ in range(S)]
-    empty = [Bar(1) for _ in range(S)]
+    full_w = [Bar(1) for _ in range(SR)]
+    empty_w = [Bar(8) for _ in range(SR)]
+    full_b = [Bar(8) for _ in range(SB)]
+    empty_b = [Bar(1) for _ in range(SB)]
     full_a = [Bar(8) for _ in range(SA)]
     empty_a = [Bar(1) for _ in range(SA)]
-    raw = [None] * S                                   # step whose raw box a slot holds
-    rows = [[None] * S for _ in range(8)]              # step whose activation rows warp w put in a slot
+    raw = [None] * SR                                  # step whose raw box a slot holds
+    rows = [[None] * SB for _ in range(8)]             # step whose activation rows warp w put in a slot
     atile = [[None] * 8 for _ in range(SA)]            # step whose tile rows warp w dequantised
-    reading_stage, reading_a = set(), set()            # slots an MMA in flight reads
+    raw_readers = [set() for _ in range(SR)]           # warps that still have to read a raw box
+    reading_b, reading_a = set(), set()                # slots an MMA in flight reads
     events, now = [], [0]
 
     def later(fn, lo, hi):
@@ -63,35 +65,36 @@ def run(S, SA, D, nk, seed):
 
     def producer():
         def issue(j):
-            s = j % S
-            assert s not in reading_stage, ("raw box overwritten while an MMA reads its stage", j)
+            s = j % SR
+            assert not raw_readers[s], ("raw box overwritten before every warp read it", j)
             full_w[s].expect_tx(1)
 
             def land(s=s, j=j):
                 raw[s] = j
+                raw_readers[s] = set(range(8))
                 full_w[s].complete_tx(1)
             later(land, 5, 60)
-        for j in range(min(nk, S)):
+        for j in range(min(nk, SR)):
             issue(j)
-        for j in range(S, nk):
-            while not empty[j % S].done(((j // S) - 1) & 1):
+        for j in range(SR, nk):
+            while not empty_w[j % SR].done(((j // SR) - 1) & 1):
                 yield
             issue(j)
 
     def mma():
         for j in range(nk):
-            s, a = j % S, j % SA
-            while not (full_a[a].done((j // SA) & 1) and full_b[s].done((j // S) & 1)):
+            s, a = j % SB, j % SA
+            while not (full_a[a].done((j // SA) & 1) and full_b[s].done((j // SB) & 1)):
                 yield
             assert all(rows[w][s] == j for w in range(8)), ("activation tile", j)
             assert all(t == j for t in atile[a]), ("dequantised tile", j)
-            reading_stage.add(s)
+            reading_b.add(s)
             reading_a.add(a)
 
             def finish(s=s, a=a):
-                reading_stage.discard(s)
+                reading_b.discard(s)
                 reading_a.discard(a)
-                empty[s].arrive()
+                empty_b[s].arrive()
                 empty_a[a].arrive()
             later(finish, 3, 30)
             yield
@@ -100,10 +103,10 @@ def run(S, SA, D, nk, seed):
         groups = []                                    # committed cp.async groups: landing flags
 
         def load_act(j):
-            assert j % S not in reading_stage, ("activation slot overwritten while an MMA reads it", j)
+            assert j % SB not in reading_b, ("activation slot overwritten while an MMA reads it", j)
             flag = {"landed": False}
 
-            def land(s=j % S, j=j, flag=flag):
+            def land(s=j % SB, j=j, flag=flag):
                 rows[w][s] = j
                 flag["landed"] = True
             later(land, 2, 50)
@@ -111,25 +114,27 @@ def run(S, SA, D, nk, seed):
         for j in range(D):
             groups.append(load_act(j) if j < nk else [])
         for j in range(nk):
-            s, a = j % S, j % SA
-            while not full_w[s].done((j // S) & 1):
+            r, b, a = j % SR, j % SB, j % SA
+            while not full_w[r].done((j // SR) & 1):
                 yield
             if j >= SA:
                 while not empty_a[a].done(((j // SA) - 1) & 1):
                     yield
-            assert raw[s] == j, ("raw box", j)
+            assert raw[r] == j, ("raw box", j)
             assert a not in reading_a, ("dequantised tile overwritten while an MMA reads it", j)
             atile[a][w] = j
+            raw_readers[r].discard(w)
             yield
             full_a[a].arrive()
+            empty_w[r].arrive()
             while not all(f["landed"] for g in groups[:len(groups) - (D - 1)] for f in g):
                 yield                                  # cp.async.wait_group D - 1
-            full_b[s].arrive()
+            full_b[b].arrive()
             jn = j + D
             g = []
             if jn < nk:
-                if jn >= S:
-                    while not empty[jn % S].done(((jn // S) - 1) & 1):
+                if jn >= SB:
+                    while not empty_b[jn % SB].done(((jn // SB) - 1) & 1):
                         yield
                 g = load_act(jn)
             groups.append(g)
@@ -155,23 +160,24 @@ def run(S, SA, D, nk, seed):
 
 
 def ring_depths(qb_bytes, bn):
-    """(S, SA, D) as the kernel's Cfg<QT, BN, 2> computes them."""
+    """(SA, SB, SR, DB) as the kernel's Cfg<QT, BN, 2> computes them."""
+    q4 = qb_bytes == 16
     a_bytes = 2 * 128 * 64 * 2
     b_bytes = 2 * bn * 64 * 2
-    rq = 2 * 32 * (8 * qb_bytes + 16)
-    stage = b_bytes + (rq + 1023) // 1024 * 1024
-    sa = 2
-    s = min(6, (220 * 1024 - sa * a_bytes) // stage)
-    d = s - 2 if s >= 5 else s - 1
-    return s, sa, d
+    rq_slot = (2 * 32 * (8 * qb_bytes + 16) + 1023) // 1024 * 1024
+    sa = 3 if q4 and bn == 64 else 2
+    sr = 2 if not q4 and bn == 128 else 3
+    sb = min(6, (220 * 1024 - sa * a_bytes - sr * rq_slot) // b_bytes)
+    db = sb - sa if sb - sa >= 2 else sb - 1
+    return sa, sb, sr, db
 
 
 @pytest.mark.parametrize("qb_bytes,bn", [(16, 64), (16, 128), (32, 64), (32, 128)])   # Q4_0 / Q8_0 x BN
 def test_ring_protocol(qb_bytes, bn):
-    S, SA, D = ring_depths(qb_bytes, bn)
+    SA, SB, SR, DB = ring_depths(qb_bytes, bn)
     for nk in (1, 2, 3, 5, 7, 64):
         for seed in range(3):
-            run(S, SA, D, nk, seed)
+            run(SA, SB, SR, DB, nk, seed)
 
 
 def test_model_catches_a_missing_wait():
@@ -182,4 +188,4 @@ def test_model_catches_a_missing_wait():
     exec(compile(src, "mutated", "exec"), ns)
     with pytest.raises(AssertionError):
         for seed in range(5):
-            ns["run"](6, 2, 4, 64, seed)
+            ns["run"](3, 6, 3, 3, 64, seed)
