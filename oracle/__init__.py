@@ -74,6 +74,8 @@ def lib():
         L.orc_round_to_half.restype = dp
         L.orc_round_to_half.argtypes = [dp]
         L.orc_matvec.argtypes = [i32, vp, i64, i64, vp, vp]
+        L.orc_matmat.argtypes = [i32, vp, i64, i64, vp, i64, vp]
+        L.orc_set_elide.argtypes = [vp, i32]
         L.orc_rmsnorm.argtypes = [vp, i64, vp, dp, vp]
         L.orc_rope.argtypes = [vp, i32, i64, dp]
         L.orc_silu.restype = dp
@@ -124,6 +126,15 @@ def matvec(qtype: int, W: np.ndarray, n: int, k: int, x) -> np.ndarray:
     y = np.empty(n, dtype=np.float64)
     lib().orc_matvec(qtype, _p(W), n, k, _p(x), _p(y))
     return y
+
+
+def matmat(qtype: int, W: np.ndarray, n: int, k: int, X) -> np.ndarray:
+    """Y [T][n] = X [T][k] times the stored matrix W [n][k] transposed (every token as matvec)."""
+    W = np.ascontiguousarray(W, dtype=np.uint8)
+    X = np.ascontiguousarray(np.atleast_2d(X), dtype=np.float64)
+    Y = np.empty((X.shape[0], n), dtype=np.float64)
+    lib().orc_matmat(qtype, _p(W), n, k, _p(X), X.shape[0], _p(Y))
+    return Y
 
 
 def rmsnorm(x, g, eps: float) -> np.ndarray:
@@ -209,6 +220,10 @@ class Context:
         if rc != 0:
             raise IndexError("no such cell")
         return k, v
+
+    def set_elide(self, on: bool):
+        """Last layer: tokens whose logits are not flagged compute only K and V (on, the default)."""
+        lib().orc_set_elide(self.h, 1 if on else 0)
 
     def set_trace(self, layer: int):
         lib().orc_set_trace(self.h, layer)

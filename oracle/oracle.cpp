@@ -34,7 +34,17 @@
  *   positions NULL -> filled from the sequence's last position + 1; logits flags NULL ->
  *   only the last token; more new cells than the cache has free -> 1, nothing committed;
  *   a flagged token whose logits are not all finite -> -3, the cells of its ubatch (consecutive
- *   chunks of n_ubatch tokens) removed again, earlier ubatches kept, no rows reported.
+ *   chunks of n_ubatch tokens) removed again; earlier ubatches stay in the cache and their
+ *   logits rows stay reported (the decode loop copies each ubatch's rows into the output buffer
+ *   before it runs the next ubatch, and a failure returns from inside that loop).
+ *
+ * Evaluation order: a ubatch runs layer by layer over blocks of at most 256 of its tokens (the
+ * way a ubatch's graph runs every layer over all its tokens, step 13c); inside a layer every
+ * token's K and V are stored before any token of the block attends, and the causal mask limits
+ * token t to the cells of its sequence with pos <= pos_t, so each token computes exactly what it
+ * would alone. Every matrix-vector product is one sum in increasing k, whatever the block size.
+ * In the last layer a token whose logits are not flagged computes only its K and V: the rest of
+ * that layer feeds nothing but its own logits (step 13c, only the output rows go on to the head).
  *
  * Readings where the pages are silent (each is a choice of this implementation):
  *   Q8_0 block = fp16 d + int8 q[32], w = d*q; Q4_0 block = fp16 d + 16 bytes, element j in
@@ -96,17 +106,18 @@ void dequant_row(int type, const uint8_t *row, int64_t n, double *out) {
         }
         return;
     }
-    for (int64_t i = 0; i < n; ++i) {
-        int64_t b = i / 32, e = i % 32;
-        if (type == T_Q8_0) {
-            const uint8_t *blk = row + b * 34;
-            double d = half_to_double((uint16_t)(blk[0] | (blk[1] << 8)));
-            out[i] = d * (double)(int8_t)blk[2 + e];
-        } else {
-            const uint8_t *blk = row + b * 18;
-            double d = half_to_double((uint16_t)(blk[0] | (blk[1] << 8)));
-            int q = e < 16 ? (blk[2 + e] & 0x0f) : (blk[2 + e - 16] >> 4);
-            out[i] = d * (double)(q - 8);
+    const int64_t bsz = type == T_Q8_0 ? 34 : 18;
+    for (int64_t b = 0; b * 32 < n; ++b) {
+        const uint8_t *blk = row + b * bsz;
+        const double d = half_to_double((uint16_t)(blk[0] | (blk[1] << 8)));   /* the block's scale */
+        const int64_t m = n - b * 32 < 32 ? n - b * 32 : 32;
+        for (int64_t e = 0; e < m; ++e) {
+            if (type == T_Q8_0) {
+                out[b * 32 + e] = d * (double)(int8_t)blk[2 + e];
+            } else {
+                int q = e < 16 ? (blk[2 + e] & 0x0f) : (blk[2 + e - 16] >> 4);
+                out[b * 32 + e] = d * (double)(q - 8);
+            }
         }
     }
 }
@@ -130,9 +141,10 @@ class Pool {
         for (int t = 1; t < n_; ++t) workers_.emplace_back([this, t, start] { loop(t, start); });
     }
     int size() const { return n_; }
-    /* fn(lo, hi) over [0, n) in n_ contiguous chunks; the caller runs chunk 0. */
-    void parallel_for(int64_t n, const std::function<void(int64_t, int64_t)> &fn) {
-        if (n_ == 1 || n < 64) { fn(0, n); return; }
+    /* fn(lo, hi) over [0, n) in n_ contiguous chunks; the caller runs chunk 0. Fewer than
+     * min_n items run on the calling thread alone. */
+    void parallel_for(int64_t n, const std::function<void(int64_t, int64_t)> &fn, int64_t min_n = 64) {
+        if (n_ == 1 || n < min_n) { fn(0, n); return; }
         {
             std::unique_lock<std::mutex> lk(m_);
             job_ = &fn; total_ = n; pending_ = n_ - 1; ++gen_;
@@ -182,18 +194,42 @@ class Pool {
 Pool &pool() { static Pool p(1); return p; }
 
 /* ------------------------------------------------------------------ ops */
-/* y[n] = sum_k W[n][k] x[k]: W stored row-major, row n = the K inputs of output n. */
-void matvec(int type, const uint8_t *W, int64_t N, int64_t K, const double *x, double *y) {
+/* Y[t][n] = sum_k W[n][k] X[t][k] for the T rows of X: W stored row-major (row n = the K inputs
+ * of output n), X [T][K] and Y [T][N] row-major. Every output is one sum in increasing k of
+ * products rounded before they are added (no fused multiply-add), so it does not depend on T or
+ * on the thread count. A row is dequantized once per group of 8 tokens (the last tokens of X, fewer
+ * than 8, one by one). */
+template <int G>
+void matmat_group(const double *w, int64_t K, const double *xg, double *s) {
+    for (int j = 0; j < G; ++j) s[j] = 0.0;
+    for (int64_t k = 0; k < K; ++k)
+        for (int j = 0; j < G; ++j) s[j] += w[k] * xg[k * G + j];
+}
+
+void matmat(int type, const uint8_t *W, int64_t N, int64_t K, const double *X, int64_t T, double *Y) {
+    constexpr int G = 8;
     const int64_t rb = row_bytes(type, K);
     pool().parallel_for(N, [&](int64_t lo, int64_t hi) {
-        std::vector<double> w(K);
-        for (int64_t n = lo; n < hi; ++n) {
-            dequant_row(type, W + n * rb, K, w.data());
-            double s = 0.0;
-            for (int64_t k = 0; k < K; ++k) s += w[k] * x[k];
-            y[n] = s;
+        std::vector<double> w(K), xg((size_t)K * G);
+        for (int64_t t0 = 0; t0 < T;) {
+            const int g = T - t0 >= G ? G : 1;
+            for (int64_t k = 0; k < K; ++k)               /* the group's inputs, side by side per k */
+                for (int j = 0; j < g; ++j) xg[k * g + j] = X[(t0 + j) * K + k];
+            for (int64_t n = lo; n < hi; ++n) {
+                dequant_row(type, W + n * rb, K, w.data());
+                double s[G];
+                if (g == G) matmat_group<G>(w.data(), K, xg.data(), s);
+                else matmat_group<1>(w.data(), K, xg.data(), s);
+                for (int j = 0; j < g; ++j) Y[(t0 + j) * N + n] = s[j];
+            }
+            t0 += g;
         }
     });
+}
+
+/* y[n] = sum_k W[n][k] x[k]: one token of matmat. */
+void matvec(int type, const uint8_t *W, int64_t N, int64_t K, const double *x, double *y) {
+    matmat(type, W, N, K, x, 1, y);
 }
 
 void rmsnorm(const double *x, int64_t n, const float *g, double eps, double *y) {
@@ -270,65 +306,122 @@ struct Ctx {
     uint32_t n_ctx, n_seq_max, n_ubatch;
     std::vector<Seq> seqs;
     int64_t used = 0;
-    /* trace of one layer for the most recent token: x in, q after RoPE, o, x after attention */
+    bool elide = true;   /* last layer: K and V only for tokens whose logits are not flagged */
+    /* trace of one layer for the most recent token that ran it whole: x in, q after RoPE, o,
+     * x after attention */
     int32_t trace_layer = -1;
     std::vector<double> tr_x, tr_q, tr_o, tr_x1;
 };
 
 int64_t kv_width(const Hparams &hp) { return (int64_t)hp.n_head_kv * hp.head_dim; }
 
-/* Runs one validated token through every layer, appending its cell; logits if flagged. */
-void forward_token(Ctx &c, int32_t tok, int32_t pos, int32_t seq, double *logits, int32_t *argmax) {
+constexpr int64_t kBlock = 256;   /* tokens evaluated layer by layer together */
+
+/* Runs tokens tok[0..T) (validated; positions continue their sequences) through every layer,
+ * appending their cells, and writes the logits and argmax of the flagged ones, in order. */
+void run_block(Ctx &c, int64_t T, const int32_t *tok, const int32_t *pos, const int32_t *seq, const int8_t *flag,
+               double *logits, int32_t *argmax) {
     const Model &m = *c.m;
     const Hparams &hp = m.hp;
-    const int64_t d = hp.n_embd, hd = hp.head_dim, H = hp.n_head, KVW = kv_width(hp), F = hp.n_ff;
-    const int64_t F_pad = (F + 31) / 32 * 32, L = hp.n_layer;
-    std::vector<double> x(d), xn(d), q(H * hd), k(KVW), v(KVW), o(H * hd), y(d), g(F), u(F), h(F_pad, 0.0);
-    dequant_row(hp.t_embd, m.tok_embd + (int64_t)tok * row_bytes(hp.t_embd, d), d, x.data());
-
-    Seq &s = c.seqs[seq];
-    s.k.resize(L);
-    s.v.resize(L);
-    const int64_t cell = pos;                                  /* positions of a sequence are 0..n-1 */
+    const int64_t d = hp.n_embd, hd = hp.head_dim, H = hp.n_head, KVH = hp.n_head_kv, KVW = kv_width(hp);
+    const int64_t F = hp.n_ff, F_pad = (F + 31) / 32 * 32, L = hp.n_layer;
+    std::vector<double> X((size_t)T * d), XN((size_t)T * d), Y((size_t)T * d);
+    for (int64_t t = 0; t < T; ++t)
+        dequant_row(hp.t_embd, m.tok_embd + (int64_t)tok[t] * row_bytes(hp.t_embd, d), d, &X[t * d]);
+    std::vector<int64_t> all(T), out;
+    for (int64_t t = 0; t < T; ++t) {
+        all[t] = t;
+        if (flag[t]) out.push_back(t);
+    }
+    for (int64_t t = 0; t < T; ++t) {   /* room for the new cells */
+        Seq &s = c.seqs[seq[t]];
+        s.k.resize(L);
+        s.v.resize(L);
+    }
+    /* gathers rows idx of A [.][w] into B [idx.size()][w] and back */
+    auto gather = [](const std::vector<double> &A, int64_t w, const std::vector<int64_t> &idx, std::vector<double> &B) {
+        B.resize(idx.size() * w);
+        for (size_t i = 0; i < idx.size(); ++i) std::memcpy(&B[i * w], &A[idx[i] * w], w * sizeof(double));
+    };
 
     for (int64_t l = 0; l < L; ++l) {
         const Layer &W = m.layers[l];
-        rmsnorm(x.data(), d, W.attn_norm, hp.rms_eps, xn.data());
-        matvec(hp.t_linear, W.wq, H * hd, d, xn.data(), q.data());
-        matvec(hp.t_linear, W.wk, KVW, d, xn.data(), k.data());
-        matvec(hp.t_linear, W.wv, KVW, d, xn.data(), v.data());
-        for (int64_t hh = 0; hh < H; ++hh) rope(q.data() + hh * hd, (int)hd, pos, hp.rope_theta);
-        for (int64_t hh = 0; hh < hp.n_head_kv; ++hh) rope(k.data() + hh * hd, (int)hd, pos, hp.rope_theta);
-        s.k[l].resize((size_t)(cell + 1) * KVW);
-        s.v[l].resize((size_t)(cell + 1) * KVW);
-        for (int64_t e = 0; e < KVW; ++e) {
-            s.k[l][cell * KVW + e] = round_to_half(k[e]);
-            s.v[l][cell * KVW + e] = round_to_half(v[e]);
+        /* the tokens that run the whole layer: all but, in the last layer, the unflagged ones */
+        const std::vector<int64_t> &full = (l == L - 1 && c.elide) ? out : all;
+        const int64_t nf = (int64_t)full.size();
+        for (int64_t t = 0; t < T; ++t) rmsnorm(&X[t * d], d, W.attn_norm, hp.rms_eps, &XN[t * d]);
+        std::vector<double> K((size_t)T * KVW), V((size_t)T * KVW), XF, Q((size_t)nf * H * hd);
+        matmat(hp.t_linear, W.wk, KVW, d, XN.data(), T, K.data());
+        matmat(hp.t_linear, W.wv, KVW, d, XN.data(), T, V.data());
+        gather(XN, d, full, XF);
+        matmat(hp.t_linear, W.wq, H * hd, d, XF.data(), nf, Q.data());
+        for (int64_t i = 0; i < nf; ++i)
+            for (int64_t h = 0; h < H; ++h) rope(&Q[(i * H + h) * hd], (int)hd, pos[full[i]], hp.rope_theta);
+        for (int64_t t = 0; t < T; ++t) {   /* K after RoPE and V, rounded to f16, into the cells */
+            for (int64_t h = 0; h < KVH; ++h) rope(&K[t * KVW + h * hd], (int)hd, pos[t], hp.rope_theta);
+            Seq &s = c.seqs[seq[t]];
+            const int64_t cell = pos[t];   /* positions of a sequence are 0..n-1 */
+            if ((int64_t)s.k[l].size() < (cell + 1) * KVW) {
+                s.k[l].resize((size_t)(cell + 1) * KVW);
+                s.v[l].resize((size_t)(cell + 1) * KVW);
+            }
+            for (int64_t e = 0; e < KVW; ++e) {
+                s.k[l][cell * KVW + e] = round_to_half(K[t * KVW + e]);
+                s.v[l][cell * KVW + e] = round_to_half(V[t * KVW + e]);
+            }
         }
-        attend_gqa(q.data(), s.k[l].data(), s.v[l].data(), pos + 1, (int)H, hp.n_head_kv, (int)hd, o.data());
-        if (l == c.trace_layer) { c.tr_x = x; c.tr_q = q; c.tr_o = o; }
-        matvec(hp.t_linear, W.wo, d, H * hd, o.data(), y.data());
-        for (int64_t i = 0; i < d; ++i) x[i] += y[i];
-        if (l == c.trace_layer) c.tr_x1 = x;
-        rmsnorm(x.data(), d, W.ffn_norm, hp.rms_eps, xn.data());
-        matvec(hp.t_linear, W.w_gate, F, d, xn.data(), g.data());
-        matvec(hp.t_linear, W.w_up, F, d, xn.data(), u.data());
-        for (int64_t i = 0; i < F; ++i) h[i] = silu(g[i]) * u[i];
-        matvec(hp.t_linear, W.w_down, d, F_pad, h.data(), y.data());
-        for (int64_t i = 0; i < d; ++i) x[i] += y[i];
+        if (nf == 0) continue;
+        /* attention: query head h of token t over the cells of its sequence with pos <= pos_t */
+        std::vector<double> O((size_t)nf * H * hd);
+        const int group = (int)(H / KVH);
+        pool().parallel_for(nf * H, [&](int64_t lo, int64_t hi) {
+            for (int64_t i = lo; i < hi; ++i) {
+                const int64_t f = i / H, h = i % H, t = full[f];
+                const Seq &s = c.seqs[seq[t]];
+                const int64_t kv = h / group;
+                attend_head(&Q[i * hd], s.k[l].data() + kv * hd, s.v[l].data() + kv * hd, pos[t] + 1, KVW, (int)hd,
+                            &O[i * hd]);
+            }
+        }, 2);
+        if (l == c.trace_layer) {
+            const int64_t f = nf - 1, t = full[f];
+            c.tr_x.assign(&X[t * d], &X[t * d] + d);
+            c.tr_q.assign(&Q[f * H * hd], &Q[f * H * hd] + H * hd);
+            c.tr_o.assign(&O[f * H * hd], &O[f * H * hd] + H * hd);
+        }
+        matmat(hp.t_linear, W.wo, d, H * hd, O.data(), nf, Y.data());
+        for (int64_t i = 0; i < nf; ++i)
+            for (int64_t e = 0; e < d; ++e) X[full[i] * d + e] += Y[i * d + e];
+        if (l == c.trace_layer) c.tr_x1.assign(&X[full[nf - 1] * d], &X[full[nf - 1] * d] + d);
+        /* SwiGLU feed-forward; ffn_down's inputs past n_ff are zero */
+        for (int64_t i = 0; i < nf; ++i) rmsnorm(&X[full[i] * d], d, W.ffn_norm, hp.rms_eps, &XN[i * d]);
+        std::vector<double> G((size_t)nf * F), U((size_t)nf * F), Hh((size_t)nf * F_pad, 0.0);
+        matmat(hp.t_linear, W.w_gate, F, d, XN.data(), nf, G.data());
+        matmat(hp.t_linear, W.w_up, F, d, XN.data(), nf, U.data());
+        for (int64_t i = 0; i < nf; ++i)
+            for (int64_t e = 0; e < F; ++e) Hh[i * F_pad + e] = silu(G[i * F + e]) * U[i * F + e];
+        matmat(hp.t_linear, W.w_down, d, F_pad, Hh.data(), nf, Y.data());
+        for (int64_t i = 0; i < nf; ++i)
+            for (int64_t e = 0; e < d; ++e) X[full[i] * d + e] += Y[i * d + e];
     }
-    s.n = pos + 1;
-    c.used += 1;
-
-    if (logits) {
-        rmsnorm(x.data(), d, m.output_norm, hp.rms_eps, xn.data());
-        const uint8_t *Wout = m.output ? m.output : m.tok_embd;
-        int tout = m.output ? hp.t_out : hp.t_embd;
-        matvec(tout, Wout, hp.n_vocab, d, xn.data(), logits);
+    for (int64_t t = 0; t < T; ++t) {
+        Seq &s = c.seqs[seq[t]];
+        if (pos[t] + 1 > s.n) s.n = pos[t] + 1;
+        c.used += 1;
+    }
+    if (out.empty()) return;
+    /* final norm and the head for the flagged tokens (step 14) */
+    const int64_t no = (int64_t)out.size();
+    for (int64_t i = 0; i < no; ++i) rmsnorm(&X[out[i] * d], d, m.output_norm, hp.rms_eps, &XN[i * d]);
+    const uint8_t *Wout = m.output ? m.output : m.tok_embd;
+    const int tout = m.output ? hp.t_out : hp.t_embd;
+    matmat(tout, Wout, hp.n_vocab, d, XN.data(), no, logits);
+    for (int64_t i = 0; i < no; ++i) {
+        const double *lg = logits + i * hp.n_vocab;
         int32_t best = 0;
-        for (int32_t i = 1; i < hp.n_vocab; ++i)
-            if (logits[i] > logits[best]) best = i;
-        *argmax = best;
+        for (int32_t j = 1; j < hp.n_vocab; ++j)
+            if (lg[j] > lg[best]) best = j;
+        argmax[i] = best;
     }
 }
 
@@ -448,31 +541,47 @@ int32_t orc_decode(void *cv, int32_t n_tokens, const int32_t *token, const int32
         flag[i] = flags_in ? (flags_in[i] != 0) : (int8_t)(i == n_tokens - 1);
     }
     if (c->used + n_tokens > (int64_t)c->n_ctx) return 1;
+    /* ubatches: consecutive chunks of n_ubatch tokens, each evaluated in blocks of kBlock */
+    std::vector<double> tmp;
     int32_t row = 0;
-    for (int32_t i = 0; i < n_tokens; ++i) {
+    for (int32_t u0 = 0; u0 < n_tokens; u0 += (int32_t)c->n_ubatch) {
+        const int32_t u1 = u0 + (int32_t)c->n_ubatch < n_tokens ? u0 + (int32_t)c->n_ubatch : n_tokens;
+        int32_t nu = 0;
+        for (int32_t i = u0; i < u1; ++i) nu += flag[i];
         double *lg = nullptr;
-        std::vector<double> tmp;
-        int32_t am = -1;
-        if (flag[i]) {
-            if (logits_out) lg = logits_out + (int64_t)row * hp.n_vocab;
-            else { tmp.resize(hp.n_vocab); lg = tmp.data(); }
+        if (logits_out) {
+            lg = logits_out + (int64_t)row * hp.n_vocab;
+        } else {
+            tmp.resize((size_t)nu * hp.n_vocab);
+            lg = tmp.data();
         }
-        forward_token(*c, token[i], pos[i], seq[i], lg, &am);
-        if (flag[i]) {
-            /* a logit that is not finite fails the ubatch (step 13, a failed compute: its cells
-             * are removed again); earlier ubatches stay */
-            for (int32_t j = 0; j < hp.n_vocab; ++j)
-                if (!std::isfinite(lg[j])) {
-                    rollback(*c, i - i % (int32_t)c->n_ubatch, i, seq.data(), pos.data());
-                    return -3;
-                }
-            if (argmax_out) argmax_out[row] = am;
-            ++row;
+        std::vector<int32_t> am(nu > 0 ? nu : 1);
+        int32_t r = 0;
+        for (int32_t b0 = u0; b0 < u1; b0 += (int32_t)kBlock) {
+            const int32_t b1 = b0 + (int32_t)kBlock < u1 ? b0 + (int32_t)kBlock : u1;
+            run_block(*c, b1 - b0, token + b0, pos.data() + b0, seq.data() + b0, flag.data() + b0,
+                      lg + (int64_t)r * hp.n_vocab, am.data() + r);
+            for (int32_t i = b0; i < b1; ++i) r += flag[i];
         }
+        /* a logit that is not finite fails the ubatch (step 13, a failed compute: its cells are
+         * removed again); earlier ubatches and their rows stay */
+        for (int64_t j = 0; j < (int64_t)nu * hp.n_vocab; ++j)
+            if (!std::isfinite(lg[j])) {
+                rollback(*c, u0, u1 - 1, seq.data(), pos.data());
+                if (n_out) *n_out = row;
+                return -3;
+            }
+        if (argmax_out)
+            for (int32_t i = 0; i < nu; ++i) argmax_out[row + i] = am[i];
+        row += nu;
     }
     if (n_out) *n_out = row;
     return 0;
 }
+
+/* Last layer: 1 = tokens whose logits are not flagged compute only their K and V (the default),
+ * 0 = every token runs the whole layer. The results are the same either way. */
+void orc_set_elide(void *cv, int32_t on) { ((Ctx *)cv)->elide = on != 0; }
 
 /* Record intermediates of `layer` for each token run (the last one is kept); -1 = off. */
 void orc_set_trace(void *cv, int32_t layer) { ((Ctx *)cv)->trace_layer = layer; }
@@ -494,6 +603,9 @@ double orc_half_to_double(uint16_t h) { return half_to_double(h); }
 double orc_round_to_half(double x) { return round_to_half(x); }
 void orc_matvec(int32_t type, const void *W, int64_t N, int64_t K, const double *x, double *y) {
     matvec(type, (const uint8_t *)W, N, K, x, y);
+}
+void orc_matmat(int32_t type, const void *W, int64_t N, int64_t K, const double *X, int64_t T, double *Y) {
+    matmat(type, (const uint8_t *)W, N, K, X, T, Y);
 }
 void orc_rmsnorm(const double *x, int64_t n, const float *g, double eps, double *y) { rmsnorm(x, n, g, eps, y); }
 void orc_rope(double *x, int32_t hd, int64_t pos, double theta) { rope(x, hd, pos, theta); }

@@ -372,7 +372,9 @@ def test_default_flags_select_last_token(tiny_model):
 
 def test_non_finite_logits_fail_their_ubatch():
     """A flagged row whose logits are not finite is a failed compute (-3): the cells of its
-    ubatch are removed again, earlier ubatches and their rows stay."""
+    ubatch are removed again; earlier ubatches stay in the cache, and so do their logits rows,
+    which the decode loop copied out before the failing ubatch ran (step 12: each ubatch's rows
+    are copied into the output buffer inside the loop, and the failure returns from it)."""
     import dataclasses
     cfg = synth.CONFIGS["tiny"]
     host = synth.make_model(cfg)
@@ -385,10 +387,102 @@ def test_non_finite_logits_fail_their_ubatch():
     rc, lg, am = octx.decode([1, bad], logits=[1, 1])
     assert rc == -3 and lg.shape[0] == 0 and octx.seq_pos_max(0) == -1
     # ubatches [1, 2] [3, bad] [5]: the bad token's K/V reach token 5, whose row fails; the
-    # first two ubatches stay (positions 0..3), no rows are reported
+    # first two ubatches stay (positions 0..3) with the one row they flagged (token 2)
     octx = oracle.Context(om, cfg.n_ctx, 1, 2)
     rc, lg, am = octx.decode([1, 2, 3, bad, 5], logits=[0, 1, 0, 0, 1])
-    assert rc == -3 and lg.shape[0] == 0
+    assert rc == -3 and lg.shape[0] == 1 and am.shape[0] == 1
     assert octx.seq_pos_max(0) == 3
+    good = oracle.Context(om, cfg.n_ctx, 1, 2)
+    rc2, lg2, am2 = good.decode([1, 2], logits=[0, 1])    # that row alone, from a clean context
+    assert rc2 == 0 and np.array_equal(lg, lg2) and np.array_equal(am, am2)
     rc, lg, am = octx.decode([9], logits=[1])             # the sequence goes on from position 4
-    assert rc == -3 and octx.seq_pos_max(0) == 3           # (its K/V still include the bad cell)
+    assert rc == -3 and lg.shape[0] == 0 and octx.seq_pos_max(0) == 3   # (its K/V still include the bad cell)
+
+
+# ----------------------------------------------------------------------------- evaluation order
+@pytest.mark.parametrize("T", [1, 3, 8, 13, 17])
+def test_matmat_rows_equal_matvec_and_brute_force(T):
+    """Every token of a block product is the same k-ordered sum as its own matrix-vector
+    product (bit for bit), and both are the plain product of the dequantized matrix."""
+    K, N = 704, 37
+    w = synth.normal(11, T, N * K, 0.0, 0.05).reshape(N, K)
+    rows = synth.encode(w, synth.Q4_0)
+    X = np.random.default_rng(T).normal(size=(T, K))
+    Y = oracle.matmat(synth.Q4_0, rows, N, K, X)
+    for t in range(T):
+        assert np.array_equal(Y[t], oracle.matvec(synth.Q4_0, rows, N, K, X[t])), t
+    assert np.allclose(Y, X @ oracle.dequant_matrix(synth.Q4_0, rows, K).T, rtol=1e-12, atol=1e-14)
+
+
+def test_blocks_of_a_long_ubatch_equal_stepwise_decode(tiny_model):
+    """A 300-token ubatch runs as two blocks (256 + 44 tokens) layer by layer; it must equal 300
+    single-token decodes bit for bit, rows and cells."""
+    toks = synth.uniform_int(TINY.token_seed, 77, 300, 0, TINY.n_vocab)
+    a = _ctx(tiny_model, n_ctx=512)
+    flags = np.zeros(300, np.int8)
+    flags[[0, 255, 256, 299]] = 1
+    rc, la, ia = a.decode(toks, logits=flags)
+    assert rc == 0 and la.shape[0] == 4
+    b = _ctx(tiny_model, n_ctx=512)
+    rows = []
+    for i, t in enumerate(toks):
+        rc, lb, _ = b.decode([t], logits=[flags[i]])
+        assert rc == 0
+        if flags[i]:
+            rows.append(lb[0])
+    assert np.array_equal(la, np.stack(rows))
+    for l in range(TINY.n_layer):
+        for p in (0, 100, 255, 256, 299):
+            assert all(np.array_equal(u, v) for u, v in zip(a.kv_get(0, p, l), b.kv_get(0, p, l)))
+
+
+def _elision_case(cfg, n_layer, n_tok, flags_at):
+    host = synth.make_model(cfg, n_layer=n_layer)
+    om = oracle.Model(host)
+    toks = synth.prompt_tokens(cfg, n_tok)
+    flags = np.zeros(n_tok, np.int8)
+    flags[flags_at] = 1
+    out = []
+    for elide in (True, False):
+        c = oracle.Context(om, 512, 1, 512)
+        c.set_elide(elide)
+        rc, lg, am = c.decode(toks, logits=flags)
+        assert rc == 0 and lg.shape[0] == len(flags_at)
+        rc2, lg2, am2 = c.decode([int(am[-1])])           # a step that attends the elided tokens' cells
+        assert rc2 == 0
+        cells = [c.kv_get(0, p, l) for l in range(n_layer) for p in range(n_tok + 1)]
+        out.append((lg, am, lg2, am2, cells))
+    (la, aa, la2, aa2, ca), (lb, ab, lb2, ab2, cb) = out
+    assert np.array_equal(la, lb) and np.array_equal(aa, ab)
+    assert np.array_equal(la2, lb2) and np.array_equal(aa2, ab2)
+    assert all(np.array_equal(x[0], y[0]) and np.array_equal(x[1], y[1]) for x, y in zip(ca, cb))
+
+
+def test_last_layer_elision_is_exact_tiny():
+    """Unflagged tokens computing only K and V in the last layer changes no logit and no cell."""
+    _elision_case(TINY, 2, 20, [0, 9, 19])
+
+
+def test_last_layer_elision_is_exact_1b_shape():
+    _elision_case(synth.CONFIGS["1b"], 16, 10, [3, 9])
+
+
+@pytest.mark.parametrize("n_threads", [2, 8])
+def test_thread_count_changes_nothing(tiny_model, n_threads):
+    """The pool's chunking (rows of every product, query heads of attention) must not change a
+    bit of the result: the same batch with 1 and with several threads."""
+    toks = synth.uniform_int(TINY.token_seed, 78, 70, 0, TINY.n_vocab)
+    seqs = np.arange(70) % 3
+    res = []
+    for n in (1, n_threads):
+        oracle.set_threads(n)
+        try:
+            c = _ctx(tiny_model, n_ctx=256, n_seq=3)
+            rc, lg, am = c.decode(toks, seq=seqs, logits=np.ones(70))
+            assert rc == 0
+            res.append((lg, am, [c.kv_get(s, p, l) for s in range(3) for p in (0, 11, 22) for l in (0, 1)]))
+        finally:
+            oracle.set_threads(1)
+    (la, aa, ca), (lb, ab, cb) = res
+    assert np.array_equal(la, lb) and np.array_equal(aa, ab)
+    assert all(np.array_equal(x[0], y[0]) and np.array_equal(x[1], y[1]) for x, y in zip(ca, cb))
