@@ -250,6 +250,124 @@ def time_sampler(n_vocab, stream, iters=50):
     return out
 
 
+def decode_bytes_seqs(cfg, host, ctx_lens):
+    """Algorithmic HBM bytes of one decode ubatch whose tokens attend ctx_lens cells each: every
+    weight as stored once (one embedding row per token) plus the K/V of every attended cell."""
+    w = host.output.nbytes + host.output_norm.nbytes
+    for L in host.layers:
+        w += sum(v.nbytes for v in L.values())
+    kv_cell = cfg.n_layer * cfg.n_head_kv * cfg.head_dim * 2 * 2
+    return w + host.tok_embd.shape[1] * len(ctx_lens) + kv_cell * int(np.sum(ctx_lens))
+
+
+def timed(stream, fn):
+    """Device milliseconds of fn() between CUDA events on `stream` (synchronized on both sides)."""
+    import torch
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1)
+
+
+def run_workloads(names, gm8, host8, stream, hbm, bf16):
+    """Throughput of the other named workloads, each a warm-up run then one timed run; tokens/s and
+    the fraction of the roofline that bounds each phase (decode: algorithmic bytes over the measured
+    HBM bandwidth; prefill: algorithmic flops over the measured bf16 tensor peak)."""
+    import torch
+
+    import llama_ubatch_forward_gb300 as lcx
+    import synth
+    from llama_ubatch_forward_gb300.torch_io import upload
+    out = {}
+
+    def prefill_decode(key, cfg, host, gm, n_prompt, n_ub, n_ctx, n_dec):
+        ctx = lcx.Context(gm, n_ctx, 1, n_ub, stream=stream)
+        prompt = synth.prompt_tokens(cfg, n_prompt)
+        gen = torch.zeros(n_dec, dtype=torch.int32, device="cuda")
+        am = np.zeros(1, np.int32)
+        res = {}
+        for rep in range(2):   # warm-up, then timed
+            ctx.kv_clear()
+            pre = timed(stream, lambda: ctx.decode(prompt, argmax_out=am))
+            dec = timed(stream, lambda: ctx.decode_greedy(0, int(am[0]), n_dec, gen))
+            res = {"prefill_ms": pre, "decode_ms": dec}
+        del ctx
+        dec_b = decode_bytes_per_step(cfg, host, n_prompt, n_dec) / n_dec
+        pf = prefill_flops(cfg, n_prompt)
+        dgbs = dec_b * n_dec / (res["decode_ms"] / 1e3) / 1e9
+        ptf = pf / (res["prefill_ms"] / 1e3) / 1e12
+        out[key] = {"workload": f"{cfg.name}: {n_prompt}-token prompt in ubatches of {n_ub}, then {n_dec} greedy "
+                                f"decode steps", "warmup": 1, "steps": 1,
+                    "decode": {"value": round(n_dec / (res["decode_ms"] / 1e3), 2), "unit": "tokens/s",
+                               "bytes_per_step": round(dec_b), "achieved_gbs": round(dgbs, 1),
+                               "frac": round(dgbs / hbm, 4), "bound": "hbm"},
+                    "prefill": {"value": round(n_prompt / (res["prefill_ms"] / 1e3), 1), "unit": "tokens/s",
+                                "flops": pf, "achieved_tflops": round(ptf, 2), "frac": round(ptf / bf16, 4),
+                                "bound": "tensor"}}
+        log(f"[bench] {key}: {json.dumps(out[key])}")
+
+    if "1b" in names:
+        cfg = synth.CONFIGS["1b"]
+        host = synth.make_model(cfg)
+        gm = upload(host)
+        prefill_decode("1b", cfg, host, gm, 512, 512, cfg.n_ctx, 128)
+        del gm, host
+    if "long" in names:
+        # the long-context workload runs on the 8B-shape model itself (its own prompt draw)
+        cfg = synth.CONFIGS["long"]
+        prefill_decode("long", cfg, host8, gm8, 32768, 2048, cfg.n_ctx, 128)
+    if "multiseq" in names:
+        cfg = synth.CONFIGS["multiseq"]
+        n_seq, n_steps = 64, 128
+        lens = synth.multiseq_prompt_lengths(cfg, n_seq)
+        prompts = [synth.prompt_tokens(cfg, int(lens[s]), s) for s in range(n_seq)]
+        ctx = lcx.Context(gm8, cfg.n_ctx, n_seq, 512, stream=stream)
+        seqs = np.arange(n_seq, dtype=np.int32)
+        flags = np.ones(n_seq, np.int8)
+        am = np.zeros(n_seq, np.int32)
+        res = {}
+        for rep in range(2):   # warm-up, then timed
+            ctx.kv_clear()
+            first = np.zeros(n_seq, np.int32)
+
+            def prefill():
+                one = np.zeros(1, np.int32)
+                for sq in range(n_seq):
+                    assert ctx.decode(prompts[sq], seq_id=np.full(prompts[sq].size, sq, np.int32),
+                                      argmax_out=one) == 0
+                    first[sq] = one[0]
+
+            def decode():
+                toks = first.copy()
+                for _ in range(n_steps):
+                    assert ctx.decode(toks, seq_id=seqs, logits=flags, argmax_out=am) == 0
+                    toks = am.copy()
+
+            res = {"prefill_ms": timed(stream, prefill), "decode_ms": timed(stream, decode)}
+        del ctx
+        n_pre = int(np.sum(lens))
+        step_bytes = [decode_bytes_seqs(cfg, host8, lens + i + 1) for i in range(n_steps)]
+        dgbs = sum(step_bytes) / (res["decode_ms"] / 1e3) / 1e9
+        pf = sum(prefill_flops(cfg, int(n)) - 2 * cfg.n_vocab * cfg.n_embd for n in lens) + \
+            n_seq * 2 * cfg.n_vocab * cfg.n_embd
+        ptf = pf / (res["prefill_ms"] / 1e3) / 1e12
+        out["multiseq"] = {
+            "workload": f"multiseq: {n_seq} sequences, prompts of {int(lens.min())}-{int(lens.max())} tokens "
+                        f"({n_pre} in total) prefilled in ubatches of 512, then {n_steps} steps of one "
+                        f"{n_seq}-token ubatch (one token per sequence, every row flagged, host argmax per step)",
+            "warmup": 1, "steps": 1,
+            "decode": {"value": round(n_seq * n_steps / (res["decode_ms"] / 1e3), 1), "unit": "tokens/s",
+                       "bytes_per_step": round(sum(step_bytes) / n_steps), "achieved_gbs": round(dgbs, 1),
+                       "frac": round(dgbs / hbm, 4), "bound": "hbm"},
+            "prefill": {"value": round(n_pre / (res["prefill_ms"] / 1e3), 1), "unit": "tokens/s", "flops": pf,
+                        "achieved_tflops": round(ptf, 2), "frac": round(ptf / bf16, 4), "bound": "tensor"}}
+        log(f"[bench] multiseq: {json.dumps(out['multiseq'])}")
+    return out
+
+
 def run_lcx(a, rank, world):
     import torch
 
@@ -350,6 +468,13 @@ def run_lcx(a, rank, world):
             timeline = {"error": str(ex)}
 
     hbm, bf16, bf16_sus, src = peaks()
+    workloads = None
+    if a.workloads and not a.layers and cfg.name == "8b":
+        names = [w for w in a.workloads.split(",") if w]
+        try:
+            workloads = run_workloads(names, gm, host, stream, hbm, bf16)
+        except Exception as ex:  # reported, never costs the main line
+            workloads = {"error": repr(ex)}
     g = prof["gemv"]
     # one launch per decode token: the persistent step kernel (weights, KV and head in one launch)
     step_kernel = g["launches"] == n_dec and prof["attention"]["launches"] == 0
@@ -382,13 +507,15 @@ def run_lcx(a, rank, world):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "q4_0 weights x f32 (decode GEMV), f16 x f16 -> f32 (prefill matmul)",
+        "dtype": "q4_0/q8_0 weights (as stored) x activations split per 32-block into int8 hi + lo "
+                 "(about 14 bits; integer dot products, f32 accumulation) in decode; weights dequantized to "
+                 "f16 x activations as f16 hi + lo pairs (about 22 bits) -> f32 on the tensor cores in prefill",
         "data": "synthetic (seeded N(0,0.02) weights, uniform token ids)",
         "config": workload_config(a, cfg, n_prompt, n_dec, n_ub, world),
         "prefill": {"value": round(prefill_tps, 1), "unit": "tokens/s",
                     "achieved_tflops": round(pre_tf, 2),
                     "roofline_frac": round(pre_tf / bf16, 4)},
-        "decode_roofline": {"bytes_per_step": dec_bytes, "achieved_gbs": round(dec_gbs, 1), "peak": hbm,
+        "decode_roofline": {"bytes_per_step": round(dec_bytes / n_dec), "achieved_gbs": round(dec_gbs, 1), "peak": hbm,
                             "frac": round(dec_gbs / hbm, 4), "peak_source": src},
         "roofline": {"bound": "hbm", "kernel": dom_kernel,
                      "achieved": round(gemv_gbs, 1), "peak": hbm, "unit": "GB/s",
@@ -397,7 +524,11 @@ def run_lcx(a, rank, world):
                      "avg_launch_us": round(g["ms"] * 1e3 / max(1, g["launches"]), 2)},
         "roofline_prefill": {"bound": "tensor", "kernel": "gemm (prefill matmuls)", "achieved": round(gemm_tf, 2),
                              "peak": bf16, "unit": "TFLOP/s", "frac": round(gemm_tf / bf16, 4), "traffic": None,
-                             "peak_source": src},
+                             "peak_source": src, "issued_tflops": round(2 * gemm_tf, 2),
+                             "issued_frac": round(2 * gemm_tf / bf16, 4),
+                             "note": "achieved counts 2 T N K algorithmic flops; every MMA multiplies the weights by "
+                                     "the activations' f16 hi and lo parts, so twice that is issued and the "
+                                     "design's ceiling is 0.5 of the peak in algorithmic flops"},
         "kernel_profile": {ph: {k: {"launches": v["launches"], "ms": round(v["ms"], 3),
                                     "GBps": round(v["bytes"] / v["ms"] / 1e6, 1) if v["ms"] else None,
                                     "TFLOPps": round(v["flops"] / v["ms"] / 1e9, 2) if v["ms"] else None}
@@ -410,6 +541,7 @@ def run_lcx(a, rank, world):
         "gpu_launches": int(launches_per_step * a.steps),
         "sampler": sampler,
         **({"timeline": timeline} if timeline is not None else {}),
+        **({"workloads": workloads} if workloads is not None else {}),
         "clocks": clk,
     }
     if rank == 0:
@@ -453,7 +585,9 @@ def run_reference(a, rank, world):
         "value": round(v, 4), "unit": "tokens/s", "n_gpus": world, "steps": a.steps, "warmup": a.warmup,
         "ms_per_step": round(1e3 * sum(times) / a.steps, 1), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,0.02) weights, uniform token ids)",
-        "config": workload_config(a, cfg, n_prompt, n_dec, n_ub, world),
+        "config": {**workload_config(a, cfg, n_prompt, n_dec, n_ub, world),
+                   "sample": f"each step times {per} decode steps after a 4-token prompt of the same model (the "
+                             f"fp64 oracle cannot run the full workload in minutes)"},
         "cpu_baseline": {"value": round(v, 4), "unit": "tokens/s", "cores": n, "kind": "oracle", "sample": sample},
         "e2e": {"value": round(v, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
@@ -473,6 +607,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--timeline", type=int, default=0,
                     help="diagnostics: per-phase timeline of the decode step over this many tokens (0: off)")
+    ap.add_argument("--workloads", default="1b,long,multiseq",
+                    help="other named workloads measured after the main one (comma list; empty: none)")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling only: the first N layers of the model (0: all); the line is then not the workload's")
     a = ap.parse_args()

@@ -91,7 +91,9 @@ enum {
     LCX_ABORTED = 2,         /* the abort callback stopped the batch between ubatches */
     LCX_INVALID = -1,        /* invalid batch or argument */
     LCX_ALLOC_FAILED = -2,   /* device or host allocation failed */
-    LCX_COMPUTE_FAILED = -3  /* a CUDA launch or copy failed; the failed ubatch's cells are rolled back */
+    LCX_COMPUTE_FAILED = -3  /* a computation failed (a CUDA launch or copy, a kernel's timed-out wait, or a
+                                logits row holding a value that is not finite): the failed ubatch's cells
+                                and those of later ubatches are rolled back (step 12) */
 };
 
 /* Builds a model over the caller's weights. The model keeps its own device copy of every layer
@@ -125,15 +127,23 @@ void lcx_ctx_free(lcx_ctx *ctx);
  *               batch order (step 14, the logits buffer).
  *   argmax_out: host or device int32 [n_out] or NULL: the index of each row's largest logit
  *               (lowest index on ties).
- * Outputs are stream-ordered; when argmax_out is host memory the call synchronizes the stream
- * before returning. Returns an LCX_* code. */
+ * When the batch has output rows the call synchronizes the stream before it returns (to copy a
+ * host argmax_out and to check the logits); otherwise it returns as soon as the work is queued.
+ * A logits row holding a value that is not finite (NaN or infinity) fails its ubatch as a failed
+ * computation does (step 12, return -3): LCX_COMPUTE_FAILED, the cells of that ubatch and of the
+ * later ones released, the earlier ubatches kept in the cache with their rows (which the decode
+ * loop copied out before the failed ubatch ran) -- lcx_n_outputs tells how many rows are valid.
+ * Returns an LCX_* code. */
 int32_t lcx_decode(lcx_ctx *ctx, lcx_batch batch, float *logits_out, int32_t *argmax_out);
 
 /* Greedy generation on the device (the article's generation loop, step 15, with the sampler
  * replaced by argmax): decodes `token` for sequence `seq` at its next position, then n_steps-1
  * further single-token steps, each fed the argmax of the previous one without a host round
  * trip. tokens_out (host or device int32 [n_steps]) receives the argmax of every step.
- * Reserves all n_steps cells first (LCX_NO_KV_SLOT if they do not fit). */
+ * Reserves all n_steps cells first (LCX_NO_KV_SLOT if they do not fit). Synchronizes the stream
+ * before it returns. A step whose logits hold a value that is not finite fails with
+ * LCX_COMPUTE_FAILED: its cell and those of the later steps are released, the earlier steps stay
+ * and lcx_n_outputs gives their number (their tokens are in tokens_out). */
 int32_t lcx_decode_greedy(lcx_ctx *ctx, int32_t seq, int32_t token, int32_t n_steps, int32_t *tokens_out);
 
 /* Frees every cell (the memory clear of the KV-cache section): every sequence becomes empty. */
@@ -142,7 +152,9 @@ void lcx_kv_clear(lcx_ctx *ctx);
 /* The last position stored for `seq`, or -1 if it has none or seq is out of range. */
 int32_t lcx_seq_pos_max(const lcx_ctx *ctx, int32_t seq);
 
-/* Output rows written by the last lcx_decode (0 after a failed one). */
+/* Output rows written by the last lcx_decode (or steps of the last lcx_decode_greedy). After a
+ * call that stopped (LCX_ABORTED, LCX_COMPUTE_FAILED), the rows of the ubatches that completed
+ * before it; 0 after LCX_INVALID or LCX_NO_KV_SLOT. */
 int32_t lcx_n_outputs(const lcx_ctx *ctx);
 
 /* Abort callback (step 12, abort -> 2): called on the host before every ubatch after the
@@ -167,6 +179,7 @@ typedef struct {
     int64_t n_cells_used;      /* cells currently holding K/V */
     uint32_t n_ctx;            /* cells in the cache (after rounding) */
     uint32_t n_pages;          /* KV pages allocated (page = 64 cells of one sequence) */
+    int64_t n_gemm_wide;       /* tensor-core matmul launches that took 128-token tiles (large ubatches) */
 } lcx_stats;
 void lcx_get_stats(const lcx_ctx *ctx, lcx_stats *out);
 
@@ -246,7 +259,9 @@ int32_t lcx_attention(int32_t T, int32_t n_head, int32_t n_head_kv, int32_t head
  * LCX_ATTENTION_NOALLOC_SCRATCH_BYTES inside the library, present on every GPU that loads the
  * library until the process exits. The call allocates nothing.
  *   - The first call on a device looks up that array's device address (once per device, with
- *     the device current); make that first call before any stream capture.
+ *     the device current); make that first call before any stream capture. The address is kept
+ *     for the life of the process: after a cudaDeviceReset of a device, do not call this entry
+ *     point on that device again.
  *   - Calls whose scratch need (lcx_attention_workspace_size) exceeds the array are rejected
  *     with LCX_INVALID and a message in lcx_last_error().
  *   - Every call on a device shares the one array: calls that overlap on the GPU (on different

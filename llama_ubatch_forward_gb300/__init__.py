@@ -16,6 +16,7 @@ _lib = None
 LCX_F16, LCX_Q4_0, LCX_Q8_0 = 1, 2, 8
 LCX_OK, LCX_NO_KV_SLOT, LCX_ABORTED = 0, 1, 2
 LCX_INVALID, LCX_ALLOC_FAILED, LCX_COMPUTE_FAILED = -1, -2, -3
+LCX_ATTENTION_NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024   # as include/lcx.h
 
 SYMBOLS = ("lcx_model_create", "lcx_model_free", "lcx_ctx_create", "lcx_ctx_free", "lcx_decode",
            "lcx_decode_greedy", "lcx_kv_clear", "lcx_seq_pos_max", "lcx_n_outputs", "lcx_set_abort",
@@ -59,7 +60,7 @@ class lcx_sampler(ctypes.Structure):
 class lcx_stats(ctypes.Structure):
     _fields_ = [("n_decode", ctypes.c_int64), ("n_ubatch", ctypes.c_int64), ("n_ubatch_last", ctypes.c_int32),
                 ("n_outputs_last", ctypes.c_int32), ("n_kernels", ctypes.c_int64), ("n_cells_used", ctypes.c_int64),
-                ("n_ctx", ctypes.c_uint32), ("n_pages", ctypes.c_uint32)]
+                ("n_ctx", ctypes.c_uint32), ("n_pages", ctypes.c_uint32), ("n_gemm_wide", ctypes.c_int64)]
 
 
 class lcx_kernel_profile(ctypes.Structure):

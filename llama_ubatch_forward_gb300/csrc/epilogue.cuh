@@ -15,6 +15,11 @@ __device__ __forceinline__ unsigned long long argmax_key(float v, int idx) {
     return ((unsigned long long)b << 32) | (unsigned long long)(0xffffffffu - (uint32_t)idx);
 }
 
+// A logit that is not finite fails its ubatch (step 13: a failed compute returns -3 and the
+// ubatch's cells are removed again). The first ubatch (or greedy step) of the call to produce one
+// leaves its tag (index + 1) in the context's non-finite word; the host reads it after the call.
+__device__ __forceinline__ void note_nonfinite(const FwdArgs &a) { atomicCAS(a.nonfinite, 0, a.tag); }
+
 // SiLU with the fast exponential and division (relative error about 1e-6; the exponential
 // saturates to inf for very negative g, where the quotient is then 0)
 __device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
@@ -75,6 +80,7 @@ __device__ __forceinline__ void epi_quad_in(const FwdArgs &a, int layer, int t, 
                 lr[r0 + j] = v[j];
                 unsigned long long k = argmax_key(v[j], r0 + j);
                 best = k > best ? k : best;
+                if (!isfinite(v[j])) note_nonfinite(a);
             }
     } else if (EPI == EPI_QKV) {
         const int qw = a.H * a.hd, kw = a.KV * a.hd;

@@ -310,12 +310,7 @@ cudaError_t run_g(const FwdArgs &a, int layer, int chunk, int ns, bool out16, cu
 }  // namespace
 
 int attention_splits(const FwdArgs &a, int max_natt, int *chunk) {
-    static int n_sm = 0;
-    if (!n_sm) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
-    }
+    const int n_sm = device_sm_count();
     // one CTA per SM: the next kernel's CTAs (started early, waiting for this one) leave room for
     // about one attention CTA per SM, so a second wave would double the latency
     const int target = n_sm;

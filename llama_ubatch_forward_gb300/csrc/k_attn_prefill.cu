@@ -251,13 +251,9 @@ cudaError_t launch_attention_prefill(const FwdArgs &a, int layer, cudaStream_t s
     ++launches;
     const dim3 grid(a.ub.n_qtiles, a.H);
     if (a.hd == 128) {
-        static bool attr = false;
-        if (!attr) {
-            cudaError_t e = cudaFuncSetAttribute(k_attn_prefill<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 4 * FA_BK * 128 * 2);
-            if (e != cudaSuccess) return e;
-            attr = true;
-        }
+        cudaError_t e = func_attr_once((const void *)k_attn_prefill<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       4 * FA_BK * 128 * 2);
+        if (e != cudaSuccess) return e;
         return launch_pdl(k_attn_prefill<128>, grid, dim3(128), (size_t)4 * FA_BK * 128 * 2, s, a, layer);
     }
     if (a.hd == 64) return launch_pdl(k_attn_prefill<64>, grid, dim3(128), (size_t)4 * FA_BK * 64 * 2, s, a, layer);

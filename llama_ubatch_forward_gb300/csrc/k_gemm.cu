@@ -115,14 +115,14 @@ cudaError_t dispatch(const QMat &W, Epi epi, int T, const __half *A, const __hal
 }  // namespace
 
 cudaError_t launch_gemm(const QMat &W, Epi epi, int T, const __half *A, const __half *A_lo, const FwdArgs &a,
-                        int layer, cudaStream_t s, int64_t &launches) {
+                        int layer, cudaStream_t s, int64_t &launches, int64_t *wide) {
     // The tensor-core kernel is the GEMM; LCX_GEMM_SIMT=1 selects this CUDA-core version instead
     // (same results up to summation order), for cross-checking the two on a device.
     static const bool simt = [] {
         const char *e = getenv("LCX_GEMM_SIMT");
         return e && e[0] == '1';
     }();
-    if (!simt) return launch_gemm_tc(W, epi, T, A, A_lo, a, layer, s, launches);
+    if (!simt) return launch_gemm_tc(W, epi, T, A, A_lo, a, layer, s, launches, wide);
     ++launches;
     if (W.type == Q4) return dispatch<Q4>(W, epi, T, A, A_lo, a, layer, s);
     if (W.type == Q8) return dispatch<Q8>(W, epi, T, A, A_lo, a, layer, s);

@@ -26,6 +26,7 @@
 // without further work.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 #include <vector>
 
@@ -114,26 +115,28 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
 // the next boxes stream in while the tensor pipe works). With SA = 3 the dequantisation of step j
 // waits only for the MMAs of step j - 3, so it overlaps the MMAs of steps j - 2 and j - 1; the
 // activations run DB steps ahead into the slot freed by the MMAs of step j + DB - SB, which are
-// never later than those the A ring waits for.
+// never later than those the A ring waits for (when DB = SB - SA).
+// MT weight tiles of 128 rows per CTA (1 or 2) share each activation tile of BN tokens.
 template <int QT, int BN, int MT>
 struct Cfg {
     static constexpr int QB = QT == Q8 ? 32 : 16;          // quant bytes per 32-element block
     static constexpr int A_BYTES = MT * BM * BK * 2;      // f16 weight tiles (one slot of the A ring)
     static constexpr int B_BYTES = 2 * BN * BK * 2;       // f16 activation tiles: high and low parts
     static constexpr int PB = 8 * QB + 16;                // one block pair of a row quad (QMat)
-    static constexpr int RQ_BYTES = MT * (BM / 4) * PB;   // raw tiles: 32 quads x one block pair
+    static constexpr int RQ_BYTES = MT * (BM / 4) * PB;   // raw tiles: 32 quads per tile x one block pair
     static constexpr int RQ_SLOT = ((RQ_BYTES + 1023) / 1024) * 1024;
-    static constexpr int SA = (QT == Q4 && BN == 64) ? 3 : 2;
-    static constexpr int SR = (QT == Q8 && BN == 128) ? 2 : 3;
+    static constexpr int SA = (MT == 2 && QT == Q4 && BN == 64) ? 3 : 2;
+    static constexpr int SR = (MT == 2 && QT == Q8 && BN == 128) ? 2 : 3;
     static constexpr int SB_FIT = (220 * 1024 - SA * A_BYTES - SR * RQ_SLOT) / B_BYTES;
     static constexpr int SB = SB_FIT < 6 ? SB_FIT : 6;
     static constexpr int DB = SB - SA >= 2 ? SB - SA : SB - 1;   // activation prefetch distance
     static_assert(SB >= 2 && DB >= 1, "the activation prefetch needs at least two slots");
     static constexpr int SMEM = SA * A_BYTES + SB * B_BYTES + SR * RQ_SLOT + 1024 /* align */ + 512 /* barriers */;
     static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
-    // per weight tile, W A_hi and W A_lo side by side: one MMA of N = 2 BN over the stacked tiles
-    static constexpr int TMEM_COLS = MT * 2 * BN <= 128 ? 128 : MT * 2 * BN <= 256 ? 256 : 512;
-    static_assert(MT * 2 * BN <= 512, "tensor memory holds 512 columns");
+    // per weight tile one accumulator of BN columns: W A_hi and W A_lo are accumulated into it
+    static constexpr int TMEM_COLS = MT * BN <= 128 ? 128 : MT * BN <= 256 ? 256 : 512;
+    static_assert(MT * BN <= 512, "tensor memory holds 512 columns");
+    static_assert(BN <= 256, "one MMA covers at most 256 columns");
 };
 
 struct GemmParams {
@@ -143,16 +146,17 @@ struct GemmParams {
     int row_base;   // unused (tiles start at blockIdx.x * 128 or, for SwiGLU, chunk c * 256)
 };
 
-// Dequantise row `row` (0..127) of one raw tile -- 32 row quads x one block pair, as stored
-// (QMat) -- into the swizzled f16 tile.
-template <int QT>
-__device__ __forceinline__ void dequant_row(const uint8_t *rq, uint8_t *atile, int row) {
+// Dequantise blocks b0 .. b0 + NBLK - 1 (of the step's block pair) of row `row` (0..127) of one
+// raw tile -- 32 row quads x one block pair, as stored (QMat) -- into the swizzled f16 tile.
+template <int QT, int NBLK>
+__device__ __forceinline__ void dequant_row(const uint8_t *rq, uint8_t *atile, int row, int b0) {
     constexpr int QB = QT == Q8 ? 32 : 16, PB = 8 * QB + 16;
     const uint8_t *q = rq + (row >> 2) * PB + (row & 3) * 2 * QB;
     const __half *sc = reinterpret_cast<const __half *>(rq + (row >> 2) * PB + 8 * QB);
     uint8_t *dst = atile + row * 128;
 #pragma unroll
-    for (int blk = 0; blk < 2; ++blk) {
+    for (int bb = 0; bb < NBLK; ++bb) {
+        const int blk = b0 + bb;
         const __half2 d2 = __half2half2(sc[blk * 4 + (row & 3)]);
         if (QT == Q4) {
             const uint4 w = *reinterpret_cast<const uint4 *>(q + blk * 16);
@@ -209,11 +213,10 @@ __device__ __forceinline__ void dequant_row(const uint8_t *rq, uint8_t *atile, i
     }
 }
 
-template <int QT, int BN, int EPI>
+template <int QT, int BN, int MT, int EPI>
 __global__ void __launch_bounds__(320, 1)
     k_gemm_tc(const __half *__restrict__ A_hi, const __half *__restrict__ A_lo, const int K,
               const __grid_constant__ CUtensorMap tm_w, const GemmParams p, const FwdArgs a, const int layer) {
-    constexpr int MT = 2;   // two 128-row weight tiles share every activation tile
     using C = Cfg<QT, BN, MT>;
     constexpr int SA = C::SA, SB = C::SB, SR = C::SR;
     extern __shared__ uint8_t smem_raw[];
@@ -230,9 +233,11 @@ __global__ void __launch_bounds__(320, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m_tile = blockIdx.x, tok0 = blockIdx.y * BN;
     const int nk = p.nk;
-    // first weight row of each M tile: two adjacent 128-row tiles (for gate/up each holds 16
+    // first weight row of each M tile: MT adjacent 128-row tiles (for gate/up each holds 16
     // gate quads interleaved with their 16 up quads)
-    const int row0[MT] = {m_tile * 2 * BM, m_tile * 2 * BM + BM};
+    int row0[MT];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) row0[mt] = (m_tile * MT + mt) * BM;
     auto a_tile = [&](int aslot, int mt) { return smem + aslot * C::A_BYTES + mt * BM * BK * 2; };
     auto b_tile = [&](int slot) { return act_ring + slot * C::B_BYTES; };
     auto rq_tile = [&](int slot, int mt) { return raw_ring + slot * C::RQ_SLOT + mt * (BM / 4) * C::PB; };
@@ -253,7 +258,7 @@ __global__ void __launch_bounds__(320, 1)
         mbar_init(acc_bar, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 1) {   // tensor-memory accumulator: MT x BN f32 columns, 128 lanes
+    if (warp == 1) {   // tensor-memory accumulators: MT x BN f32 columns, 128 lanes
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
                      ::"r"(saddr(tmem_slot)), "r"((uint32_t)C::TMEM_COLS));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
@@ -267,7 +272,7 @@ __global__ void __launch_bounds__(320, 1)
         // ---------------------------------------------------------------- producer
         if (lane == 0) {
             bool ok = true;
-            auto issue_w = [&](int j) {   // quants and scales of the 64 quads of both tiles: one box
+            auto issue_w = [&](int j) {   // quants and scales of the 32 MT quads of the tiles: one box
                 const int slot = j % SR;
                 mbar_expect_tx(&full_w[slot], C::RQ_BYTES);
                 tma_2d(rq_tile(slot, 0), &tm_w, j * (C::PB / 4), row0[0] / 4, &full_w[slot]);
@@ -288,23 +293,27 @@ __global__ void __launch_bounds__(320, 1)
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_f16(BM, 2 * BN);   // the high and low parts stacked: N = 2 BN
+            constexpr uint32_t idesc = idesc_f16(BM, BN);
             bool ok = true;
             for (int j = 0; j < nk; ++j) {
                 const int slot = j % SB, aslot = j % SA;
                 if (!(ok = mbar_wait(&full_a[aslot], (j / SA) & 1) && mbar_wait(&full_b[slot], (j / SB) & 1))) break;
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                 const uint32_t bbase = saddr(b_tile(slot));
-                // the activation tile's high rows then low rows form one K-major operand of 2 BN
-                // rows, so each MMA computes W A_hi and W A_lo into adjacent accumulator columns;
-                // the two weight tiles alternate so consecutive MMAs use different accumulators
+                // W A_hi then W A_lo into the same accumulator (the activation tile's high rows,
+                // then its low rows, BN rows each); the weight tiles alternate so consecutive MMAs
+                // of one part use different accumulators
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk) {
 #pragma unroll
-                    for (int mt = 0; mt < MT; ++mt) {
-                        const uint32_t abase = saddr(a_tile(aslot, mt));
-                        mma_f16(tmem + mt * 2 * BN, sw128_desc(abase + kk * 32), sw128_desc(bbase + kk * 32), idesc,
-                                (j > 0 || kk > 0) ? 1u : 0u);
+                    for (int hl = 0; hl < 2; ++hl) {
+#pragma unroll
+                        for (int mt = 0; mt < MT; ++mt) {
+                            const uint32_t abase = saddr(a_tile(aslot, mt));
+                            mma_f16(tmem + mt * BN, sw128_desc(abase + kk * 32),
+                                    sw128_desc(bbase + hl * BN * BK * 2 + kk * 32), idesc,
+                                    (j > 0 || kk > 0 || hl > 0) ? 1u : 0u);
+                        }
                     }
                 }
                 mma_commit(&empty_b[slot]);   // the activation slot is free once these MMAs have read it
@@ -315,10 +324,12 @@ __global__ void __launch_bounds__(320, 1)
         }
     } else {
         // ---------------------------------------------------------------- activations, dequant, epilogue
-        // 8 warps: warps 2..5 own weight tile 0, warps 6..9 tile 1 (dequant and epilogue); all 8
-        // load the activation tiles
+        // 8 warps. Dequantisation: with two weight tiles, warps 2..5 own tile 0 and warps 6..9
+        // tile 1, a row per thread; with one, two threads per row, a block each. All 8 load the
+        // activation tiles and run the epilogue (see below).
         const int wt = threadIdx.x - 64;           // 0..255
-        const int my_mt = wt >> 7, drow = wt & 127;
+        const int my_mt = MT == 2 ? wt >> 7 : 0;
+        const int drow = MT == 2 ? wt & 127 : wt >> 1, dblk = MT == 2 ? 0 : wt & 1;
         // activation tile of stage j: 2 parts x BN rows x 8 chunks of 16 bytes; thread wt copies
         // chunk wt % 8 of rows wt / 8 + 32 u, each to its 128-byte-swizzled place; rows past the
         // last token are zero-filled
@@ -354,7 +365,7 @@ __global__ void __launch_bounds__(320, 1)
             // the A slot is free once the MMAs of step j - SA are done
             if (ok && j >= SA) ok = __all_sync(0xffffffffu, mbar_wait(&empty_a[aslot], ((j / SA) - 1) & 1));
             if (!ok) break;
-            dequant_row<QT>(rq_tile(rslot, my_mt), a_tile(aslot, my_mt), drow);
+            dequant_row<QT, 3 - MT>(rq_tile(rslot, my_mt), a_tile(aslot, my_mt), drow, dblk);
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic writes -> tensor-core reads
             __syncwarp();
             if (lane == 0) {
@@ -381,19 +392,17 @@ __global__ void __launch_bounds__(320, 1)
         const bool acc_ok = __all_sync(0xffffffffu, ok && mbar_wait(acc_bar, 0));
         if (acc_ok) {
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            // a warp reads the TMEM lanes of its quarter (warp % 4); with two tiles warps 2..5 take
+            // tile 0 and 6..9 tile 1, all BN columns; with one tile the two warps of a quarter
+            // take half of the columns each
             const int q = warp & 3;                 // TMEM lane quarter of this warp
             const int lrow = q * 32 + lane;         // row within the tile
             const int r = row0[my_mt] + lrow;       // weight row
-            const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16) + my_mt * 2 * BN;
-            for (int cb = 0; cb < BN / 32; ++cb) {
-                uint32_t vv[32];   // W (A_hi + A_lo): the high-part columns plus the low-part columns
-                {
-                    uint32_t lo[32];
-                    tmem_ld32(tq + cb * 32, vv);
-                    tmem_ld32(tq + BN + cb * 32, lo);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) vv[i] = __float_as_uint(__uint_as_float(vv[i]) + __uint_as_float(lo[i]));
-                }
+            const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16) + my_mt * BN;
+            const int cb0 = MT == 2 ? 0 : (wt >> 7) * (BN / 64), cb1 = MT == 2 ? BN / 32 : cb0 + BN / 64;
+            for (int cb = cb0; cb < cb1; ++cb) {
+                uint32_t vv[32];   // W (A_hi + A_lo)
+                tmem_ld32(tq + cb * 32, vv);
                 if (EPI == EPI_SWIGLU) {   // rows 8f'..8f'+3 gate, 8f'+4..8f'+7 up of features 4f'..
                     const int f = (r >> 3) * 4 + (lrow & 3);
                     const bool gate = (lane & 7) < 4;
@@ -432,6 +441,7 @@ __global__ void __launch_bounds__(320, 1)
                             if (t < p.T && r < p.N) {
                                 a.logits[(size_t)t * a.V + r] = v;
                                 key = argmax_key(v, r);
+                                if (!isfinite(v)) note_nonfinite(a);
                             }
 #pragma unroll
                             for (int o = 16; o; o >>= 1) {
@@ -520,65 +530,86 @@ bool make_map_2d(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int e
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int QT, int BN, int EPI>
+template <int QT, int BN, int MT, int EPI>
 cudaError_t run(const QMat &W, int T, const __half *A, const __half *A_lo, const FwdArgs &a, int layer, cudaStream_t s) {
-    constexpr int MT = 2;
     using C = Cfg<QT, BN, MT>;
-    auto kern = k_gemm_tc<QT, BN, EPI>;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    auto kern = k_gemm_tc<QT, BN, MT, EPI>;
+    cudaError_t e = func_attr_once((const void *)kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
     if (!W.tm_ready) return cudaErrorInvalidValue;
     GemmParams p{W.N, T, W.K / BK, 0};
-    const int m_tiles = (W.N_pad + 2 * BM - 1) / (2 * BM);   // rows past N_pad read as zeros
+    const int m_tiles = (W.N_pad + MT * BM - 1) / (MT * BM);   // rows past N_pad read as zeros
     dim3 grid(m_tiles, (T + BN - 1) / BN);
     return launch_pdl(kern, grid, dim3(320), (size_t)C::SMEM, s, A, A_lo, W.K,
-                      *reinterpret_cast<const CUtensorMap *>(W.tm_w), p, a, layer);
+                      *reinterpret_cast<const CUtensorMap *>(MT == 2 ? W.tm_w : W.tm_w1), p, a, layer);
 }
 
-template <int QT, int BN>
+template <int QT, int BN, int MT>
 cudaError_t dispatch(const QMat &W, Epi epi, int T, const __half *A, const __half *A_lo, const FwdArgs &a, int layer,
                      cudaStream_t s) {
     switch (epi) {
-        case EPI_QKV: return run<QT, BN, EPI_QKV>(W, T, A, A_lo, a, layer, s);
-        case EPI_RESID: return run<QT, BN, EPI_RESID>(W, T, A, A_lo, a, layer, s);
-        case EPI_SWIGLU: return run<QT, BN, EPI_SWIGLU>(W, T, A, A_lo, a, layer, s);
-        case EPI_LOGITS: return run<QT, BN, EPI_LOGITS>(W, T, A, A_lo, a, layer, s);
+        case EPI_QKV: return run<QT, BN, MT, EPI_QKV>(W, T, A, A_lo, a, layer, s);
+        case EPI_RESID: return run<QT, BN, MT, EPI_RESID>(W, T, A, A_lo, a, layer, s);
+        case EPI_SWIGLU: return run<QT, BN, MT, EPI_SWIGLU>(W, T, A, A_lo, a, layer, s);
+        case EPI_LOGITS: return run<QT, BN, MT, EPI_LOGITS>(W, T, A, A_lo, a, layer, s);
     }
     return cudaErrorInvalidValue;
+}
+
+template <int QT>
+cudaError_t dispatch_shape(int bn, int mt, const QMat &W, Epi epi, int T, const __half *A, const __half *A_lo,
+                           const FwdArgs &a, int layer, cudaStream_t s) {
+    if (bn == 64) return dispatch<QT, 64, 2>(W, epi, T, A, A_lo, a, layer, s);
+    if (bn == 128 && mt == 1) return dispatch<QT, 128, 1>(W, epi, T, A, A_lo, a, layer, s);
+    if (bn == 128) return dispatch<QT, 128, 2>(W, epi, T, A, A_lo, a, layer, s);
+    return dispatch<QT, 256, 1>(W, epi, T, A, A_lo, a, layer, s);
 }
 
 }  // namespace tc
 
 bool make_weight_maps(QMat &W) {
     // the storage as [N_pad / 4 quads][quad_bytes] in 4-byte units; a box is one block pair
-    // (quants and scales) of 64 quads: both 128-row tiles of a CTA
+    // (quants and scales) of 64 quads (two 128-row tiles of a CTA) or of 32 (one tile)
     const int pb = W.pair_bytes();
-    CUtensorMap *m = reinterpret_cast<CUtensorMap *>(W.tm_w);
-    W.tm_ready = tc::make_map_2d(m, W.w, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, W.quad_bytes() / 4, (uint64_t)W.N_pad / 4,
-                                 W.quad_bytes(), (uint32_t)(pb / 4), (uint32_t)(tc::BM / 2), CU_TENSOR_MAP_SWIZZLE_NONE);
+    W.tm_ready = tc::make_map_2d(reinterpret_cast<CUtensorMap *>(W.tm_w), W.w, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4,
+                                 W.quad_bytes() / 4, (uint64_t)W.N_pad / 4, W.quad_bytes(), (uint32_t)(pb / 4),
+                                 (uint32_t)(tc::BM / 2), CU_TENSOR_MAP_SWIZZLE_NONE) &&
+                 tc::make_map_2d(reinterpret_cast<CUtensorMap *>(W.tm_w1), W.w, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4,
+                                 W.quad_bytes() / 4, (uint64_t)W.N_pad / 4, W.quad_bytes(), (uint32_t)(pb / 4),
+                                 (uint32_t)(tc::BM / 4), CU_TENSOR_MAP_SWIZZLE_NONE);
     return W.tm_ready;
 }
 
-cudaError_t launch_gemm_tc(const QMat &W, Epi epi, int T, const __half *A, const __half *A_lo, const FwdArgs &a,
-                           int layer, cudaStream_t s, int64_t &launches) {
-    ++launches;
-    static int n_sm = 0;
-    if (!n_sm) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+// Tile shape of a launch: BN tokens x MT 128-row weight tiles per CTA, from a cost model per K
+// step (cycles of one SM): the MMAs take 4 BN MT (128 x BN x 16 per MMA, hi and lo parts, four
+// per 64-wide step, about 4096 multiply-adds a cycle), the dequantisation of MT tiles about
+// 435 MT, given a 30% margin since it must also hide its waits; the launch takes as many of
+// those steps as its waves of CTAs. Ties go to fewer CTAs (less activation traffic).
+void gemm_shape(int N_pad, int T, int n_sm, int *bn, int *mt) {
+    static const int cand[4][2] = {{64, 2}, {128, 1}, {128, 2}, {256, 1}};
+    long best = -1, best_ctas = 0;
+    for (const auto &c : cand) {
+        const long ctas = (long)((N_pad + c[1] * 128 - 1) / (c[1] * 128)) * ((T + c[0] - 1) / c[0]);
+        const long waves = (ctas + n_sm - 1) / n_sm;
+        const long step = std::max<long>(4L * c[0] * c[1], 566L * c[1]);
+        const long cost = waves * step;
+        if (best < 0 || cost < best || (cost == best && ctas < best_ctas)) {
+            best = cost;
+            best_ctas = ctas;
+            *bn = c[0];
+            *mt = c[1];
+        }
     }
-    // 64-token tiles when 128-token tiles would leave SMs idle
-    const int m_tiles = (W.N_pad + 255) / 256;
-    const bool small = (long)m_tiles * ((T + 127) / 128) < (long)n_sm;
-    if (W.type == Q4)
-        return small ? tc::dispatch<Q4, 64>(W, epi, T, A, A_lo, a, layer, s) : tc::dispatch<Q4, 128>(W, epi, T, A, A_lo, a, layer, s);
-    if (W.type == Q8)
-        return small ? tc::dispatch<Q8, 64>(W, epi, T, A, A_lo, a, layer, s) : tc::dispatch<Q8, 128>(W, epi, T, A, A_lo, a, layer, s);
+}
+
+cudaError_t launch_gemm_tc(const QMat &W, Epi epi, int T, const __half *A, const __half *A_lo, const FwdArgs &a,
+                           int layer, cudaStream_t s, int64_t &launches, int64_t *wide) {
+    ++launches;
+    int bn = 64, mt = 2;
+    gemm_shape(W.N_pad, T, device_sm_count(), &bn, &mt);
+    if (bn >= 128 && wide) ++*wide;
+    if (W.type == Q4) return tc::dispatch_shape<Q4>(bn, mt, W, epi, T, A, A_lo, a, layer, s);
+    if (W.type == Q8) return tc::dispatch_shape<Q8>(bn, mt, W, epi, T, A, A_lo, a, layer, s);
     return cudaErrorInvalidValue;
 }
 

@@ -21,6 +21,7 @@
 // (The copy engine's cost is per copy much more than per byte: copies of about 32 KB keep HBM
 // near its peak, copies of a few KB cap a CTA far below it.)
 #pragma once
+#include <math_constants.h>
 #include "epilogue.cuh"
 
 namespace lcx {
@@ -202,13 +203,15 @@ __device__ void stage_token(const GemvParams &p, int t, uint8_t *stage_t, float 
     if (lane == 0) red[t][warp] = ss;
 }
 
-// RMS factor of token t from the partial sums left by stage_token (1 without norm gains).
+// Output scale of token t from the partial sums left by stage_token: the RMS factor with norm
+// gains, else 1. A non-finite sum of squares (a NaN or an infinity in x) makes it NaN: the int8
+// split clamps such values to finite codes, so the scale is what carries them to the output.
+__device__ __forceinline__ float finite_or_nan(float tot, float rs) { return tot < CUDART_INF_F ? rs : CUDART_NAN_F; }
 __device__ __forceinline__ float token_rs(const GemvParams &p, const FwdArgs &a, float (*red)[8], int t) {
-    if (!p.in.g) return 1.f;
     float tot = 0.f;
 #pragma unroll
     for (int w = 0; w < 8; ++w) tot += red[t][w];
-    return 1.0f / sqrtf(tot / (float)p.K + a.eps);
+    return finite_or_nan(tot, p.in.g ? 1.0f / sqrtf(tot / (float)p.K + a.eps) : 1.f);
 }
 
 // ---------------------------------------------------------------- TMA-bulk streaming kernel
@@ -514,14 +517,9 @@ cudaError_t run(const GemvParams &p, const FwdArgs &a, int layer, cudaStream_t s
     constexpr int QB = QT == Q8 ? 32 : 16;
     const StagePlan pl = stage_plan(p.nb, QB, NT, EPI == EPI_SWIGLU, (size_t)kGemvSmemTotal);
     if (pl.slots < 2) return cudaErrorInvalidConfiguration;
-    static int n_sm = 0;
-    if (!n_sm) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemvSmemTotal);
-        if (e != cudaSuccess) return e;
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
-    }
+    cudaError_t e = func_attr_once((const void *)kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemvSmemTotal);
+    if (e != cudaSuccess) return e;
+    const int n_sm = device_sm_count();
     const int n_stages = (p.n_tasks + pl.tps - 1) / pl.tps;
     int grid = n_stages < n_sm ? n_stages : n_sm;
     if (grid < 1) grid = 1;

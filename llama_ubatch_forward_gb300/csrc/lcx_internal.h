@@ -32,8 +32,10 @@ struct QMat {
     int N = 0, N_pad = 0;   // logical and padded rows
     int K = 0, nb = 0;      // padded input width (nb * 32) and blocks per row
     uint8_t *w = nullptr;   // the quad-interleaved storage
-    // TMA descriptor (CUtensorMap) of the storage for the tensor-core GEMM
+    // TMA descriptors (CUtensorMap) of the storage for the tensor-core GEMM: boxes of 64 quads
+    // (two 128-row tiles) and of 32 quads (one tile)
     alignas(64) unsigned char tm_w[128] = {};
+    alignas(64) unsigned char tm_w1[128] = {};
     bool tm_ready = false;
     int qb() const { return type == Q4 ? 16 : 32; }
     int pair_bytes() const { return 8 * qb() + 16; }
@@ -100,6 +102,9 @@ struct FwdArgs {
     int32_t *att_cnt;  // [T][KV] arrival counters, zero between launches
     int att_max_split;
     int32_t *err;      // device error word: set by a kernel whose bounded wait timed out
+    int32_t *nonfinite;// 0, or the tag of the first ubatch of the call whose logits held a value
+                       // that is not finite (written once, by compare-and-swap)
+    int32_t tag;       // this ubatch's (or greedy step's) index in the call + 1
     unsigned long long *trace;   // NULL, or [slots][4] timestamps (first start, first past wait, last staged, last end)
     bool pdl;                    // launched inside the forward's chain of dependent launches
     int trace_slot;              // this launch's slot
@@ -136,11 +141,12 @@ bool gemv_fits(const QMat &W, int T);
 
 // GEMM for larger T: A = A_hi + A_lo, f16 activations [T][K] split in two parts
 cudaError_t launch_gemm(const QMat &W, Epi epi, int T, const __half *A, const __half *A_lo, const FwdArgs &a,
-                        int layer, cudaStream_t s, int64_t &launches);
+                        int layer, cudaStream_t s, int64_t &launches, int64_t *wide = nullptr);
 
 // tcgen05 GEMM (k_gemm_tc.cu) and the TMA descriptors of a weight matrix it needs
+// (*wide, if given, counts the launches that took tiles of 128 or more tokens)
 cudaError_t launch_gemm_tc(const QMat &W, Epi epi, int T, const __half *A, const __half *A_lo, const FwdArgs &a,
-                           int layer, cudaStream_t s, int64_t &launches);
+                           int layer, cudaStream_t s, int64_t &launches, int64_t *wide = nullptr);
 bool make_weight_maps(QMat &W);
 
 // attention over the cache for every token of the ubatch; writes o32 (f32) or o16
@@ -167,6 +173,7 @@ struct DecodeStep {
     size_t smem = 0;
     int grid = 0;
     int n_ph = 0;
+    int l2_ahead = 0;            // stages per CTA prefetched into L2 past the ring's
     double weight_bytes = 0;     // stored weight bytes one step streams (without the head)
     double head_bytes = 0;
 };
@@ -178,6 +185,13 @@ cudaError_t decode_step_reset(const DecodeStep &ds, const FwdArgs &a, cudaStream
 cudaError_t launch_decode_step(const DecodeStep &ds, const FwdArgs &a, const void *tok_embd, int t_embd,
                                int32_t *amax_dst, int n_att, cudaStream_t s, int64_t &launches);
 
+// Sets a kernel attribute once per (kernel, device): the first launch on each device does it,
+// under a lock, so several host threads and several devices are safe. value must not change
+// between calls for the same kernel and attribute.
+cudaError_t func_attr_once(const void *kern, cudaFuncAttribute attr, int value);
+// SMs of the current device (looked up once per device).
+int device_sm_count();
+
 // Launch with programmatic dependent launch allowed: the kernel may start while the previous
 // kernel on the stream finishes; it must execute griddepcontrol.wait before reading anything
 // the previous kernels wrote (and before writing anything they read).
@@ -185,11 +199,7 @@ cudaError_t launch_decode_step(const DecodeStep &ds, const FwdArgs &a, const voi
 // never make an SM re-split its L1 and shared memory between launches.
 template <typename F>
 inline void prefer_max_shared(F *kern) {
-    static bool done = false;   // one per kernel instantiation
-    if (!done) {
-        cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
-        done = true;
-    }
+    func_attr_once((const void *)kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
 }
 
 template <typename... KArgs, typename... Args>

@@ -12,7 +12,10 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <set>
+#include <tuple>
 #include <string>
 #include <vector>
 
@@ -39,6 +42,37 @@ namespace lcx {
 void set_error_text(const char *msg) {
     std::lock_guard<std::mutex> lk(g_err_mu);
     g_err = msg;
+}
+
+namespace {
+std::mutex g_attr_mu;
+std::set<std::tuple<const void *, int, int>> g_attr_done;   // (kernel, device, attribute)
+std::map<int, int> g_sm_count;                               // device -> SMs
+}  // namespace
+
+cudaError_t func_attr_once(const void *kern, cudaFuncAttribute attr, int value) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(g_attr_mu);
+    const auto key = std::make_tuple(kern, dev, (int)attr);
+    if (g_attr_done.count(key)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, attr, value);
+    if (e == cudaSuccess) g_attr_done.insert(key);
+    return e;
+}
+
+int device_sm_count() {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> lk(g_attr_mu);
+    auto it = g_sm_count.find(dev);
+    if (it != g_sm_count.end()) return it->second;
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) return 1;
+    g_sm_count[dev] = n;
+    return n;
 }
 }  // namespace lcx
 
@@ -223,6 +257,7 @@ struct lcx_ctx {
     cudaEvent_t meta_ev[2] = {nullptr, nullptr};
     int meta_slot = 0;
     int32_t *amax_host = nullptr;  // pinned argmax staging
+    int32_t *status_host = nullptr; // pinned copy of the device error and non-finite words
     int amax_cap = 0;
     int max_att_split = 64;
     DecodeStep step;             // persistent one-token decode step, prepared at first use
@@ -253,6 +288,7 @@ static void free_ctx_device(lcx_ctx *c) {
     if (c->meta_dev) cudaFree(c->meta_dev);
     if (c->meta_host) cudaFreeHost(c->meta_host);
     if (c->amax_host) cudaFreeHost(c->amax_host);
+    if (c->status_host) cudaFreeHost(c->status_host);
     for (auto &e : c->meta_ev)
         if (e) cudaEventDestroy(e);
 }
@@ -374,6 +410,8 @@ extern "C" lcx_ctx *lcx_ctx_create(lcx_model *m, uint32_t n_ctx, uint32_t n_seq_
         a.att_cnt = carve<int32_t>(p, (size_t)T * KV);
         c->amax_dev = carve<int32_t>(p, (size_t)std::max<int>(T, 4096));
         a.err = carve<int32_t>(p, 64);
+        a.nonfinite = a.err + 1;
+        a.tag = 1;
         a.d = d; a.H = H; a.KV = KV; a.hd = hd; a.F = hp.n_ff; a.F_pad = Fp; a.V = V; a.L = L;
         a.eps = hp.rms_eps;
         a.kc = c->kc; a.vc = c->vc; a.n_pages = c->n_pages;
@@ -388,6 +426,7 @@ extern "C" lcx_ctx *lcx_ctx_create(lcx_model *m, uint32_t n_ctx, uint32_t n_seq_
     if (e == cudaSuccess) ok(cudaHostAlloc((void **)&c->meta_host, (size_t)2 * c->meta_cap * 4, cudaHostAllocDefault), "pinned");
     c->amax_cap = std::max<int>(T, 4096);
     if (e == cudaSuccess) ok(cudaHostAlloc((void **)&c->amax_host, (size_t)c->amax_cap * 4, cudaHostAllocDefault), "pinned");
+    if (e == cudaSuccess) ok(cudaHostAlloc((void **)&c->status_host, 2 * sizeof(int32_t), cudaHostAllocDefault), "pinned");
     for (auto &ev : c->meta_ev)
         if (e == cudaSuccess) ok(cudaEventCreateWithFlags(&ev, cudaEventDisableTiming), "event");
     if (e == cudaSuccess) ok(launch_rope_table(c->rope, (int)c->n_ctx, hd, (double)hp.rope_theta, c->stream), "rope table");
@@ -635,6 +674,7 @@ cudaError_t run_forward(lcx_ctx *c, FwdArgs &a, int max_natt, double att_cells, 
     const lcx_hparams &hp = m->hp;
     cudaStream_t s = c->stream;
     int64_t &nl = c->st.n_kernels;
+    int64_t *wide = &c->st.n_gemm_wide;
     const double T = a.T, d = a.d, qw = (double)a.H * a.hd, kvw = (double)a.KV * a.hd, F = a.F;
     cudaError_t e;
     // a one-token ubatch runs as one persistent launch where the step kernel applies
@@ -684,7 +724,7 @@ cudaError_t run_forward(lcx_ctx *c, FwdArgs &a, int max_natt, double att_cells, 
         if (e == cudaSuccess) {
             ProfScope ps(c, cls, w_qkv + T * d * ab + T * (qw * 4 + kvw * 4), 2 * T * (qw + 2 * kvw) * d, &a);
             e = gemv ? launch_gemv(D.qkv, EPI_QKV, a.T, GemvIn{a.x, nullptr, D.attn_norm}, a, l, s, nl)
-                     : launch_gemm(D.qkv, EPI_QKV, a.T, a.xh, a.xh_lo, a, l, s, nl);
+                     : launch_gemm(D.qkv, EPI_QKV, a.T, a.xh, a.xh_lo, a, l, s, nl, wide);
         }
         if (e == cudaSuccess) {
             ProfScope ps(c, PC_ATTN, att_bytes, att_flops, &a);
@@ -695,7 +735,7 @@ cudaError_t run_forward(lcx_ctx *c, FwdArgs &a, int max_natt, double att_cells, 
         if (e == cudaSuccess) {
             ProfScope ps(c, cls, w_o + T * qw * ab + T * d * 8, 2 * T * d * qw, &a);
             e = gemv ? launch_gemv(D.wo, EPI_RESID, a.T, GemvIn{a.o32, nullptr, nullptr}, a, l, s, nl)
-                     : launch_gemm(D.wo, EPI_RESID, a.T, a.o16, a.o16_lo, a, l, s, nl);
+                     : launch_gemm(D.wo, EPI_RESID, a.T, a.o16, a.o16_lo, a, l, s, nl, wide);
         }
         if (e == cudaSuccess && !gemv) {
             ProfScope ps(c, PC_OTHER, T * d * 6, 0);
@@ -704,12 +744,12 @@ cudaError_t run_forward(lcx_ctx *c, FwdArgs &a, int max_natt, double att_cells, 
         if (e == cudaSuccess) {
             ProfScope ps(c, cls, w_gu + T * d * ab + T * F * ab, 2 * T * 2 * F * d, &a);
             e = gemv ? launch_gemv(D.gateup, EPI_SWIGLU, a.T, GemvIn{a.x, nullptr, D.ffn_norm}, a, l, s, nl)
-                     : launch_gemm(D.gateup, EPI_SWIGLU, a.T, a.xh, a.xh_lo, a, l, s, nl);
+                     : launch_gemm(D.gateup, EPI_SWIGLU, a.T, a.xh, a.xh_lo, a, l, s, nl, wide);
         }
         if (e == cudaSuccess) {
             ProfScope ps(c, cls, w_dn + T * F * ab + T * d * 8, 2 * T * d * F, &a);
             e = gemv ? launch_gemv(D.down, EPI_RESID, a.T, GemvIn{a.h32, nullptr, nullptr}, a, l, s, nl)
-                     : launch_gemm(D.down, EPI_RESID, a.T, a.h16, a.h16_lo, a, l, s, nl);
+                     : launch_gemm(D.down, EPI_RESID, a.T, a.h16, a.h16_lo, a, l, s, nl, wide);
         }
     }
     if (e != cudaSuccess || a.n_out == 0) return e;
@@ -725,7 +765,7 @@ cudaError_t run_forward(lcx_ctx *c, FwdArgs &a, int max_natt, double att_cells, 
         if (e == cudaSuccess) {
             // the logits GEMM reads the gathered rows as its tokens
             ProfScope ps(c, PC_GEMM, w_head + no * d * 2 + no * a.V * 4, 2 * no * a.V * d);
-            e = launch_gemm(m->head, EPI_LOGITS, a.n_out, a.xh, a.xh_lo, a, -1, s, nl);
+            e = launch_gemm(m->head, EPI_LOGITS, a.n_out, a.xh, a.xh_lo, a, -1, s, nl, wide);
         }
     }
     if (e == cudaSuccess) {
@@ -737,16 +777,28 @@ cudaError_t run_forward(lcx_ctx *c, FwdArgs &a, int max_natt, double att_cells, 
 
 }  // namespace
 
-// Reads and clears the device error word (a kernel's bounded wait timed out). Synchronizes.
-static bool device_error_raised(lcx_ctx *c) {
-    int32_t v = 0;
-    if (cudaMemcpy(&v, c->base.err, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return true;
-    if (!v) return false;
-    cudaMemset(c->base.err, 0, sizeof(v));
-    decode_step_reset(c->step, c->base, c->stream);   // counters a stopped step may have left
+// Queues the copy of the device status words (after `extra`, if any, a queued copy) and
+// synchronizes the stream. Returns the first failing tag of the call: 0 when every ubatch (or step)
+// succeeded, the tag of the first whose logits were not all finite, or -1 when a kernel's bounded
+// wait timed out (which ubatch is unknown) or the stream failed. Clears the words it found set.
+static int32_t read_status(lcx_ctx *c) {
+    cudaError_t e = cudaMemcpyAsync(c->status_host, c->base.err, 2 * sizeof(int32_t), cudaMemcpyDeviceToHost, c->stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(c->stream);
+    if (e != cudaSuccess) {
+        set_err("decode", e);
+        return -1;
+    }
+    const int32_t timed_out = c->status_host[0], nf = c->status_host[1];
+    if (!timed_out && !nf) return 0;
+    cudaMemsetAsync(c->base.err, 0, 2 * sizeof(int32_t), c->stream);
+    if (timed_out) decode_step_reset(c->step, c->base, c->stream);   // counters a stopped step may have left
     cudaStreamSynchronize(c->stream);
-    set_error_text("a kernel's bounded wait timed out");
-    return true;
+    if (timed_out) {
+        set_error_text("a kernel's bounded wait timed out");
+        return -1;
+    }
+    set_error_text("a logits row holds a value that is not finite");
+    return nf;
 }
 
 extern "C" int32_t lcx_decode(lcx_ctx *c, lcx_batch batch, float *logits_out, int32_t *argmax_out) {
@@ -794,12 +846,15 @@ extern "C" int32_t lcx_decode(lcx_ctx *c, lcx_batch batch, float *logits_out, in
         if (c->host_only && (int)k == c->fail_ubatch) {   // as a failed launch below
             c->fail_ubatch = -1;
             release_cells(c, P, u.i0);
+            c->n_outputs_last = u.row0;
+            c->st.n_outputs_last = u.row0;
             return LCX_COMPUTE_FAILED;
         }
         if (!c->host_only) {
             FwdArgs a = c->base;
             a.T = u.T;
             a.n_out = u.n_out;
+            a.tag = (int32_t)k + 1;
             cudaError_t e = upload_meta(c, P, u, a.ub);
             a.tok_src = a.ub.tok;
             if (logits_out) a.logits = logits_out + (size_t)u.row0 * c->hp.n_vocab;
@@ -814,22 +869,35 @@ extern "C" int32_t lcx_decode(lcx_ctx *c, lcx_batch batch, float *logits_out, in
             if (e != cudaSuccess) {
                 set_err("decode", e);
                 release_cells(c, P, u.i0);
+                c->n_outputs_last = u.row0;
+                c->st.n_outputs_last = u.row0;
                 return LCX_COMPUTE_FAILED;
             }
         }
         c->st.n_ubatch++;
         done = (int)k + 1;
     }
-    if (!c->host_only && argmax_out && !amax_dev && n_out_total > 0) {
-        cudaError_t e = cudaMemcpyAsync(c->amax_host, c->amax_dev, (size_t)n_out_total * 4, cudaMemcpyDeviceToHost,
-                                        c->stream);
-        if (e == cudaSuccess) e = cudaStreamSynchronize(c->stream);
-        if (e != cudaSuccess) {
-            set_err("argmax copy", e);
+    if (!c->host_only && n_out_total > 0) {
+        // one synchronization: the argmax rows (host buffer) and the status words. A logit that is
+        // not finite fails its ubatch: its cells and those of the later ubatches are released, the
+        // rows of the earlier ubatches stay (step 12: they were copied out before it ran)
+        const bool host_am = argmax_out && !amax_dev;
+        cudaError_t e = cudaSuccess;
+        if (host_am)
+            e = cudaMemcpyAsync(c->amax_host, c->amax_dev, (size_t)n_out_total * 4, cudaMemcpyDeviceToHost, c->stream);
+        const int32_t bad = e == cudaSuccess ? read_status(c) : -1;
+        if (e != cudaSuccess) set_err("argmax copy", e);
+        if (bad != 0) {
+            const int k = bad > 0 && bad <= (int)ubs.size() ? bad - 1 : 0;
+            release_cells(c, P, ubs[k].i0);
+            if (host_am && bad > 0) std::memcpy(argmax_out, c->amax_host, (size_t)ubs[k].row0 * 4);
+            c->st.n_decode++;
+            c->st.n_ubatch_last = k;
+            c->st.n_outputs_last = ubs[k].row0;
+            c->n_outputs_last = ubs[k].row0;
             return LCX_COMPUTE_FAILED;
         }
-        if (device_error_raised(c)) return LCX_COMPUTE_FAILED;
-        std::memcpy(argmax_out, c->amax_host, (size_t)n_out_total * 4);
+        if (host_am) std::memcpy(argmax_out, c->amax_host, (size_t)n_out_total * 4);
     }
     c->st.n_decode++;
     c->st.n_ubatch_last = done;
@@ -888,6 +956,7 @@ extern "C" int32_t lcx_decode_greedy(lcx_ctx *c, int32_t seq, int32_t token, int
             FwdArgs a = c->base;
             a.T = 1;
             a.n_out = 1;
+            a.tag = step + 1;
             a.ub.pos = d + i;
             a.ub.seq = d + ns + i;
             a.ub.cell = d + 2 * ns + i;
@@ -902,11 +971,24 @@ extern "C" int32_t lcx_decode_greedy(lcx_ctx *c, int32_t seq, int32_t token, int
         if (e == cudaSuccess && tokens_out) {
             if (out_dev)
                 e = cudaMemcpyAsync(tokens_out + c0, c->amax_dev, (size_t)ns * 4, cudaMemcpyDeviceToDevice, c->stream);
-            else {
+            else
                 e = cudaMemcpyAsync(c->amax_host, c->amax_dev, (size_t)ns * 4, cudaMemcpyDeviceToHost, c->stream);
-                if (e == cudaSuccess) e = cudaStreamSynchronize(c->stream);
-                if (e == cudaSuccess && device_error_raised(c)) e = cudaErrorLaunchFailure;
-                if (e == cudaSuccess) std::memcpy(tokens_out + c0, c->amax_host, (size_t)ns * 4);
+        }
+        if (e == cudaSuccess) {
+            // the chunk's status: a step whose logits are not all finite fails it and every later
+            // step (their cells are released); the earlier steps stay
+            const int32_t bad = read_status(c);
+            const int first_bad = bad > 0 && bad - 1 >= c0 && bad - 1 < c0 + ns ? bad - 1 : bad != 0 ? c0 : -1;
+            if (tokens_out && !out_dev)
+                std::memcpy(tokens_out + c0, c->amax_host, (size_t)((first_bad >= 0 ? first_bad : c0 + ns) - c0) * 4);
+            if (first_bad >= 0) {
+                release_cells(c, P, first_bad);
+                c->st.n_decode++;
+                c->st.n_ubatch += first_bad;
+                c->st.n_ubatch_last = first_bad;
+                c->st.n_outputs_last = first_bad;
+                c->n_outputs_last = first_bad;
+                return LCX_COMPUTE_FAILED;
             }
         }
         if (e == cudaSuccess && c0 + ns < n_steps) {

@@ -159,22 +159,28 @@ def run(SA, SB, SR, D, nk, seed):
     raise AssertionError("deadlock")
 
 
-def ring_depths(qb_bytes, bn):
-    """(SA, SB, SR, DB) as the kernel's Cfg<QT, BN, 2> computes them."""
+def ring_depths(qb_bytes, bn, mt):
+    """(SA, SB, SR, DB) as the kernel's Cfg<QT, BN, MT> computes them."""
     q4 = qb_bytes == 16
-    a_bytes = 2 * 128 * 64 * 2
+    a_bytes = mt * 128 * 64 * 2
     b_bytes = 2 * bn * 64 * 2
-    rq_slot = (2 * 32 * (8 * qb_bytes + 16) + 1023) // 1024 * 1024
-    sa = 3 if q4 and bn == 64 else 2
-    sr = 2 if not q4 and bn == 128 else 3
+    rq_slot = (mt * 32 * (8 * qb_bytes + 16) + 1023) // 1024 * 1024
+    sa = 3 if mt == 2 and q4 and bn == 64 else 2
+    sr = 2 if mt == 2 and not q4 and bn == 128 else 3
     sb = min(6, (220 * 1024 - sa * a_bytes - sr * rq_slot) // b_bytes)
     db = sb - sa if sb - sa >= 2 else sb - 1
+    assert sb >= 2 and db >= 1
+    assert sa * a_bytes + sb * b_bytes + sr * rq_slot + 1024 + 512 <= 227 * 1024
     return sa, sb, sr, db
 
 
-@pytest.mark.parametrize("qb_bytes,bn", [(16, 64), (16, 128), (32, 64), (32, 128)])   # Q4_0 / Q8_0 x BN
-def test_ring_protocol(qb_bytes, bn):
-    SA, SB, SR, DB = ring_depths(qb_bytes, bn)
+# every tile shape the launcher picks from (BN tokens x MT weight tiles), for Q4_0 and Q8_0
+SHAPES = [(qb, bn, mt) for qb in (16, 32) for bn, mt in ((64, 2), (128, 1), (128, 2), (256, 1))]
+
+
+@pytest.mark.parametrize("qb_bytes,bn,mt", SHAPES)
+def test_ring_protocol(qb_bytes, bn, mt):
+    SA, SB, SR, DB = ring_depths(qb_bytes, bn, mt)
     for nk in (1, 2, 3, 5, 7, 64):
         for seed in range(3):
             run(SA, SB, SR, DB, nk, seed)

@@ -185,11 +185,6 @@ def _prefix_parity(cfg, n_prompt, n_decode, n_ubatch, n_ctx):
     return errs
 
 
-def test_1b_prefix():
-    errs = _prefix_parity(synth.CONFIGS["1b"], 64, 3, 512, 4096)
-    print("1b rel errors", errs)
-
-
 def test_8b_prefix():
     errs = _prefix_parity(synth.CONFIGS["8b"], 12, 3, 512, 8192)
     print("8b rel errors", errs)

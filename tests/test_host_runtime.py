@@ -163,8 +163,9 @@ def test_failed_ubatch_rolls_back_like_the_oracle():
     assert c.inject_failure(1) == 0
     # tokens of two sequences, ubatches of 2: [s0 p0, s1 p0] [s0 p1, s1 p1] [s0 p2]
     toks, seqs = [1, 2, 3, 4, 5], [0, 1, 0, 1, 0]
-    assert c.decode(toks, seq_id=seqs) == lcx.LCX_COMPUTE_FAILED
-    assert (c.seq_pos_max(0), c.seq_pos_max(1), c.n_outputs()) == (0, 0, 0)
+    assert c.decode(toks, seq_id=seqs, logits=[1, 0, 1, 1, 1]) == lcx.LCX_COMPUTE_FAILED
+    # the first ubatch stays, with its one row; the failed and the later ubatch go
+    assert (c.seq_pos_max(0), c.seq_pos_max(1), c.n_outputs()) == (0, 0, 1)
     assert c.stats().n_cells_used == 2
     assert c.decode([6, 7], seq_id=[0, 1]) == 0              # the failure was one-shot
     assert (c.seq_pos_max(0), c.seq_pos_max(1)) == (1, 1)
@@ -176,8 +177,8 @@ def test_failed_ubatch_rolls_back_like_the_oracle():
     emb = host.tok_embd.copy()
     emb[bad].view(np.uint16)[:] = 0x7E00
     octx = oracle.Context(oracle.Model(dataclasses.replace(host, tok_embd=emb)), 256, 2, 2)
-    rc, _, _ = octx.decode([1, 2, bad, 4, 5], seq=seqs, logits=[0, 0, 1, 0, 0])
-    assert rc == -3 and (octx.seq_pos_max(0), octx.seq_pos_max(1)) == (0, 0)
+    rc, lg, _ = octx.decode([1, 2, bad, 4, 5], seq=seqs, logits=[1, 0, 1, 1, 1])
+    assert rc == -3 and (octx.seq_pos_max(0), octx.seq_pos_max(1)) == (0, 0) and lg.shape[0] == 1
 
 
 def test_inject_failure_needs_a_host_only_context():

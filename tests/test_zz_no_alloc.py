@@ -9,6 +9,7 @@ test before it; it also passes alone in a fresh process."""
 import numpy as np
 import pytest
 
+import oracle
 import synth
 
 torch = pytest.importorskip("torch")
@@ -33,7 +34,9 @@ def case(seed, H, KV, hd, lengths, queries):
         k += n
     cells = n_pages * KV * PAGE * hd
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    host = dict(pt=pt, seq=np.array([s for s, _ in queries], np.int32), pos=np.array([p for _, p in queries], np.int32))
     return dict(
+        host=host,
         q=dev(synth.normal(seed, 3, len(queries) * H * hd, 0.0, 0.2).reshape(len(queries), H * hd)),
         kc=dev(synth.normal(seed, 1, cells, 0.0, 1.0).astype(np.float16).reshape(n_pages, KV, PAGE, hd)),
         vc=dev(synth.normal(seed, 2, cells, 0.0, 1.0).astype(np.float16).reshape(n_pages, KV, PAGE, hd)),
@@ -57,6 +60,21 @@ def without_allocation(c):
     return out
 
 
+def oracle_rows(c, rows):
+    """The oracle's attention of query rows `rows`: the cells 0..pos of the query's sequence."""
+    q, kc, vc = (c[k].cpu().numpy() for k in ("q", "kc", "vc"))
+    h = c["host"]
+    out = {}
+    for t in rows:
+        s, p = int(h["seq"][t]), int(h["pos"][t])
+        idx = np.arange(p + 1)
+        pages = h["pt"][s][idx // PAGE]
+        K = kc[pages, :, idx % PAGE, :].astype(np.float64).reshape(p + 1, -1)
+        Vv = vc[pages, :, idx % PAGE, :].astype(np.float64).reshape(p + 1, -1)
+        out[t] = oracle.attend_gqa(q[t].astype(np.float64), K, Vv, c["H"], c["KV"], c["hd"])
+    return out
+
+
 def test_noalloc_matches_workspace_entry_on_two_calls():
     lcx.build()
     cases = [case(41, 32, 8, 128, [32896], [(0, 32895), (0, 20000)]),
@@ -66,6 +84,34 @@ def test_noalloc_matches_workspace_entry_on_two_calls():
         ref = with_workspace(c)
         torch.cuda.synchronize()
         assert torch.isfinite(got).all()
-        err = (torch.linalg.vector_norm(got.double() - ref.double(), dim=1) /
-               torch.linalg.vector_norm(ref.double(), dim=1)).max().item()
-        assert err <= TOL, err
+        # the same kernel with the same split of the cells: bit for bit the same result
+        assert torch.equal(got, ref)
+        want = oracle_rows(c, range(got.shape[0]))
+        g = got.double().cpu().numpy()
+        for t, w in want.items():
+            err = np.linalg.norm(g[t] - w) / np.linalg.norm(w)
+            assert err <= TOL, (t, err)
+
+
+def test_noalloc_rejects_a_call_beyond_its_scratch():
+    """A call whose scratch need exceeds the fixed array is refused on the host, before any
+    launch, with LCX_INVALID and a message."""
+    lcx.build()
+    H, KV, hd, max_pos = 32, 8, 128, 32000
+    T = 1
+    while lcx.attention_workspace_size(T, H, KV, hd, max_pos) <= lcx.LCX_ATTENTION_NOALLOC_SCRATCH_BYTES:
+        T *= 2
+    assert T <= 4096
+    max_pages = max_pos // PAGE + 1
+    # buffers of the sizes the call names; every page id is 0 and in bounds
+    q = torch.zeros((T, H * hd), dtype=torch.float32, device="cuda")
+    kc = torch.zeros((1, KV, PAGE, hd), dtype=torch.float16, device="cuda")
+    pt = torch.zeros((1, max_pages), dtype=torch.int32, device="cuda")
+    pos = torch.full((T,), max_pos, dtype=torch.int32, device="cuda")
+    seq = torch.zeros((T,), dtype=torch.int32, device="cuda")
+    out = torch.full_like(q, 7.0)
+    rc = lcx.attention_noalloc(q, kc, kc, pt, pos, seq, max_pos, out)
+    torch.cuda.synchronize()
+    assert rc == lcx.LCX_INVALID
+    assert "LCX_ATTENTION_NOALLOC_SCRATCH_BYTES" in lcx.lib().lcx_last_error().decode()
+    assert bool((out == 7.0).all())                      # nothing ran
