@@ -365,7 +365,7 @@ __global__ void __launch_bounds__(320, 1)
             // the A slot is free once the MMAs of step j - SA are done
             if (ok && j >= SA) ok = __all_sync(0xffffffffu, mbar_wait(&empty_a[aslot], ((j / SA) - 1) & 1));
             if (!ok) break;
-            dequant_row<QT, 3 - MT>(rq_tile(rslot, my_mt), a_tile(aslot, my_mt), drow, dblk);
+            dequant_row<QT, MT>(rq_tile(rslot, my_mt), a_tile(aslot, my_mt), drow, dblk);
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic writes -> tensor-core reads
             __syncwarp();
             if (lane == 0) {
