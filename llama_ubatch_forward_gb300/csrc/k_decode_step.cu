@@ -140,10 +140,6 @@ cudaError_t decode_step_prepare(DecodeStep &ds, const DevLayer *layers, int n_la
     ds.x_bytes = x_bytes;
     ds.smem = smem;
     ds.grid = n_sm;   // one CTA per SM: the ring takes most of an SM's shared memory
-    // L2 prefetch distance in stages per CTA (about 36 KB each): 8 keep ~44 MB of the weights
-    // ahead of the rings in L2 (LCX_STEP_L2_AHEAD overrides it; 0 turns it off)
-    ds.l2_ahead = 8;
-    if (const char *v = getenv("LCX_STEP_L2_AHEAD")) ds.l2_ahead = std::max(0, std::min(64, atoi(v)));
     ds.n_ph = (int)ph.size();
     ds.weight_bytes = 0;
     const int qw = a.H * a.hd, kvw = a.KV * a.hd;
@@ -194,7 +190,6 @@ cudaError_t launch_decode_step(const DecodeStep &ds, const FwdArgs &a, const voi
     sa.att_ns = ns;
     sa.att_chunk = chunk;
     sa.kvh_quads = (a.H / a.KV + 2) * a.hd / 4;
-    sa.l2_ahead = ds.l2_ahead;
     sa.tok_embd = reinterpret_cast<const uint8_t *>(tok_embd);
     sa.t_embd = t_embd;   // the ABI type codes equal QType
     sa.amax_dst = amax_dst;

@@ -59,7 +59,6 @@ struct StepArgs {
                            // head h written so far; zero between launches
     int att_ns, att_chunk; // attention splits of this token: att_ns ranges of att_chunk cells
     int kvh_quads;         // QKV row quads per KV head and layer: (n_head / n_head_kv + 2) head_dim / 4
-    int l2_ahead;          // stages past the ring's whose weights are prefetched into L2 (0: none)
     const uint8_t *tok_embd;
     int t_embd;
     int32_t *amax_dst;     // argmax of the logits row (n_out == 1)
@@ -73,10 +72,6 @@ __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned *p) {
     return v;
 }
 __device__ __forceinline__ int ld_volatile_i32(const int32_t *p) { return *reinterpret_cast<const volatile int32_t *>(p); }
-
-// Named barriers over the 256 threads: wait for all of them, or only count this warp in.
-__device__ __forceinline__ void named_sync(int id) { asm volatile("bar.sync %0, 256;" ::"r"(id) : "memory"); }
-__device__ __forceinline__ void named_arrive(int id) { asm volatile("bar.arrive %0, 256;" ::"r"(id) : "memory"); }
 
 // OR of a predicate over the 256 consumer threads (also a barrier among them)
 __device__ __forceinline__ bool consumer_any(bool v) {
@@ -470,45 +465,16 @@ __host__ __device__ constexpr int attn_scratch_bytes(int hd, int g) { return (3 
 constexpr int kFeedThread = 255;
 struct Feeder {
     int ph, st, issued;
-    int pph, pst;   // L2 prefetch cursor: s.l2_ahead stages past the ring's cursor
 };
 
-// Moves a cursor (phase ph, stage st) to the next stage this CTA takes that exists; ph == n_ph
-// once the sequence is exhausted.
-__device__ __forceinline__ void cursor_settle(const StepPhase *tab, int n_ph, int &ph, int &st) {
-    while (ph < n_ph && st >= tab[ph].n_stages) {
-        ++ph;
-        st = blockIdx.x;
-    }
-}
-
-// Bytes and first byte of stage st of phase ph (a SwiGLU stage's quad count rounds up to even).
-__device__ __forceinline__ const uint8_t *stage_span(const StepPhase &P, bool swiglu, int st, uint32_t &bytes) {
-    const int tasks = min(P.pl.tps, P.p.n_tasks - st * P.pl.tps);
-    const int quads = swiglu ? tasks + (tasks & 1) : tasks;
-    bytes = (uint32_t)quads * (uint32_t)P.pl.quad_bytes;
-    return P.p.w + (size_t)st * P.pl.tps * P.pl.quad_bytes;
-}
-
-// L2 prefetch of the prefetch cursor's stage (weights only: they do not depend on the step), then
-// the cursor moves on. The weights of the stages after the ring's stream into L2 while the CTA
-// waits on barriers, stages activations or attends, so HBM keeps working through those spans and
-// the ring's later copies hit L2.
-__device__ __forceinline__ void prefetch_one(const StepPhase *tab, int n_ph, int L, Feeder &f) {
-    cursor_settle(tab, n_ph, f.pph, f.pst);
-    if (f.pph >= n_ph) return;
-    uint32_t bytes;
-    const uint8_t *src = stage_span(tab[f.pph], f.pph != 4 * L && f.pph % 4 == PH_GU, f.pst, bytes);
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-    f.pst += gridDim.x;
-}
-
 // Issues the cursor's stage into ring slot issued % slots and advances the cursor; nothing once
-// the sequence is exhausted. tab: the phase table (shared memory). Then the stage l2_ahead
-// further on goes to L2.
+// the sequence is exhausted. tab: the phase table (shared memory).
 __device__ __forceinline__ void feed_one(const StepArgs &s, const StepPhase *tab, int n_ph, int L, Feeder &f,
-                                         uint8_t *ring, uint64_t *full, bool pf = true) {
-    cursor_settle(tab, n_ph, f.ph, f.st);
+                                         uint8_t *ring, uint64_t *full) {
+    while (f.ph < n_ph && f.st >= tab[f.ph].n_stages) {
+        ++f.ph;
+        f.st = blockIdx.x;
+    }
     if (f.ph >= n_ph) return;
     const StepPhase &P = tab[f.ph];
     const int slot = f.issued % s.slots;
@@ -517,7 +483,6 @@ __device__ __forceinline__ void feed_one(const StepArgs &s, const StepPhase *tab
     else issue_stage<EPI_RESID>(P.p, P.pl, f.st, dst, &full[slot]);
     f.st += gridDim.x;
     ++f.issued;
-    if (pf && s.l2_ahead > 0) prefetch_one(tab, n_ph, L, f);
 }
 
 // Stages x (token 0) for a matrix with nb blocks: as stage_token, in a rolled loop over pairs of
@@ -837,38 +802,22 @@ __device__ __noinline__ void step_gemv(const StepArgs &s, const StepPhase *tab, 
     unsigned long long best = gs.best;
     Feeder f = gs.f;
     const int tps = P.pl.tps, n_tasks = P.p.n_tasks;
-    // Stages in pairs: every warp computes both stages' dot products into part[q] (q = pair
-    // index & 1); then one warp applies the pair's epilogues (lanes 0-15 the first stage's tasks,
-    // lanes 16-31 the second's) while the others go on to the next pair. The epilogue duty rotates
-    // over the 8 warps, so no warp carries it for every pair. Named barriers (all 256 threads)
-    // order this:
-    //   DONE(q) = 2 + q: the pair's dot products are all in part[q] and every warp is past its
-    //     reads of the pair's ring slots. The epilogue warp and the feeding warp wait for it, the
-    //     others only arrive.
-    //   FREE(q) = 4 + q: the epilogue warp of a pair arrives when it is done reading part[q]; the
-    //     other warps wait for that two pairs later, before they write part[q] again.
-    // (A model check of this protocol on the CPU -- every interleaving class, the phase ends --
-    // lives with the tests.)
-    const int warp = threadIdx.x >> 5;
-    const bool feed_warp = warp == (kFeedThread >> 5);
-    int bi = 0;   // pair index
+    // stages in pairs: both stages' dot products, one barrier, then warp 0 and warp 1 apply the
+    // two epilogues side by side, and both slots are refilled
+    int bi = 0;   // pair index: the partial sums alternate between two buffers
 #pragma unroll 1
     for (int st = blockIdx.x; st < P.n_stages; st += 2 * gridDim.x, ++bi) {
         const int st2 = st + gridDim.x;
         const bool two = st2 < P.n_stages;
         const int slot0 = k % s.slots, slot1 = (k + 1) % s.slots;
-        const int q = bi & 1;
-        float *pk0 = part + q * 256, *pk1 = pk0 + 128;
-        const bool epi_warp = warp == (bi & 7);
-        const bool was_epi = bi >= 2 && warp == ((bi - 2) & 7);   // read part[q] two pairs ago
-        // this thread's epilogue, if any: lanes 0-15 take the tasks of the first stage, 16-31 the second's
-        const bool second = (threadIdx.x & 31) >= 16;
-        const int my_st = second ? st2 : st, e = threadIdx.x & 15;
-        const bool epi_thread = !dead && epi_warp && (!second || two) && e < min(tps, n_tasks - my_st * tps);
+        float *pk0 = part + (bi & 1) * 256, *pk1 = pk0 + 128;
+        // this thread's epilogue, if any: warp 0 takes the tasks of the first stage, warp 1 the second's
+        const int my_st = threadIdx.x < 32 ? st : st2, e = threadIdx.x & 31;
+        const bool epi_thread = !dead && threadIdx.x < 64 && (threadIdx.x < 32 || two) &&
+                                e < min(tps, n_tasks - my_st * tps);
         EpiIn ein{};
         if (epi_thread && epi == EPI_RESID) ein = epi_load<EPI_RESID>(a, 0, (my_st * tps + e) * 4, P.p.N);
         if (epi_thread && epi == EPI_QKV) ein = qkv_in(a, (my_st * tps + e) * 4, sc);
-        if (bi >= 2 && !was_epi) named_sync(4 + q);   // part[q] is no longer read
         // the pair's two stages through one copy of the dot-product code (instruction cache)
 #pragma unroll 1
         for (int u = 0; u < (two ? 2 : 1); ++u) {
@@ -879,29 +828,23 @@ __device__ __noinline__ void step_gemv(const StepArgs &s, const StepPhase *tab, 
             }
             if (!dead) dots_rt<QT>(P, mp, ring + (size_t)slot * s.slot_bytes, xq, bk, u ? pk1 : pk0);
         }
-        if (epi_warp || feed_warp) named_sync(2 + q);
-        else named_arrive(2 + q);
-        if (epi_thread) epilogue_rt(P, mp, epi, a, layer, my_st, e, second ? pk1 : pk0, rs, ein, best, sc.pub);
-        if (epi_warp) named_arrive(4 + q);
-        // every warp is past its reads of the slots (DONE above): refill them
+        consumer_sync();
+        if (epi_thread) epilogue_rt(P, mp, epi, a, layer, my_st, e, threadIdx.x < 32 ? pk0 : pk1, rs, ein, best, sc.pub);
+        // every warp is past its reads of the slots (the barrier above): refill them
         if (threadIdx.x == kFeedThread && !dead) {
             feed_one(s, tab, n_ph, a.L, f, ring, full);
             if (two) feed_one(s, tab, n_ph, a.L, f, ring, full);
         }
         k += two ? 2 : 1;
     }
-    // the FREE arrivals of the last two pairs are taken here, so every barrier ends the phase
-    // balanced; then the whole CTA meets (the epilogues of the last pair are done)
-    for (int j = bi - 2 < 0 ? 0 : bi - 2; j < bi; ++j)
-        if (warp != (j & 7)) named_sync(4 + (j & 1));
-    consumer_sync();
     gs.k = k;
     gs.dead = dead;
     gs.best = best;
     gs.f = f;
     if (epi == EPI_QKV) {
-        // publish this CTA's quads, one release reduction per KV head: the barrier above orders
-        // every epilogue thread's stores before it
+        // publish this CTA's quads, one release reduction per KV head: the barrier orders every
+        // epilogue thread's stores before it
+        consumer_sync();
         if ((int)threadIdx.x < a.KV) {
             const unsigned n = sc.pub[threadIdx.x];
             if (n && !dead) asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(s.sync + 16 + threadIdx.x), "r"(n) : "memory");
@@ -945,21 +888,10 @@ __global__ void __launch_bounds__(256, 1) k_decode_step(const __grid_constant__ 
     }
     __syncthreads();
     const StepConst sc{s_rope, s_cell, s_pub};
-    GemvState gs{0, Feeder{0, (int)blockIdx.x, 0, 0, (int)blockIdx.x}, false, 0ull};
-    // fill the ring: the weights do not depend on anything this step computes; the prefetch
-    // cursor starts slots + l2_ahead stages in (every ring fill below moves it by one more)
-    if (threadIdx.x == kFeedThread) {
-        for (int i = 0; s.l2_ahead > 0 && i < s.slots + s.l2_ahead; ++i) {
-            cursor_settle(tab, n_ph, gs.f.pph, gs.f.pst);
-            if (i >= s.slots && gs.f.pph < n_ph) {
-                uint32_t bytes;
-                const uint8_t *src = stage_span(tab[gs.f.pph], gs.f.pph != 4 * L && gs.f.pph % 4 == PH_GU, gs.f.pst, bytes);
-                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-            }
-            gs.f.pst += gridDim.x;
-        }
-        for (int i = 0; i < s.slots; ++i) feed_one(s, tab, n_ph, L, gs.f, ring, full, false);
-    }
+    GemvState gs{0, Feeder{0, (int)blockIdx.x, 0}, false, 0ull};
+    // fill the ring: the weights do not depend on anything this step computes
+    if (threadIdx.x == kFeedThread)
+        for (int i = 0; i < s.slots; ++i) feed_one(s, tab, n_ph, L, gs.f, ring, full);
 
     __shared__ float red[8];
     __shared__ __align__(16) float part[2 * 2 * 16 * 8];   // [batch parity][stage of the pair][16 rows][8]

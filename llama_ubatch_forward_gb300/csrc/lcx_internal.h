@@ -173,7 +173,6 @@ struct DecodeStep {
     size_t smem = 0;
     int grid = 0;
     int n_ph = 0;
-    int l2_ahead = 0;            // stages per CTA prefetched into L2 past the ring's
     double weight_bytes = 0;     // stored weight bytes one step streams (without the head)
     double head_bytes = 0;
 };
