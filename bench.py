@@ -260,6 +260,13 @@ def decode_bytes_seqs(cfg, host, ctx_lens):
     return w + host.tok_embd.shape[1] * len(ctx_lens) + kv_cell * int(np.sum(ctx_lens))
 
 
+def summarize_profile(pr):
+    return {k: {"launches": v["launches"], "ms": round(v["ms"], 3),
+                "GBps": round(v["bytes"] / v["ms"] / 1e6, 1) if v["ms"] else None,
+                "TFLOPps": round(v["flops"] / v["ms"] / 1e9, 2) if v["ms"] else None}
+            for k, v in pr.items() if v["launches"]}
+
+
 def timed(stream, fn):
     """Device milliseconds of fn() between CUDA events on `stream` (synchronized on both sides)."""
     import torch
@@ -294,6 +301,15 @@ def run_workloads(names, gm8, host8, stream, hbm, bf16):
             pre = timed(stream, lambda: ctx.decode(prompt, argmax_out=am))
             dec = timed(stream, lambda: ctx.decode_greedy(0, int(am[0]), n_dec, gen))
             res = {"prefill_ms": pre, "decode_ms": dec}
+        # per-kernel-class device time of the same run (events around every launch), after timing
+        ctx.kv_clear()
+        ctx.set_profiling(True)
+        ctx.decode(prompt, argmax_out=am)
+        prof_pre = ctx.profile()
+        ctx.set_profiling(True)
+        ctx.decode_greedy(0, int(am[0]), n_dec, gen)
+        prof_dec = ctx.profile()
+        ctx.set_profiling(False)
         del ctx
         dec_b = decode_bytes_per_step(cfg, host, n_prompt, n_dec) / n_dec
         pf = prefill_flops(cfg, n_prompt)
@@ -306,7 +322,8 @@ def run_workloads(names, gm8, host8, stream, hbm, bf16):
                                "frac": round(dgbs / hbm, 4), "bound": "hbm"},
                     "prefill": {"value": round(n_prompt / (res["prefill_ms"] / 1e3), 1), "unit": "tokens/s",
                                 "flops": pf, "achieved_tflops": round(ptf, 2), "frac": round(ptf / bf16, 4),
-                                "bound": "tensor"}}
+                                "bound": "tensor"},
+                    "kernel_profile": {"prefill": summarize_profile(prof_pre), "decode": summarize_profile(prof_dec)}}
         log(f"[bench] {key}: {json.dumps(out[key])}")
 
     if "1b" in names:
@@ -347,6 +364,14 @@ def run_workloads(names, gm8, host8, stream, hbm, bf16):
                     toks = am.copy()
 
             res = {"prefill_ms": timed(stream, prefill), "decode_ms": timed(stream, decode)}
+        # per-kernel-class device time of 8 more decode steps (events around every launch)
+        ctx.set_profiling(True)
+        toks = am.copy()
+        for _ in range(8):
+            assert ctx.decode(toks, seq_id=seqs, logits=flags, argmax_out=am) == 0
+            toks = am.copy()
+        prof_dec = ctx.profile()
+        ctx.set_profiling(False)
         del ctx
         n_pre = int(np.sum(lens))
         step_bytes = [decode_bytes_seqs(cfg, host8, lens + i + 1) for i in range(n_steps)]
@@ -363,7 +388,8 @@ def run_workloads(names, gm8, host8, stream, hbm, bf16):
                        "bytes_per_step": round(sum(step_bytes) / n_steps), "achieved_gbs": round(dgbs, 1),
                        "frac": round(dgbs / hbm, 4), "bound": "hbm"},
             "prefill": {"value": round(n_pre / (res["prefill_ms"] / 1e3), 1), "unit": "tokens/s", "flops": pf,
-                        "achieved_tflops": round(ptf, 2), "frac": round(ptf / bf16, 4), "bound": "tensor"}}
+                        "achieved_tflops": round(ptf, 2), "frac": round(ptf / bf16, 4), "bound": "tensor"},
+            "kernel_profile": {"decode_8_steps": summarize_profile(prof_dec)}}
         log(f"[bench] multiseq: {json.dumps(out['multiseq'])}")
     return out
 

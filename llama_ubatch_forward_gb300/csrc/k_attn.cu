@@ -39,11 +39,13 @@ __global__ void __launch_bounds__(128) k_attn(const FwdArgs a, const int layer, 
     const int32_t *ptrow = a.pt + (size_t)seq * a.max_pages_per_seq;
     const size_t layer_base = (size_t)layer * a.n_pages;
     const int fresh = n_att - a.T;   // cells at positions >= fresh may come from this ubatch
-    uint4 kraw[4][DPL / 8];
-    uint2 vraw[16];
-    // K/V of the super-group of 16 cells at j0 (inside one page); `only_fresh` re-reads just the
-    // cells this ubatch may have written
-    auto load_sg = [&](int j0, bool only_fresh) {
+    // two buffers of one super-group's K/V each: the next super-group's loads are in flight while
+    // the current one is used
+    uint4 kA[4][DPL / 8], kB[4][DPL / 8];
+    uint2 vA[16], vB[16];
+    // K/V of the super-group of 16 cells at j0 (inside one page) into (kraw, vraw); `only_fresh`
+    // re-reads just the cells this ubatch may have written
+    auto load_sg = [&](int j0, bool only_fresh, uint4 (&kraw)[4][DPL / 8], uint2 (&vraw)[16]) {
         const int page = ptrow[j0 / kPage];
         const size_t row0 = ((layer_base + page) * a.KV + kvh) * kPage + (j0 % kPage);
 #pragma unroll
@@ -71,12 +73,12 @@ __global__ void __launch_bounds__(128) k_attn(const FwdArgs a, const int layer, 
         }
     };
     const int j_first = c0 + warp * 16;
-    if (sp < ns_t && j_first < c1) load_sg(j_first, false);
+    if (sp < ns_t && j_first < c1) load_sg(j_first, false, kA, vA);
     LCX_PDL_WAIT();
     LCX_PDL_TRIGGER();
     LCX_TRACE(a, 1);
     if (sp >= ns_t) return;
-    if (j_first < c1 && j_first + 16 > fresh) load_sg(j_first, true);
+    if (j_first < c1 && j_first + 16 > fresh) load_sg(j_first, true, kA, vA);
     const int qw = a.H * HD;
     const float scale = rsqrtf((float)HD);
 
@@ -101,9 +103,8 @@ __global__ void __launch_bounds__(128) k_attn(const FwdArgs a, const int layer, 
     }
 
     // Each warp takes super-groups of 16 consecutive cells (inside one 64-cell page): all K and
-    // V loads of a super-group are issued before any of them is used.
-    for (int j0 = j_first; j0 < c1; j0 += 64) {
-        if (j0 != j_first) load_sg(j0, false);
+    // V loads of a super-group are issued before any of them is used, one super-group ahead.
+    auto consume = [&](int j0, const uint4 (&kraw)[4][DPL / 8], const uint2 (&vraw)[16]) {
 #pragma unroll
         for (int g4 = 0; g4 < 4; ++g4) {
             if (j0 + 4 * g4 >= c1) break;
@@ -178,6 +179,13 @@ __global__ void __launch_bounds__(128) k_attn(const FwdArgs a, const int layer, 
                 }
             }
         }
+        };
+    for (int j0 = j_first; j0 < c1; j0 += 128) {
+        if (j0 + 64 < c1) load_sg(j0 + 64, false, kB, vB);
+        consume(j0, kA, vA);
+        if (j0 + 64 >= c1) break;
+        if (j0 + 128 < c1) load_sg(j0 + 128, false, kA, vA);
+        consume(j0 + 64, kB, vB);
     }
 
     LCX_TRACE(a, 2);
@@ -316,9 +324,14 @@ int attention_splits(const FwdArgs &a, int max_natt, int *chunk) {
     const int target = n_sm;
     const int units = a.T * a.KV;
     int ns = units >= target ? 1 : (target + units - 1) / units;
+    // inside the forward, no CTA walks more than att_max_chunk cells: with many units (a ubatch of
+    // one token per sequence over long contexts) one CTA per unit would leave the longest context's
+    // CTAs running alone at the end
+    if (a.att_max_chunk > 0) ns = max(ns, (max_natt + a.att_max_chunk - 1) / a.att_max_chunk);
     int by_len = (max_natt + 63) / 64;
     ns = ns < by_len ? ns : by_len;
     ns = ns < a.att_max_split ? ns : a.att_max_split;
+    if (a.att_rows_cap > 0) ns = min(ns, max(1, a.att_rows_cap / units));   // partial rows available
     if (ns < 1) ns = 1;
     int ch = (max_natt + ns - 1) / ns;
     ch = (ch + 15) / 16 * 16;

@@ -142,8 +142,11 @@ struct Cfg {
 struct GemmParams {
     int N;          // logical rows (outputs) of W
     int T;          // tokens
-    int nk;         // K / 64
-    int row_base;   // unused (tiles start at blockIdx.x * 128 or, for SwiGLU, chunk c * 256)
+    int nk;         // K / 64: steps of the whole contraction
+    int ks;         // splits of the K steps (gridDim.z); 1: the CTA applies the epilogue itself
+    int N_pad;      // rows of the partial sums' layout
+    float *part;    // ks > 1: partial sums [ks][T][N_pad] f32
+    int32_t *cnt;   // ks > 1: arrival counter per output tile (zero between launches)
 };
 
 // Dequantise blocks b0 .. b0 + NBLK - 1 (of the step's block pair) of row `row` (0..127) of one
@@ -232,7 +235,10 @@ __global__ void __launch_bounds__(320, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_bar + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m_tile = blockIdx.x, tok0 = blockIdx.y * BN;
-    const int nk = p.nk;
+    // this CTA's K steps: split blockIdx.z of p.ks (equal runs; the last may be short)
+    const int nk_per = (p.nk + p.ks - 1) / p.ks;
+    const int kb = blockIdx.z * nk_per;
+    const int nk = max(0, min(p.nk, kb + nk_per) - kb);
     // first weight row of each M tile: MT adjacent 128-row tiles (for gate/up each holds 16
     // gate quads interleaved with their 16 up quads)
     int row0[MT];
@@ -275,7 +281,7 @@ __global__ void __launch_bounds__(320, 1)
             auto issue_w = [&](int j) {   // quants and scales of the 32 MT quads of the tiles: one box
                 const int slot = j % SR;
                 mbar_expect_tx(&full_w[slot], C::RQ_BYTES);
-                tma_2d(rq_tile(slot, 0), &tm_w, j * (C::PB / 4), row0[0] / 4, &full_w[slot]);
+                tma_2d(rq_tile(slot, 0), &tm_w, (kb + j) * (C::PB / 4), row0[0] / 4, &full_w[slot]);
             };
             const int pre = nk < SR ? nk : SR;
             for (int j = 0; j < pre; ++j) issue_w(j);
@@ -342,7 +348,7 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
                 for (int u = 0; u < BN / 32; ++u) {
                     const int r = (wt >> 3) + 32 * u, t = tok0 + r;
-                    const __half *src = src0 + (size_t)(t < p.T ? t : 0) * K + j * BK + c * 8;
+                    const __half *src = src0 + (size_t)(t < p.T ? t : 0) * K + (size_t)(kb + j) * BK + c * 8;
                     const uint32_t dst = saddr(bt + hl * BN * BK * 2 + r * 128 + ((c ^ (r & 7)) << 4));
                     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
                                  "r"(t < p.T ? 16 : 0) : "memory");
@@ -390,19 +396,16 @@ __global__ void __launch_bounds__(320, 1)
         asm volatile("cp.async.wait_all;" ::: "memory");   // nothing in flight when the CTA ends
         if (!ok) atomicExch(a.err, 1);
         const bool acc_ok = __all_sync(0xffffffffu, ok && mbar_wait(acc_bar, 0));
-        if (acc_ok) {
-            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            // a warp reads the TMEM lanes of its quarter (warp % 4); with two tiles warps 2..5 take
-            // tile 0 and 6..9 tile 1, all BN columns; with one tile the two warps of a quarter
-            // take half of the columns each
-            const int q = warp & 3;                 // TMEM lane quarter of this warp
-            const int lrow = q * 32 + lane;         // row within the tile
-            const int r = row0[my_mt] + lrow;       // weight row
-            const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16) + my_mt * BN;
-            const int cb0 = MT == 2 ? 0 : (wt >> 7) * (BN / 64), cb1 = MT == 2 ? BN / 32 : cb0 + BN / 64;
-            for (int cb = cb0; cb < cb1; ++cb) {
-                uint32_t vv[32];   // W (A_hi + A_lo)
-                tmem_ld32(tq + cb * 32, vv);
+        // a warp reads the TMEM lanes of its quarter (warp % 4); with two tiles warps 2..5 take
+        // tile 0 and 6..9 tile 1, all BN columns; with one tile the two warps of a quarter take
+        // half of the columns each
+        const int q = warp & 3;                 // TMEM lane quarter of this warp
+        const int lrow = q * 32 + lane;         // row within the tile
+        const int r = row0[my_mt] + lrow;       // weight row
+        const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16) + my_mt * BN;
+        const int cb0 = MT == 2 ? 0 : (wt >> 7) * (BN / 64), cb1 = MT == 2 ? BN / 32 : cb0 + BN / 64;
+        // the fused epilogue of 32 tokens (chunk cb) of this thread's row, from their sums vv
+        auto epilogue = [&](int cb, uint32_t (&vv)[32]) {
                 if (EPI == EPI_SWIGLU) {   // rows 8f'..8f'+3 gate, 8f'+4..8f'+7 up of features 4f'..
                     const int f = (r >> 3) * 4 + (lrow & 3);
                     const bool gate = (lane & 7) < 4;
@@ -414,7 +417,7 @@ __global__ void __launch_bounds__(320, 1)
                         if (gate && t < p.T && f < a.F)
                             store_split(a.h16, a.h16_lo, (size_t)t * a.F_pad + f, silu_f(g) * u);
                     }
-                    continue;
+                    return;
                 }
                 // every load of a 16-token group is issued before its first store: a store may
                 // alias a later load, so mixing them would serialise one L2 round trip per element
@@ -488,9 +491,64 @@ __global__ void __launch_bounds__(320, 1)
                         }
                     }
                 }
+        };
+        if (acc_ok) asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        else if (ok) atomicExch(a.err, 1);
+        if (p.ks == 1) {
+            if (acc_ok)
+                for (int cb = cb0; cb < cb1; ++cb) {
+                    uint32_t vv[32];   // W (A_hi + A_lo)
+                    tmem_ld32(tq + cb * 32, vv);
+                    epilogue(cb, vv);
+                }
+        } else {
+            // split K: every CTA of an output tile stores its partial sums; the last of them to
+            // arrive adds the ks partials in split order and applies the epilogue. The counter is
+            // bumped even after a failed wait, so it always returns to zero.
+            __shared__ int s_last;
+            if (acc_ok)
+                for (int cb = cb0; cb < cb1; ++cb) {
+                    uint32_t vv[32];
+                    tmem_ld32(tq + cb * 32, vv);
+                    float *dst = p.part + ((size_t)blockIdx.z * p.T) * p.N_pad + r;
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int t = tok0 + cb * 32 + i;
+                        if (t < p.T && r < p.N_pad) __stcg(dst + (size_t)t * p.N_pad, __uint_as_float(vv[i]));
+                    }
+                }
+            asm volatile("bar.sync 1, 256;" ::: "memory");   // the 8 epilogue warps' stores are done
+            if (wt == 0) {
+                __threadfence();
+                const int prev = atomicAdd(p.cnt + blockIdx.x * gridDim.y + blockIdx.y, 1);
+                s_last = prev == p.ks - 1;
             }
-        } else if (ok) {
-            atomicExch(a.err, 1);
+            asm volatile("bar.sync 1, 256;" ::: "memory");
+            if (s_last) {
+                __threadfence();
+                for (int cb = cb0; cb < cb1; ++cb) {
+                    // split by split, the 32 tokens' loads all in flight before they are added
+                    float sum[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) sum[i] = 0.f;
+                    for (int z = 0; z < p.ks; ++z) {
+                        const float *src = p.part + ((size_t)z * p.T) * p.N_pad + r;
+                        float v[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const int t = min(tok0 + cb * 32 + i, p.T - 1);
+                            v[i] = r < p.N_pad ? __ldcg(src + (size_t)t * p.N_pad) : 0.f;
+                        }
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) sum[i] += v[i];
+                    }
+                    uint32_t vv[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) vv[i] = __float_as_uint(sum[i]);
+                    epilogue(cb, vv);
+                }
+                if (wt == 0) p.cnt[blockIdx.x * gridDim.y + blockIdx.y] = 0;
+            }
         }
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -531,38 +589,40 @@ bool make_map_2d(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int e
 }
 
 template <int QT, int BN, int MT, int EPI>
-cudaError_t run(const QMat &W, int T, const __half *A, const __half *A_lo, const FwdArgs &a, int layer, cudaStream_t s) {
+cudaError_t run(const QMat &W, int T, int ks, const __half *A, const __half *A_lo, const FwdArgs &a, int layer,
+                cudaStream_t s) {
     using C = Cfg<QT, BN, MT>;
     auto kern = k_gemm_tc<QT, BN, MT, EPI>;
     cudaError_t e = func_attr_once((const void *)kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     if (!W.tm_ready) return cudaErrorInvalidValue;
-    GemmParams p{W.N, T, W.K / BK, 0};
+    GemmParams p{W.N, T, W.K / BK, ks, W.N_pad, a.gemm_part, a.gemm_cnt};
     const int m_tiles = (W.N_pad + MT * BM - 1) / (MT * BM);   // rows past N_pad read as zeros
-    dim3 grid(m_tiles, (T + BN - 1) / BN);
+    dim3 grid(m_tiles, (T + BN - 1) / BN, ks);
     return launch_pdl(kern, grid, dim3(320), (size_t)C::SMEM, s, A, A_lo, W.K,
                       *reinterpret_cast<const CUtensorMap *>(MT == 2 ? W.tm_w : W.tm_w1), p, a, layer);
 }
 
 template <int QT, int BN, int MT>
-cudaError_t dispatch(const QMat &W, Epi epi, int T, const __half *A, const __half *A_lo, const FwdArgs &a, int layer,
-                     cudaStream_t s) {
+cudaError_t dispatch(const QMat &W, Epi epi, int T, int ks, const __half *A, const __half *A_lo, const FwdArgs &a,
+                     int layer, cudaStream_t s) {
     switch (epi) {
-        case EPI_QKV: return run<QT, BN, MT, EPI_QKV>(W, T, A, A_lo, a, layer, s);
-        case EPI_RESID: return run<QT, BN, MT, EPI_RESID>(W, T, A, A_lo, a, layer, s);
-        case EPI_SWIGLU: return run<QT, BN, MT, EPI_SWIGLU>(W, T, A, A_lo, a, layer, s);
-        case EPI_LOGITS: return run<QT, BN, MT, EPI_LOGITS>(W, T, A, A_lo, a, layer, s);
+        case EPI_QKV: return run<QT, BN, MT, EPI_QKV>(W, T, ks, A, A_lo, a, layer, s);
+        case EPI_RESID: return run<QT, BN, MT, EPI_RESID>(W, T, ks, A, A_lo, a, layer, s);
+        case EPI_SWIGLU: return run<QT, BN, MT, EPI_SWIGLU>(W, T, ks, A, A_lo, a, layer, s);
+        case EPI_LOGITS: return run<QT, BN, MT, EPI_LOGITS>(W, T, ks, A, A_lo, a, layer, s);
     }
     return cudaErrorInvalidValue;
 }
 
 template <int QT>
-cudaError_t dispatch_shape(int bn, int mt, const QMat &W, Epi epi, int T, const __half *A, const __half *A_lo,
+cudaError_t dispatch_shape(const GemmShape &g, const QMat &W, Epi epi, int T, const __half *A, const __half *A_lo,
                            const FwdArgs &a, int layer, cudaStream_t s) {
-    if (bn == 64) return dispatch<QT, 64, 2>(W, epi, T, A, A_lo, a, layer, s);
-    if (bn == 128 && mt == 1) return dispatch<QT, 128, 1>(W, epi, T, A, A_lo, a, layer, s);
-    if (bn == 128) return dispatch<QT, 128, 2>(W, epi, T, A, A_lo, a, layer, s);
-    return dispatch<QT, 256, 1>(W, epi, T, A, A_lo, a, layer, s);
+    if (g.bn == 64 && g.mt == 1) return dispatch<QT, 64, 1>(W, epi, T, g.ks, A, A_lo, a, layer, s);
+    if (g.bn == 64) return dispatch<QT, 64, 2>(W, epi, T, g.ks, A, A_lo, a, layer, s);
+    if (g.bn == 128 && g.mt == 1) return dispatch<QT, 128, 1>(W, epi, T, g.ks, A, A_lo, a, layer, s);
+    if (g.bn == 128) return dispatch<QT, 128, 2>(W, epi, T, g.ks, A, A_lo, a, layer, s);
+    return dispatch<QT, 256, 1>(W, epi, T, g.ks, A, A_lo, a, layer, s);
 }
 
 }  // namespace tc
@@ -580,36 +640,48 @@ bool make_weight_maps(QMat &W) {
     return W.tm_ready;
 }
 
-// Tile shape of a launch: BN tokens x MT 128-row weight tiles per CTA, from a cost model per K
-// step (cycles of one SM): the MMAs take 4 BN MT (128 x BN x 16 per MMA, hi and lo parts, four
-// per 64-wide step, about 4096 multiply-adds a cycle), the dequantisation of MT tiles about
-// 435 MT, given a 30% margin since it must also hide its waits; the launch takes as many of
-// those steps as its waves of CTAs. Ties go to fewer CTAs (less activation traffic).
-void gemm_shape(int N_pad, int T, int n_sm, int *bn, int *mt) {
-    static const int cand[4][2] = {{64, 2}, {128, 1}, {128, 2}, {256, 1}};
-    long best = -1, best_ctas = 0;
+// Tile shape of a launch: BN tokens x MT 128-row weight tiles per CTA, and the K steps split
+// over ks CTAs, from a cost model per K step (cycles of one SM): the MMAs take 4 BN MT (128 x BN x
+// 16 per MMA, hi and lo parts, four per 64-wide step, about 4096 multiply-adds a cycle), the
+// dequantisation of MT tiles about 435 MT, given a 30% margin since it must also hide its waits;
+// the launch takes as many of those steps as each CTA runs, times its waves of CTAs. A split adds
+// the partial sums' round trip (the last CTA of a tile reads ks partial tiles from L2; about
+// 10000 + 16 BN MT ks cycles, so a split is taken only where the CTAs would otherwise leave many
+// SMs idle: on the 8B shape, the 64-token ubatches' QKV, O and down projections). Ties go to
+// fewer CTAs (less activation traffic). Splits need room in the context's partial-sum scratch.
+GemmShape gemm_shape(int N_pad, int T, int nk, int n_sm, size_t part_bytes, int max_tiles) {
+    static const int cand[5][2] = {{64, 1}, {64, 2}, {128, 1}, {128, 2}, {256, 1}};
+    GemmShape best{64, 2, 1};
+    long best_cost = -1, best_ctas = 0;
     for (const auto &c : cand) {
-        const long ctas = (long)((N_pad + c[1] * 128 - 1) / (c[1] * 128)) * ((T + c[0] - 1) / c[0]);
-        const long waves = (ctas + n_sm - 1) / n_sm;
+        const long tiles = (long)((N_pad + c[1] * 128 - 1) / (c[1] * 128)) * ((T + c[0] - 1) / c[0]);
         const long step = std::max<long>(4L * c[0] * c[1], 566L * c[1]);
-        const long cost = waves * step;
-        if (best < 0 || cost < best || (cost == best && ctas < best_ctas)) {
-            best = cost;
-            best_ctas = ctas;
-            *bn = c[0];
-            *mt = c[1];
+        for (int ks = 1; ks <= 8; ++ks) {
+            if (ks > 1 && (nk / ks < 4 || tiles * ks > 2L * n_sm || tiles > max_tiles ||
+                           (size_t)ks * T * N_pad * 4 > part_bytes))
+                break;
+            if ((long)(ks - 1) * ((nk + ks - 1) / ks) >= nk) continue;   // every split gets K steps
+            const long ctas = tiles * ks;
+            const long waves = (ctas + n_sm - 1) / n_sm;
+            const long cost = waves * ((nk + ks - 1) / ks) * step + (ks > 1 ? 10000L + ks * 16L * c[0] * c[1] : 0L);
+            if (best_cost < 0 || cost < best_cost || (cost == best_cost && ctas < best_ctas)) {
+                best_cost = cost;
+                best_ctas = ctas;
+                best = GemmShape{c[0], c[1], ks};
+            }
         }
     }
+    return best;
 }
 
 cudaError_t launch_gemm_tc(const QMat &W, Epi epi, int T, const __half *A, const __half *A_lo, const FwdArgs &a,
                            int layer, cudaStream_t s, int64_t &launches, int64_t *wide) {
     ++launches;
-    int bn = 64, mt = 2;
-    gemm_shape(W.N_pad, T, device_sm_count(), &bn, &mt);
-    if (bn >= 128 && wide) ++*wide;
-    if (W.type == Q4) return tc::dispatch_shape<Q4>(bn, mt, W, epi, T, A, A_lo, a, layer, s);
-    if (W.type == Q8) return tc::dispatch_shape<Q8>(bn, mt, W, epi, T, A, A_lo, a, layer, s);
+    const GemmShape g = gemm_shape(W.N_pad, T, W.K / tc::BK, device_sm_count(), a.gemm_part ? a.gemm_part_bytes : 0,
+                                   a.gemm_cnt ? kGemmMaxTiles : 0);
+    if (g.bn >= 128 && wide) ++*wide;
+    if (W.type == Q4) return tc::dispatch_shape<Q4>(g, W, epi, T, A, A_lo, a, layer, s);
+    if (W.type == Q8) return tc::dispatch_shape<Q8>(g, W, epi, T, A, A_lo, a, layer, s);
     return cudaErrorInvalidValue;
 }
 

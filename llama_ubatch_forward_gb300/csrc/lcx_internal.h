@@ -100,7 +100,12 @@ struct FwdArgs {
     // attention scratch
     float *att_part;   // partial (m, l, acc[hd]) per (token, q head, split)
     int32_t *att_cnt;  // [T][KV] arrival counters, zero between launches
+    float *gemm_part;  // split-K partial sums of the tensor-core GEMM (NULL: no splits)
+    size_t gemm_part_bytes;
+    int32_t *gemm_cnt; // [kGemmMaxTiles] its per-tile arrival counters, zero between launches
     int att_max_split;
+    int att_max_chunk; // > 0: cells per attention CTA at most (inside the forward; 0 for the stand-alone call)
+    int att_rows_cap;  // > 0: partial rows the attention scratch holds (T * KV * splits at most)
     int32_t *err;      // device error word: set by a kernel whose bounded wait timed out
     int32_t *nonfinite;// 0, or the tag of the first ubatch of the call whose logits held a value
                        // that is not finite (written once, by compare-and-swap)
@@ -143,7 +148,15 @@ bool gemv_fits(const QMat &W, int T);
 cudaError_t launch_gemm(const QMat &W, Epi epi, int T, const __half *A, const __half *A_lo, const FwdArgs &a,
                         int layer, cudaStream_t s, int64_t &launches, int64_t *wide = nullptr);
 
-// tcgen05 GEMM (k_gemm_tc.cu) and the TMA descriptors of a weight matrix it needs
+// tcgen05 GEMM (k_gemm_tc.cu) and the TMA descriptors of a weight matrix it needs. A launch's tile
+// shape: bn tokens x mt 128-row weight tiles per CTA, K steps split over ks CTAs (partial sums in
+// FwdArgs::gemm_part, at most kGemmMaxTiles output tiles per split launch).
+struct GemmShape {
+    int bn, mt, ks;
+};
+constexpr int kGemmMaxTiles = 4096;
+constexpr size_t kGemmPartBytes = (size_t)32 << 20;   // split-K partial sums per context
+GemmShape gemm_shape(int N_pad, int T, int nk, int n_sm, size_t part_bytes, int max_tiles);
 // (*wide, if given, counts the launches that took tiles of 128 or more tokens)
 cudaError_t launch_gemm_tc(const QMat &W, Epi epi, int T, const __half *A, const __half *A_lo, const FwdArgs &a,
                            int layer, cudaStream_t s, int64_t &launches, int64_t *wide = nullptr);

@@ -367,7 +367,9 @@ extern "C" lcx_ctx *lcx_ctx_create(lcx_model *m, uint32_t n_ctx, uint32_t n_seq_
     // workspace
     int n_sm = 0;
     cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, m->device);
-    const size_t part_rows = (size_t)2 * 4 * (n_sm > 0 ? n_sm : 160) + (size_t)T * KV;   // see attention_splits
+    // attention partials: the split-K attention's (max, sum, acc) rows, see attention_splits
+    const size_t part_rows = std::max<size_t>((size_t)2 * 4 * (n_sm > 0 ? n_sm : 160) + (size_t)T * KV,
+                                              std::min<size_t>((size_t)T * KV * 16, 16384));
     const int G = H / KV;
     size_t ws = 0;
     const size_t sizes[] = {
@@ -387,6 +389,8 @@ extern "C" lcx_ctx *lcx_ctx_create(lcx_model *m, uint32_t n_ctx, uint32_t n_seq_
         (size_t)T * KV * 4,                  // attention counters
         (size_t)std::max<int>(T, 4096) * 4,  // argmax per output row
         256,                                 // device error word
+        T > kGemvMaxT ? kGemmPartBytes : 0,  // split-K partial sums of the tensor-core GEMM
+        T > kGemvMaxT ? (size_t)kGemmMaxTiles * 4 : 0,   // their per-tile counters
     };
     for (size_t s : sizes) ws += (s + 255) / 256 * 256;
     if (e == cudaSuccess) ok(cudaMalloc(&c->ws, ws), "workspace");
@@ -412,12 +416,19 @@ extern "C" lcx_ctx *lcx_ctx_create(lcx_model *m, uint32_t n_ctx, uint32_t n_seq_
         a.err = carve<int32_t>(p, 64);
         a.nonfinite = a.err + 1;
         a.tag = 1;
+        if (T > kGemvMaxT) {
+            a.gemm_part = carve<float>(p, kGemmPartBytes / 4);
+            a.gemm_part_bytes = kGemmPartBytes;
+            a.gemm_cnt = carve<int32_t>(p, kGemmMaxTiles);
+        }
         a.d = d; a.H = H; a.KV = KV; a.hd = hd; a.F = hp.n_ff; a.F_pad = Fp; a.V = V; a.L = L;
         a.eps = hp.rms_eps;
         a.kc = c->kc; a.vc = c->vc; a.n_pages = c->n_pages;
         a.pt = c->pt; a.max_pages_per_seq = c->max_pages_per_seq;
         a.rope = c->rope;
         a.att_max_split = c->max_att_split;
+        a.att_max_chunk = 512;
+        a.att_rows_cap = (int)part_rows;
         a.pdl = true;
     }
     // metadata: per token tok, pos, seq, cell, out_row + up to 2 page-table updates (2 ints each)

@@ -175,7 +175,7 @@ def ring_depths(qb_bytes, bn, mt):
 
 
 # every tile shape the launcher picks from (BN tokens x MT weight tiles), for Q4_0 and Q8_0
-SHAPES = [(qb, bn, mt) for qb in (16, 32) for bn, mt in ((64, 2), (128, 1), (128, 2), (256, 1))]
+SHAPES = [(qb, bn, mt) for qb in (16, 32) for bn, mt in ((64, 1), (64, 2), (128, 1), (128, 2), (256, 1))]
 
 
 @pytest.mark.parametrize("qb_bytes,bn,mt", SHAPES)
