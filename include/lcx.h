@@ -146,6 +146,20 @@ int32_t lcx_decode(lcx_ctx *ctx, lcx_batch batch, float *logits_out, int32_t *ar
  * and lcx_n_outputs gives their number (their tokens are in tokens_out). */
 int32_t lcx_decode_greedy(lcx_ctx *ctx, int32_t seq, int32_t token, int32_t n_steps, int32_t *tokens_out);
 
+/* KV layout of a context (step 10 and step 12, init_batch). unified != 0 (the default): one cell
+ * store of n_ctx cells shared by all sequences, batches cut into consecutive chunks of n_ubatch
+ * tokens (split_simple). unified == 0: a stream per sequence -- each sequence may hold at most
+ * n_ctx_seq = n_ctx / n_seq_max cells (a batch that would exceed it returns LCX_NO_KV_SLOT with
+ * nothing committed) -- and batches are cut by split_equal: each ubatch takes the same number of
+ * next tokens from every sequence that has tokens left (the lowest sequence ids first, at most
+ * n_ubatch sequences), as many as the shortest of them has left and at most n_ubatch divided by
+ * their number, sequence by sequence in position order. Logits rows stay in batch order either
+ * way. When a batch of a context with a stream per sequence stops (LCX_ABORTED or
+ * LCX_COMPUTE_FAILED), its completed ubatches stay in the cache but no rows are reported (they
+ * are not the batch's first rows). Only while the context holds no cell (after creation or
+ * lcx_kv_clear): LCX_INVALID otherwise. */
+int32_t lcx_ctx_set_kv_unified(lcx_ctx *ctx, int32_t unified);
+
 /* Frees every cell (the memory clear of the KV-cache section): every sequence becomes empty. */
 void lcx_kv_clear(lcx_ctx *ctx);
 

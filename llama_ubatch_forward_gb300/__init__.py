@@ -22,7 +22,7 @@ SYMBOLS = ("lcx_model_create", "lcx_model_free", "lcx_ctx_create", "lcx_ctx_free
            "lcx_decode_greedy", "lcx_kv_clear", "lcx_seq_pos_max", "lcx_n_outputs", "lcx_set_abort",
            "lcx_get_stats", "lcx_ctx_create_host_only", "lcx_get_rows", "lcx_last_error", "lcx_set_profiling",
            "lcx_get_profile", "lcx_attention_workspace_size", "lcx_attention", "lcx_attention_noalloc",
-           "lcx_kv_read", "lcx_get_trace", "lcx_sample", "lcx_ctx_inject_failure")
+           "lcx_kv_read", "lcx_get_trace", "lcx_sample", "lcx_ctx_inject_failure", "lcx_ctx_set_kv_unified")
 
 
 def build(force: bool = False) -> str:
@@ -96,6 +96,8 @@ def lib():
         L.lcx_decode_greedy.restype = i32
         L.lcx_decode_greedy.argtypes = [vp, i32, i32, i32, vp]
         L.lcx_kv_clear.argtypes = [vp]
+        L.lcx_ctx_set_kv_unified.restype = i32
+        L.lcx_ctx_set_kv_unified.argtypes = [vp, i32]
         L.lcx_seq_pos_max.restype = i32
         L.lcx_seq_pos_max.argtypes = [vp, i32]
         L.lcx_n_outputs.restype = i32
@@ -210,6 +212,10 @@ class Context:
 
     def kv_clear(self):
         lib().lcx_kv_clear(self.h)
+
+    def set_kv_unified(self, unified: bool) -> int:
+        """One cell store for all sequences (True, the default) or a stream per sequence."""
+        return lib().lcx_ctx_set_kv_unified(self.h, 1 if unified else 0)
 
     def inject_failure(self, ubatch: int) -> int:
         """Host-only contexts: ubatch `ubatch` of the next decode fails as a failed launch would."""

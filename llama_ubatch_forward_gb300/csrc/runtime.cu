@@ -233,6 +233,7 @@ struct lcx_ctx {
     lcx_hparams hp{};
     bool host_only = false;
     int fail_ubatch = -1;   // host-only contexts: this ubatch of the next lcx_decode fails (-3)
+    bool kv_unified = true; // one cell store for all sequences; else a stream of n_ctx / n_seq_max per sequence
     uint32_t n_ctx = 0, n_seq_max = 0, n_ubatch = 0;
     cudaStream_t stream = nullptr;
     int n_pages = 0, max_pages_per_seq = 0;
@@ -536,7 +537,15 @@ static int32_t fill_batch(const lcx_ctx *c, const lcx_batch &b, Plan &P) {
 // Reserves a cell for every token (all or nothing): 1 if the cache cannot hold the batch.
 static int32_t reserve_cells(lcx_ctx *c, Plan &P) {
     const int n = (int)P.tok.size();
-    if (c->cells_used + n > (int64_t)c->n_ctx) return LCX_NO_KV_SLOT;
+    if (c->kv_unified) {
+        if (c->cells_used + n > (int64_t)c->n_ctx) return LCX_NO_KV_SLOT;
+    } else {   // a stream per sequence: n_ctx_seq = n_ctx / n_seq_max cells each (step 10)
+        const int64_t n_ctx_seq = (int64_t)c->n_ctx / c->n_seq_max;
+        std::vector<int64_t> len(c->n_seq_max);
+        for (uint32_t q = 0; q < c->n_seq_max; ++q) len[q] = c->seqs[q].len;
+        for (int i = 0; i < n; ++i)
+            if (++len[P.seq[i]] > n_ctx_seq) return LCX_NO_KV_SLOT;
+    }
     P.cell.resize(n);
     P.pt_idx.clear();
     P.pt_page.clear();
@@ -560,26 +569,45 @@ static int32_t reserve_cells(lcx_ctx *c, Plan &P) {
     return LCX_OK;
 }
 
-// Releases the cells of tokens [from, n) of the plan (their sequences' tails).
-static void release_cells(lcx_ctx *c, const Plan &P, int from) {
-    const int n = (int)P.tok.size();
-    for (int i = n - 1; i >= from; --i) {
-        SeqState &S = c->seqs[P.seq[i]];
-        S.len = P.pos[i];
+// Releases the cells of the plan's tokens marked in `rel` (for each sequence a tail of its
+// tokens: ubatches take every sequence's tokens in position order).
+static void release_tokens(lcx_ctx *c, const Plan &P, const std::vector<char> &rel) {
+    std::vector<int32_t> len(c->n_seq_max, -1);
+    int cnt = 0;
+    for (size_t i = 0; i < rel.size(); ++i)
+        if (rel[i]) {
+            const int32_t q = P.seq[i];
+            if (len[q] < 0 || P.pos[i] < len[q]) len[q] = P.pos[i];
+            ++cnt;
+        }
+    for (uint32_t q = 0; q < c->n_seq_max; ++q) {
+        if (len[q] < 0) continue;
+        SeqState &S = c->seqs[q];
+        S.len = len[q];
         while ((int)S.pages.size() * kPage > S.len + (kPage - 1) && !S.pages.empty()) {
             c->free_pages.push_back(S.pages.back());
             S.pages.pop_back();
         }
     }
-    c->cells_used -= (n - from);
+    c->cells_used -= cnt;
+}
+
+// Releases the cells of tokens [from, n) of the plan (their sequences' tails).
+static void release_cells(lcx_ctx *c, const Plan &P, int from) {
+    std::vector<char> rel(P.tok.size(), 0);
+    for (size_t i = (size_t)from; i < rel.size(); ++i) rel[i] = 1;
+    release_tokens(c, P, rel);
 }
 
 // --------------------------------------------------------------------- forward of one ubatch
 namespace {
 
 struct Ub {
-    int i0, T;           // tokens [i0, i0 + T) of the plan
-    int n_out, row0;     // output rows and the batch row of the first
+    std::vector<int> idx;   // the plan's tokens in this ubatch, in ubatch order
+    int T = 0, n_out = 0;   // tokens and output rows
+    int row0 = 0;           // batch-order output row of its first flagged token
+    bool contig = true;     // its flagged tokens' batch rows are row0, row0 + 1, ... in ubatch order
+    std::vector<int> rows;  // batch-order output row of each flagged token, in ubatch order
 };
 
 bool is_device_ptr(const void *p) {
@@ -595,18 +623,19 @@ bool is_device_ptr(const void *p) {
 // device UbDev view.
 cudaError_t upload_meta(lcx_ctx *c, const Plan &P, const Ub &u, UbDev &ub) {
     const int T = u.T;
+    const std::vector<int> &x = u.idx;
     // updates whose first token lies in this ubatch
+    std::vector<char> mine(P.tok.size(), 0);
+    for (int i : x) mine[i] = 1;
     std::vector<int> upd;
     for (size_t k = 0; k < P.pt_tok.size(); ++k)
-        if (P.pt_tok[k] >= u.i0 && P.pt_tok[k] < u.i0 + T) upd.push_back((int)k);
+        if (mine[P.pt_tok[k]]) upd.push_back((int)k);
     // query tiles: runs of consecutive positions of one sequence, cut every 64 tokens
     std::vector<int32_t> tiles;
     for (int i = 0; i < T;) {
         int n = 1;
-        while (i + n < T && n < 64 && P.seq[u.i0 + i + n] == P.seq[u.i0 + i] &&
-               P.pos[u.i0 + i + n] == P.pos[u.i0 + i] + n)
-            ++n;
-        tiles.insert(tiles.end(), {i, n, P.seq[u.i0 + i], P.pos[u.i0 + i]});
+        while (i + n < T && n < 64 && P.seq[x[i + n]] == P.seq[x[i]] && P.pos[x[i + n]] == P.pos[x[i]] + n) ++n;
+        tiles.insert(tiles.end(), {i, n, P.seq[x[i]], P.pos[x[i]]});
         i += n;
     }
     const int ntiles = (int)tiles.size() / 4;
@@ -621,11 +650,11 @@ cudaError_t upload_meta(lcx_ctx *c, const Plan &P, const Ub &u, UbDev &ub) {
     int32_t *tok = h, *pos = h + T, *seq = h + 2 * T, *cell = h + 3 * T, *orow = h + 4 * T, *pu = h + 5 * T;
     int no = 0;
     for (int i = 0; i < T; ++i) {
-        tok[i] = P.tok[u.i0 + i];
-        pos[i] = P.pos[u.i0 + i];
-        seq[i] = P.seq[u.i0 + i];
-        cell[i] = P.cell[u.i0 + i];
-        if (P.flag[u.i0 + i]) orow[no++] = i;
+        tok[i] = P.tok[x[i]];
+        pos[i] = P.pos[x[i]];
+        seq[i] = P.seq[x[i]];
+        cell[i] = P.cell[x[i]];
+        if (P.flag[x[i]]) orow[no++] = i;
     }
     for (size_t k = 0; k < upd.size(); ++k) {
         pu[2 * k] = P.pt_idx[upd[k]];
@@ -812,6 +841,84 @@ static int32_t read_status(lcx_ctx *c) {
     return nf;
 }
 
+// The ubatches of a validated batch (step 12, init_batch): with one cell store, consecutive chunks
+// of n_ubatch tokens (split_simple); with a stream per sequence, split_equal: each ubatch takes the
+// same number of next tokens from every sequence that has tokens left (the lowest sequence ids
+// first, at most n_ubatch sequences) -- as many as the shortest of them has left and at most
+// n_ubatch divided by their number -- sequence by sequence in position order. Output rows stay in
+// batch order: row of a flagged token = flagged tokens before it in the batch.
+static std::vector<Ub> split_batch(const lcx_ctx *c, const Plan &P) {
+    const int n = (int)P.tok.size();
+    std::vector<int> brow(n, -1);
+    int n_rows = 0;
+    for (int i = 0; i < n; ++i)
+        if (P.flag[i]) brow[i] = n_rows++;
+    std::vector<Ub> ubs;
+    if (c->kv_unified) {
+        for (int i0 = 0; i0 < n; i0 += (int)c->n_ubatch) {
+            Ub u;
+            for (int i = i0; i < n && i < i0 + (int)c->n_ubatch; ++i) u.idx.push_back(i);
+            ubs.push_back(std::move(u));
+        }
+    } else {
+        std::vector<std::vector<int>> left(c->n_seq_max);
+        for (int i = 0; i < n; ++i) left[P.seq[i]].push_back(i);
+        std::vector<size_t> taken(c->n_seq_max, 0);
+        for (;;) {
+            std::vector<uint32_t> ss;
+            for (uint32_t q = 0; q < c->n_seq_max && ss.size() < c->n_ubatch; ++q)
+                if (taken[q] < left[q].size()) ss.push_back(q);
+            if (ss.empty()) break;
+            size_t k = c->n_ubatch / ss.size();
+            for (uint32_t q : ss) k = std::min(k, left[q].size() - taken[q]);
+            Ub u;
+            for (uint32_t q : ss)
+                for (size_t j = 0; j < k; ++j) u.idx.push_back(left[q][taken[q] + j]);
+            for (uint32_t q : ss) taken[q] += k;
+            ubs.push_back(std::move(u));
+        }
+    }
+    for (Ub &u : ubs) {
+        u.T = (int)u.idx.size();
+        for (int i : u.idx)
+            if (P.flag[i]) u.rows.push_back(brow[i]);
+        u.n_out = (int)u.rows.size();
+        u.row0 = u.n_out ? u.rows[0] : 0;
+        for (int j = 0; j < u.n_out; ++j) u.contig = u.contig && u.rows[j] == u.row0 + j;
+    }
+    return ubs;
+}
+
+// Releases the cells of ubatch k and of every later one.
+static void release_ubatches(lcx_ctx *c, const Plan &P, const std::vector<Ub> &ubs, size_t k) {
+    std::vector<char> rel(P.tok.size(), 0);
+    for (size_t j = k; j < ubs.size(); ++j)
+        for (int i : ubs[j].idx) rel[i] = 1;
+    release_tokens(c, P, rel);
+}
+
+// Rows kept after the batch stopped before ubatch k: with one store the ubatches ran in batch order,
+// so the rows before k's are the batch's first rows; with a stream per sequence they are not a
+// prefix of the batch's rows, and none is reported.
+static int rows_kept(const lcx_ctx *c, const std::vector<Ub> &ubs, size_t k) {
+    return c->kv_unified ? ubs[k].row0 : 0;
+}
+
+// Copies rows [0, n) of a ubatch's outputs (scratch) to their batch-order rows, one copy per run
+// of consecutive rows: `w` elements of `esz` bytes per row.
+static cudaError_t scatter_rows(const Ub &u, const void *src, void *dst, size_t w, size_t esz, cudaMemcpyKind kind,
+                                cudaStream_t s) {
+    cudaError_t e = cudaSuccess;
+    for (int j = 0; j < u.n_out && e == cudaSuccess;) {
+        int r = 1;
+        while (j + r < u.n_out && u.rows[j + r] == u.rows[j] + r) ++r;
+        e = cudaMemcpyAsync((uint8_t *)dst + (size_t)u.rows[j] * w * esz, (const uint8_t *)src + (size_t)j * w * esz,
+                            (size_t)r * w * esz, kind, s);
+        j += r;
+    }
+    return e;
+}
+
 extern "C" int32_t lcx_decode(lcx_ctx *c, lcx_batch batch, float *logits_out, int32_t *argmax_out) {
     if (!c) return LCX_INVALID;
     c->n_outputs_last = 0;
@@ -821,19 +928,12 @@ extern "C" int32_t lcx_decode(lcx_ctx *c, lcx_batch batch, float *logits_out, in
     if (c->host_only && logits_out) return LCX_INVALID;
     rc = reserve_cells(c, P);
     if (rc != LCX_OK) return rc;
-    const int n = (int)P.tok.size();
-    // ubatches: consecutive chunks of at most n_ubatch tokens (split_simple)
-    std::vector<Ub> ubs;
-    int row = 0;
-    for (int i0 = 0; i0 < n; i0 += (int)c->n_ubatch) {
-        Ub u{i0, std::min<int>((int)c->n_ubatch, n - i0), 0, row};
-        for (int i = 0; i < u.T; ++i) u.n_out += P.flag[i0 + i];
-        row += u.n_out;
-        ubs.push_back(u);
-    }
-    const int n_out_total = row;
+    std::vector<Ub> ubs = split_batch(c, P);
+    int n_out_total = 0;
+    for (const Ub &u : ubs) n_out_total += u.n_out;
     const bool amax_dev = argmax_out && !c->host_only && is_device_ptr(argmax_out);
-    if (argmax_out && !amax_dev && !c->host_only && n_out_total > c->amax_cap) {
+    const bool host_am = argmax_out && !amax_dev && !c->host_only;
+    if (host_am && n_out_total > c->amax_cap) {
         int32_t *nh = nullptr;
         if (cudaHostAlloc((void **)&nh, (size_t)n_out_total * 4, cudaHostAllocDefault) != cudaSuccess) {
             release_cells(c, P, 0);
@@ -843,23 +943,21 @@ extern "C" int32_t lcx_decode(lcx_ctx *c, lcx_batch batch, float *logits_out, in
         c->amax_host = nh;
         c->amax_cap = n_out_total;
     }
+    auto stop = [&](size_t k, int32_t code) {
+        release_ubatches(c, P, ubs, k);
+        c->st.n_decode++;
+        c->st.n_ubatch_last = (int32_t)k;
+        c->st.n_outputs_last = rows_kept(c, ubs, k);
+        c->n_outputs_last = c->st.n_outputs_last;
+        return code;
+    };
     int done = 0;
     for (size_t k = 0; k < ubs.size(); ++k) {
         const Ub &u = ubs[k];
-        if (k > 0 && c->abort_cb && c->abort_cb(c->abort_ud)) {
-            release_cells(c, P, u.i0);
-            c->st.n_decode++;
-            c->st.n_ubatch_last = (int32_t)k;
-            c->st.n_outputs_last = u.row0;
-            c->n_outputs_last = u.row0;
-            return LCX_ABORTED;
-        }
+        if (k > 0 && c->abort_cb && c->abort_cb(c->abort_ud)) return stop(k, LCX_ABORTED);
         if (c->host_only && (int)k == c->fail_ubatch) {   // as a failed launch below
             c->fail_ubatch = -1;
-            release_cells(c, P, u.i0);
-            c->n_outputs_last = u.row0;
-            c->st.n_outputs_last = u.row0;
-            return LCX_COMPUTE_FAILED;
+            return stop(k, LCX_COMPUTE_FAILED);
         }
         if (!c->host_only) {
             FwdArgs a = c->base;
@@ -868,21 +966,29 @@ extern "C" int32_t lcx_decode(lcx_ctx *c, lcx_batch batch, float *logits_out, in
             a.tag = (int32_t)k + 1;
             cudaError_t e = upload_meta(c, P, u, a.ub);
             a.tok_src = a.ub.tok;
-            if (logits_out) a.logits = logits_out + (size_t)u.row0 * c->hp.n_vocab;
+            // rows in batch order: written in place when they are consecutive, else through the
+            // context's scratch and copied to their rows
+            const bool direct = u.contig;
+            if (logits_out && direct) a.logits = logits_out + (size_t)u.row0 * c->hp.n_vocab;
             int max_natt = 0;
             double cells = 0;
-            for (int i = 0; i < u.T; ++i) {
-                max_natt = std::max(max_natt, P.pos[u.i0 + i] + 1);
-                cells += P.pos[u.i0 + i] + 1;
+            for (int i : u.idx) {
+                max_natt = std::max(max_natt, P.pos[i] + 1);
+                cells += P.pos[i] + 1;
             }
-            int32_t *dst = amax_dev ? argmax_out + u.row0 : c->amax_dev + u.row0;
+            int32_t *dst = amax_dev && direct ? argmax_out + u.row0 : c->amax_dev;
             if (e == cudaSuccess) e = run_forward(c, a, max_natt, cells, dst);
+            if (e == cudaSuccess && u.n_out > 0) {
+                if (logits_out && !direct)
+                    e = scatter_rows(u, c->base.logits, logits_out, c->hp.n_vocab, 4, cudaMemcpyDeviceToDevice, c->stream);
+                if (e == cudaSuccess && amax_dev && !direct)
+                    e = scatter_rows(u, c->amax_dev, argmax_out, 1, 4, cudaMemcpyDeviceToDevice, c->stream);
+                if (e == cudaSuccess && host_am)
+                    e = scatter_rows(u, c->amax_dev, c->amax_host, 1, 4, cudaMemcpyDeviceToHost, c->stream);
+            }
             if (e != cudaSuccess) {
                 set_err("decode", e);
-                release_cells(c, P, u.i0);
-                c->n_outputs_last = u.row0;
-                c->st.n_outputs_last = u.row0;
-                return LCX_COMPUTE_FAILED;
+                return stop(k, LCX_COMPUTE_FAILED);
             }
         }
         c->st.n_ubatch++;
@@ -892,21 +998,11 @@ extern "C" int32_t lcx_decode(lcx_ctx *c, lcx_batch batch, float *logits_out, in
         // one synchronization: the argmax rows (host buffer) and the status words. A logit that is
         // not finite fails its ubatch: its cells and those of the later ubatches are released, the
         // rows of the earlier ubatches stay (step 12: they were copied out before it ran)
-        const bool host_am = argmax_out && !amax_dev;
-        cudaError_t e = cudaSuccess;
-        if (host_am)
-            e = cudaMemcpyAsync(c->amax_host, c->amax_dev, (size_t)n_out_total * 4, cudaMemcpyDeviceToHost, c->stream);
-        const int32_t bad = e == cudaSuccess ? read_status(c) : -1;
-        if (e != cudaSuccess) set_err("argmax copy", e);
+        const int32_t bad = read_status(c);
         if (bad != 0) {
-            const int k = bad > 0 && bad <= (int)ubs.size() ? bad - 1 : 0;
-            release_cells(c, P, ubs[k].i0);
-            if (host_am && bad > 0) std::memcpy(argmax_out, c->amax_host, (size_t)ubs[k].row0 * 4);
-            c->st.n_decode++;
-            c->st.n_ubatch_last = k;
-            c->st.n_outputs_last = ubs[k].row0;
-            c->n_outputs_last = ubs[k].row0;
-            return LCX_COMPUTE_FAILED;
+            const size_t k = bad > 0 && bad <= (int)ubs.size() ? (size_t)(bad - 1) : 0;
+            if (host_am) std::memcpy(argmax_out, c->amax_host, (size_t)rows_kept(c, ubs, k) * 4);
+            return stop(k, LCX_COMPUTE_FAILED);
         }
         if (host_am) std::memcpy(argmax_out, c->amax_host, (size_t)n_out_total * 4);
     }
@@ -914,6 +1010,12 @@ extern "C" int32_t lcx_decode(lcx_ctx *c, lcx_batch batch, float *logits_out, in
     c->st.n_ubatch_last = done;
     c->st.n_outputs_last = n_out_total;
     c->n_outputs_last = n_out_total;
+    return LCX_OK;
+}
+
+extern "C" int32_t lcx_ctx_set_kv_unified(lcx_ctx *c, int32_t unified) {
+    if (!c || c->cells_used != 0) return LCX_INVALID;
+    c->kv_unified = unified != 0;
     return LCX_OK;
 }
 

@@ -76,6 +76,8 @@ def lib():
         L.orc_matvec.argtypes = [i32, vp, i64, i64, vp, vp]
         L.orc_matmat.argtypes = [i32, vp, i64, i64, vp, i64, vp]
         L.orc_set_elide.argtypes = [vp, i32]
+        L.orc_set_kv_unified.restype = i32
+        L.orc_set_kv_unified.argtypes = [vp, i32]
         L.orc_rmsnorm.argtypes = [vp, i64, vp, dp, vp]
         L.orc_rope.argtypes = [vp, i32, i64, dp]
         L.orc_silu.restype = dp
@@ -224,6 +226,10 @@ class Context:
     def set_elide(self, on: bool):
         """Last layer: tokens whose logits are not flagged compute only K and V (on, the default)."""
         lib().orc_set_elide(self.h, 1 if on else 0)
+
+    def set_kv_unified(self, on: bool) -> int:
+        """One KV store for all sequences (True, the default) or a stream per sequence (False)."""
+        return lib().orc_set_kv_unified(self.h, 1 if on else 0)
 
     def set_trace(self, layer: int):
         lib().orc_set_trace(self.h, layer)

@@ -56,6 +56,7 @@
  * Parity pins: every function here is pinned by tests that do not call it to check itself
  * (hand-computed blocks, closed forms, invariants, brute force on tiny shapes).
  */
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <condition_variable>
@@ -307,6 +308,7 @@ struct Ctx {
     std::vector<Seq> seqs;
     int64_t used = 0;
     bool elide = true;   /* last layer: K and V only for tokens whose logits are not flagged */
+    bool unified = true; /* one KV store shared by all sequences; else one stream per sequence */
     /* trace of one layer for the most recent token that ran it whole: x in, q after RoPE, o,
      * x after attention */
     int32_t trace_layer = -1;
@@ -540,42 +542,104 @@ int32_t orc_decode(void *cv, int32_t n_tokens, const int32_t *token, const int32
         if ((int64_t)pos[i] != expect) return -1;
         flag[i] = flags_in ? (flags_in[i] != 0) : (int8_t)(i == n_tokens - 1);
     }
-    if (c->used + n_tokens > (int64_t)c->n_ctx) return 1;
-    /* ubatches: consecutive chunks of n_ubatch tokens, each evaluated in blocks of kBlock */
-    std::vector<double> tmp;
-    int32_t row = 0;
-    for (int32_t u0 = 0; u0 < n_tokens; u0 += (int32_t)c->n_ubatch) {
-        const int32_t u1 = u0 + (int32_t)c->n_ubatch < n_tokens ? u0 + (int32_t)c->n_ubatch : n_tokens;
-        int32_t nu = 0;
-        for (int32_t i = u0; i < u1; ++i) nu += flag[i];
-        double *lg = nullptr;
-        if (logits_out) {
-            lg = logits_out + (int64_t)row * hp.n_vocab;
-        } else {
-            tmp.resize((size_t)nu * hp.n_vocab);
-            lg = tmp.data();
+    /* capacity (step 10 and init_batch): one shared store of n_ctx cells, or, with a stream per
+     * sequence, n_ctx_seq = n_ctx / n_seq_max cells for each sequence */
+    if (c->unified) {
+        if (c->used + n_tokens > (int64_t)c->n_ctx) return 1;
+    } else {
+        const int64_t n_ctx_seq = (int64_t)c->n_ctx / c->n_seq_max;
+        for (uint32_t s = 0; s < c->n_seq_max; ++s)
+            if (next[s] > n_ctx_seq) return 1;
+    }
+    /* ubatches (step 12, init_batch): with one store, consecutive chunks of n_ubatch tokens
+     * (split_simple); with a stream per sequence, split_equal: every ubatch takes the same number
+     * of next tokens from each sequence that has tokens left (the lowest sequence ids first, at
+     * most n_ubatch sequences): as many as the shortest of them has left, and at most n_ubatch
+     * divided by their number; inside the ubatch, sequence by sequence in position order */
+    std::vector<std::vector<int32_t>> ubs;
+    if (c->unified) {
+        for (int32_t u0 = 0; u0 < n_tokens; u0 += (int32_t)c->n_ubatch) {
+            std::vector<int32_t> u;
+            for (int32_t i = u0; i < n_tokens && i < u0 + (int32_t)c->n_ubatch; ++i) u.push_back(i);
+            ubs.push_back(u);
         }
+    } else {
+        std::vector<std::vector<int32_t>> left(c->n_seq_max);   /* each sequence's tokens, in batch order */
+        for (int32_t i = 0; i < n_tokens; ++i) left[seq[i]].push_back(i);
+        std::vector<size_t> taken(c->n_seq_max, 0);
+        for (;;) {
+            std::vector<uint32_t> ss;
+            for (uint32_t s = 0; s < c->n_seq_max && ss.size() < c->n_ubatch; ++s)
+                if (taken[s] < left[s].size()) ss.push_back(s);
+            if (ss.empty()) break;
+            size_t k = c->n_ubatch / ss.size();
+            for (uint32_t s : ss) k = std::min(k, left[s].size() - taken[s]);
+            std::vector<int32_t> u;
+            for (uint32_t s : ss)
+                for (size_t j = 0; j < k; ++j) u.push_back(left[s][taken[s] + j]);
+            for (uint32_t s : ss) taken[s] += k;
+            ubs.push_back(u);
+        }
+    }
+    /* output rows in batch order: the row of flagged token i is the number of flagged tokens before it */
+    std::vector<int32_t> brow(n_tokens, -1);
+    int32_t n_rows = 0;
+    for (int32_t i = 0; i < n_tokens; ++i)
+        if (flag[i]) brow[i] = n_rows++;
+    std::vector<double> tmp;
+    int32_t row = 0;   /* rows done, ubatch by ubatch */
+    for (const std::vector<int32_t> &u : ubs) {
+        const int32_t nt = (int32_t)u.size();
+        std::vector<int32_t> ut(nt), up(nt), us(nt);
+        std::vector<int8_t> uf(nt);
+        int32_t nu = 0;
+        for (int32_t i = 0; i < nt; ++i) {
+            ut[i] = token[u[i]];
+            up[i] = pos[u[i]];
+            us[i] = seq[u[i]];
+            uf[i] = flag[u[i]];
+            nu += uf[i];
+        }
+        tmp.resize((size_t)(nu > 0 ? nu : 1) * hp.n_vocab);
         std::vector<int32_t> am(nu > 0 ? nu : 1);
         int32_t r = 0;
-        for (int32_t b0 = u0; b0 < u1; b0 += (int32_t)kBlock) {
-            const int32_t b1 = b0 + (int32_t)kBlock < u1 ? b0 + (int32_t)kBlock : u1;
-            run_block(*c, b1 - b0, token + b0, pos.data() + b0, seq.data() + b0, flag.data() + b0,
-                      lg + (int64_t)r * hp.n_vocab, am.data() + r);
-            for (int32_t i = b0; i < b1; ++i) r += flag[i];
+        for (int32_t b0 = 0; b0 < nt; b0 += (int32_t)kBlock) {
+            const int32_t b1 = b0 + (int32_t)kBlock < nt ? b0 + (int32_t)kBlock : nt;
+            run_block(*c, b1 - b0, ut.data() + b0, up.data() + b0, us.data() + b0, uf.data() + b0,
+                      tmp.data() + (int64_t)r * hp.n_vocab, am.data() + r);
+            for (int32_t i = b0; i < b1; ++i) r += uf[i];
         }
         /* a logit that is not finite fails the ubatch (step 13, a failed compute: its cells are
-         * removed again); earlier ubatches and their rows stay */
+         * removed again); earlier ubatches stay, and so do their rows when they are the first
+         * rows of the batch (one store: the ubatches run in batch order); with a stream per
+         * sequence the rows of a stopped batch are not reported */
         for (int64_t j = 0; j < (int64_t)nu * hp.n_vocab; ++j)
-            if (!std::isfinite(lg[j])) {
-                rollback(*c, u0, u1 - 1, seq.data(), pos.data());
-                if (n_out) *n_out = row;
+            if (!std::isfinite(tmp[j])) {
+                for (int32_t i = nt - 1; i >= 0; --i) rollback(*c, u[i], u[i], seq.data(), pos.data());
+                if (n_out) *n_out = c->unified ? row : 0;
                 return -3;
             }
-        if (argmax_out)
-            for (int32_t i = 0; i < nu; ++i) argmax_out[row + i] = am[i];
+        r = 0;
+        for (int32_t i = 0; i < nt; ++i)
+            if (uf[i]) {
+                if (logits_out)
+                    std::memcpy(logits_out + (int64_t)brow[u[i]] * hp.n_vocab, tmp.data() + (int64_t)r * hp.n_vocab,
+                                (size_t)hp.n_vocab * sizeof(double));
+                if (argmax_out) argmax_out[brow[u[i]]] = am[r];
+                ++r;
+            }
         row += nu;
     }
     if (n_out) *n_out = row;
+    return 0;
+}
+
+/* 1: one KV store shared by every sequence (the default); 0: a stream per sequence, each of
+ * n_ctx / n_seq_max cells, batches cut by split_equal. Only while the store is empty. */
+int32_t orc_set_kv_unified(void *cv, int32_t on) {
+    Ctx *c = (Ctx *)cv;
+    if (c->used != 0) return -1;
+    c->unified = on != 0;
     return 0;
 }
 

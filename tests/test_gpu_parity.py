@@ -188,3 +188,31 @@ def _prefix_parity(cfg, n_prompt, n_decode, n_ubatch, n_ctx):
 def test_8b_prefix():
     errs = _prefix_parity(synth.CONFIGS["8b"], 12, 3, 512, 8192)
     print("8b rel errors", errs)
+
+
+def test_tiny_stream_per_sequence(tiny):
+    """A stream per sequence: split_equal ubatches whose flagged rows are not consecutive in the
+    batch (written through the scratch and copied to their batch-order rows), host and device
+    argmax, against the oracle run the same way."""
+    host, gm, om = tiny
+    toks = synth.uniform_int(TINY.token_seed, 555, 23, 0, TINY.n_vocab)
+    seqs = np.array([0, 1, 2, 0, 0, 2, 1, 0, 2, 2, 0, 1, 1, 2, 0, 0, 1, 2, 2, 0, 1, 0, 2], np.int32)
+    flags = (synth.uniform_int(TINY.token_seed, 556, 23, 0, 3) > 0).astype(np.int8)
+    octx = oracle.Context(om, 384, 3, 4)
+    assert octx.set_kv_unified(False) == 0
+    ctx = lcx.Context(gm, 384, 3, 4)
+    assert ctx.set_kv_unified(False) == 0
+    rc_o, ref, am_o = octx.decode(toks, seq=seqs, logits=flags)
+    rc, lg, am = gpu_decode(ctx, TINY.n_vocab, toks, seq=seqs, flags=flags)
+    assert rc == rc_o == 0
+    check_rows(lg, am, ref, am_o, "split_equal prefill")
+    # one step for every sequence, device argmax
+    nxt = np.array([5, 6, 7], np.int32)
+    rc_o, ref, am_o = octx.decode(nxt, seq=[1, 2, 0], logits=np.ones(3))
+    out = torch.full((3, TINY.n_vocab), float("nan"), dtype=torch.float32, device="cuda")
+    amd = torch.full((3,), -1, dtype=torch.int32, device="cuda")
+    assert ctx.decode(nxt, seq_id=[1, 2, 0], logits=np.ones(3), logits_out=out, argmax_out=amd) == 0
+    torch.cuda.synchronize()
+    check_rows(out.cpu().numpy(), amd.cpu().numpy(), ref, am_o, "split_equal step")
+    for s in range(3):
+        assert ctx.seq_pos_max(s) == octx.seq_pos_max(s)

@@ -100,13 +100,16 @@ def test_pages_recycle_across_clears():
         c.kv_clear()
 
 
-def test_rules_match_the_oracle_on_random_streams():
-    """Same return code and positions as the oracle for random valid and invalid batches."""
+@pytest.mark.parametrize("unified", [True, False])
+def test_rules_match_the_oracle_on_random_streams(unified):
+    """Same return code and positions as the oracle for random valid and invalid batches, with one
+    shared cell store and with a stream per sequence (its own capacity rule)."""
     m = synth.make_model(TINY, n_layer=1)
     rng = np.random.default_rng(11)
     for trial in range(3):
         oc = oracle.Context(oracle.Model(m), 256, 3, 512)
         hc = _host_ctx(n_ctx=256, n_seq=3, n_ubatch=7)
+        assert oc.set_kv_unified(unified) == 0 and hc.set_kv_unified(unified) == 0
         for step in range(25):
             n = int(rng.integers(0, 40))
             toks = rng.integers(-1, TINY.n_vocab + 1, n) if rng.random() < 0.2 else rng.integers(0, TINY.n_vocab, n)
@@ -183,3 +186,30 @@ def test_failed_ubatch_rolls_back_like_the_oracle():
 
 def test_inject_failure_needs_a_host_only_context():
     assert lcx.lib().lcx_ctx_inject_failure(None, 0) == lcx.LCX_INVALID
+
+
+def test_split_equal_failures_roll_back_like_the_oracle():
+    """A stream per sequence: batches are cut by split_equal. A failure injected at ubatch k
+    (host only) releases the same cells as the oracle's failed ubatch k (a NaN embedding in it), and
+    no rows are reported."""
+    import dataclasses
+    seqs = np.array([0, 1, 2, 0, 1, 2, 0, 2, 0, 0], np.int32)
+    base = np.array([11, 12, 13, 14, 15, 16, 17, 18, 19, 20], np.int32)
+    host = synth.make_model(TINY, n_layer=1)
+    emb = host.tok_embd.copy()
+    emb[7].view(np.uint16)[:] = 0x7E00
+    om = oracle.Model(dataclasses.replace(host, tok_embd=emb))
+    # ubatches {0,1,2} {3,4,5} {6,7} {8,9}: a bad token at index 5 fails ubatch 1, at 8 ubatch 3
+    for where, k in ((5, 1), (8, 3), (6, 2)):
+        toks = base.copy()
+        toks[where] = 7
+        oc = oracle.Context(om, 256, 3, 4)
+        oc.set_kv_unified(False)
+        assert oc.decode(toks, seq=seqs, logits=np.ones(10, np.int8))[0] == -3
+        hc = _host_ctx(n_ctx=256, n_seq=3, n_ubatch=4)
+        assert hc.set_kv_unified(False) == 0 and hc.inject_failure(k) == 0
+        assert hc.decode(base, seq_id=seqs, logits=np.ones(10, np.int8)) == lcx.LCX_COMPUTE_FAILED
+        assert hc.n_outputs() == 0
+        assert [hc.seq_pos_max(s) for s in range(3)] == [oc.seq_pos_max(s) for s in range(3)], (where, k)
+    hc = _host_ctx(n_ctx=256, n_seq=3, n_ubatch=4)
+    assert hc.decode([1], seq_id=[0]) == 0 and hc.set_kv_unified(False) == lcx.LCX_INVALID   # cells held

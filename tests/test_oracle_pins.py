@@ -486,3 +486,61 @@ def test_thread_count_changes_nothing(tiny_model, n_threads):
     (la, aa, ca), (lb, ab, cb) = res
     assert np.array_equal(la, lb) and np.array_equal(aa, ab)
     assert all(np.array_equal(x[0], y[0]) and np.array_equal(x[1], y[1]) for x, y in zip(ca, cb))
+
+
+# ----------------------------------------------------------------------------- a stream per sequence
+def test_stream_per_sequence_capacity_and_rows():
+    """With a stream per sequence (step 10: the cache is divided by n_ctx_seq = n_ctx / n_seq_max),
+    a batch that would give one sequence more than n_ctx_seq cells is refused with 1 and nothing is
+    committed; the logits rows come back in batch order and equal those of one shared store (the
+    split changes nothing but the order of evaluation)."""
+    m = synth.make_model(TINY)
+    om = oracle.Model(m)
+    c = oracle.Context(om, 256, 2, 4)
+    assert c.set_kv_unified(False) == 0
+    assert c.decode(np.arange(129) % 50, seq=np.zeros(129, np.int32))[0] == 1    # 129 > 256 / 2
+    assert c.seq_pos_max(0) == -1
+    assert c.decode(np.arange(128) % 50, seq=np.zeros(128, np.int32))[0] == 0
+    assert c.decode([3], seq=[0])[0] == 1 and c.decode([3], seq=[1])[0] == 0
+    shared = oracle.Context(om, 256, 2, 4)
+    assert shared.decode(np.arange(129) % 50, seq=np.zeros(129, np.int32))[0] == 0   # one store: fits
+    # rows in batch order, equal to the shared store's
+    toks = synth.prompt_tokens(TINY, 11, 3)
+    seqs = np.array([0, 1, 2, 0, 0, 2, 1, 0, 2, 2, 0], np.int32)
+    flags = np.array([1, 0, 1, 1, 0, 1, 1, 0, 0, 1, 1], np.int8)
+    a = oracle.Context(om, 256, 3, 4)
+    a.set_kv_unified(False)
+    b = oracle.Context(om, 256, 3, 4)
+    ra, rb = a.decode(toks, seq=seqs, logits=flags), b.decode(toks, seq=seqs, logits=flags)
+    assert ra[0] == rb[0] == 0 and np.array_equal(ra[1], rb[1]) and np.array_equal(ra[2], rb[2])
+    assert c.set_kv_unified(True) == -1                                            # cells held
+
+
+def test_split_equal_ubatches_by_their_rollback():
+    """split_equal with n_ubatch 4 over sequences 0 (5 tokens), 1 (2) and 2 (3): the ubatches are
+    {s0p0, s1p0, s2p0}, {s0p1, s1p1, s2p1}, {s0p2, s2p2}, {s0p3, s0p4}. A NaN embedding at s2p1,
+    flagged, fails the second ubatch: only the first stays (every sequence back to position 0), no
+    rows are reported; a NaN at s0p3 fails the fourth: sequences 1 and 2 complete, 0 keeps 0..2."""
+    import dataclasses
+    host = synth.make_model(TINY)
+    bad = 7
+    emb = host.tok_embd.copy()
+    emb[bad].view(np.uint16)[:] = 0x7E00
+    om = oracle.Model(dataclasses.replace(host, tok_embd=emb))
+    seqs = np.array([0, 1, 2, 0, 1, 2, 0, 2, 0, 0], np.int32)      # s0 at 0,3,6,8,9; s1 at 1,4; s2 at 2,5,7
+    base = np.array([11, 12, 13, 14, 15, 16, 17, 18, 19, 20], np.int32)
+    for where, keep in ((5, (0, 0, 0)), (8, (2, 1, 2))):
+        toks = base.copy()
+        toks[where] = bad
+        c = oracle.Context(om, 256, 3, 4)
+        c.set_kv_unified(False)
+        rc, lg, _ = c.decode(toks, seq=seqs, logits=np.ones(10, np.int8))
+        assert rc == -3 and lg.shape[0] == 0
+        assert tuple(c.seq_pos_max(s) for s in range(3)) == keep, (where, keep)
+    # the same batch in one shared store (consecutive chunks of 4): the bad token at index 5 fails
+    # the second chunk (tokens 4..7); the first chunk's 4 rows stay
+    toks = base.copy()
+    toks[5] = bad
+    c = oracle.Context(om, 256, 3, 4)
+    rc, lg, _ = c.decode(toks, seq=seqs, logits=np.ones(10, np.int8))
+    assert rc == -3 and lg.shape[0] == 4 and tuple(c.seq_pos_max(s) for s in range(3)) == (1, 0, 0)
