@@ -643,19 +643,29 @@ bool make_weight_maps(QMat &W) {
 // Tile shape of a launch: BN tokens x MT 128-row weight tiles per CTA, and the K steps split
 // over ks CTAs, from a cost model per K step (cycles of one SM): the MMAs take 4 BN MT (128 x BN x
 // 16 per MMA, hi and lo parts, four per 64-wide step, about 4096 multiply-adds a cycle), the
-// dequantisation of MT tiles about 435 MT, given a 30% margin since it must also hide its waits;
+// dequantisation of MT tiles about 435 MT, given a 30% margin since it must also hide its waits,
+// and the activation tile's L2 round trip over the shape's prefetch distance;
 // the launch takes as many of those steps as each CTA runs, times its waves of CTAs. A split adds
 // the partial sums' round trip (the last CTA of a tile reads ks partial tiles from L2; about
-// 10000 + 16 BN MT ks cycles, so a split is taken only where the CTAs would otherwise leave many
-// SMs idle: on the 8B shape, the 64-token ubatches' QKV, O and down projections). Ties go to
+// 25000 + 16 BN MT ks cycles, measured, so a split is taken only where the CTAs would otherwise
+// leave many SMs idle: on the 8B shape, the 64-token ubatches' QKV, O and down projections and the
+// 512-token ubatch's down projection). Ties go to
 // fewer CTAs (less activation traffic). Splits need room in the context's partial-sum scratch.
-GemmShape gemm_shape(int N_pad, int T, int nk, int n_sm, size_t part_bytes, int max_tiles) {
+GemmShape gemm_shape(int type, int N_pad, int T, int nk, int n_sm, size_t part_bytes, int max_tiles) {
     static const int cand[5][2] = {{64, 1}, {64, 2}, {128, 1}, {128, 2}, {256, 1}};
+    // activation prefetch distance of each shape (its ring depths), Q4_0 and Q8_0
+    static const int db[2][5] = {{tc::Cfg<Q4, 64, 1>::DB, tc::Cfg<Q4, 64, 2>::DB, tc::Cfg<Q4, 128, 1>::DB,
+                                  tc::Cfg<Q4, 128, 2>::DB, tc::Cfg<Q4, 256, 1>::DB},
+                                 {tc::Cfg<Q8, 64, 1>::DB, tc::Cfg<Q8, 64, 2>::DB, tc::Cfg<Q8, 128, 1>::DB,
+                                  tc::Cfg<Q8, 128, 2>::DB, tc::Cfg<Q8, 256, 1>::DB}};
     GemmShape best{64, 2, 1};
     long best_cost = -1, best_ctas = 0;
-    for (const auto &c : cand) {
+    for (int ci = 0; ci < 5; ++ci) {
+        const int *c = cand[ci];
         const long tiles = (long)((N_pad + c[1] * 128 - 1) / (c[1] * 128)) * ((T + c[0] - 1) / c[0]);
-        const long step = std::max<long>(4L * c[0] * c[1], 566L * c[1]);
+        // a step also waits for its activation tile, loaded DB steps ahead from L2 (about 4000
+        // cycles under load, measured: 64-step launches of each shape on the 8B 512-token ubatch)
+        const long step = std::max<long>(std::max<long>(4L * c[0] * c[1], 566L * c[1]), 4000L / db[type == Q8][ci]);
         for (int ks = 1; ks <= 8; ++ks) {
             if (ks > 1 && (nk / ks < 4 || tiles * ks > 2L * n_sm || tiles > max_tiles ||
                            (size_t)ks * T * N_pad * 4 > part_bytes))
@@ -663,7 +673,7 @@ GemmShape gemm_shape(int N_pad, int T, int nk, int n_sm, size_t part_bytes, int 
             if ((long)(ks - 1) * ((nk + ks - 1) / ks) >= nk) continue;   // every split gets K steps
             const long ctas = tiles * ks;
             const long waves = (ctas + n_sm - 1) / n_sm;
-            const long cost = waves * ((nk + ks - 1) / ks) * step + (ks > 1 ? 10000L + ks * 16L * c[0] * c[1] : 0L);
+            const long cost = waves * ((nk + ks - 1) / ks) * step + (ks > 1 ? 25000L + ks * 16L * c[0] * c[1] : 0L);
             if (best_cost < 0 || cost < best_cost || (cost == best_cost && ctas < best_ctas)) {
                 best_cost = cost;
                 best_ctas = ctas;
@@ -677,8 +687,8 @@ GemmShape gemm_shape(int N_pad, int T, int nk, int n_sm, size_t part_bytes, int 
 cudaError_t launch_gemm_tc(const QMat &W, Epi epi, int T, const __half *A, const __half *A_lo, const FwdArgs &a,
                            int layer, cudaStream_t s, int64_t &launches, int64_t *wide) {
     ++launches;
-    const GemmShape g = gemm_shape(W.N_pad, T, W.K / tc::BK, device_sm_count(), a.gemm_part ? a.gemm_part_bytes : 0,
-                                   a.gemm_cnt ? kGemmMaxTiles : 0);
+    const GemmShape g = gemm_shape(W.type, W.N_pad, T, W.K / tc::BK, device_sm_count(),
+                                   a.gemm_part ? a.gemm_part_bytes : 0, a.gemm_cnt ? kGemmMaxTiles : 0);
     if (g.bn >= 128 && wide) ++*wide;
     if (W.type == Q4) return tc::dispatch_shape<Q4>(g, W, epi, T, A, A_lo, a, layer, s);
     if (W.type == Q8) return tc::dispatch_shape<Q8>(g, W, epi, T, A, A_lo, a, layer, s);

@@ -156,7 +156,7 @@ struct GemmShape {
 };
 constexpr int kGemmMaxTiles = 4096;
 constexpr size_t kGemmPartBytes = (size_t)32 << 20;   // split-K partial sums per context
-GemmShape gemm_shape(int N_pad, int T, int nk, int n_sm, size_t part_bytes, int max_tiles);
+GemmShape gemm_shape(int type, int N_pad, int T, int nk, int n_sm, size_t part_bytes, int max_tiles);
 // (*wide, if given, counts the launches that took tiles of 128 or more tokens)
 cudaError_t launch_gemm_tc(const QMat &W, Epi epi, int T, const __half *A, const __half *A_lo, const FwdArgs &a,
                            int layer, cudaStream_t s, int64_t &launches, int64_t *wide = nullptr);
