@@ -31,11 +31,11 @@ import numpy as np  # noqa: E402
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the persistent
-# decode step on the 8B shape, from the ncu launch list of the current kernel (decode at ~520
-# attended positions): 4644.99 MB on average over 32 launches, of which the K/V of those
-# positions are 68.2 MB. The K/V part is rescaled to the context of the run being reported.
-STEP_NCU_TRAFFIC_BYTES = 4644.99e6
-STEP_NCU_KV_POSITIONS = 520.5
+# decode step over its algorithmic bytes, from one ncu capture of the current kernel on the 8B
+# shape cut to 4 layers (1057.9 MB read + 18.2 MB written against 1057.4 MB of stored weights and
+# attended K/V): the step's traffic grows with the layers and cells it processes, so the full
+# launch's traffic is this ratio times its algorithmic bytes.
+STEP_NCU_TRAFFIC_RATIO = (1057.894e6 + 18.201e6) / 1057.4e6
 
 
 def log(*a):
@@ -509,8 +509,7 @@ def run_lcx(a, rank, world):
         dom_kernel = "k_decode_step (persistent: every matmul, attention and the head of a token in one launch)"
         dom_traffic = None
         if cfg.name == "8b" and not a.layers:
-            avg_pos = n_prompt + (n_dec + 1) / 2.0
-            dom_traffic = round(STEP_NCU_TRAFFIC_BYTES + kv_pos_bytes * (avg_pos - STEP_NCU_KV_POSITIONS))
+            dom_traffic = round(STEP_NCU_TRAFFIC_RATIO * decode_bytes_per_step(cfg, host, n_prompt, n_dec) / n_dec)
     else:
         dom_kernel = "gemv (weight-streaming, all decode matmuls)"
         dom_traffic = None   # separate launches (LCX_DECODE_STEP=0): no current counters
