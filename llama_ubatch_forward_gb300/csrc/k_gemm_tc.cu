@@ -14,14 +14,18 @@
 //               W A_lo into the same accumulator, so the activations keep about 22 bits and only
 //               the f16 rounding of the dequantised weights remains; each stage's tcgen05.commit
 //               frees its shared-memory slot;
-//   warps 2..9  load the activation tiles [BN][64] f16 (high and low parts) with cp.async, S - 2
-//               (S - 1 with fewer than 5 slots) stages ahead, writing the 128-byte swizzle themselves; dequantise the raw blocks of
-//               their row (warps 2..5 tile 0, warps 6..9 tile 1) into the K-major SWIZZLE_128B f16
-//               tile the MMA reads ((q - 8) or q is exact in f16, then one f16 multiply by the
-//               block scale); then run their tile's epilogue from TMEM with tcgen05.ld.
-// The copy engine's cost is per copy (about 0.4 us each, whatever the size up to several KB) and
-// per 128-byte row, so the activation tiles -- 4 bytes per element, re-read by every weight tile
-// pair -- go through the load/store path instead, and the engine moves one box per stage.
+//   warps 2..9  dequantise the raw blocks (with two weight tiles warps 2..5 tile 0, warps 6..9
+//               tile 1) into the K-major SWIZZLE_128B f16 tile the MMA reads ((q - 8) or q is
+//               exact in f16, then one f16 multiply by the block scale); then run the epilogue
+//               from TMEM with tcgen05.ld;
+//   warp 10     loads the activation tiles [BN][64] f16 (high and low parts) with TMA into the
+//               SWIZZLE_128B layout, as many steps ahead as the activation ring holds. The CTAs of
+//               a cluster (CL consecutive weight tiles, one token tile) share every activation
+//               tile: each loads 1/CL of its rows, multicast to all of them, and a slot is reused
+//               once every CTA's MMAs of the cluster have released it (their commits arrive on
+//               all the cluster's barriers). The activations, 4 bytes per element and re-read by
+//               every weight tile, thus cross L2 once per cluster, and no dequantising warp waits
+//               on an activation load.
 // All mbarrier waits are bounded; a timeout sets the context's error word and the CTA finishes
 // without further work.
 #include <cudaTypedefs.h>
@@ -65,6 +69,27 @@ __device__ __forceinline__ void tma_2d(void *dst, const CUtensorMap *map, int x,
     asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
                  ::"r"(saddr(dst)), "l"((uint64_t)map), "r"(x), "r"(y), "r"(saddr(bar)) : "memory");
 }
+// the same box into the same shared-memory offsets of every CTA in `mask` (bytes counted on each
+// destination CTA's barrier at the same offset)
+__device__ __forceinline__ void tma_2d_mc(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar, uint16_t mask) {
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster "
+                 "[%0], [%1, {%2, %3}], [%4], %5;"
+                 ::"r"(saddr(dst)), "l"((uint64_t)map), "r"(x), "r"(y), "r"(saddr(bar)), "h"(mask) : "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_size() {
+    uint32_t n;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(n));
+    return n;
+}
+// every thread of every CTA of the cluster: arrive (release) and wait (acquire)
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
 
 // Shared-memory matrix descriptor of a K-major operand tile in the 128-byte swizzle layout:
 // rows of 128 bytes, 8-row groups 1024 bytes apart.
@@ -90,6 +115,11 @@ __device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t adesc, uint64_
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(saddr(bar)) : "memory");
 }
+// the commit's arrival on the barrier at the same offset in every CTA of `mask`
+__device__ __forceinline__ void mma_commit_mc(uint64_t *bar, uint16_t mask) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+                 ::"r"(saddr(bar)), "h"(mask) : "memory");
+}
 
 template <int N>
 struct Regs {
@@ -110,12 +140,11 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
 }
 
 // Shared memory: three rings. The dequantised f16 weight tiles (SA slots, the largest part of a
-// step); the activation tiles (SB slots, freed by the MMAs that read them); the raw weight boxes
-// (SR slots, freed by the dequantising warps as soon as they have read them -- not by the MMA, so
-// the next boxes stream in while the tensor pipe works). With SA = 3 the dequantisation of step j
-// waits only for the MMAs of step j - 3, so it overlaps the MMAs of steps j - 2 and j - 1; the
-// activations run DB steps ahead into the slot freed by the MMAs of step j + DB - SB, which are
-// never later than those the A ring waits for (when DB = SB - SA).
+// step); the activation tiles (SB slots, freed by the MMAs of every CTA of the cluster that read
+// them); the raw weight boxes (SR slots, freed by the dequantising warps as soon as they have read
+// them -- not by the MMA, so the next boxes stream in while the tensor pipe works). With SA = 3 the
+// dequantisation of step j waits only for the MMAs of step j - 3, so it overlaps the MMAs of steps
+// j - 2 and j - 1.
 // MT weight tiles of 128 rows per CTA (1 or 2) share each activation tile of BN tokens.
 template <int QT, int BN, int MT>
 struct Cfg {
@@ -129,8 +158,8 @@ struct Cfg {
     static constexpr int SR = (MT == 2 && QT == Q8 && BN == 128) ? 2 : 3;
     static constexpr int SB_FIT = (220 * 1024 - SA * A_BYTES - SR * RQ_SLOT) / B_BYTES;
     static constexpr int SB = SB_FIT < 6 ? SB_FIT : 6;
-    static constexpr int DB = SB - SA >= 2 ? SB - SA : SB - 1;   // activation prefetch distance
-    static_assert(SB >= 2 && DB >= 1, "the activation prefetch needs at least two slots");
+    static constexpr int DB = SB - 1;   // activation prefetch distance (the loader runs a ring ahead)
+    static_assert(SB >= 2, "the activation prefetch needs at least two slots");
     static constexpr int SMEM = SA * A_BYTES + SB * B_BYTES + SR * RQ_SLOT + 1024 /* align */ + 512 /* barriers */;
     static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
     // per weight tile one accumulator of BN columns: W A_hi and W A_lo are accumulated into it
@@ -217,8 +246,8 @@ __device__ __forceinline__ void dequant_row(const uint8_t *rq, uint8_t *atile, i
 }
 
 template <int QT, int BN, int MT, int EPI>
-__global__ void __launch_bounds__(320, 1)
-    k_gemm_tc(const __half *__restrict__ A_hi, const __half *__restrict__ A_lo, const int K,
+__global__ void __launch_bounds__(352, 1)
+    k_gemm_tc(const __grid_constant__ CUtensorMap tm_ahi, const __grid_constant__ CUtensorMap tm_alo,
               const __grid_constant__ CUtensorMap tm_w, const GemmParams p, const FwdArgs a, const int layer) {
     using C = Cfg<QT, BN, MT>;
     constexpr int SA = C::SA, SB = C::SB, SR = C::SR;
@@ -235,6 +264,9 @@ __global__ void __launch_bounds__(320, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_bar + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m_tile = blockIdx.x, tok0 = blockIdx.y * BN;
+    // the cluster: CL CTAs of consecutive weight tiles sharing this token tile
+    const int CL = (int)cluster_size(), crank = (int)cluster_rank();
+    const uint16_t cmask = (uint16_t)((1u << CL) - 1u);
     // this CTA's K steps: split blockIdx.z of p.ks (equal runs; the last may be short)
     const int nk_per = (p.nk + p.ks - 1) / p.ks;
     const int kb = blockIdx.z * nk_per;
@@ -254,8 +286,8 @@ __global__ void __launch_bounds__(320, 1)
             mbar_init(&empty_w[i], 8);   // one arrival per dequantising warp
         }
         for (int i = 0; i < SB; ++i) {
-            mbar_init(&full_b[i], 8);    // one arrival per loading warp
-            mbar_init(&empty_b[i], 1);
+            mbar_init(&full_b[i], 1);     // the loader's expect_tx; the bytes come from every CTA's share
+            mbar_init(&empty_b[i], CL);   // one MMA commit from each CTA of the cluster
         }
         for (int i = 0; i < SA; ++i) {
             mbar_init(&full_a[i], 8);   // one arrival per dequantising warp
@@ -273,8 +305,40 @@ __global__ void __launch_bounds__(320, 1)
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = *tmem_slot;
+    // every CTA's barriers are initialised before any peer multicasts into this one or arrives here
+    if (CL > 1) cluster_sync_all();
 
-    if (warp == 0) {
+    if (warp == 10) {
+        // ---------------------------------------------------------------- activation loader
+        if (lane == 0) {
+            bool ok = true;
+            constexpr int PART_ROWS_MAX = BN;
+            const int prow = BN / CL;             // this CTA's share of the tile's rows
+            const uint32_t part_bytes = (uint32_t)prow * BK * 2;
+            LCX_PDL_WAIT();   // the activations are the previous kernel's output
+            int issued = 0;
+            for (int j = 0; j < nk && ok; ++j) {
+                const int slot = j % SB;
+                if (j >= SB && !(ok = mbar_wait(&empty_b[slot], ((j / SB) - 1) & 1))) break;
+                mbar_expect_tx(&full_b[slot], (uint32_t)C::B_BYTES);
+                uint8_t *bt = b_tile(slot);
+                const int x = (kb + j) * BK, y = tok0 + crank * prow;
+                if (CL > 1) {
+                    tma_2d_mc(bt + crank * prow * 128, &tm_ahi, x, y, &full_b[slot], cmask);
+                    tma_2d_mc(bt + BN * BK * 2 + crank * prow * 128, &tm_alo, x, y, &full_b[slot], cmask);
+                } else {
+                    tma_2d(bt, &tm_ahi, x, y, &full_b[slot]);
+                    tma_2d(bt + BN * BK * 2, &tm_alo, x, y, &full_b[slot]);
+                }
+                issued = j + 1;
+                (void)part_bytes;
+                (void)PART_ROWS_MAX;
+            }
+            if (!ok) atomicExch(a.err, 1);
+            // every step issued has landed in this CTA before it ends (each CTA waits for its own copy)
+            for (int j = (issued > SB ? issued - SB : 0); j < issued; ++j) mbar_wait(&full_b[j % SB], (j / SB) & 1);
+        }
+    } else if (warp == 0) {
         // ---------------------------------------------------------------- producer
         if (lane == 0) {
             bool ok = true;
@@ -322,8 +386,11 @@ __global__ void __launch_bounds__(320, 1)
                         }
                     }
                 }
-                mma_commit(&empty_b[slot]);   // the activation slot is free once these MMAs have read it
-                mma_commit(&empty_a[aslot]);  // and so is the A slot
+                // the activation slot is free once these MMAs (in every CTA of the cluster) have read
+                // it, and so is the A slot
+                if (CL > 1) mma_commit_mc(&empty_b[slot], cmask);
+                else mma_commit(&empty_b[slot]);
+                mma_commit(&empty_a[aslot]);
             }
             if (!ok) atomicExch(a.err, 1);
             mma_commit(acc_bar);
@@ -331,42 +398,16 @@ __global__ void __launch_bounds__(320, 1)
     } else {
         // ---------------------------------------------------------------- activations, dequant, epilogue
         // 8 warps. Dequantisation: with two weight tiles, warps 2..5 own tile 0 and warps 6..9
-        // tile 1, a row per thread; with one, two threads per row, a block each. All 8 load the
-        // activation tiles and run the epilogue (see below).
+        // tile 1, a row per thread; with one, two threads per row, a block each. All 8 run the
+        // epilogue (see below).
         const int wt = threadIdx.x - 64;           // 0..255
         const int my_mt = MT == 2 ? wt >> 7 : 0;
         const int drow = MT == 2 ? wt & 127 : wt >> 1, dblk = MT == 2 ? 0 : wt & 1;
-        // activation tile of stage j: 2 parts x BN rows x 8 chunks of 16 bytes; thread wt copies
-        // chunk wt % 8 of rows wt / 8 + 32 u, each to its 128-byte-swizzled place; rows past the
-        // last token are zero-filled
-        auto load_act = [&](int j) {
-            uint8_t *bt = b_tile(j % SB);
-            const int c = wt & 7;
-#pragma unroll
-            for (int hl = 0; hl < 2; ++hl) {
-                const __half *src0 = hl ? A_lo : A_hi;
-#pragma unroll
-                for (int u = 0; u < BN / 32; ++u) {
-                    const int r = (wt >> 3) + 32 * u, t = tok0 + r;
-                    const __half *src = src0 + (size_t)(t < p.T ? t : 0) * K + (size_t)(kb + j) * BK + c * 8;
-                    const uint32_t dst = saddr(bt + hl * BN * BK * 2 + r * 128 + ((c ^ (r & 7)) << 4));
-                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-                                 "r"(t < p.T ? 16 : 0) : "memory");
-                }
-            }
-        };
-        // activations run D steps ahead, into the slot the MMAs of step j + D - SB read (no later
-        // than the step whose A slot the dequantisation of step j waits for, when DB = SB - SA)
-        constexpr int D = C::DB;
         bool ok = true;
-        LCX_PDL_WAIT();   // the activations are the previous kernel's output
+        LCX_PDL_WAIT();   // the epilogue reads the previous kernels' output
         LCX_PDL_TRIGGER();
-        for (int j = 0; j < D; ++j) {   // stages 0 .. D-1 ahead (their slots start free)
-            if (j < nk) load_act(j);
-            asm volatile("cp.async.commit_group;" ::: "memory");
-        }
         for (int j = 0; j < nk; ++j) {
-            const int rslot = j % SR, bslot = j % SB, aslot = j % SA;
+            const int rslot = j % SR, aslot = j % SA;
             ok = __all_sync(0xffffffffu, mbar_wait(&full_w[rslot], (j / SR) & 1));   // warp-uniform
             // the A slot is free once the MMAs of step j - SA are done
             if (ok && j >= SA) ok = __all_sync(0xffffffffu, mbar_wait(&empty_a[aslot], ((j / SA) - 1) & 1));
@@ -378,22 +419,7 @@ __global__ void __launch_bounds__(320, 1)
                 mbar_arrive(&full_a[aslot]);
                 mbar_arrive(&empty_w[rslot]);   // this warp's rows of the raw box are read
             }
-            // step j's activation copies have landed: of the D + j groups committed so far, all
-            // but the D - 1 newest
-            asm volatile("cp.async.wait_group %0;" ::"n"(D - 1) : "memory");
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&full_b[bslot]);
-            // prefetch step j + D into the slot step j + D - SB used, once its MMAs are done
-            const int jn = j + D;
-            if (jn < nk) {
-                if (jn >= SB) ok = __all_sync(0xffffffffu, mbar_wait(&empty_b[jn % SB], ((jn / SB) - 1) & 1));
-                if (!ok) break;
-                load_act(jn);
-            }
-            asm volatile("cp.async.commit_group;" ::: "memory");
         }
-        asm volatile("cp.async.wait_all;" ::: "memory");   // nothing in flight when the CTA ends
         if (!ok) atomicExch(a.err, 1);
         const bool acc_ok = __all_sync(0xffffffffu, ok && mbar_wait(acc_bar, 0));
         // a warp reads the TMEM lanes of its quarter (warp % 4); with two tiles warps 2..5 take
@@ -553,6 +579,9 @@ __global__ void __launch_bounds__(320, 1)
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
+    // no CTA leaves while a peer's commit may still arrive on its barriers or a peer's copy land in
+    // its shared memory (every CTA is past its accumulator wait and its loader's last landing here)
+    if (CL > 1) cluster_sync_all();
     if (warp == 1) {
         __syncwarp();
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
@@ -598,9 +627,36 @@ cudaError_t run(const QMat &W, int T, int ks, const __half *A, const __half *A_l
     if (!W.tm_ready) return cudaErrorInvalidValue;
     GemmParams p{W.N, T, W.K / BK, ks, W.N_pad, a.gemm_part, a.gemm_cnt};
     const int m_tiles = (W.N_pad + MT * BM - 1) / (MT * BM);   // rows past N_pad read as zeros
-    dim3 grid(m_tiles, (T + BN - 1) / BN, ks);
-    return launch_pdl(kern, grid, dim3(320), (size_t)C::SMEM, s, A, A_lo, W.K,
-                      *reinterpret_cast<const CUtensorMap *>(MT == 2 ? W.tm_w : W.tm_w1), p, a, layer);
+    // clusters of CL = 2 consecutive weight tiles share each activation tile (a CTA loads BN / 2
+    // rows of it for both); the grid is padded to whole clusters (an extra tile reads zero rows).
+    // Pairs, not fours: a cluster's CTAs must fit one GPC together, and with 220 KB of shared memory
+    // each, larger clusters would leave a GPC's odd SMs idle.
+    const int CL = m_tiles >= 2 ? 2 : 1;
+    // activation maps: [T][K] f16 row-major; box 64 elements (128 bytes) x BN / CL rows, 128-byte
+    // swizzle (the K-major layout the MMA reads); rows past T read as zeros
+    alignas(64) CUtensorMap tm_hi, tm_lo;
+    if (!make_map_2d(&tm_hi, A, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (uint64_t)W.K, (uint64_t)T, (uint64_t)W.K * 2, BK,
+                     (uint32_t)(BN / CL), CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map_2d(&tm_lo, A_lo, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (uint64_t)W.K, (uint64_t)T, (uint64_t)W.K * 2, BK,
+                     (uint32_t)(BN / CL), CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((m_tiles + CL - 1) / CL * CL, (T + BN - 1) / BN, ks);
+    cfg.blockDim = dim3(352);
+    cfg.dynamicSmemBytes = (size_t)C::SMEM;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = CL;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    prefer_max_shared(kern);
+    return cudaLaunchKernelEx(&cfg, kern, tm_hi, tm_lo, *reinterpret_cast<const CUtensorMap *>(MT == 2 ? W.tm_w : W.tm_w1),
+                              p, a, layer);
 }
 
 template <int QT, int BN, int MT>

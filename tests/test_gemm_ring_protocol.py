@@ -1,13 +1,15 @@
 """Model check of the tensor-core GEMM's shared-memory ring protocol (k_gemm_tc.cu), on the CPU.
 
 compute-sanitizer's race checks are not available for this kernel's GPU, so the protocol is checked
-as a model: the producer warp (raw weight boxes by TMA), the MMA issuer and the 8 dequantising /
-activation-loading warps run as coroutines over the kernel's loop structure, slot indices and
-barrier parities, with mbarriers modelled by their phase and arrival counts (try_wait.parity p
-succeeds once the phase of parity p has completed) and every copy and MMA completing after a random
-delay. For every ring depth the kernel instantiates, all K steps must finish without a deadlock,
-every read must see the data of its own K step, and no slot may be overwritten while the MMAs of an
-earlier step still read it.
+as a model: for each CTA of a cluster, the producer warp (raw weight boxes by TMA), the activation
+loader (its share of every activation tile, multicast to all CTAs of the cluster), the MMA issuer
+(whose commits free the activation slot in every CTA) and the 8 dequantising warps run as
+coroutines over the kernel's loop structure, slot indices and barrier parities, with mbarriers
+modelled by their phase, arrival and transaction counts (try_wait.parity p succeeds once the phase
+of parity p has completed) and every copy and MMA completing after a random delay. For every ring
+depth the kernel instantiates, with clusters of one and two CTAs, all K steps must finish without
+a deadlock, every read must see the data of its own K step (every share of the activation tile),
+and no slot may be overwritten while the MMAs of any CTA still read it.
 """
 import random
 
@@ -34,7 +36,9 @@ class Bar:
         self._check()
 
     def _check(self):
-        assert self.pending >= 0 and self.tx >= 0, "barrier over-arrived"
+        # the transaction count may go below zero for a while (a peer's multicast share can land
+        # before this CTA's loader announced the step's bytes); arrivals may not
+        assert self.pending >= 0, "barrier over-arrived"
         if self.pending == 0 and self.tx == 0:
             self.phase += 1
             self.pending = self.count
@@ -43,105 +47,114 @@ class Bar:
         return (self.phase & 1) != parity
 
 
-def run(SA, SB, SR, D, nk, seed):
-    """One CTA's K loop: SR raw-box slots (freed by the dequantising warps), SB activation slots
-    (freed by the MMA commit), SA dequantised-tile slots, activations D steps ahead."""
+def run(SA, SB, SR, nk, seed, CL=2, drop_loader_wait=False):
+    """One cluster of CL CTAs running the K loop. Per CTA: SR raw-box slots (freed by the
+    dequantising warps), SA dequantised-tile slots, SB activation slots. The activation tile of a
+    step is loaded in CL shares, one by each CTA's loader, each share multicast to every CTA of the
+    cluster; a CTA's activation slot is free once the MMAs of every CTA have read it (their commits
+    arrive on every CTA's empty barrier)."""
     rnd = random.Random(seed)
-    full_w = [Bar(1) for _ in range(SR)]
-    empty_w = [Bar(8) for _ in range(SR)]
-    full_b = [Bar(8) for _ in range(SB)]
-    empty_b = [Bar(1) for _ in range(SB)]
-    full_a = [Bar(8) for _ in range(SA)]
-    empty_a = [Bar(1) for _ in range(SA)]
-    raw = [None] * SR                                  # step whose raw box a slot holds
-    rows = [[None] * SB for _ in range(8)]             # step whose activation rows warp w put in a slot
-    atile = [[None] * 8 for _ in range(SA)]            # step whose tile rows warp w dequantised
-    raw_readers = [set() for _ in range(SR)]           # warps that still have to read a raw box
-    reading_b, reading_a = set(), set()                # slots an MMA in flight reads
     events, now = [], [0]
 
     def later(fn, lo, hi):
         events.append((now[0] + rnd.randint(lo, hi), fn))
 
-    def producer():
+    class Cta:
+        def __init__(self):
+            self.full_w = [Bar(1) for _ in range(SR)]
+            self.empty_w = [Bar(8) for _ in range(SR)]
+            self.full_b = [Bar(1) for _ in range(SB)]
+            self.empty_b = [Bar(CL) for _ in range(SB)]
+            self.full_a = [Bar(8) for _ in range(SA)]
+            self.empty_a = [Bar(1) for _ in range(SA)]
+            self.raw = [None] * SR
+            self.shares = [dict() for _ in range(SB)]     # slot -> {share: step} landed
+            self.atile = [[None] * 8 for _ in range(SA)]
+            self.raw_readers = [set() for _ in range(SR)]
+            self.reading_b, self.reading_a = set(), set()
+
+    ctas = [Cta() for _ in range(CL)]
+
+    def producer(c):
+        C = ctas[c]
+
         def issue(j):
             s = j % SR
-            assert not raw_readers[s], ("raw box overwritten before every warp read it", j)
-            full_w[s].expect_tx(1)
+            assert not C.raw_readers[s], ("raw box overwritten before every warp read it", j)
+            C.full_w[s].expect_tx(1)
 
             def land(s=s, j=j):
-                raw[s] = j
-                raw_readers[s] = set(range(8))
-                full_w[s].complete_tx(1)
+                C.raw[s] = j
+                C.raw_readers[s] = set(range(8))
+                C.full_w[s].complete_tx(1)
             later(land, 5, 60)
         for j in range(min(nk, SR)):
             issue(j)
         for j in range(SR, nk):
-            while not empty_w[j % SR].done(((j // SR) - 1) & 1):
+            while not C.empty_w[j % SR].done(((j // SR) - 1) & 1):
                 yield
             issue(j)
 
-    def mma():
+    def loader(c):
+        C = ctas[c]
+        for j in range(nk):
+            s = j % SB
+            if j >= SB and not drop_loader_wait:
+                while not C.empty_b[s].done(((j // SB) - 1) & 1):
+                    yield
+            C.full_b[s].expect_tx(CL)            # the whole tile: CL shares
+            for d in range(CL):                  # this CTA's share, multicast to every CTA
+                D = ctas[d]
+                assert s not in D.reading_b, ("activation slot overwritten while an MMA reads it", j, d)
+
+                def land(D=D, s=s, j=j, c=c):
+                    D.shares[s][c] = j
+                    D.full_b[s].complete_tx(1)
+                later(land, 2, 50)
+            yield
+
+    def mma(c):
+        C = ctas[c]
         for j in range(nk):
             s, a = j % SB, j % SA
-            while not (full_a[a].done((j // SA) & 1) and full_b[s].done((j // SB) & 1)):
+            while not (C.full_a[a].done((j // SA) & 1) and C.full_b[s].done((j // SB) & 1)):
                 yield
-            assert all(rows[w][s] == j for w in range(8)), ("activation tile", j)
-            assert all(t == j for t in atile[a]), ("dequantised tile", j)
-            reading_b.add(s)
-            reading_a.add(a)
+            assert all(C.shares[s].get(d) == j for d in range(CL)), ("activation tile", j, C.shares[s])
+            assert all(t == j for t in C.atile[a]), ("dequantised tile", j)
+            C.reading_b.add(s)
+            C.reading_a.add(a)
 
             def finish(s=s, a=a):
-                reading_b.discard(s)
-                reading_a.discard(a)
-                empty_b[s].arrive()
-                empty_a[a].arrive()
+                C.reading_b.discard(s)
+                C.reading_a.discard(a)
+                for D in ctas:                    # the commit arrives on every CTA's empty barrier
+                    D.empty_b[s].arrive()
+                C.empty_a[a].arrive()
             later(finish, 3, 30)
             yield
 
-    def warp(w):
-        groups = []                                    # committed cp.async groups: landing flags
-
-        def load_act(j):
-            assert j % SB not in reading_b, ("activation slot overwritten while an MMA reads it", j)
-            flag = {"landed": False}
-
-            def land(s=j % SB, j=j, flag=flag):
-                rows[w][s] = j
-                flag["landed"] = True
-            later(land, 2, 50)
-            return [flag]
-        for j in range(D):
-            groups.append(load_act(j) if j < nk else [])
+    def warp(c, w):
+        C = ctas[c]
         for j in range(nk):
-            r, b, a = j % SR, j % SB, j % SA
-            while not full_w[r].done((j // SR) & 1):
+            r, a = j % SR, j % SA
+            while not C.full_w[r].done((j // SR) & 1):
                 yield
             if j >= SA:
-                while not empty_a[a].done(((j // SA) - 1) & 1):
+                while not C.empty_a[a].done(((j // SA) - 1) & 1):
                     yield
-            assert raw[r] == j, ("raw box", j)
-            assert a not in reading_a, ("dequantised tile overwritten while an MMA reads it", j)
-            atile[a][w] = j
-            raw_readers[r].discard(w)
+            assert C.raw[r] == j, ("raw box", j)
+            assert a not in C.reading_a, ("dequantised tile overwritten while an MMA reads it", j)
+            C.atile[a][w] = j
+            C.raw_readers[r].discard(w)
             yield
-            full_a[a].arrive()
-            empty_w[r].arrive()
-            while not all(f["landed"] for g in groups[:len(groups) - (D - 1)] for f in g):
-                yield                                  # cp.async.wait_group D - 1
-            full_b[b].arrive()
-            jn = j + D
-            g = []
-            if jn < nk:
-                if jn >= SB:
-                    while not empty_b[jn % SB].done(((jn // SB) - 1) & 1):
-                        yield
-                g = load_act(jn)
-            groups.append(g)
+            C.full_a[a].arrive()
+            C.empty_w[r].arrive()
 
-    agents = [producer(), mma()] + [warp(w) for w in range(8)]
+    agents = []
+    for c in range(CL):
+        agents += [producer(c), loader(c), mma(c)] + [warp(c, w) for w in range(8)]
     alive = [True] * len(agents)
-    for _ in range(200000):
+    for _ in range(400000):
         if not any(alive):
             return
         events.sort(key=lambda e: e[0])
@@ -160,7 +173,7 @@ def run(SA, SB, SR, D, nk, seed):
 
 
 def ring_depths(qb_bytes, bn, mt):
-    """(SA, SB, SR, DB) as the kernel's Cfg<QT, BN, MT> computes them."""
+    """(SA, SB, SR) as the kernel's Cfg<QT, BN, MT> computes them."""
     q4 = qb_bytes == 16
     a_bytes = mt * 128 * 64 * 2
     b_bytes = 2 * bn * 64 * 2
@@ -168,10 +181,9 @@ def ring_depths(qb_bytes, bn, mt):
     sa = 3 if mt == 2 and q4 and bn == 64 else 2
     sr = 2 if mt == 2 and not q4 and bn == 128 else 3
     sb = min(6, (220 * 1024 - sa * a_bytes - sr * rq_slot) // b_bytes)
-    db = sb - sa if sb - sa >= 2 else sb - 1
-    assert sb >= 2 and db >= 1
+    assert sb >= 2
     assert sa * a_bytes + sb * b_bytes + sr * rq_slot + 1024 + 512 <= 227 * 1024
-    return sa, sb, sr, db
+    return sa, sb, sr
 
 
 # every tile shape the launcher picks from (BN tokens x MT weight tiles), for Q4_0 and Q8_0
@@ -179,19 +191,28 @@ SHAPES = [(qb, bn, mt) for qb in (16, 32) for bn, mt in ((64, 1), (64, 2), (128,
 
 
 @pytest.mark.parametrize("qb_bytes,bn,mt", SHAPES)
-def test_ring_protocol(qb_bytes, bn, mt):
-    SA, SB, SR, DB = ring_depths(qb_bytes, bn, mt)
-    for nk in (1, 2, 3, 5, 7, 64):
-        for seed in range(3):
-            run(SA, SB, SR, DB, nk, seed)
+@pytest.mark.parametrize("CL", [1, 2])
+def test_ring_protocol(qb_bytes, bn, mt, CL):
+    SA, SB, SR = ring_depths(qb_bytes, bn, mt)
+    for nk in (1, 2, 3, 5, 7, 40):
+        for seed in range(2):
+            run(SA, SB, SR, nk, seed, CL=CL)
 
 
 def test_model_catches_a_missing_wait():
     """The check is not vacuous: dropping the dequantising warps' wait for a free tile slot races."""
     import inspect
-    src = inspect.getsource(run).replace("while not empty_a[a].done(((j // SA) - 1) & 1):", "while False:")
+    src = inspect.getsource(run).replace("while not C.empty_a[a].done(((j // SA) - 1) & 1):", "while False:")
     ns = {"random": random, "Bar": Bar}
     exec(compile(src, "mutated", "exec"), ns)
     with pytest.raises(AssertionError):
         for seed in range(5):
-            ns["run"](3, 6, 3, 3, 64, seed)
+            ns["run"](3, 6, 3, 40, seed)
+
+
+def test_model_catches_a_loader_that_does_not_wait_for_the_cluster():
+    """A loader that reuses an activation slot without waiting for every CTA's MMAs overwrites a
+    tile a peer still reads."""
+    with pytest.raises(AssertionError):
+        for seed in range(20):
+            run(2, 2, 3, 40, seed, CL=2, drop_loader_wait=True)
