@@ -234,6 +234,17 @@ lcx_ctx *lcx_ctx_create_host_only(const lcx_hparams *hp, uint32_t n_ctx, uint32_
  * Returns LCX_INVALID for a context with a device. */
 int32_t lcx_ctx_inject_failure(lcx_ctx *ctx, int32_t ubatch);
 
+/* Testing aid for the prefill matmuls (the tensor-core GEMM of every ubatch of more than 8
+ * tokens): every later launch, in every context of the process, takes the tile shape bn tokens x
+ * mt 128-row weight tiles with its K steps split over ks CTAs, instead of the shape its cost
+ * model picks -- so each compiled shape can be checked against the oracle on small models. bn
+ * is 64, 128 or 256; mt is 1 or 2 (1 with bn 256); ks is 1 to 8. A launch where the forced split
+ * does not fit (fewer than 4 K steps a split, or no room in the partial-sum scratch) runs with
+ * ks = 1. bn = 0 restores the cost model. Results differ from the default only by summation
+ * order. Returns LCX_OK, or LCX_INVALID for a shape that is not compiled. Not thread-safe
+ * against decodes running at the same time. */
+int32_t lcx_set_gemm_tile(int32_t bn, int32_t mt, int32_t ks);
+
 /* Row gather with dequantisation to float32 (step 13b, ggml_get_rows on the token
  * embeddings): out[i][:] = the n_cols values of row ids[i] of `table` (stored type `type`).
  * ids and out are DEVICE pointers; runs on cuda_stream. Returns LCX_OK or LCX_INVALID /

@@ -22,7 +22,8 @@ SYMBOLS = ("lcx_model_create", "lcx_model_free", "lcx_ctx_create", "lcx_ctx_free
            "lcx_decode_greedy", "lcx_kv_clear", "lcx_seq_pos_max", "lcx_n_outputs", "lcx_set_abort",
            "lcx_get_stats", "lcx_ctx_create_host_only", "lcx_get_rows", "lcx_last_error", "lcx_set_profiling",
            "lcx_get_profile", "lcx_attention_workspace_size", "lcx_attention", "lcx_attention_noalloc",
-           "lcx_kv_read", "lcx_get_trace", "lcx_sample", "lcx_ctx_inject_failure", "lcx_ctx_set_kv_unified")
+           "lcx_kv_read", "lcx_get_trace", "lcx_sample", "lcx_ctx_inject_failure", "lcx_ctx_set_kv_unified",
+           "lcx_set_gemm_tile")
 
 
 def build(force: bool = False) -> str:
@@ -116,6 +117,8 @@ def lib():
         L.lcx_attention_noalloc.argtypes = [i32, i32, i32, i32, vp, vp, vp, i32, vp, i32, vp, vp, i32, vp, vp]
         L.lcx_ctx_inject_failure.restype = i32
         L.lcx_ctx_inject_failure.argtypes = [vp, i32]
+        L.lcx_set_gemm_tile.restype = i32
+        L.lcx_set_gemm_tile.argtypes = [i32, i32, i32]
         L.lcx_sample.restype = i32
         L.lcx_sample.argtypes = [ctypes.POINTER(lcx_sampler), vp, i32, i32, vp, i32, vp, vp, vp]
         L.lcx_get_trace.restype = i32
@@ -270,6 +273,11 @@ class Context:
         s = lcx_stats()
         lib().lcx_get_stats(self.h, ctypes.byref(s))
         return s
+
+
+def set_gemm_tile(bn: int = 0, mt: int = 1, ks: int = 1) -> int:
+    """Force the prefill GEMM's tile shape for every later launch (bn = 0: the cost model's)."""
+    return lib().lcx_set_gemm_tile(bn, mt, ks)
 
 
 def get_rows(qtype: int, table, n_rows: int, n_cols: int, ids, out, stream=None) -> int:

@@ -11,9 +11,10 @@
 //               (64 row quads of the quad-interleaved layout; issued before the grid-dependency
 //               wait: the weights do not depend on the previous kernel);
 //   warp 1      allocates the TMEM accumulator and issues tcgen05.mma from one lane -- W A_hi and
-//               W A_lo into the same accumulator, so the activations keep about 22 bits and only
-//               the f16 rounding of the dequantised weights remains; each stage's tcgen05.commit
-//               frees its shared-memory slot;
+//               W A_lo (with BN <= 128 as one MMA over both parts' rows, N = 2 BN, the epilogue
+//               adding the two halves; with BN = 256 into the same accumulator), so the
+//               activations keep about 22 bits and only the f16 rounding of the dequantised
+//               weights remains; each stage's tcgen05.commit frees its shared-memory slots;
 //   warps 2..9  dequantise the raw blocks (with two weight tiles warps 2..5 tile 0, warps 6..9
 //               tile 1) into the K-major SWIZZLE_128B f16 tile the MMA reads ((q - 8) or q is
 //               exact in f16, then one f16 multiply by the block scale); then run the epilogue
@@ -31,9 +32,11 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 #include <vector>
 
+#include "../../include/lcx.h"
 #include "epilogue.cuh"
 
 namespace lcx {
@@ -162,9 +165,16 @@ struct Cfg {
     static_assert(SB >= 2, "the activation prefetch needs at least two slots");
     static constexpr int SMEM = SA * A_BYTES + SB * B_BYTES + SR * RQ_SLOT + 1024 /* align */ + 512 /* barriers */;
     static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
-    // per weight tile one accumulator of BN columns: W A_hi and W A_lo are accumulated into it
-    static constexpr int TMEM_COLS = MT * BN <= 128 ? 128 : MT * BN <= 256 ? 256 : 512;
-    static_assert(MT * BN <= 512, "tensor memory holds 512 columns");
+    // Per weight tile one accumulator. With BN <= 128 the high and low activation rows form one
+    // B operand of 2 BN rows (the ring slot holds them contiguously), so one MMA of N = 2 BN
+    // computes W A_hi into the accumulator's first BN columns and W A_lo into the next BN, and the
+    // epilogue adds the two; an MMA of N = 256 keeps the tensor pipe far busier than two of N = 128
+    // (each instruction has a fixed cost, and the N = 256 form reads the weight tile once for
+    // twice the products). With BN = 256 the two parts are accumulated into the same BN columns.
+    static constexpr bool STACK = BN <= 128;
+    static constexpr int ACC_COLS = STACK ? 2 * BN : BN;   // TMEM columns per weight tile
+    static constexpr int TMEM_COLS = MT * ACC_COLS <= 128 ? 128 : MT * ACC_COLS <= 256 ? 256 : 512;
+    static_assert(MT * ACC_COLS <= 512, "tensor memory holds 512 columns");
     static_assert(BN <= 256, "one MMA covers at most 256 columns");
 };
 
@@ -363,24 +373,25 @@ __global__ void __launch_bounds__(352, 1)
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_f16(BM, BN);
+            constexpr int NP = C::STACK ? 1 : 2;                      // MMAs per weight tile and k
+            constexpr uint32_t idesc = idesc_f16(BM, C::STACK ? 2 * BN : BN);
             bool ok = true;
             for (int j = 0; j < nk; ++j) {
                 const int slot = j % SB, aslot = j % SA;
                 if (!(ok = mbar_wait(&full_a[aslot], (j / SA) & 1) && mbar_wait(&full_b[slot], (j / SB) & 1))) break;
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                 const uint32_t bbase = saddr(b_tile(slot));
-                // W A_hi then W A_lo into the same accumulator (the activation tile's high rows,
-                // then its low rows, BN rows each); the weight tiles alternate so consecutive MMAs
-                // of one part use different accumulators
+                // stacked: one MMA over the high and low rows together (2 BN rows of B, 2 BN
+                // accumulator columns); otherwise W A_hi then W A_lo into the same BN columns. The
+                // weight tiles alternate so consecutive MMAs use different accumulators.
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk) {
 #pragma unroll
-                    for (int hl = 0; hl < 2; ++hl) {
+                    for (int hl = 0; hl < NP; ++hl) {
 #pragma unroll
                         for (int mt = 0; mt < MT; ++mt) {
                             const uint32_t abase = saddr(a_tile(aslot, mt));
-                            mma_f16(tmem + mt * BN, sw128_desc(abase + kk * 32),
+                            mma_f16(tmem + mt * C::ACC_COLS, sw128_desc(abase + kk * 32),
                                     sw128_desc(bbase + hl * BN * BK * 2 + kk * 32), idesc,
                                     (j > 0 || kk > 0 || hl > 0) ? 1u : 0u);
                         }
@@ -428,7 +439,17 @@ __global__ void __launch_bounds__(352, 1)
         const int q = warp & 3;                 // TMEM lane quarter of this warp
         const int lrow = q * 32 + lane;         // row within the tile
         const int r = row0[my_mt] + lrow;       // weight row
-        const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16) + my_mt * BN;
+        const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16) + my_mt * C::ACC_COLS;
+        // the sums of 32 tokens (chunk cb) of this thread's row: W (A_hi + A_lo)
+        auto acc_ld = [&](int cb, uint32_t (&vv)[32]) {
+            tmem_ld32(tq + cb * 32, vv);
+            if (C::STACK) {
+                uint32_t lo[32];
+                tmem_ld32(tq + BN + cb * 32, lo);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) vv[i] = __float_as_uint(__uint_as_float(vv[i]) + __uint_as_float(lo[i]));
+            }
+        };
         const int cb0 = MT == 2 ? 0 : (wt >> 7) * (BN / 64), cb1 = MT == 2 ? BN / 32 : cb0 + BN / 64;
         // the fused epilogue of 32 tokens (chunk cb) of this thread's row, from their sums vv
         auto epilogue = [&](int cb, uint32_t (&vv)[32]) {
@@ -523,8 +544,8 @@ __global__ void __launch_bounds__(352, 1)
         if (p.ks == 1) {
             if (acc_ok)
                 for (int cb = cb0; cb < cb1; ++cb) {
-                    uint32_t vv[32];   // W (A_hi + A_lo)
-                    tmem_ld32(tq + cb * 32, vv);
+                    uint32_t vv[32];
+                    acc_ld(cb, vv);
                     epilogue(cb, vv);
                 }
         } else {
@@ -535,7 +556,7 @@ __global__ void __launch_bounds__(352, 1)
             if (acc_ok)
                 for (int cb = cb0; cb < cb1; ++cb) {
                     uint32_t vv[32];
-                    tmem_ld32(tq + cb * 32, vv);
+                    acc_ld(cb, vv);
                     float *dst = p.part + ((size_t)blockIdx.z * p.T) * p.N_pad + r;
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
@@ -740,11 +761,25 @@ GemmShape gemm_shape(int type, int N_pad, int T, int nk, int n_sm, size_t part_b
     return best;
 }
 
+// a forced tile shape (lcx_set_gemm_tile): bn | mt << 12 | ks << 16, 0 for none
+static std::atomic<int> g_forced_tile{0};
+
 cudaError_t launch_gemm_tc(const QMat &W, Epi epi, int T, const __half *A, const __half *A_lo, const FwdArgs &a,
                            int layer, cudaStream_t s, int64_t &launches, int64_t *wide) {
     ++launches;
-    const GemmShape g = gemm_shape(W.type, W.N_pad, T, W.K / tc::BK, device_sm_count(),
-                                   a.gemm_part ? a.gemm_part_bytes : 0, a.gemm_cnt ? kGemmMaxTiles : 0);
+    const int nk = W.K / tc::BK;
+    const size_t part_bytes = a.gemm_part ? a.gemm_part_bytes : 0;
+    const int max_tiles = a.gemm_cnt ? kGemmMaxTiles : 0;
+    GemmShape g;
+    if (const int f = g_forced_tile.load(std::memory_order_relaxed)) {
+        g = GemmShape{f & 0xFFF, (f >> 12) & 0xF, f >> 16};
+        const long tiles = (long)((W.N_pad + g.mt * 128 - 1) / (g.mt * 128)) * ((T + g.bn - 1) / g.bn);
+        if (g.ks > 1 && (nk / g.ks < 4 || tiles > max_tiles || (size_t)g.ks * T * W.N_pad * 4 > part_bytes ||
+                         (long)(g.ks - 1) * ((nk + g.ks - 1) / g.ks) >= nk))
+            g.ks = 1;
+    } else {
+        g = gemm_shape(W.type, W.N_pad, T, nk, device_sm_count(), part_bytes, max_tiles);
+    }
     if (g.bn >= 128 && wide) ++*wide;
     if (W.type == Q4) return tc::dispatch_shape<Q4>(g, W, epi, T, A, A_lo, a, layer, s);
     if (W.type == Q8) return tc::dispatch_shape<Q8>(g, W, epi, T, A, A_lo, a, layer, s);
@@ -752,3 +787,14 @@ cudaError_t launch_gemm_tc(const QMat &W, Epi epi, int T, const __half *A, const
 }
 
 }  // namespace lcx
+
+extern "C" int32_t lcx_set_gemm_tile(int32_t bn, int32_t mt, int32_t ks) {
+    if (bn == 0) {
+        lcx::g_forced_tile.store(0);
+        return LCX_OK;
+    }
+    const bool ok = ((bn == 64 || bn == 128) && (mt == 1 || mt == 2)) || (bn == 256 && mt == 1);
+    if (!ok || ks < 1 || ks > 8) return LCX_INVALID;
+    lcx::g_forced_tile.store(bn | mt << 12 | ks << 16);
+    return LCX_OK;
+}
