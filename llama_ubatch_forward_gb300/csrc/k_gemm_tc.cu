@@ -124,12 +124,11 @@ __device__ __forceinline__ void mma_commit_mc(uint64_t *bar, uint16_t mask) {
                  ::"r"(saddr(bar)), "h"(mask) : "memory");
 }
 
-template <int N>
-struct Regs {
-    uint32_t r[N];
-};
-
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+// A TMEM load of 32 columns of this warp's 32 lanes, without its wait: several loads may be in
+// flight before one tmem_ld_wait. The wait names the destination registers as operands it
+// modifies, so no read of them can be scheduled before it; regs_ready does the same for a
+// further array, placed after the wait.
+__device__ __forceinline__ void tmem_ld32_issue(uint32_t taddr, uint32_t (&v)[32]) {
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 "
                  "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
                  "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
@@ -139,8 +138,32 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
                    "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]),
                    "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
                  : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
+#define LCX_REGS32(v)                                                                                          \
+    "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]), "+r"(v[6]), "+r"(v[7]), "+r"(v[8]), \
+        "+r"(v[9]), "+r"(v[10]), "+r"(v[11]), "+r"(v[12]), "+r"(v[13]), "+r"(v[14]), "+r"(v[15]), "+r"(v[16]),   \
+        "+r"(v[17]), "+r"(v[18]), "+r"(v[19]), "+r"(v[20]), "+r"(v[21]), "+r"(v[22]), "+r"(v[23]), "+r"(v[24]),  \
+        "+r"(v[25]), "+r"(v[26]), "+r"(v[27]), "+r"(v[28]), "+r"(v[29]), "+r"(v[30]), "+r"(v[31])
+__device__ __forceinline__ void tmem_ld_wait(uint32_t (&v)[32]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" : LCX_REGS32(v)::"memory");
+}
+__device__ __forceinline__ void regs_ready(uint32_t (&v)[32]) { asm volatile("" : LCX_REGS32(v)); }
+#undef LCX_REGS32
+
+// The 8 dequantising / epilogue warps (256 threads) on named barrier 1.
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+// true for all 256 threads if `pred` holds in every one of them
+__device__ __forceinline__ bool epi_all(bool pred) {
+    uint32_t r;
+    asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\tbar.red.and.pred p, 1, 256, q;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(r) : "r"((uint32_t)pred) : "memory");
+    return r != 0;
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // Shared memory: three rings. The dequantised f16 weight tiles (SA slots, the largest part of a
 // step); the activation tiles (SB slots, freed by the MMAs of every CTA of the cluster that read
@@ -164,6 +187,10 @@ struct Cfg {
     static constexpr int DB = SB - 1;   // activation prefetch distance (the loader runs a ring ahead)
     static_assert(SB >= 2, "the activation prefetch needs at least two slots");
     static constexpr int SMEM = SA * A_BYTES + SB * B_BYTES + SR * RQ_SLOT + 1024 /* align */ + 512 /* barriers */;
+    // the A and B rings, reused by the epilogue for its staged operands
+    static constexpr int STAGE = SA * A_BYTES + SB * B_BYTES;
+    static_assert(8 * BN + BN * 128 * 4 <= STAGE, "positions, cells and RoPE rows of the tile's tokens");
+    static_assert(BN * MT * BM * 4 <= STAGE, "residual rows of the tile");
     static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
     // Per weight tile one accumulator. With BN <= 128 the high and low activation rows form one
     // B operand of 2 BN rows (the ring slot holds them contiguously), so one MMA of N = 2 BN
@@ -433,127 +460,169 @@ __global__ void __launch_bounds__(352, 1)
         }
         if (!ok) atomicExch(a.err, 1);
         const bool acc_ok = __all_sync(0xffffffffu, ok && mbar_wait(acc_bar, 0));
+        // one answer for the 8 warps, so every named barrier below is reached by all of them
+        const bool cta_ok = epi_all(acc_ok);
+        if (acc_ok) asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        else if (ok) atomicExch(a.err, 1);
         // a warp reads the TMEM lanes of its quarter (warp % 4); with two tiles warps 2..5 take
         // tile 0 and 6..9 tile 1, all BN columns; with one tile the two warps of a quarter take
         // half of the columns each
         const int q = warp & 3;                 // TMEM lane quarter of this warp
         const int lrow = q * 32 + lane;         // row within the tile
         const int r = row0[my_mt] + lrow;       // weight row
+        const int rc = my_mt * BM + lrow;       // row within the CTA's MT tiles
+        constexpr int RW = MT * BM;             // rows of the CTA
         const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16) + my_mt * C::ACC_COLS;
-        // the sums of 32 tokens (chunk cb) of this thread's row: W (A_hi + A_lo)
+        // the sums of 32 tokens (chunk cb) of this thread's row: W (A_hi + A_lo); both halves'
+        // loads are in flight before the one wait
         auto acc_ld = [&](int cb, uint32_t (&vv)[32]) {
-            tmem_ld32(tq + cb * 32, vv);
             if (C::STACK) {
                 uint32_t lo[32];
-                tmem_ld32(tq + BN + cb * 32, lo);
+                tmem_ld32_issue(tq + cb * 32, vv);
+                tmem_ld32_issue(tq + BN + cb * 32, lo);
+                tmem_ld_wait(vv);
+                regs_ready(lo);
 #pragma unroll
                 for (int i = 0; i < 32; ++i) vv[i] = __float_as_uint(__uint_as_float(vv[i]) + __uint_as_float(lo[i]));
+            } else {
+                tmem_ld32_issue(tq + cb * 32, vv);
+                tmem_ld_wait(vv);
             }
         };
         const int cb0 = MT == 2 ? 0 : (wt >> 7) * (BN / 64), cb1 = MT == 2 ? BN / 32 : cb0 + BN / 64;
-        // the fused epilogue of 32 tokens (chunk cb) of this thread's row, from their sums vv
-        auto epilogue = [&](int cb, uint32_t (&vv)[32]) {
-                if (EPI == EPI_SWIGLU) {   // rows 8f'..8f'+3 gate, 8f'+4..8f'+7 up of features 4f'..
-                    const int f = (r >> 3) * 4 + (lrow & 3);
-                    const bool gate = (lane & 7) < 4;
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const float g = __uint_as_float(vv[i]);
-                        const float u = __shfl_down_sync(0xffffffffu, g, 4);
-                        const int t = tok0 + cb * 32 + i;
-                        if (gate && t < p.T && f < a.F)
-                            store_split(a.h16, a.h16_lo, (size_t)t * a.F_pad + f, silu_f(g) * u);
-                    }
-                    return;
+
+        // Operands of the epilogue staged in shared memory: once the accumulator is complete every
+        // activation and weight tile has been consumed and no copy is in flight, so the A and B
+        // rings (contiguous from the base) are free. All 256 threads copy with cp.async, every
+        // copy in flight before one wait:
+        //   QKV    the tokens' positions and cells, then the RoPE (cos, sin) rows of their positions;
+        //   RESID  the residual rows x[t][rows of the CTA] of the CTA's tokens.
+        const int qw = a.H * a.hd, kw = a.KV * a.hd;
+        int *s_pos = reinterpret_cast<int *>(smem), *s_cell = s_pos + BN;
+        float2 *s_rope = reinterpret_cast<float2 *>(smem + 8 * BN);
+        float *s_x = reinterpret_cast<float *>(smem);
+        const bool any_rot = EPI == EPI_QKV && row0[0] < qw + kw;
+        if (EPI == EPI_QKV) {
+            if (cta_ok)
+                for (int i = wt; i < BN; i += 256) {
+                    const int t = min(tok0 + i, p.T - 1);
+                    s_pos[i] = __ldg(a.ub.pos + t);
+                    s_cell[i] = __ldg(a.ub.cell + t);
                 }
-                // every load of a 16-token group is issued before its first store: a store may
-                // alias a later load, so mixing them would serialise one L2 round trip per element
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    if (EPI == EPI_RESID) {
-                        float xo[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const int t = tok0 + cb * 32 + 16 * h + i;
-                            xo[i] = t < p.T && r < p.N ? __ldcg(a.x + (size_t)t * a.d + r) : 0.f;
-                        }
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const int t = tok0 + cb * 32 + 16 * h + i;
-                            if (t < p.T && r < p.N) a.x[(size_t)t * a.d + r] = xo[i] + __uint_as_float(vv[16 * h + i]);
-                        }
-                    } else if (EPI == EPI_LOGITS) {
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const int t = tok0 + cb * 32 + 16 * h + i;
-                            const float v = __uint_as_float(vv[16 * h + i]);
-                            unsigned long long key = 0ull;
-                            if (t < p.T && r < p.N) {
-                                a.logits[(size_t)t * a.V + r] = v;
-                                key = argmax_key(v, r);
-                                if (!isfinite(v)) note_nonfinite(a);
-                            }
-#pragma unroll
-                            for (int o = 16; o; o >>= 1) {
-                                const unsigned long long other = __shfl_xor_sync(0xffffffffu, key, o);
-                                key = other > key ? other : key;
-                            }
-                            if (lane == 0 && key) atomicMax(&a.amax_key[t], key);
-                        }
-                    } else {   // EPI_QKV: rotate (q, k) pairs of adjacent rows, store q f32 and k, v f16
-                        const int qw = a.H * a.hd, kw = a.KV * a.hd;
-                        const bool rot = r < qw + kw;
-                        const int dim = (r < qw ? r : r - qw) & (a.hd - 1);   // hd is 64 or 128
-                        int cell[16];
-                        float2 cs[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {   // token metadata and RoPE pairs, all loads first
-                            const int t = tok0 + cb * 32 + 16 * h + i;
-                            const int pos = t < p.T ? __ldg(a.ub.pos + t) : 0;
-                            cell[i] = t < p.T ? __ldg(a.ub.cell + t) : 0;
-                            cs[i] = rot ? __ldg(a.rope + (size_t)pos * (a.hd / 2) + dim / 2) : make_float2(1.f, 0.f);
-                        }
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const int t = tok0 + cb * 32 + 16 * h + i;
-                            const float v = __uint_as_float(vv[16 * h + i]);
-                            const float partner = __shfl_xor_sync(0xffffffffu, v, 1);
-                            if (t < p.T && r < qw + 2 * kw && (lane & 1) == 0) {
-                                float y0 = v, y1 = partner;
-                                if (rot) {
-                                    const float z0 = y0 * cs[i].x - y1 * cs[i].y, z1 = y0 * cs[i].y + y1 * cs[i].x;
-                                    y0 = z0;
-                                    y1 = z1;
-                                }
-                                if (r < qw) {
-                                    *reinterpret_cast<float2 *>(a.q + (size_t)t * qw + r) = make_float2(y0, y1);
-                                } else {
-                                    const bool isk = r < qw + kw;
-                                    const int rr = isk ? r - qw : r - qw - kw;
-                                    const int sh = __ffs(a.hd) - 1;
-                                    __half *dst = (isk ? a.kc : a.vc) + kv_off(a, layer, cell[i], rr >> sh, rr & (a.hd - 1));
-                                    *reinterpret_cast<__half2 *>(dst) = __floats2half2_rn(y0, y1);
-                                }
-                            }
-                        }
-                    }
+            epi_sync();
+            if (cta_ok && any_rot) {
+                const int chunks = a.hd / 4;   // 16-byte pieces of a row of hd / 2 pairs
+                for (int i = wt; i < BN * chunks; i += 256) {
+                    const int tt = i / chunks, c = i - tt * chunks;
+                    cp_async16(saddr(s_rope) + (uint32_t)i * 16, a.rope + (size_t)s_pos[tt] * (a.hd / 2) + c * 2);
                 }
+                cp_async_wait_all();
+            }
+            epi_sync();
+        }
+        // x rows of the CTA's tokens [first, first + n) into s_x[t - first][RW] (rows past N and
+        // tokens past T are not read)
+        auto stage_x = [&](int first, int n, float *dst) {
+            constexpr int CPR = RW / 4;   // 16-byte pieces a token
+            for (int i = wt; i < n * CPR; i += 256) {
+                const int tt = i / CPR, c = i - tt * CPR;
+                const int t = tok0 + first + tt, rr = row0[0] + 4 * c;
+                if (t < p.T && rr < p.N) cp_async16(saddr(dst) + (uint32_t)i * 16, a.x + (size_t)t * a.d + rr);
+            }
         };
-        if (acc_ok) asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        else if (ok) atomicExch(a.err, 1);
+        if (EPI == EPI_RESID && p.ks == 1) {
+            if (cta_ok) {
+                stage_x(0, BN, s_x);
+                cp_async_wait_all();
+            }
+            epi_sync();
+        }
+
+        // the fused epilogue of 32 tokens (chunk cb) of this thread's row, from their sums vv;
+        // sx: the staged residual rows of those tokens (RESID)
+        auto epilogue = [&](int cb, uint32_t (&vv)[32], const float *sx) {
+            if (EPI == EPI_SWIGLU) {
+                // rows 8f'..8f'+3 gate, 8f'+4..8f'+7 up of features 4f'..: the gate lane takes the
+                // chunk's first 16 tokens and its up partner (lane + 4) the last 16, each sending
+                // the other the half it needs
+                const int f = (r >> 3) * 4 + (lrow & 3);
+                const bool gate = (lane & 7) < 4;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float lo_half = __uint_as_float(vv[i]), hi_half = __uint_as_float(vv[16 + i]);
+                    const float mine = gate ? lo_half : hi_half;
+                    const float other = __shfl_xor_sync(0xffffffffu, gate ? hi_half : lo_half, 4);
+                    const float g = gate ? mine : other, u = gate ? other : mine;
+                    const int t = tok0 + cb * 32 + (gate ? i : 16 + i);
+                    if (t < p.T && f < a.F) store_split(a.h16, a.h16_lo, (size_t)t * a.F_pad + f, silu_f(g) * u);
+                }
+            } else if (EPI == EPI_RESID) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int t = tok0 + cb * 32 + i;
+                    if (t < p.T && r < p.N) a.x[(size_t)t * a.d + r] = sx[i * RW + rc] + __uint_as_float(vv[i]);
+                }
+            } else if (EPI == EPI_LOGITS) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int t = tok0 + cb * 32 + i;
+                    const float v = __uint_as_float(vv[i]);
+                    unsigned long long key = 0ull;
+                    if (t < p.T && r < p.N) {
+                        a.logits[(size_t)t * a.V + r] = v;
+                        key = argmax_key(v, r);
+                        if (!isfinite(v)) note_nonfinite(a);
+                    }
+#pragma unroll
+                    for (int o = 16; o; o >>= 1) {
+                        const unsigned long long other = __shfl_xor_sync(0xffffffffu, key, o);
+                        key = other > key ? other : key;
+                    }
+                    if (lane == 0 && key) atomicMax(&a.amax_key[t], key);
+                }
+            } else {   // EPI_QKV: rotate (q, k) pairs of adjacent rows, store q f32 and k, v f16
+                const bool rot = r < qw + kw;
+                const int dim = (r < qw ? r : r - qw) & (a.hd - 1);   // hd is 64 or 128
+                const int sh = __ffs(a.hd) - 1;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int tt = cb * 32 + i, t = tok0 + tt;
+                    const float v = __uint_as_float(vv[i]);
+                    const float partner = __shfl_xor_sync(0xffffffffu, v, 1);
+                    if (t < p.T && r < qw + 2 * kw && (lane & 1) == 0) {
+                        float y0 = v, y1 = partner;
+                        if (rot) {
+                            const float2 cs = s_rope[tt * (a.hd / 2) + dim / 2];
+                            const float z0 = y0 * cs.x - y1 * cs.y, z1 = y0 * cs.y + y1 * cs.x;
+                            y0 = z0;
+                            y1 = z1;
+                        }
+                        if (r < qw) {
+                            *reinterpret_cast<float2 *>(a.q + (size_t)t * qw + r) = make_float2(y0, y1);
+                        } else {
+                            const bool isk = r < qw + kw;
+                            const int rr = isk ? r - qw : r - qw - kw;
+                            __half *dst = (isk ? a.kc : a.vc) + kv_off(a, layer, s_cell[tt], rr >> sh, rr & (a.hd - 1));
+                            *reinterpret_cast<__half2 *>(dst) = __floats2half2_rn(y0, y1);
+                        }
+                    }
+                }
+            }
+        };
         if (p.ks == 1) {
-            if (acc_ok)
+            if (cta_ok)
                 for (int cb = cb0; cb < cb1; ++cb) {
                     uint32_t vv[32];
                     acc_ld(cb, vv);
-                    epilogue(cb, vv);
+                    epilogue(cb, vv, s_x + cb * 32 * RW);
                 }
         } else {
             // split K: every CTA of an output tile stores its partial sums; the last of them to
-            // arrive adds the ks partials in split order and applies the epilogue. The counter is
-            // bumped even after a failed wait, so it always returns to zero.
+            // arrive adds the ks partials in split order (its own from tensor memory, the others
+            // staged in shared memory) and applies the epilogue. The counter is bumped even after
+            // a failed wait, so it always returns to zero.
             __shared__ int s_last;
-            if (acc_ok)
+            if (cta_ok)
                 for (int cb = cb0; cb < cb1; ++cb) {
                     uint32_t vv[32];
                     acc_ld(cb, vv);
@@ -564,35 +633,109 @@ __global__ void __launch_bounds__(352, 1)
                         if (t < p.T && r < p.N_pad) __stcg(dst + (size_t)t * p.N_pad, __uint_as_float(vv[i]));
                     }
                 }
-            asm volatile("bar.sync 1, 256;" ::: "memory");   // the 8 epilogue warps' stores are done
+            epi_sync();   // the 8 epilogue warps' stores are done
             if (wt == 0) {
                 __threadfence();
                 const int prev = atomicAdd(p.cnt + blockIdx.x * gridDim.y + blockIdx.y, 1);
                 s_last = prev == p.ks - 1;
             }
-            asm volatile("bar.sync 1, 256;" ::: "memory");
+            epi_sync();
             if (s_last) {
                 __threadfence();
-                for (int cb = cb0; cb < cb1; ++cb) {
-                    // split by split, the 32 tokens' loads all in flight before they are added
-                    float sum[32];
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) sum[i] = 0.f;
-                    for (int z = 0; z < p.ks; ++z) {
-                        const float *src = p.part + ((size_t)z * p.T) * p.N_pad + r;
-                        float v[32];
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            const int t = min(tok0 + cb * 32 + i, p.T - 1);
-                            v[i] = r < p.N_pad ? __ldcg(src + (size_t)t * p.N_pad) : 0.f;
+                // token groups of G tokens (a multiple of 32): the other splits' partials of the
+                // group and, for RESID, its residual rows, staged together
+                const int n_in = p.ks - 1 + (EPI == EPI_RESID ? 1 : 0);
+                const int stage_bytes = C::STAGE - (EPI == EPI_QKV ? 8 * BN + BN * 128 * 4 : 0);
+                const int per_chunk = n_in * 32 * RW * 4;
+                int G = (stage_bytes / per_chunk) * 32;
+                G = G > BN ? BN : G;
+                uint8_t *sbase = smem + (EPI == EPI_QKV ? C::STAGE - stage_bytes : 0);
+                if (G >= 32) {
+                    for (int g0 = 0; g0 < BN; g0 += G) {
+                        float *sp = reinterpret_cast<float *>(sbase);   // [n_in][G][RW]
+                        const int gn = min(G, BN - g0);                  // tokens of this group
+                        if (cta_ok) {
+                            int slot = 0;
+                            for (int z = 0; z < p.ks; ++z) {
+                                if (z == (int)blockIdx.z) continue;
+                                float *d = sp + (size_t)slot * G * RW;
+                                constexpr int CPR = RW / 4;
+                                for (int i = wt; i < gn * CPR; i += 256) {
+                                    const int tt = i / CPR, c = i - tt * CPR;
+                                    const int t = tok0 + g0 + tt, rr = row0[0] + 4 * c;
+                                    if (t < p.T && rr < p.N_pad)
+                                        cp_async16(saddr(d) + (uint32_t)i * 16,
+                                                   p.part + ((size_t)z * p.T + t) * p.N_pad + rr);
+                                }
+                                ++slot;
+                            }
+                            if (EPI == EPI_RESID) stage_x(g0, gn, sp + (size_t)slot * G * RW);
+                            cp_async_wait_all();
                         }
+                        epi_sync();
+                        if (cta_ok)
+                            for (int cb = max(cb0, g0 / 32); cb < min(cb1, (g0 + G) / 32); ++cb) {
+                                uint32_t own[32];
+                                acc_ld(cb, own);
+                                const int tb = cb * 32 - g0;   // first token of the chunk in the group
+                                float sum[32];
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) sum[i] += v[i];
+                                for (int i = 0; i < 32; ++i) sum[i] = 0.f;
+                                int slot = 0;
+                                for (int z = 0; z < p.ks; ++z) {
+                                    if (z == (int)blockIdx.z) {
+#pragma unroll
+                                        for (int i = 0; i < 32; ++i) sum[i] += __uint_as_float(own[i]);
+                                    } else {
+                                        const float *src = sp + ((size_t)slot * G + tb) * RW + rc;
+#pragma unroll
+                                        for (int i = 0; i < 32; ++i) sum[i] += src[i * RW];
+                                        ++slot;
+                                    }
+                                }
+                                uint32_t vv[32];
+#pragma unroll
+                                for (int i = 0; i < 32; ++i) vv[i] = __float_as_uint(sum[i]);
+                                epilogue(cb, vv, sp + ((size_t)(p.ks - 1) * G + tb) * RW);
+                            }
+                        epi_sync();   // the group's staging space is reused by the next group
                     }
-                    uint32_t vv[32];
+                } else if (cta_ok) {
+                    // too many splits to stage one chunk: the partials straight from L2
+                    for (int cb = cb0; cb < cb1; ++cb) {
+                        float sum[32];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) vv[i] = __float_as_uint(sum[i]);
-                    epilogue(cb, vv);
+                        for (int i = 0; i < 32; ++i) sum[i] = 0.f;
+                        for (int z = 0; z < p.ks; ++z) {
+                            const float *src = p.part + ((size_t)z * p.T) * p.N_pad + r;
+                            float v[32];
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) {
+                                const int t = min(tok0 + cb * 32 + i, p.T - 1);
+                                v[i] = r < p.N_pad ? __ldcg(src + (size_t)t * p.N_pad) : 0.f;
+                            }
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) sum[i] += v[i];
+                        }
+                        uint32_t vv[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) vv[i] = __float_as_uint(sum[i]);
+                        if (EPI == EPI_RESID) {
+                            float xo[32];
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) {
+                                const int t = tok0 + cb * 32 + i;
+                                xo[i] = t < p.T && r < p.N ? __ldcg(a.x + (size_t)t * a.d + r) : 0.f;
+                            }
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) {
+                                const int t = tok0 + cb * 32 + i;
+                                if (t < p.T && r < p.N) a.x[(size_t)t * a.d + r] = xo[i] + sum[i];
+                            }
+                        } else {
+                            epilogue(cb, vv, nullptr);
+                        }
+                    }
                 }
                 if (wt == 0) p.cnt[blockIdx.x * gridDim.y + blockIdx.y] = 0;
             }
