@@ -189,7 +189,7 @@ struct Cfg {
     static constexpr int SMEM = SA * A_BYTES + SB * B_BYTES + SR * RQ_SLOT + 1024 /* align */ + 512 /* barriers */;
     // the A and B rings, reused by the epilogue for its staged operands
     static constexpr int STAGE = SA * A_BYTES + SB * B_BYTES;
-    static_assert(8 * BN + BN * 128 * 4 <= STAGE, "positions, cells and RoPE rows of the tile's tokens");
+    static_assert(16 * BN + BN * 128 * 4 <= STAGE, "positions, cells and RoPE rows of the tile's tokens");
     static_assert(BN * MT * BM * 4 <= STAGE, "residual rows of the tile");
     static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
     // Per weight tile one accumulator. With BN <= 128 the high and low activation rows form one
@@ -498,8 +498,11 @@ __global__ void __launch_bounds__(352, 1)
         //   QKV    the tokens' positions and cells, then the RoPE (cos, sin) rows of their positions;
         //   RESID  the residual rows x[t][rows of the CTA] of the CTA's tokens.
         const int qw = a.H * a.hd, kw = a.KV * a.hd;
-        int *s_pos = reinterpret_cast<int *>(smem), *s_cell = s_pos + BN;
-        float2 *s_rope = reinterpret_cast<float2 *>(smem + 8 * BN);
+        // s_coff: a token's cache cell as an element offset within (layer, kv head) of the cache
+        // [L][n_pages][KV][kPage][hd]: page * KV * kPage * hd + slot * hd
+        long long *s_coff = reinterpret_cast<long long *>(smem);
+        int *s_pos = reinterpret_cast<int *>(smem + 8 * BN);
+        float2 *s_rope = reinterpret_cast<float2 *>(smem + 16 * BN);
         float *s_x = reinterpret_cast<float *>(smem);
         const bool any_rot = EPI == EPI_QKV && row0[0] < qw + kw;
         if (EPI == EPI_QKV) {
@@ -507,7 +510,8 @@ __global__ void __launch_bounds__(352, 1)
                 for (int i = wt; i < BN; i += 256) {
                     const int t = min(tok0 + i, p.T - 1);
                     s_pos[i] = __ldg(a.ub.pos + t);
-                    s_cell[i] = __ldg(a.ub.cell + t);
+                    const int cell = __ldg(a.ub.cell + t);
+                    s_coff[i] = ((long long)(cell / kPage) * a.KV * kPage + cell % kPage) * a.hd;
                 }
             epi_sync();
             if (cta_ok && any_rot) {
@@ -581,30 +585,32 @@ __global__ void __launch_bounds__(352, 1)
                     if (lane == 0 && key) atomicMax(&a.amax_key[t], key);
                 }
             } else {   // EPI_QKV: rotate (q, k) pairs of adjacent rows, store q f32 and k, v f16
-                const bool rot = r < qw + kw;
-                const int dim = (r < qw ? r : r - qw) & (a.hd - 1);   // hd is 64 or 128
-                const int sh = __ffs(a.hd) - 1;
+                // Every lane stores its own row, so no branch diverges within a warp: a rotated
+                // pair (even row e, odd row e + 1) is y_e = v_e cos - v_o sin and y_o = v_o cos +
+                // v_e sin, i.e. y = v cos + s v_partner sin with s = -1 on the even lane and +1 on
+                // the odd one; V rows keep v (a select, so the compiler can issue every token's
+                // shared-memory load and shuffle ahead of the predicated stores).
+                const bool isq = r < qw, rot = r < qw + kw;
+                const bool store_row = r < qw + 2 * kw;
+                const float sgn = (lane & 1) ? 1.f : -1.f;
+                const int dim = (isq ? r : r - qw) & (a.hd - 1);   // hd is 64 or 128
+                const int rr = isq ? 0 : (rot ? r - qw : r - qw - kw);
+                const int sh = __ffs(a.hd) - 1, hd2 = a.hd / 2;
+                float *qdst = a.q + r;
+                __half *kvdst = (rot ? a.kc : a.vc) +
+                                (((size_t)layer * a.n_pages * a.KV + (rr >> sh)) * kPage) * a.hd + dim;
+                const float2 *rope = s_rope + dim / 2;
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     const int tt = cb * 32 + i, t = tok0 + tt;
                     const float v = __uint_as_float(vv[i]);
                     const float partner = __shfl_xor_sync(0xffffffffu, v, 1);
-                    if (t < p.T && r < qw + 2 * kw && (lane & 1) == 0) {
-                        float y0 = v, y1 = partner;
-                        if (rot) {
-                            const float2 cs = s_rope[tt * (a.hd / 2) + dim / 2];
-                            const float z0 = y0 * cs.x - y1 * cs.y, z1 = y0 * cs.y + y1 * cs.x;
-                            y0 = z0;
-                            y1 = z1;
-                        }
-                        if (r < qw) {
-                            *reinterpret_cast<float2 *>(a.q + (size_t)t * qw + r) = make_float2(y0, y1);
-                        } else {
-                            const bool isk = r < qw + kw;
-                            const int rr = isk ? r - qw : r - qw - kw;
-                            __half *dst = (isk ? a.kc : a.vc) + kv_off(a, layer, s_cell[tt], rr >> sh, rr & (a.hd - 1));
-                            *reinterpret_cast<__half2 *>(dst) = __floats2half2_rn(y0, y1);
-                        }
+                    const float2 cs = rope[tt * hd2];
+                    const float z = fmaf(sgn * partner, cs.y, v * cs.x);
+                    const float y = rot ? z : v;
+                    if (store_row && t < p.T) {
+                        if (isq) qdst[(size_t)t * qw] = y;
+                        else kvdst[s_coff[tt]] = __float2half_rn(y);
                     }
                 }
             }
@@ -645,7 +651,7 @@ __global__ void __launch_bounds__(352, 1)
                 // token groups of G tokens (a multiple of 32): the other splits' partials of the
                 // group and, for RESID, its residual rows, staged together
                 const int n_in = p.ks - 1 + (EPI == EPI_RESID ? 1 : 0);
-                const int stage_bytes = C::STAGE - (EPI == EPI_QKV ? 8 * BN + BN * 128 * 4 : 0);
+                const int stage_bytes = C::STAGE - (EPI == EPI_QKV ? 16 * BN + BN * 128 * 4 : 0);
                 const int per_chunk = n_in * 32 * RW * 4;
                 int G = (stage_bytes / per_chunk) * 32;
                 G = G > BN ? BN : G;
