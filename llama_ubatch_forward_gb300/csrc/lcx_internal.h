@@ -168,6 +168,9 @@ cudaError_t launch_attention(const FwdArgs &a, int layer, int max_natt, bool out
 int attention_splits(const FwdArgs &a, int max_natt, int *chunk);
 // tensor-core attention over the ubatch's query tiles (k_attn_prefill.cu); writes o16 / o16_lo
 cudaError_t launch_attention_prefill(const FwdArgs &a, int layer, cudaStream_t s, int64_t &launches);
+// the tensor-core (tcgen05) prefill attention: 4 query heads per KV head, head_dim 64 or 128
+bool attention_prefill_tc_fits(const FwdArgs &a);
+cudaError_t launch_attention_prefill_tc(const FwdArgs &a, int layer, cudaStream_t s, int64_t &launches);
 // Scratch bytes one attention launch needs (partials, then arrival counters at
 // *counter_offset); 0 when every token fits in a single split.
 size_t attention_scratch_bytes(const FwdArgs &a, int max_natt, size_t *counter_offset);
