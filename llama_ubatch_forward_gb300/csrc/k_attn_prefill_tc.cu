@@ -91,10 +91,18 @@ __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.
 
 // f16 high part of x and the f16 rounding of the rest, packed for two elements (x0 in the low half)
 __device__ __forceinline__ void split_pack(float x0, float x1, uint32_t &hi, uint32_t &lo) {
-    const __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
-    const __half l0 = __float2half_rn(x0 - __half2float(h0)), l1 = __float2half_rn(x1 - __half2float(h1));
-    hi = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
-    lo = (uint32_t)__half_as_ushort(l0) | ((uint32_t)__half_as_ushort(l1) << 16);
+    const __half2 h = __floats2half2_rn(x0, x1);
+    const float2 hf = __half22float2(h);
+    const __half2 l = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
+    hi = *reinterpret_cast<const uint32_t *>(&h);
+    lo = *reinterpret_cast<const uint32_t *>(&l);
+}
+
+// 2^x by the hardware approximation (relative error about 2^-22; results below 2^-126 flush to 0)
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 template <int HD>
@@ -104,8 +112,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     using C = Cfg<HD>;
     extern __shared__ uint8_t smem_raw[];
     // this CTA's 32 tokens: half of a 64-token query tile of the ubatch
-    const int4 tile = a.ub.qtiles[blockIdx.x >> 1];
-    const int half = blockIdx.x & 1;
+    // the ubatch's last tiles (the most key tiles under the causal mask) are scheduled first
+    const int4 tile = a.ub.qtiles[a.ub.n_qtiles - 1 - (int)(blockIdx.x >> 1)];
+    const int half = 1 - (int)(blockIdx.x & 1);
     const int tok0 = tile.x + TQ * half, ntok = min(TQ, tile.y - TQ * half), seq = tile.z, p0 = tile.w + TQ * half;
     if (ntok <= 0) return;   // the whole CTA, before any barrier or allocation
     const int kvh = blockIdx.y;
@@ -260,39 +269,45 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             ok = __all_sync(0xffffffffu, mbar_wait(&s_full[b], (j >> 1) & 1));
             if (!ok) break;
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            // two passes over the row's 128 scores, 32 at a time: the maximum, then P
-            const int cpos0 = j * BC;
-            auto scaled = [&](uint32_t (&v)[32], int c) {   // scaled scores, the causal mask applied
+            uint32_t sv[4][32];
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    v[i] = __float_as_uint((cpos0 + c * 32 + i <= qpos) ? __uint_as_float(v[i]) * scale : -CUDART_INF_F);
-            };
+            for (int c = 0; c < 4; ++c) tmem_ld32_issue(tl + b * BC + c * 32, sv[c]);
+            tmem_ld_wait(sv[0]);
+            regs_ready(sv[1]);
+            regs_ready(sv[2]);
+            regs_ready(sv[3]);
+            // the causal mask, on the tiles that hold a cell after the CTA's first position (the
+            // same answer for every row of the CTA)
+            const int cpos0 = j * BC;
+            if (cpos0 + BC - 1 > p0) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (cpos0 + c * 32 + i > qpos) sv[c][i] = __float_as_uint(-CUDART_INF_F);
+            }
             float mx = -CUDART_INF_F;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t sv[32];
-                tmem_ld32_issue(tl + b * BC + c * 32, sv);
-                tmem_ld_wait(sv);
-                scaled(sv, c);
+            for (int c = 0; c < 4; ++c)
 #pragma unroll
-                for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(sv[i]));
-            }
-            const float m_new = fmaxf(m, mx);   // finite: every row sees cell 0 in tile 0
-            const float alpha = exp2f(m - m_new);
-            // P = 2^(s - m_new) as f16 high + low parts, written over the chunk's own 32 columns:
+                for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(sv[c][i]));
+            // The reference maximum m moves only when the tile's maximum exceeds it by more than
+            // 8 (so P <= 2^8, exact enough in the f16 high + low pair); O and l are rescaled
+            // only then, and the final O / l uses the same m throughout. Tile 0 holds cell 0 for
+            // every row, so m is finite from the first tile on.
+            const float mxs = mx * scale;
+            const float m_new = mxs > m + 8.f ? mxs : m;
+            const float alpha = ex2_approx(m - m_new);
+            // P = 2^(s scale - m) as f16 high + low parts, written over the chunk's own 32 columns:
             // cells 32c..32c+31 -> high parts in columns 32c..32c+15, low parts in 32c+16..32c+31
             float psum = 0.f;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-                uint32_t sv[32];
-                tmem_ld32_issue(tl + b * BC + c * 32, sv);
-                tmem_ld_wait(sv);
-                scaled(sv, c);
                 uint32_t ph[16], pl[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const float e0 = exp2f(__uint_as_float(sv[2 * i]) - m_new);
-                    const float e1 = exp2f(__uint_as_float(sv[2 * i + 1]) - m_new);
+                    const float e0 = ex2_approx(fmaf(__uint_as_float(sv[c][2 * i]), scale, -m_new));
+                    const float e1 = ex2_approx(fmaf(__uint_as_float(sv[c][2 * i + 1]), scale, -m_new));
                     psum += e0 + e1;
                     split_pack(e0, e1, ph[i], pl[i]);
                 }

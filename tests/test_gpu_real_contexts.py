@@ -10,7 +10,8 @@ acceptance bar (per-row relative L2 <= 5e-3, argmax equal where the oracle's top
 1e-2):
 
   * 8B shape, 2 layers: a 2048-token prompt in ubatches of 512 (the tensor-core matmuls with
-    128-token tiles for gate/up, asserted through the launch counter; prefill flash attention),
+    128-token tiles for gate/up, asserted through the launch counter; prefill flash attention on
+    mma.sync for the first ubatch and on tcgen05 from position 1024 on),
     then 8 decode steps at positions 2048+ (the persistent one-token step: Q4_0, head_dim 128,
     4 query heads per KV head, attention split over many CTAs);
   * 8B shape, 1 layer: the long-context workload's 32768-token prompt in ubatches of 2048, then
@@ -18,6 +19,8 @@ acceptance bar (per-row relative L2 <= 5e-3, argmax equal where the oracle's top
   * 8B shape, 1 layer: 64 sequences in one cache with prompt lengths drawn as the 64-sequence
     workload draws them, divided by 4 (to bound the oracle's time), each prefilled in ubatches of
     512, then 2 steps of one 64-token ubatch (one token per sequence, every row flagged);
+  * 1B shape, 2 layers: a 1536-token prompt in ubatches of 512 (head_dim 64 on the tensor-core
+    prefill attention);
   * 1B shape, all 16 layers: a 512-token prompt in one ubatch, then 4 decode steps.
 """
 import dataclasses
@@ -138,6 +141,26 @@ def test_8b_one_layer_64_sequences(host8):
         toks = am.astype(np.int32)
     for s in (0, 31, 63):
         assert ctx.seq_pos_max(s) == octx.seq_pos_max(s) == int(lens[s]) + 1
+
+
+def test_1b_two_layers_1536_prompt():
+    # head_dim 64 on the tensor-core prefill attention (ubatches of 512 up to position 1536: the
+    # last two attend at least 1024 cells)
+    cfg = synth.CONFIGS["1b"]
+    lcx.build()
+    oracle.set_threads()
+    host = synth.make_model(cfg, n_layer=2)
+    gm, om = upload(host), oracle.Model(host)
+    n = 1536
+    prompt = synth.prompt_tokens(cfg, n)
+    flags = np.zeros(n, np.int8)
+    flags[[0, 700, 1023, 1024, 1300, 1535]] = 1
+    octx = oracle.Context(om, cfg.n_ctx, 1, 512)
+    ctx = lcx.Context(gm, cfg.n_ctx, 1, 512)
+    rc, ref, am = octx.decode(prompt, logits=flags)
+    rc2, lg, am2 = gpu_decode(ctx, cfg.n_vocab, prompt, flags=flags)
+    assert rc == rc2 == 0
+    check_rows(lg, am2, ref, am, "1b 1536 prefill")
 
 
 def test_1b_full_depth_512_prompt_then_decode():
