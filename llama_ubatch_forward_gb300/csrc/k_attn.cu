@@ -20,6 +20,13 @@ namespace lcx {
 
 namespace {
 
+// 2^x by the hardware approximation (relative error about 2^-22; results below 2^-126 flush to 0)
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 template <int HD, int G, bool OUT16>
 __global__ void __launch_bounds__(128) k_attn(const FwdArgs a, const int layer, const int chunk, const int n_split) {
     constexpr int DPL = HD / 8;    // dims per lane in Q.K (8 lanes per cell)
@@ -80,7 +87,7 @@ __global__ void __launch_bounds__(128) k_attn(const FwdArgs a, const int layer, 
     if (sp >= ns_t) return;
     if (j_first < c1 && j_first + 16 > fresh) load_sg(j_first, true, kA, vA);
     const int qw = a.H * HD;
-    const float scale = rsqrtf((float)HD);
+    const float scale = rsqrtf((float)HD) * 1.4426950408889634f;   // scores in the log2 domain
 
     // this lane's Q slice for the QK step: dims (lane % 8) * DPL .. + DPL, pre-scaled
     float qr[G][DPL];
@@ -103,61 +110,60 @@ __global__ void __launch_bounds__(128) k_attn(const FwdArgs a, const int layer, 
     }
 
     // Each warp takes super-groups of 16 consecutive cells (inside one 64-cell page): all K and
-    // V loads of a super-group are issued before any of them is used, one super-group ahead.
+    // V loads of a super-group are issued before any of them is used, one super-group ahead. The
+    // 16 cells' scores are computed first and take one online-softmax step together (one
+    // maximum, one rescaling of the accumulators), in the log2 domain (q carries log2(e)).
     auto consume = [&](int j0, const uint4 (&kraw)[4][DPL / 8], const uint2 (&vraw)[16]) {
+        float s[4][G];   // cell j0 + 4 g4 + cgrp, query head g (every lane of the cell holds it)
 #pragma unroll
         for (int g4 = 0; g4 < 4; ++g4) {
-            if (j0 + 4 * g4 >= c1) break;
-            const int j = j0 + 4 * g4 + cgrp;   // this lane's cell in the group
-            const bool valid = j < c1;
-            float s[G];
-            {
-                float kf[DPL];
+            const bool valid = j0 + 4 * g4 + cgrp < c1;
+            float kf[DPL];
 #pragma unroll
-                for (int i = 0; i < DPL / 8; ++i) {
-                    const __half2 *h2 = reinterpret_cast<const __half2 *>(&kraw[g4][i]);
+            for (int i = 0; i < DPL / 8; ++i) {
+                const __half2 *h2 = reinterpret_cast<const __half2 *>(&kraw[g4][i]);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 f = __half22float2(h2[e]);
-                        kf[8 * i + 2 * e] = f.x;
-                        kf[8 * i + 2 * e + 1] = f.y;
-                    }
-                }
-#pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    float d = 0.f;
-#pragma unroll
-                    for (int i = 0; i < DPL; ++i) d = fmaf(qr[g][i], kf[i], d);
-                    s[g] = d;
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = __half22float2(h2[e]);
+                    kf[8 * i + 2 * e] = f.x;
+                    kf[8 * i + 2 * e + 1] = f.y;
                 }
             }
 #pragma unroll
             for (int g = 0; g < G; ++g) {
-                float d = s[g];
+                float d = 0.f;
+#pragma unroll
+                for (int i = 0; i < DPL; ++i) d = fmaf(qr[g][i], kf[i], d);
                 d += __shfl_xor_sync(0xffffffffu, d, 1);
                 d += __shfl_xor_sync(0xffffffffu, d, 2);
                 d += __shfl_xor_sync(0xffffffffu, d, 4);
-                s[g] = valid ? d : -CUDART_INF_F;
+                s[g4][g] = valid ? d : -CUDART_INF_F;
             }
-            // online softmax over the 4 cells of the group
-            float p[G];
+        }
+        // one online-softmax step over the 16 cells (cell j0 is always valid: m stays finite)
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
-                float mx = s[g];
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-                const float mn = fmaxf(m[g], mx);
-                const float alpha = expf(m[g] - mn);
-                p[g] = expf(s[g] - mn);
-                float ps = p[g];
-                ps += __shfl_xor_sync(0xffffffffu, ps, 8);
-                ps += __shfl_xor_sync(0xffffffffu, ps, 16);
-                l[g] = l[g] * alpha + ps;   // lanes l, l^8, l^16, l^24 hold the group's 4 cells
-                m[g] = mn;
+        for (int g = 0; g < G; ++g) {
+            float mx = fmaxf(fmaxf(s[0][g], s[1][g]), fmaxf(s[2][g], s[3][g]));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+            const float mn = fmaxf(m[g], mx);
+            const float alpha = ex2_approx(m[g] - mn);
+            float ps = 0.f;
 #pragma unroll
-                for (int i = 0; i < DPV; ++i) acc[g][i] *= alpha;
+            for (int g4 = 0; g4 < 4; ++g4) {
+                s[g4][g] = ex2_approx(s[g4][g] - mn);   // now the weight p of the cell
+                ps += s[g4][g];
             }
-            // P.V: lane owns dims lane * DPV .. + DPV
+            ps += __shfl_xor_sync(0xffffffffu, ps, 8);
+            ps += __shfl_xor_sync(0xffffffffu, ps, 16);
+            l[g] = l[g] * alpha + ps;   // lanes l, l^8, l^16, l^24 hold the group's 4 cells
+            m[g] = mn;
+#pragma unroll
+            for (int i = 0; i < DPV; ++i) acc[g][i] *= alpha;
+        }
+        // P.V: lane owns dims lane * DPV .. + DPV
+#pragma unroll
+        for (int g4 = 0; g4 < 4; ++g4) {
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 if (j0 + 4 * g4 + c >= c1) break;
@@ -173,13 +179,13 @@ __global__ void __launch_bounds__(128) k_attn(const FwdArgs a, const int layer, 
                 }
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
-                    const float pc = __shfl_sync(0xffffffffu, p[g], 8 * c);
+                    const float pc = __shfl_sync(0xffffffffu, s[g4][g], 8 * c);
 #pragma unroll
                     for (int i = 0; i < DPV; ++i) acc[g][i] = fmaf(pc, vf[i], acc[g][i]);
                 }
             }
         }
-        };
+    };
     for (int j0 = j_first; j0 < c1; j0 += 128) {
         if (j0 + 64 < c1) load_sg(j0 + 64, false, kB, vB);
         consume(j0, kA, vA);
@@ -211,7 +217,7 @@ __global__ void __launch_bounds__(128) k_attn(const FwdArgs a, const int layer, 
         float L = 0.f, A = 0.f;
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
-            const float f = sm_m[w][g] == -CUDART_INF_F ? 0.f : expf(sm_m[w][g] - M);
+            const float f = sm_m[w][g] == -CUDART_INF_F ? 0.f : exp2f(sm_m[w][g] - M);
             L += sm_l[w][g] * f;
             A += sm_acc[w][g][dd] * f;
         }
@@ -245,7 +251,7 @@ __global__ void __launch_bounds__(128) k_attn(const FwdArgs a, const int layer, 
         return;
     }
     __threadfence();
-    // merge weights of the splits: w_s = exp(M_s - M*) / L*, one warp per query head
+    // merge weights of the splits: w_s = 2^(M_s - M*) / L*, one warp per query head
     __shared__ float sw[64][G];
     for (int g = warp; g < G; g += 4) {
         float ms[2], ls[2];
@@ -262,7 +268,7 @@ __global__ void __launch_bounds__(128) k_attn(const FwdArgs a, const int layer, 
         float e[2], L = 0.f;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            e[h] = lane + 32 * h < ns_t ? expf(ms[h] - M) : 0.f;
+            e[h] = lane + 32 * h < ns_t ? exp2f(ms[h] - M) : 0.f;
             L += e[h] * ls[h];
         }
 #pragma unroll
