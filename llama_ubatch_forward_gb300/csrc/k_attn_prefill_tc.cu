@@ -351,9 +351,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 tmem_ld32_issue(tl + O_COL + c * 32, ov);
                 tmem_ld_wait(ov);
                 if (valid) {
+                    // the row's 32 dims as f16 high + low parts, 16-byte stores (8 dims each)
                     const size_t oi = (size_t)(tok0 + lane) * qw + head * HD + c * 32;
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) store_split(a.o16, a.o16_lo, oi + i, __uint_as_float(ov[i]) * inv);
+                    for (int v8 = 0; v8 < 4; ++v8) {
+                        uint32_t hi[4], lo[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            split_pack(__uint_as_float(ov[8 * v8 + 2 * e]) * inv, __uint_as_float(ov[8 * v8 + 2 * e + 1]) * inv,
+                                       hi[e], lo[e]);
+                        *reinterpret_cast<uint4 *>(a.o16 + oi + 8 * v8) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                        *reinterpret_cast<uint4 *>(a.o16_lo + oi + 8 * v8) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                    }
                 }
             }
         }
