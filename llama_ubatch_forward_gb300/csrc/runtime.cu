@@ -678,20 +678,18 @@ cudaError_t upload_meta(lcx_ctx *c, const Plan &P, const Ub &u, UbDev &ub) {
 
 enum { PC_GEMV = 0, PC_GEMM = 1, PC_ATTN = 2, PC_OTHER = 3 };
 
-// The tensor-core prefill attention where its shape fits (4 query heads per KV head, head_dim 64
-// or 128) and the ubatch attends at least kAttnTcMinCells positions: below that the mma.sync
-// kernel (a CTA per 64 tokens and query head: twice the CTAs) fills the SMs better and was
-// measured faster (1B shape, 512-token prompt: 27 vs 35 us a layer; 8B shape, ubatches of 512 up
-// to position 2048: equal; 32768-token prompt: twice as fast on tcgen05). LCX_ATTN_MMA_SYNC=1
-// selects the mma.sync kernel everywhere (same results up to summation order), for cross-checking
-// the two on a device.
-constexpr int kAttnTcMinCells = 1024;
-static bool attention_prefill_tc(const FwdArgs &a, int max_natt) {
+// The tensor-core (tcgen05) prefill attention wherever its shape fits (4 query heads per KV head,
+// head_dim 64 or 128): measured faster than the mma.sync kernel at every length of the named
+// workloads (1B shape, 512-token prompt: 19 vs 27 us a layer; 8B shape, ubatches of 512 up to
+// position 2048: 4.9 vs 9.4 ms for the prompt; 32768-token prompt: 0.61 vs 1.35 s).
+// LCX_ATTN_MMA_SYNC=1 selects the mma.sync kernel everywhere (same results up to summation order),
+// for cross-checking the two on a device.
+static bool attention_prefill_tc(const FwdArgs &a) {
     static const bool mma_sync = [] {
         const char *e = getenv("LCX_ATTN_MMA_SYNC");
         return e && e[0] == '1';
     }();
-    return !mma_sync && max_natt >= kAttnTcMinCells && attention_prefill_tc_fits(a);
+    return !mma_sync && attention_prefill_tc_fits(a);
 }
 
 // Brackets one launch with events when profiling is on; in trace mode gives the launch a slot of
@@ -787,7 +785,7 @@ cudaError_t run_forward(lcx_ctx *c, FwdArgs &a, int max_natt, double att_cells, 
             // long runs of one sequence (prefill): tensor-core tiles; single tokens: split-K
             const bool tiles = !gemv && a.ub.n_qtiles > 0 && a.ub.n_qtiles * 8 <= a.T;
             e = !tiles ? launch_attention(a, l, max_natt, !gemv, s, nl)
-                : attention_prefill_tc(a, max_natt) ? launch_attention_prefill_tc(a, l, s, nl)
+                : attention_prefill_tc(a) ? launch_attention_prefill_tc(a, l, s, nl)
                                           : launch_attention_prefill(a, l, s, nl);
         }
         if (e == cudaSuccess) {

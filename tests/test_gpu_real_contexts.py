@@ -10,8 +10,8 @@ acceptance bar (per-row relative L2 <= 5e-3, argmax equal where the oracle's top
 1e-2):
 
   * 8B shape, 2 layers: a 2048-token prompt in ubatches of 512 (the tensor-core matmuls with
-    128-token tiles for gate/up, asserted through the launch counter; prefill flash attention on
-    mma.sync for the first ubatch and on tcgen05 from position 1024 on),
+    128-token tiles for gate/up, asserted through the launch counter; tcgen05 prefill flash
+    attention),
     then 8 decode steps at positions 2048+ (the persistent one-token step: Q4_0, head_dim 128,
     4 query heads per KV head, attention split over many CTAs);
   * 8B shape, 1 layer: the long-context workload's 32768-token prompt in ubatches of 2048, then
@@ -19,8 +19,8 @@ acceptance bar (per-row relative L2 <= 5e-3, argmax equal where the oracle's top
   * 8B shape, 1 layer: 64 sequences in one cache with prompt lengths drawn as the 64-sequence
     workload draws them, divided by 4 (to bound the oracle's time), each prefilled in ubatches of
     512, then 2 steps of one 64-token ubatch (one token per sequence, every row flagged);
-  * 1B shape, 2 layers: a 1536-token prompt in ubatches of 512 (head_dim 64 on the tensor-core
-    prefill attention);
+  * 1B shape, 2 layers: a 1536-token prompt in ubatches of 512 (head_dim 64 on the tcgen05
+    prefill attention across ubatches);
   * 1B shape, all 16 layers: a 512-token prompt in one ubatch, then 4 decode steps.
 """
 import dataclasses
@@ -144,8 +144,8 @@ def test_8b_one_layer_64_sequences(host8):
 
 
 def test_1b_two_layers_1536_prompt():
-    # head_dim 64 on the tensor-core prefill attention (ubatches of 512 up to position 1536: the
-    # last two attend at least 1024 cells)
+    # head_dim 64 on the tensor-core prefill attention over three ubatches of 512 (query tiles
+    # that reach back across earlier ubatches' pages)
     cfg = synth.CONFIGS["1b"]
     lcx.build()
     oracle.set_threads()
@@ -198,3 +198,42 @@ def test_1b_full_depth_512_prompt_then_decode():
             break
         assert gen[i] == int(a1[0]), (i, gen)
         tok = int(a1[0])
+
+
+_MMA_SYNC_CHILD = r"""
+import numpy as np
+import oracle, synth
+import llama_ubatch_forward_gb300 as lcx
+from llama_ubatch_forward_gb300.torch_io import upload
+from gpu_common import check_rows, gpu_decode
+cfg = synth.CONFIGS["1b"]
+lcx.build()
+oracle.set_threads()
+host = synth.make_model(cfg, n_layer=2)
+gm, om = upload(host), oracle.Model(host)
+n = 1024
+prompt = synth.prompt_tokens(cfg, n)
+flags = np.zeros(n, np.int8)
+flags[[0, 511, 512, 900, 1023]] = 1
+octx = oracle.Context(om, cfg.n_ctx, 1, 512)
+ctx = lcx.Context(gm, cfg.n_ctx, 1, 512)
+rc, ref, am = octx.decode(prompt, logits=flags)
+rc2, lg, am2 = gpu_decode(ctx, cfg.n_vocab, prompt, flags=flags)
+assert rc == rc2 == 0
+print("max err", check_rows(lg, am2, ref, am, "mma.sync attention"))
+"""
+
+
+def test_mma_sync_prefill_attention_on_the_1b_shape():
+    # LCX_ATTN_MMA_SYNC=1 (read once per process, hence a child process) puts the 1B shape's
+    # prefill attention on the mma.sync kernel, which otherwise serves only other head groupings
+    import os
+    import subprocess
+    import sys
+    here = os.path.dirname(os.path.abspath(__file__))
+    env = dict(os.environ, LCX_ATTN_MMA_SYNC="1",
+               PYTHONPATH=os.pathsep.join([here, os.path.dirname(here), os.environ.get("PYTHONPATH", "")]))
+    r = subprocess.run([sys.executable, "-c", _MMA_SYNC_CHILD], env=env, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-4000:]
+    assert "max err" in r.stdout
