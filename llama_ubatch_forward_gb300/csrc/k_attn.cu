@@ -6,12 +6,14 @@
 // of the cell range) and all n_head / n_head_kv query heads that share that KV head, so each K
 // and V row is read once for the whole group.
 //
-// Inside a CTA, 4 warps take interleaved groups of 4 cells; 8 lanes share a cell's K row for
-// the Q.K dot products (reduced with shuffles), the scores go through an online softmax, and
-// lanes own head_dim/32 output dims for the P.V accumulation. The CTA's 4 warp states are
-// merged in shared memory. With several splits, every CTA writes its partial (max, sum, acc)
-// and the last CTA of a (token, KV head) to arrive -- an arrival counter, no waiting -- merges
-// the partials in split order and writes the output. The counter is reset by that CTA.
+// Inside a CTA, 4 warps take interleaved key tiles of 16 cells, staged by cp.async into a ring of
+// three tiles per warp; the products run on the tensor cores (mma.sync m16n8k16, f16 in, f32
+// accumulate) with the query heads as the MMA rows: S = Q K^T (q as f16 high + low parts, pre-
+// scaled into the log2 domain), one online-softmax step per tile, O += P V (P as f16 high + low
+// parts). The CTA's 4 warp states are merged in shared memory. With several splits, every CTA
+// writes its partial (max, sum, acc) and the last CTA of a (token, KV head) to arrive -- an
+// arrival counter, no waiting -- merges the partials in split order and writes the output. The
+// counter is reset by that CTA.
 #include <math_constants.h>
 
 #include "epilogue.cuh"
@@ -27,182 +29,201 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
+// mma.sync m16n8k16 (f16 in, f32 accumulate) and its operand loads, as in the prefill kernel
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+// f16 high part of x and the f16 rounding of the rest, packed for two elements (x0 in the low half)
+__device__ __forceinline__ void split2(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+    const __half2 h = __floats2half2_rn(x0, x1);
+    const float2 hf = __half22float2(h);
+    const __half2 l = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
+    hi = *reinterpret_cast<const uint32_t *>(&h);
+    lo = *reinterpret_cast<const uint32_t *>(&l);
+}
+
+constexpr int AT_CELLS = 16;   // cells of a key tile
+constexpr int AT_STAGES = 3;   // key tiles in flight per warp
+
+template <int HD>
+constexpr int attn_smem_bytes() { return 4 /* warps */ * AT_STAGES * 2 * AT_CELLS * HD * 2; }
+
+// byte offset of 16-byte chunk c of row r in a [16][HD] f16 tile, chunks XOR-swizzled by row
+template <int HD>
+__device__ __forceinline__ uint32_t at_off(int r, int c) {
+    return (uint32_t)(r * HD * 2 + ((c ^ (r & 7)) << 4));
+}
+
 template <int HD, int G, bool OUT16>
 __global__ void __launch_bounds__(128) k_attn(const FwdArgs a, const int layer, const int chunk, const int n_split) {
-    constexpr int DPL = HD / 8;    // dims per lane in Q.K (8 lanes per cell)
-    constexpr int DPV = HD / 32;   // dims per lane in P.V
+    constexpr int CH = HD / 8;                 // 16-byte chunks of a K or V row
+    constexpr int TILE = AT_CELLS * HD * 2;    // bytes of a K or V tile
     const int t = blockIdx.z, kvh = blockIdx.y, sp = blockIdx.x;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g = lane >> 2, tq = lane & 3;    // fragment row (query head) and column pair
     LCX_TRACE(a, 0);
-    // The ubatch metadata, the page table and the cells of positions <= pos - T (stored by earlier
-    // ubatches) do not depend on the preceding kernel, which writes q and this ubatch's cells: each
-    // warp loads its first 16 cells into registers before waiting for that kernel, and re-reads
-    // afterwards only the cells this ubatch may have written.
     const int pos = a.ub.pos[t], seq = a.ub.seq[t];
     const int n_att = pos + 1;
     const int ns_t = (n_att + chunk - 1) / chunk;
     const int c0 = sp * chunk, c1 = min(c0 + chunk, n_att);
-    const int sub = lane & 7, cgrp = lane >> 3;
     const int32_t *ptrow = a.pt + (size_t)seq * a.max_pages_per_seq;
     const size_t layer_base = (size_t)layer * a.n_pages;
     const int fresh = n_att - a.T;   // cells at positions >= fresh may come from this ubatch
-    // two buffers of one super-group's K/V each: the next super-group's loads are in flight while
-    // the current one is used
-    uint4 kA[4][DPL / 8], kB[4][DPL / 8];
-    uint2 vA[16], vB[16];
-    // K/V of the super-group of 16 cells at j0 (inside one page) into (kraw, vraw); `only_fresh`
-    // re-reads just the cells this ubatch may have written
-    auto load_sg = [&](int j0, bool only_fresh, uint4 (&kraw)[4][DPL / 8], uint2 (&vraw)[16]) {
+    extern __shared__ __align__(128) uint8_t at_sm[];
+    const uint32_t wbase = (uint32_t)__cvta_generic_to_shared(at_sm) + warp * AT_STAGES * 2 * TILE;
+
+    // Warp w takes the 16-cell key tiles at c0 + 16 w + 64 i (each inside one page), staged by
+    // cp.async into a ring of AT_STAGES (K, V) tiles. Cells past c1 repeat cell c1 - 1 (finite
+    // values; their scores are masked), so that P = 0 times V is 0.
+    const int j_first = c0 + AT_CELLS * warp;
+    const int n_mine = j_first < c1 ? (c1 - j_first + 4 * AT_CELLS - 1) / (4 * AT_CELLS) : 0;
+    auto load_tile = [&](int i) {   // this warp's i-th tile into stage i % AT_STAGES
+        const int j0 = j_first + i * 4 * AT_CELLS;
         const int page = ptrow[j0 / kPage];
         const size_t row0 = ((layer_base + page) * a.KV + kvh) * kPage + (j0 % kPage);
+        const uint32_t kd = wbase + (i % AT_STAGES) * 2 * TILE, vd = kd + TILE;
 #pragma unroll
-        for (int g4 = 0; g4 < 4; ++g4) {
-            const int j = j0 + 4 * g4 + cgrp;
-            if (only_fresh && (j < fresh || j >= c1)) continue;
-            if (j < c1) {
-                const __half *kp = a.kc + (row0 + 4 * g4 + cgrp) * HD + sub * DPL;
-#pragma unroll
-                for (int i = 0; i < DPL / 8; ++i) kraw[g4][i] = *reinterpret_cast<const uint4 *>(kp + 8 * i);
-            } else {
-#pragma unroll
-                for (int i = 0; i < DPL / 8; ++i) kraw[g4][i] = make_uint4(0, 0, 0, 0);
-            }
-        }
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-            const int j = j0 + c;
-            if (only_fresh && j < fresh) continue;
-            if (j < c1) {
-                const __half *vp = a.vc + (row0 + c) * HD + lane * DPV;
-                if (DPV == 4) vraw[c] = *reinterpret_cast<const uint2 *>(vp);
-                else vraw[c] = make_uint2(*reinterpret_cast<const uint32_t *>(vp), 0u);
-            }
+        for (int u = 0; u < AT_CELLS * CH / 32; ++u) {
+            const int idx = u * 32 + lane, r = idx / CH, c = idx % CH;
+            const int rr = min(j0 + r, c1 - 1) - j0;   // a cell past c1 repeats the last one
+            cp_async16(kd + at_off<HD>(r, c), a.kc + (row0 + rr) * HD + c * 8);
+            cp_async16(vd + at_off<HD>(r, c), a.vc + (row0 + rr) * HD + c * 8);
         }
     };
-    const int j_first = c0 + warp * 16;
-    if (sp < ns_t && j_first < c1) load_sg(j_first, false, kA, vA);
+    // The cells of positions < fresh were stored by earlier ubatches and do not depend on the
+    // preceding kernel: the first tile is requested before waiting for it when it holds none of
+    // this ubatch's cells.
+    const bool early = sp < ns_t && n_mine > 0 && j_first + AT_CELLS <= fresh;
+    if (early) load_tile(0);
     LCX_PDL_WAIT();
     LCX_PDL_TRIGGER();
     LCX_TRACE(a, 1);
     if (sp >= ns_t) return;
-    if (j_first < c1 && j_first + 16 > fresh) load_sg(j_first, true, kA, vA);
+    if (n_mine > 0 && !early) load_tile(0);
+    cp_commit();
+#pragma unroll
+    for (int i = 1; i < AT_STAGES - 1; ++i) {
+        if (i < n_mine) load_tile(i);
+        cp_commit();
+    }
     const int qw = a.H * HD;
+
+    // Q as the A operand: rows = the G query heads of this KV head (rows >= G zero), pre-scaled
+    // by log2(e) / sqrt(hd), f16 high + low parts
     const float scale = rsqrtf((float)HD) * 1.4426950408889634f;   // scores in the log2 domain
+    uint32_t qa_hi[HD / 16][4], qa_lo[HD / 16][4];
+    {
+        const bool row_ok = g < G;
+        const float *qp = a.q + (size_t)t * qw + (size_t)(kvh * G + (row_ok ? g : 0)) * HD;
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) {
+            const int c0d = kk * 16 + 2 * tq, c1d = c0d + 8;
+            const float2 x0 = row_ok ? *reinterpret_cast<const float2 *>(qp + c0d) : make_float2(0.f, 0.f);
+            const float2 x1 = row_ok ? *reinterpret_cast<const float2 *>(qp + c1d) : make_float2(0.f, 0.f);
+            split2(x0.x * scale, x0.y * scale, qa_hi[kk][0], qa_lo[kk][0]);
+            split2(x1.x * scale, x1.y * scale, qa_hi[kk][2], qa_lo[kk][2]);
+            qa_hi[kk][1] = qa_lo[kk][1] = qa_hi[kk][3] = qa_lo[kk][3] = 0u;   // rows g + 8
+        }
+    }
+    float o[HD / 8][4];
+#pragma unroll
+    for (int d = 0; d < HD / 8; ++d) o[d][0] = o[d][1] = o[d][2] = o[d][3] = 0.f;
+    float mrow = -CUDART_INF_F, lrow = 0.f;   // row g's running maximum and (this thread's) sum
 
-    // this lane's Q slice for the QK step: dims (lane % 8) * DPL .. + DPL, pre-scaled
-    float qr[G][DPL];
+    for (int i = 0; i < n_mine; ++i) {
+        if (i + AT_STAGES - 1 < n_mine) load_tile(i + AT_STAGES - 1);
+        cp_commit();
+        cp_wait<AT_STAGES - 1>();
+        __syncwarp();
+        const int j0 = j_first + i * 4 * AT_CELLS;
+        const uint32_t kb = wbase + (i % AT_STAGES) * 2 * TILE, vb = kb + TILE;
+        // S = Q K^T for the tile's 16 cells (two n-tiles of 8)
+        float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-        const float *qp = a.q + (size_t)t * qw + (size_t)(kvh * G + g) * HD + sub * DPL;
-#pragma unroll
-        for (int i = 0; i < DPL; i += 4) {
-            const float4 v = *reinterpret_cast<const float4 *>(qp + i);
-            qr[g][i] = v.x * scale; qr[g][i + 1] = v.y * scale; qr[g][i + 2] = v.z * scale; qr[g][i + 3] = v.w * scale;
+        for (int kk = 0; kk < HD / 16; ++kk) {
+            const int mm = lane >> 3, rr = lane & 7;
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(kb + at_off<HD>(8 * (mm >> 1) + rr, 2 * kk + (mm & 1)), b0, b1, b2, b3);
+            mma16816(sc[0], qa_hi[kk], b0, b1);
+            mma16816(sc[0], qa_lo[kk], b0, b1);
+            mma16816(sc[1], qa_hi[kk], b2, b3);
+            mma16816(sc[1], qa_lo[kk], b2, b3);
         }
+        // cells past c1 masked; one online-softmax step for the tile (row g: this quad's 4 lanes)
+        float mx = -CUDART_INF_F;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                if (j0 + 8 * nt + 2 * tq + e >= c1) sc[nt][e] = -CUDART_INF_F;
+                mx = fmaxf(mx, sc[nt][e]);
+            }
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float mn = fmaxf(mrow, mx);   // finite: the tile's first cell is valid
+        const float alpha = ex2_approx(mrow - mn);
+        mrow = mn;
+        uint32_t pa_hi[4], pa_lo[4];
+        {
+            const float p00 = ex2_approx(sc[0][0] - mn), p01 = ex2_approx(sc[0][1] - mn);
+            const float p10 = ex2_approx(sc[1][0] - mn), p11 = ex2_approx(sc[1][1] - mn);
+            lrow = lrow * alpha + (p00 + p01 + p10 + p11);
+            split2(p00, p01, pa_hi[0], pa_lo[0]);   // row g, cells 2tq, 2tq+1
+            split2(p10, p11, pa_hi[2], pa_lo[2]);   // row g, cells 8 + 2tq, 8 + 2tq + 1
+            pa_hi[1] = pa_lo[1] = pa_hi[3] = pa_lo[3] = 0u;
+        }
+#pragma unroll
+        for (int d = 0; d < HD / 8; ++d) {
+            o[d][0] *= alpha;
+            o[d][1] *= alpha;
+        }
+        // O += P V (16 cells: one k-step; n-tiles of 8 dims)
+#pragma unroll
+        for (int d = 0; d < HD / 8; d += 2) {
+            const int mm = lane >> 3, rr = lane & 7;
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4_t(vb + at_off<HD>(8 * (mm & 1) + rr, d + (mm >> 1)), b0, b1, b2, b3);
+            mma16816(o[d], pa_hi, b0, b1);
+            mma16816(o[d], pa_lo, b0, b1);
+            mma16816(o[d + 1], pa_hi, b2, b3);
+            mma16816(o[d + 1], pa_lo, b2, b3);
+        }
+        __syncwarp();   // the stage is refilled AT_STAGES - 1 tiles later
     }
-    float m[G], l[G], acc[G][DPV];
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-        m[g] = -CUDART_INF_F;
-        l[g] = 0.f;
-#pragma unroll
-        for (int i = 0; i < DPV; ++i) acc[g][i] = 0.f;
-    }
-
-    // Each warp takes super-groups of 16 consecutive cells (inside one 64-cell page): all K and
-    // V loads of a super-group are issued before any of them is used, one super-group ahead. The
-    // 16 cells' scores are computed first and take one online-softmax step together (one
-    // maximum, one rescaling of the accumulators), in the log2 domain (q carries log2(e)).
-    auto consume = [&](int j0, const uint4 (&kraw)[4][DPL / 8], const uint2 (&vraw)[16]) {
-        float s[4][G];   // cell j0 + 4 g4 + cgrp, query head g (every lane of the cell holds it)
-#pragma unroll
-        for (int g4 = 0; g4 < 4; ++g4) {
-            const bool valid = j0 + 4 * g4 + cgrp < c1;
-            float kf[DPL];
-#pragma unroll
-            for (int i = 0; i < DPL / 8; ++i) {
-                const __half2 *h2 = reinterpret_cast<const __half2 *>(&kraw[g4][i]);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 f = __half22float2(h2[e]);
-                    kf[8 * i + 2 * e] = f.x;
-                    kf[8 * i + 2 * e + 1] = f.y;
-                }
-            }
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-                float d = 0.f;
-#pragma unroll
-                for (int i = 0; i < DPL; ++i) d = fmaf(qr[g][i], kf[i], d);
-                d += __shfl_xor_sync(0xffffffffu, d, 1);
-                d += __shfl_xor_sync(0xffffffffu, d, 2);
-                d += __shfl_xor_sync(0xffffffffu, d, 4);
-                s[g4][g] = valid ? d : -CUDART_INF_F;
-            }
-        }
-        // one online-softmax step over the 16 cells (cell j0 is always valid: m stays finite)
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-            float mx = fmaxf(fmaxf(s[0][g], s[1][g]), fmaxf(s[2][g], s[3][g]));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-            const float mn = fmaxf(m[g], mx);
-            const float alpha = ex2_approx(m[g] - mn);
-            float ps = 0.f;
-#pragma unroll
-            for (int g4 = 0; g4 < 4; ++g4) {
-                s[g4][g] = ex2_approx(s[g4][g] - mn);   // now the weight p of the cell
-                ps += s[g4][g];
-            }
-            ps += __shfl_xor_sync(0xffffffffu, ps, 8);
-            ps += __shfl_xor_sync(0xffffffffu, ps, 16);
-            l[g] = l[g] * alpha + ps;   // lanes l, l^8, l^16, l^24 hold the group's 4 cells
-            m[g] = mn;
-#pragma unroll
-            for (int i = 0; i < DPV; ++i) acc[g][i] *= alpha;
-        }
-        // P.V: lane owns dims lane * DPV .. + DPV
-#pragma unroll
-        for (int g4 = 0; g4 < 4; ++g4) {
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                if (j0 + 4 * g4 + c >= c1) break;
-                const uint2 raw = vraw[4 * g4 + c];
-                float vf[DPV];
-                const float2 f0 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.x));
-                vf[0] = f0.x;
-                vf[1 % DPV] = f0.y;
-                if (DPV == 4) {
-                    const float2 f1 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.y));
-                    vf[2 % DPV] = f1.x;
-                    vf[3 % DPV] = f1.y;
-                }
-#pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    const float pc = __shfl_sync(0xffffffffu, s[g4][g], 8 * c);
-#pragma unroll
-                    for (int i = 0; i < DPV; ++i) acc[g][i] = fmaf(pc, vf[i], acc[g][i]);
-                }
-            }
-        }
-    };
-    for (int j0 = j_first; j0 < c1; j0 += 128) {
-        if (j0 + 64 < c1) load_sg(j0 + 64, false, kB, vB);
-        consume(j0, kA, vA);
-        if (j0 + 64 >= c1) break;
-        if (j0 + 128 < c1) load_sg(j0 + 128, false, kA, vA);
-        consume(j0 + 64, kB, vB);
-    }
+    cp_wait<0>();
+    lrow += __shfl_xor_sync(0xffffffffu, lrow, 1);
+    lrow += __shfl_xor_sync(0xffffffffu, lrow, 2);
 
     LCX_TRACE(a, 2);
     // ---- merge the 4 warps
     __shared__ float sm_m[4][G], sm_l[4][G];
     __shared__ float sm_acc[4][G][HD];
+    if (g < G) {
+        if (tq == 0) {
+            sm_m[warp][g] = n_mine > 0 ? mrow : -CUDART_INF_F;
+            sm_l[warp][g] = lrow;
+        }
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-        if (lane == 0) { sm_m[warp][g] = m[g]; sm_l[warp][g] = l[g]; }
-#pragma unroll
-        for (int i = 0; i < DPV; ++i) sm_acc[warp][g][lane * DPV + i] = acc[g][i];
+        for (int d = 0; d < HD / 8; ++d) {
+            sm_acc[warp][g][d * 8 + 2 * tq] = o[d][0];
+            sm_acc[warp][g][d * 8 + 2 * tq + 1] = o[d][1];
+        }
     }
     __syncthreads();
     // thread -> (g, dim) pairs
@@ -301,13 +322,17 @@ __global__ void __launch_bounds__(128) k_attn(const FwdArgs a, const int layer, 
 template <int HD, int G>
 cudaError_t run(const FwdArgs &a, int layer, int chunk, int ns, bool out16, cudaStream_t s) {
     dim3 grid(ns, a.KV, a.T);
+    constexpr int smem = attn_smem_bytes<HD>();
+    auto k16 = k_attn<HD, G, true>, k32 = k_attn<HD, G, false>;
+    cudaError_t e = func_attr_once((const void *)(out16 ? k16 : k32), cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
     if (!a.pdl) {   // stand-alone call: fully ordered after the caller's preceding work
-        if (out16) k_attn<HD, G, true><<<grid, 128, 0, s>>>(a, layer, chunk, ns);
-        else k_attn<HD, G, false><<<grid, 128, 0, s>>>(a, layer, chunk, ns);
+        if (out16) k16<<<grid, 128, smem, s>>>(a, layer, chunk, ns);
+        else k32<<<grid, 128, smem, s>>>(a, layer, chunk, ns);
         return cudaGetLastError();
     }
-    if (out16) return launch_pdl(k_attn<HD, G, true>, grid, dim3(128), 0, s, a, layer, chunk, ns);
-    return launch_pdl(k_attn<HD, G, false>, grid, dim3(128), 0, s, a, layer, chunk, ns);
+    if (out16) return launch_pdl(k16, grid, dim3(128), (size_t)smem, s, a, layer, chunk, ns);
+    return launch_pdl(k32, grid, dim3(128), (size_t)smem, s, a, layer, chunk, ns);
 }
 
 template <int HD>
