@@ -90,9 +90,22 @@ struct Cfg {
     // twice the products). With BN = 256 the two parts are accumulated into the same BN columns.
     static constexpr bool STACK = BN <= 128;
     static constexpr int ACC_COLS = STACK ? 2 * BN : BN;   // TMEM columns per weight tile
-    static constexpr int TMEM_COLS = MT * ACC_COLS <= 128 ? 128 : MT * ACC_COLS <= 256 ? 256 : 512;
-    static_assert(MT * ACC_COLS <= 512, "tensor memory holds 512 columns");
+    // 64 tokens x 2 tiles: the operands swap -- the activation tile's 128 rows (64 high, 64 low)
+    // are the MMA's M and both weight tiles (256 rows, contiguous in the A ring) its N, so a K
+    // step takes 4 MMAs of N = 256 instead of 8 of N = 128; TMEM lanes are then activation rows
+    // and columns weight rows, and the epilogue transposes the sums through shared memory
+    static constexpr bool SWAP = BN == 64 && MT == 2;
+    static constexpr int TMEM_NEED = SWAP ? MT * BM : MT * ACC_COLS;
+    static constexpr int TMEM_COLS = TMEM_NEED <= 128 ? 128 : TMEM_NEED <= 256 ? 256 : 512;
+    static_assert(TMEM_NEED <= 512, "tensor memory holds 512 columns");
     static_assert(BN <= 256, "one MMA covers at most 256 columns");
+    // SWAP: the transposed sums [MT * BM rows][BN + 1] f32 (a row padded by one float, so that
+    // the threads of a warp, one weight row each, read different banks) at the end of the
+    // staging space
+    static constexpr int T_LD = BN + 1;
+    static constexpr int T_OFF = (STAGE - MT * BM * T_LD * 4) / 16 * 16;
+    static_assert(!SWAP || (16 * BN + BN * 128 * 4 <= T_OFF && BN * MT * BM * 4 <= T_OFF),
+                  "staged operands and the transposed sums side by side");
 };
 
 struct GemmParams {
@@ -291,7 +304,7 @@ __global__ void __launch_bounds__(352, 1)
         // ---------------------------------------------------------------- MMA issuer
         if (lane == 0) {
             constexpr int NP = C::STACK ? 1 : 2;                      // MMAs per weight tile and k
-            constexpr uint32_t idesc = idesc_f16(BM, C::STACK ? 2 * BN : BN);
+            constexpr uint32_t idesc = C::SWAP ? idesc_f16(2 * BN, MT * BM) : idesc_f16(BM, C::STACK ? 2 * BN : BN);
             bool ok = true;
             for (int j = 0; j < nk; ++j) {
                 const int slot = j % SB, aslot = j % SA;
@@ -301,16 +314,25 @@ __global__ void __launch_bounds__(352, 1)
                 // stacked: one MMA over the high and low rows together (2 BN rows of B, 2 BN
                 // accumulator columns); otherwise W A_hi then W A_lo into the same BN columns. The
                 // weight tiles alternate so consecutive MMAs use different accumulators.
+                if (C::SWAP) {
+                    // D[act row][weight row] += A_act (128 rows: high then low) x W^T (256 rows)
+                    const uint32_t wbase = saddr(a_tile(aslot, 0));
 #pragma unroll
-                for (int kk = 0; kk < BK / 16; ++kk) {
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        mma_f16(tmem, sw128_desc(bbase + kk * 32), sw128_desc(wbase + kk * 32), idesc,
+                                (j > 0 || kk > 0) ? 1u : 0u);
+                } else {
 #pragma unroll
-                    for (int hl = 0; hl < NP; ++hl) {
+                    for (int kk = 0; kk < BK / 16; ++kk) {
 #pragma unroll
-                        for (int mt = 0; mt < MT; ++mt) {
-                            const uint32_t abase = saddr(a_tile(aslot, mt));
-                            mma_f16(tmem + mt * C::ACC_COLS, sw128_desc(abase + kk * 32),
-                                    sw128_desc(bbase + hl * BN * BK * 2 + kk * 32), idesc,
-                                    (j > 0 || kk > 0 || hl > 0) ? 1u : 0u);
+                        for (int hl = 0; hl < NP; ++hl) {
+#pragma unroll
+                            for (int mt = 0; mt < MT; ++mt) {
+                                const uint32_t abase = saddr(a_tile(aslot, mt));
+                                mma_f16(tmem + mt * C::ACC_COLS, sw128_desc(abase + kk * 32),
+                                        sw128_desc(bbase + hl * BN * BK * 2 + kk * 32), idesc,
+                                        (j > 0 || kk > 0 || hl > 0) ? 1u : 0u);
+                            }
                         }
                     }
                 }
@@ -365,8 +387,12 @@ __global__ void __launch_bounds__(352, 1)
         const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16) + my_mt * C::ACC_COLS;
         // the sums of 32 tokens (chunk cb) of this thread's row: W (A_hi + A_lo); both halves'
         // loads are in flight before the one wait
+        float *s_t = reinterpret_cast<float *>(smem + C::T_OFF);   // SWAP: [RW rows][T_LD]
         auto acc_ld = [&](int cb, uint32_t (&vv)[32]) {
-            if (C::STACK) {
+            if (C::SWAP) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) vv[i] = __float_as_uint(s_t[rc * C::T_LD + cb * 32 + i]);
+            } else if (C::STACK) {
                 uint32_t lo[32];
                 tmem_ld32_issue(tq + cb * 32, vv);
                 tmem_ld32_issue(tq + BN + cb * 32, lo);
@@ -380,6 +406,41 @@ __global__ void __launch_bounds__(352, 1)
             }
         };
         const int cb0 = MT == 2 ? 0 : (wt >> 7) * (BN / 64), cb1 = MT == 2 ? BN / 32 : cb0 + BN / 64;
+
+        if (C::SWAP) {
+            // TMEM lane = activation row (lanes 0..63 the tokens' high parts, 64..127 their low
+            // parts), column = weight row. The low rows' warps store theirs transposed, then the
+            // high rows' warps add theirs: s_t[weight row][token] = W (A_hi + A_lo). A warp pair
+            // of a lane quarter takes half of the 256 columns each.
+            const int arow = q * 32 + lane;           // activation row of this thread's lane
+            const int col0 = (wt >> 7) * 128;         // this warp's half of the weight rows
+#pragma unroll
+            for (int pass = 0; pass < 2; ++pass) {
+                const bool mine = pass == 0 ? arow >= BN : arow < BN;   // warp-uniform
+                if (cta_ok && mine)
+                    for (int c = 0; c < 128; c += 64) {   // two 32-column loads before one wait
+                        uint32_t v0[32], v1[32];
+                        tmem_ld32_issue(tmem + ((uint32_t)(q * 32) << 16) + col0 + c, v0);
+                        tmem_ld32_issue(tmem + ((uint32_t)(q * 32) << 16) + col0 + c + 32, v1);
+                        tmem_ld_wait(v0);
+                        regs_ready(v1);
+                        const int tok = arow & (BN - 1);
+                        float *d0 = s_t + (col0 + c) * C::T_LD + tok;
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            float *a0 = d0 + i * C::T_LD, *a1 = d0 + (32 + i) * C::T_LD;
+                            if (pass == 0) {
+                                *a0 = __uint_as_float(v0[i]);
+                                *a1 = __uint_as_float(v1[i]);
+                            } else {
+                                *a0 += __uint_as_float(v0[i]);
+                                *a1 += __uint_as_float(v1[i]);
+                            }
+                        }
+                    }
+                epi_sync();
+            }
+        }
 
         // Operands of the epilogue staged in shared memory: once the accumulator is complete every
         // activation and weight tile has been consumed and no copy is in flight, so the A and B
@@ -541,11 +602,14 @@ __global__ void __launch_bounds__(352, 1)
                 // token groups of G tokens (a multiple of 32): the other splits' partials of the
                 // group and, for RESID, its residual rows, staged together
                 const int n_in = p.ks - 1 + (EPI == EPI_RESID ? 1 : 0);
-                const int stage_bytes = C::STAGE - (EPI == EPI_QKV ? 16 * BN + BN * 128 * 4 : 0);
+                // the staging space ends where the transposed sums begin (SWAP: they are the own
+                // split's sums, read while the others' are added)
+                const int stage_end = C::SWAP ? C::T_OFF : C::STAGE;
+                const int stage_bytes = stage_end - (EPI == EPI_QKV ? 16 * BN + BN * 128 * 4 : 0);
                 const int per_chunk = n_in * 32 * RW * 4;
                 int G = (stage_bytes / per_chunk) * 32;
                 G = G > BN ? BN : G;
-                uint8_t *sbase = smem + (EPI == EPI_QKV ? C::STAGE - stage_bytes : 0);
+                uint8_t *sbase = smem + (EPI == EPI_QKV ? stage_end - stage_bytes : 0);
                 if (G >= 32) {
                     for (int g0 = 0; g0 < BN; g0 += G) {
                         float *sp = reinterpret_cast<float *>(sbase);   // [n_in][G][RW]
@@ -595,6 +659,73 @@ __global__ void __launch_bounds__(352, 1)
                                 epilogue(cb, vv, sp + ((size_t)(p.ks - 1) * G + tb) * RW);
                             }
                         epi_sync();   // the group's staging space is reused by the next group
+                    }
+                } else if (stage_bytes / (32 * RW * 4) >= 1 + (EPI == EPI_RESID ? 1 : 0)) {
+                    // too many splits to stage all of one 32-token chunk: per chunk, the other
+                    // splits' partials in batches of as many as fit (in split order, added into
+                    // registers), the residual rows (RESID) in the last slot from the first batch
+                    constexpr int CB = 32 * RW * 4;                     // bytes of a staged chunk
+                    const int xs = EPI == EPI_RESID ? 1 : 0;
+                    const int per_batch = stage_bytes / CB - xs;
+                    float *sp = reinterpret_cast<float *>(sbase);     // [slot][32][RW]
+                    float *sxc = sp + (size_t)per_batch * 32 * RW;    // RESID: the chunk's x rows
+                    for (int cb = 0; cb < BN / 32; ++cb) {
+                        const bool mine = cta_ok && cb >= cb0 && cb < cb1;   // warp-uniform
+                        uint32_t own[32];
+                        if (mine) acc_ld(cb, own);
+                        float sum[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) sum[i] = 0.f;
+                        for (int z = 0; z < p.ks;) {
+                            // the batch: splits z .. ze - 1, at most per_batch of them other than ours
+                            int ze = z, n_other = 0;
+                            while (ze < p.ks && (ze == (int)blockIdx.z || n_other < per_batch)) {
+                                if (ze != (int)blockIdx.z) ++n_other;
+                                ++ze;
+                            }
+                            if (cta_ok) {
+                                constexpr int CPR = RW / 4;
+                                int slot = 0;
+                                for (int zz = z; zz < ze; ++zz) {
+                                    if (zz == (int)blockIdx.z) continue;
+                                    float *d = sp + (size_t)slot * 32 * RW;
+                                    for (int i = wt; i < 32 * CPR; i += 256) {
+                                        const int tt = i / CPR, c = i - tt * CPR;
+                                        const int t = tok0 + cb * 32 + tt, rr = row0[0] + 4 * c;
+                                        if (t < p.T && rr < p.N_pad)
+                                            cp_async16(saddr(d) + (uint32_t)i * 16,
+                                                       p.part + ((size_t)zz * p.T + t) * p.N_pad + rr);
+                                    }
+                                    ++slot;
+                                }
+                                if (EPI == EPI_RESID && z == 0) stage_x(cb * 32, 32, sxc);
+                                cp_async_wait_all();
+                            }
+                            epi_sync();
+                            if (mine) {
+                                int slot = 0;
+                                for (int zz = z; zz < ze; ++zz) {
+                                    if (zz == (int)blockIdx.z) {
+#pragma unroll
+                                        for (int i = 0; i < 32; ++i) sum[i] += __uint_as_float(own[i]);
+                                    } else {
+                                        const float *src = sp + (size_t)slot * 32 * RW + rc;
+#pragma unroll
+                                        for (int i = 0; i < 32; ++i) sum[i] += src[i * RW];
+                                        ++slot;
+                                    }
+                                }
+                            }
+                            epi_sync();   // the slots are restaged by the next batch
+                            z = ze;
+                        }
+                        if (mine) {
+                            uint32_t vv[32];
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) vv[i] = __float_as_uint(sum[i]);
+                            epilogue(cb, vv, sxc);
+                        }
+                        epi_sync();   // the x slot is restaged for the next chunk
                     }
                 } else if (cta_ok) {
                     // too many splits to stage one chunk: the partials straight from L2

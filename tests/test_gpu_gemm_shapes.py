@@ -34,8 +34,12 @@ BASE = dataclasses.replace(synth.CONFIGS["tiny"], name="gemm-shapes", index=11, 
 T = 300
 FLAGGED = np.sort(np.random.default_rng(5).choice(T, 40, replace=False))
 # (bn, mt, ks): the five compiled shapes, and splits of the K steps (ks 3 applies to the down
-# projection's 24 steps only: 8 steps in 3 splits leave fewer than 4 a split, so those run whole)
-SHAPES = [(64, 1, 1), (64, 2, 1), (128, 1, 1), (128, 2, 1), (256, 1, 1), (128, 2, 2), (64, 1, 3), (256, 1, 2)]
+# projection's 24 steps only: 8 steps in 3 splits leave fewer than 4 a split, so those run whole);
+# 64 x 2 runs with the operands swapped (the sums transposed through shared memory), also split;
+# 6 splits of the down projection (and 3 with Q8_0 at 64 x 2) stage the other splits' partial
+# sums in batches
+SHAPES = [(64, 1, 1), (64, 2, 1), (128, 1, 1), (128, 2, 1), (256, 1, 1), (128, 2, 2), (64, 1, 3), (256, 1, 2),
+          (64, 2, 2), (64, 2, 3), (128, 2, 6)]
 
 _cache = {}
 
