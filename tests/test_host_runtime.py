@@ -213,3 +213,12 @@ def test_split_equal_failures_roll_back_like_the_oracle():
         assert [hc.seq_pos_max(s) for s in range(3)] == [oc.seq_pos_max(s) for s in range(3)], (where, k)
     hc = _host_ctx(n_ctx=256, n_seq=3, n_ubatch=4)
     assert hc.decode([1], seq_id=[0]) == 0 and hc.set_kv_unified(False) == lcx.LCX_INVALID   # cells held
+
+
+def test_gemm_tile_forcing_accepts_only_compiled_shapes():
+    # the prefill GEMM's tile-shape override is host state: no device needed to set or reject it
+    for good in ((64, 1, 1), (64, 2, 3), (128, 1, 8), (128, 2, 2), (256, 1, 1)):
+        assert lcx.set_gemm_tile(*good) == lcx.LCX_OK, good
+    for bad in ((32, 1, 1), (256, 2, 1), (128, 3, 1), (128, 1, 0), (128, 1, 9), (96, 1, 1)):
+        assert lcx.set_gemm_tile(*bad) == lcx.LCX_INVALID, bad
+    assert lcx.set_gemm_tile(0) == lcx.LCX_OK
