@@ -178,6 +178,14 @@ __device__ __forceinline__ void attn_prefetch(const FwdArgs &a, int layer, int k
 // ---------------------------------------------------------------- attention
 constexpr int kMaxUnitPages = 64;   // page ids of an attention unit kept in shared memory
 
+// 2^x by the hardware approximation (relative error about 2^-22; results below 2^-126 flush to
+// 0): the attention's scores and maxima are kept in the log2 domain
+__device__ __forceinline__ float step_ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // K and V of 4 consecutive cells (inside one page), in registers: lanes 8c..8c+7 hold K dims
 // (lane & 7) * HD / 8 .. of cell c; lane l holds V dims l * HD / 32 .. of cells 0..3.
 template <int HD>
@@ -230,7 +238,7 @@ __device__ __forceinline__ void step_attention(const FwdArgs &a, int layer, int 
     const int n_att = a.ub.pos[0] + 1;
     const int c0 = sp * chunk, c1 = min(c0 + chunk, n_att);
     const int sub = lane & 7, cg = lane >> 3;
-    const float scale = rsqrtf((float)HD);
+    const float scale = rsqrtf((float)HD) * 1.4426950408889634f;   // scores in the log2 domain
     const int j_first = c0 + 4 * warp;
     {   // re-read the queued group that holds the appended cell (warp-uniform)
         const int jf = (n_att - 1) & ~3, i = (jf - j_first) >> 5;
@@ -305,8 +313,8 @@ __device__ __forceinline__ void step_attention(const FwdArgs &a, int layer, int 
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
             const float mn = fmaxf(m[g], mx);
-            const float alpha = expf(m[g] - mn);
-            p[g] = expf(s[g] - mn);
+            const float alpha = step_ex2(m[g] - mn);
+            p[g] = step_ex2(s[g] - mn);
             float ps = p[g];
             ps += __shfl_xor_sync(0xffffffffu, ps, 8);
             ps += __shfl_xor_sync(0xffffffffu, ps, 16);
@@ -359,7 +367,7 @@ __device__ __forceinline__ void step_attention(const FwdArgs &a, int layer, int 
 #pragma unroll
         for (int w = 0; w < NW; ++w) {
             const float mw = sm_m[w * G + g];
-            const float f = mw == -CUDART_INF_F ? 0.f : expf(mw - M);
+            const float f = mw == -CUDART_INF_F ? 0.f : exp2f(mw - M);
             fac[w * G + g] = f;
             L += sm_l[w * G + g] * f;
         }
@@ -402,7 +410,7 @@ __device__ __forceinline__ void step_attention(const FwdArgs &a, int layer, int 
     consumer_sync();
     if (!*flag) return;
     // the partial sums of this thread's outputs for the first 24 splits are loaded first, so their
-    // round trip overlaps the one of the weights w_s = exp(M_s - M*) / L* (one warp per query
+    // round trip overlaps the one of the weights w_s = 2^(M_s - M*) / L* (one warp per query
     // head, lanes over splits)
     constexpr int PER = (G * HD + 255) / 256, NB = 24;
     float av[PER][NB];
@@ -430,7 +438,7 @@ __device__ __forceinline__ void step_attention(const FwdArgs &a, int layer, int 
         float e[2], L = 0.f;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            e[h] = lane + 32 * h < ns ? expf(ms[h] - M) : 0.f;
+            e[h] = lane + 32 * h < ns ? exp2f(ms[h] - M) : 0.f;
             L += e[h] * ls[h];
         }
 #pragma unroll
