@@ -32,10 +32,10 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the persistent
 # decode step over its algorithmic bytes, from one ncu capture of the current kernel on the 8B
-# shape cut to 4 layers (1057.9 MB read + 18.2 MB written against 1057.4 MB of stored weights and
+# shape cut to 4 layers (1057.9 MB read + 18.1 MB written against 1057.4 MB of stored weights and
 # attended K/V): the step's traffic grows with the layers and cells it processes, so the full
 # launch's traffic is this ratio times its algorithmic bytes.
-STEP_NCU_TRAFFIC_RATIO = (1057.894e6 + 18.201e6) / 1057.4e6
+STEP_NCU_TRAFFIC_RATIO = (1057.873e6 + 18.055e6) / 1057.4e6
 
 
 def log(*a):
