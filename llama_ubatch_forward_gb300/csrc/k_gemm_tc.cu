@@ -5,8 +5,9 @@
 // shared epilogues (RoPE + KV append, residual add, SwiGLU, logits + argmax).
 //
 // Prefill is where the work is compute-bound (KV-cache section of the article: prefill loads the
-// compute units), so the contraction runs on the 5th-generation tensor cores. One CTA computes two
-// 128-row weight tiles (adjacent rows, or a gate chunk and its up chunk) against BN tokens:
+// compute units), so the contraction runs on the 5th-generation tensor cores. One CTA computes MT
+// (1 or 2) 128-row weight tiles (adjacent rows, or gate chunks and their up chunks) against BN
+// tokens (64, 128 or 256), optionally a share of the K steps (split K):
 //   warp 0      TMA producer: one box per stage holds the quants and scales of both weight tiles
 //               (64 row quads of the quad-interleaved layout; issued before the grid-dependency
 //               wait: the weights do not depend on the previous kernel);
@@ -15,10 +16,13 @@
 //               adding the two halves; with BN = 256 into the same accumulator), so the
 //               activations keep about 22 bits and only the f16 rounding of the dequantised
 //               weights remains; each stage's tcgen05.commit frees its shared-memory slots;
+//               With 64 tokens and two tiles the operands swap (the activations' 128 rows as M,
+//               both weight tiles as N = 256) and the epilogue transposes the sums first;
 //   warps 2..9  dequantise the raw blocks (with two weight tiles warps 2..5 tile 0, warps 6..9
 //               tile 1) into the K-major SWIZZLE_128B f16 tile the MMA reads ((q - 8) or q is
 //               exact in f16, then one f16 multiply by the block scale); then run the epilogue
-//               from TMEM with tcgen05.ld;
+//               from TMEM with tcgen05.ld, its operands (RoPE rows, residual rows, other splits'
+//               partial sums) staged with cp.async in the ring space the main loop has freed;
 //   warp 10     loads the activation tiles [BN][64] f16 (high and low parts) with TMA into the
 //               SWIZZLE_128B layout, as many steps ahead as the activation ring holds. The CTAs of
 //               a cluster (CL consecutive weight tiles, one token tile) share every activation
