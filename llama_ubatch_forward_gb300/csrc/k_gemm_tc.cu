@@ -8,14 +8,14 @@
 // compute units), so the contraction runs on the 5th-generation tensor cores. One CTA computes MT
 // (1 or 2) 128-row weight tiles (adjacent rows, or gate chunks and their up chunks) against BN
 // tokens (64, 128 or 256), optionally a share of the K steps (split K):
-//   warp 0      TMA producer: one box per stage holds the quants and scales of both weight tiles
+//   warp 0      TMA producer: one box per stage holds the quants and scales of the weight tiles
 //               (64 row quads of the quad-interleaved layout; issued before the grid-dependency
 //               wait: the weights do not depend on the previous kernel);
 //   warp 1      allocates the TMEM accumulator and issues tcgen05.mma from one lane -- W A_hi and
 //               W A_lo (with BN <= 128 as one MMA over both parts' rows, N = 2 BN, the epilogue
 //               adding the two halves; with BN = 256 into the same accumulator), so the
 //               activations keep about 22 bits and only the f16 rounding of the dequantised
-//               weights remains; each stage's tcgen05.commit frees its shared-memory slots;
+//               weights remains; each stage's tcgen05.commit frees its shared-memory slots.
 //               With 64 tokens and two tiles the operands swap (the activations' 128 rows as M,
 //               both weight tiles as N = 256) and the epilogue transposes the sums first;
 //   warps 2..9  dequantise the raw blocks (with two weight tiles warps 2..5 tile 0, warps 6..9
