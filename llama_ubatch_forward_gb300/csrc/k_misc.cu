@@ -119,38 +119,60 @@ cudaError_t launch_get_rows(int type, const void *table, int64_t n_cols, const i
 }
 
 // ------------------------------------------------------------------ RMSNorm -> f16
-// out[r][:] = f16(x[row r] / sqrt(mean(x^2) + eps) * g); row r of x is rows[r] (or r).
+// out[r][:] = f16(x[row r] / sqrt(mean(x^2) + eps) * g) and out_lo[r][:] the f16 rounding of the
+// rest (about 22 bits together); row r of x is rows[r] (or r).
 __global__ void k_rmsnorm_h(const float *__restrict__ x, const int32_t *__restrict__ rows, int d,
                             const float *__restrict__ g, float eps, __half *__restrict__ out, __half *__restrict__ out_lo) {
     LCX_PDL_WAIT();
     LCX_PDL_TRIGGER();
     const int r = blockIdx.x;
     const float *xr = x + (int64_t)(rows ? rows[r] : r) * d;
+    // the row's first NV x 4 x blockDim values stay in registers between the two passes (the
+    // whole row for d <= 4096 with 256 threads); a longer row's rest is read twice
+    constexpr int NV = 4;
+    float4 v[NV];
     float ss = 0.f;
-    for (int i = threadIdx.x * 4; i < d; i += blockDim.x * 4) {
-        float4 v = *reinterpret_cast<const float4 *>(xr + i);
-        ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+        const int i = (threadIdx.x + k * blockDim.x) * 4;
+        v[k] = i < d ? *reinterpret_cast<const float4 *>(xr + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+        ss += v[k].x * v[k].x + v[k].y * v[k].y + v[k].z * v[k].z + v[k].w * v[k].w;
+    }
+    for (int i = (threadIdx.x + NV * blockDim.x) * 4; i < d; i += blockDim.x * 4) {
+        const float4 u = *reinterpret_cast<const float4 *>(xr + i);
+        ss += u.x * u.x + u.y * u.y + u.z * u.z + u.w * u.w;
     }
     __shared__ float red[32];
     for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
     __syncthreads();
     if (threadIdx.x < 32) {
-        float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
-        for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (threadIdx.x == 0) red[0] = v;
+        float w = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
+        for (int o = 16; o; o >>= 1) w += __shfl_xor_sync(0xffffffffu, w, o);
+        if (threadIdx.x == 0) red[0] = w;
     }
     __syncthreads();
     const float rs = 1.0f / sqrtf(red[0] / (float)d + eps);
-    for (int i = threadIdx.x * 4; i < d; i += blockDim.x * 4) {
-        const float4 v = *reinterpret_cast<const float4 *>(xr + i);
+    // 4 values as f16 high + low parts, one 8-byte store each (a warp writes 256 contiguous bytes)
+    auto emit = [&](int i, const float4 u) {
         const float4 gg = *reinterpret_cast<const float4 *>(g + i);
+        const float y0 = u.x * rs * gg.x, y1 = u.y * rs * gg.y, y2 = u.z * rs * gg.z, y3 = u.w * rs * gg.w;
+        const __half2 h01 = __floats2half2_rn(y0, y1), h23 = __floats2half2_rn(y2, y3);
+        const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+        const __half2 l01 = __floats2half2_rn(y0 - f01.x, y1 - f01.y), l23 = __floats2half2_rn(y2 - f23.x, y3 - f23.y);
         const size_t o = (size_t)r * d + i;
-        store_split(out, out_lo, o, v.x * rs * gg.x);
-        store_split(out, out_lo, o + 1, v.y * rs * gg.y);
-        store_split(out, out_lo, o + 2, v.z * rs * gg.z);
-        store_split(out, out_lo, o + 3, v.w * rs * gg.w);
+        *reinterpret_cast<uint2 *>(out + o) =
+            make_uint2(*reinterpret_cast<const uint32_t *>(&h01), *reinterpret_cast<const uint32_t *>(&h23));
+        *reinterpret_cast<uint2 *>(out_lo + o) =
+            make_uint2(*reinterpret_cast<const uint32_t *>(&l01), *reinterpret_cast<const uint32_t *>(&l23));
+    };
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+        const int i = (threadIdx.x + k * blockDim.x) * 4;
+        if (i < d) emit(i, v[k]);
     }
+    for (int i = (threadIdx.x + NV * blockDim.x) * 4; i < d; i += blockDim.x * 4)
+        emit(i, *reinterpret_cast<const float4 *>(xr + i));
 }
 
 cudaError_t launch_rmsnorm_h(const float *x, const int32_t *rows, int T, int d, const float *g, float eps,
