@@ -407,7 +407,9 @@ cudaError_t run(const FwdArgs &a, int layer, cudaStream_t s) {
 }  // namespace tc
 
 bool attention_prefill_tc_fits(const FwdArgs &a) {
-    return a.H == tc::fa::G * a.KV && (a.hd == 64 || a.hd == 128);
+    // the cache's rows (layer, page, KV head, cell) are TMA coordinates: signed 32-bit
+    const long long rows = (long long)a.L * a.n_pages * a.KV * kPage;
+    return a.H == tc::fa::G * a.KV && (a.hd == 64 || a.hd == 128) && rows <= 0x7fffffffLL;
 }
 
 cudaError_t launch_attention_prefill_tc(const FwdArgs &a, int layer, cudaStream_t s, int64_t &launches) {
